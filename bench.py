@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Benchmark of the Prof-K top-k engine on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full selection (sample -> threshold -> filter -> fallback check
+-> exact refine and sort) over one synthetic input resident in HBM.  The
+default workload is the single huge row: N = 2^28 fp32 Pareto(1.5) values with
+random sign, k = 1024, eps = 1e-6.  Inputs are larger than L2 (1 GiB), so no
+flush is needed between steps.  Prints one JSON line (rank 0).
+
+With N > 1 GPUs (torchrun) every rank runs an independent replica of the same
+selection; there is no data-path collective.  `--impl reference` times the CPU
+oracle (plain nth_element + sort) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "single_row_2p28_pareto15_k1024"
+SECONDARY_WORKLOAD = "batchtopk_4096x65536_relu_bf16_k131072"
+NORTH_STAR_GBS = 8000.0
+CLOCK_SOAK_S = 1.5
+ORACLE_SAMPLE_ELEMS = 1 << 25
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-secondary", action="store_true", help="skip the BatchTopK side measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    return 6800.0, "fallback (6.8 TB/s)"
+
+
+def workload(name):
+    from top_selection_prof_gb300 import workloads
+    if name not in workloads.WORKLOADS:
+        raise SystemExit("unknown workload %r; choose from %s" % (name, sorted(workloads.WORKLOADS)))
+    return workloads.WORKLOADS[name]
+
+
+def make_input(cfg, seed):
+    from top_selection_prof_gb300 import workloads
+    return workloads.make(cfg["kind"], cfg["rows"], cfg["n"], seed)
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+            self.t0 = time.time()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as fh:
+            rows = [ln.strip().split(", ") for ln in fh if ln.strip()]
+        os.unlink(self.file.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# ncu traffic record for the dominant kernel (stale once the kernel changes)
+# ---------------------------------------------------------------------------
+def filter_source_sha():
+    h = hashlib.sha256()
+    for f in ("kernels_filter.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "top_selection_prof_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name, n_elems):
+    """dram bytes per filter launch from the committed ncu summary, scaled to this workload."""
+    path = os.path.join(ROOT, "profiles", "filter_kernel_ncu.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    if not sha or sha.group(1) != filter_source_sha():
+        return None
+    m = re.search(r"dram_bytes_per_element\[%s\]:\s*([0-9.eE+-]+)" % re.escape(workload_name), text)
+    if not m:
+        return None
+    return float(m.group(1)) * n_elems
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle, as it stands (baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(cfg, x):
+    """A bounded sample of the workload for the CPU oracle: a prefix of the selection."""
+    if cfg["mode"] == "global":
+        flat = x.reshape(-1)[:ORACLE_SAMPLE_ELEMS]
+        return flat[None, :], True, "first %d of the %d flattened elements, global k=%d" % (
+            flat.size, x.size, min(cfg["k"], flat.size))
+    if cfg["rows"] == 1:
+        row = x[:, :ORACLE_SAMPLE_ELEMS]
+        return row, False, "first %d of %d elements of the row, k=%d" % (row.shape[1], x.shape[1], cfg["k"])
+    rows = max(1, ORACLE_SAMPLE_ELEMS // cfg["n"])
+    return x[:rows], False, "%d of %d rows of %d, k=%d per row" % (rows, cfg["rows"], cfg["n"], cfg["k"])
+
+
+def time_oracle(cfg, x, steps, warmup):
+    from oracle import plain
+    sample, glob, desc = oracle_sample(cfg, x)
+    k = min(cfg["k"], sample.size if glob else sample.shape[1])
+    for _ in range(warmup):
+        plain.topk(sample, k, global_=glob)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        plain.topk(sample, k, global_=glob)
+        times.append(time.perf_counter() - t0)
+    per_step = statistics.mean(times)
+    return {"value": sample.size / per_step / 1e9, "unit": "G elem/s", "cores": 1, "kind": "oracle",
+            "sample": desc, "seconds_per_step": per_step}
+
+
+# ---------------------------------------------------------------------------
+# our engine
+# ---------------------------------------------------------------------------
+KERNELS_PER_STEP = {"profk": 5, "direct": 1, "exact": 2}
+
+
+def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, with_e2e=True):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import top_selection_prof_gb300 as tk
+    from top_selection_prof_gb300 import _lib
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    bf16 = x_host.dtype == np.uint16
+    x_cpu = torch.from_numpy(x_host.view(np.int16) if bf16 else x_host)
+    x_pin = x_cpu.pin_memory()
+    xd = x_pin.to(dev, non_blocking=True)
+    if bf16:
+        xd = xd.view(torch.bfloat16)
+        x_pin_t = x_pin.view(torch.bfloat16)
+    else:
+        x_pin_t = x_pin
+    torch.cuda.synchronize()
+    rows, n, k, eps = cfg["rows"], cfg["n"], cfg["k"], cfg["eps"]
+    glob = cfg["mode"] == "global"
+    n_elems = rows * n
+    bytes_per_elem = 2 if bf16 else 4
+    out_shape = (k,) if glob else (rows, k)
+    vals = torch.empty(out_shape, dtype=xd.dtype, device=dev)
+    idx = torch.empty(out_shape, dtype=torch.int64, device=dev)
+
+    # one call with stats: path, (S, t, M), R
+    _, _, st = tk.select_ex(xd, k, eps=eps, global_=glob)
+    path = st["path_name"]
+
+    lib = _lib.get()
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    code = _lib.TOPK_BF16 if bf16 else _lib.TOPK_F32
+    opt = tk.options()
+
+    def call(events=None):
+        for j in range(6):
+            opt.events[j] = events[j] if events is not None else None
+        rc = lib.topk_select_ex(xd.data_ptr(), code, rows, n, k, 1, eps, vals.data_ptr(), idx.data_ptr(), sp,
+                                int(glob), ctypes.byref(opt), None)
+        if rc != 0:
+            raise RuntimeError("topk_select_ex failed: %d" % rc)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device()) if with_clocks else None
+    if clocks:
+        clocks.start()
+        t_end = time.time() + CLOCK_SOAK_S          # untimed soak so the clock record covers load
+        while time.time() < t_end:
+            for _ in range(20):
+                call()
+            torch.cuda.synchronize()
+
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for evs in stage_ev:
+        for e in evs:
+            e.record(stream)
+    handles = [[ctypes.c_void_p(e.cuda_event).value for e in evs] for evs in stage_ev]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for s in range(steps):
+        call(handles[s] if path == "profk" else None)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = start.elapsed_time(end)
+    clock_info = clocks.stop() if clocks else None
+
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / steps
+    value = n_elems * world / (ms_step * 1e-3) / 1e9
+
+    stages = None
+    filt_ms = None
+    if path == "profk":
+        names = ["sample", "threshold", "filter", "fallback_check", "refine_sort"]
+        per = {nm: [] for nm in names}
+        for evs in stage_ev:
+            for j, nm in enumerate(names):
+                per[nm].append(evs[j].elapsed_time(evs[j + 1]))
+        stages = {nm + "_us": round(1e3 * statistics.mean(v), 2) for nm, v in per.items()}
+        filt_ms = statistics.mean(per["filter"])
+
+    peak, peak_src = load_peaks()
+    roofline = None
+    if filt_ms:
+        alg_bytes = n_elems * bytes_per_elem + st["R"] * 8
+        achieved = alg_bytes / (filt_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": recorded_traffic(name, n_elems),
+                    "kernel": "filter_kernel", "algorithmic_bytes_per_launch": alg_bytes,
+                    "peak_source": peak_src}
+
+    e2e = None
+    if with_e2e:
+        e2e_steps = max(3, min(steps, 10))
+        vals_h = torch.empty(out_shape, dtype=xd.dtype).pin_memory()
+        idx_h = torch.empty(out_shape, dtype=torch.int64).pin_memory()
+        for _ in range(2):
+            xd.copy_(x_pin_t, non_blocking=True)
+            call()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            xd.copy_(x_pin_t, non_blocking=True)
+            v2, i2 = (tk.select_global(xd, k, eps=eps) if glob else tk.select(xd, k, eps=eps))
+            vals_h.copy_(v2, non_blocking=True)
+            idx_h.copy_(i2, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / e2e_steps
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": round(n_elems * world / (ms_e2e * 1e-3) / 1e9, 3), "unit": "G elem/s",
+               "h2d_bytes_per_step": n_elems * bytes_per_elem,
+               "d2h_bytes_per_step": (k if glob else rows * k) * (bytes_per_elem + 8),
+               "ms_per_step": round(ms_e2e, 4), "steps": e2e_steps}
+
+    return {
+        "value": value, "ms_per_step": ms_step, "path": path, "stats": st, "stages": stages,
+        "roofline": roofline, "e2e": e2e, "clocks": clock_info,
+        "gpu_launches": KERNELS_PER_STEP.get(path, 0) * steps,
+        "hbm_gbs_whole_step": n_elems * bytes_per_elem / (ms_step * 1e-3) / 1e9,
+    }
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    cfg = workload(args.workload)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        x = make_input(cfg, args.seed)
+        r = time_oracle(cfg, x, args.steps, args.warmup)
+        line = {"metric": "top-k G elem/s and achieved HBM GB/s vs ~8 TB/s peak, 1xGB300", "impl": "reference",
+                "value": round(r["value"], 4), "unit": "G elem/s", "n_gpus": 0, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(r["seconds_per_step"] * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype":
+                    "bf16" if cfg["kind"].endswith("_bf16") else "f32",
+                "data": "synthetic (seeded numpy)",
+                "config": {"workload": args.workload, "rows": cfg["rows"], "n": cfg["n"], "k": cfg["k"],
+                           "eps": cfg["eps"], "mode": cfg["mode"]},
+                "cpu_baseline": {k2: r[k2] for k2 in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": round(r["value"], 4), "unit": "G elem/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    import top_selection_prof_gb300 as tk
+    tk._lib.get()   # fails loudly if the engine is not built
+
+    x = make_input(cfg, args.seed + rank)
+    res = run_ours(cfg, args.workload, x, args.steps, args.warmup, world, rank)
+
+    secondary = None
+    if not args.no_secondary and args.workload != SECONDARY_WORKLOAD:
+        c2 = workload(SECONDARY_WORKLOAD)
+        del x
+        x2 = make_input(c2, args.seed + rank)
+        r2 = run_ours(c2, SECONDARY_WORKLOAD, x2, args.steps, args.warmup, world, rank, with_clocks=False,
+                      with_e2e=False)
+        secondary = {"workload": SECONDARY_WORKLOAD, "value": round(r2["value"], 3), "unit": "G elem/s",
+                     "ms_per_step": round(r2["ms_per_step"], 4), "path": r2["path"],
+                     "hbm_gbs_whole_step": round(r2["hbm_gbs_whole_step"], 1),
+                     "frac_of_8tbs_whole_step": round(r2["hbm_gbs_whole_step"] / NORTH_STAR_GBS, 4),
+                     "roofline": r2["roofline"], "stages": r2["stages"], "R": r2["stats"]["R"],
+                     "S_t_M": [r2["stats"]["S"], r2["stats"]["t"], r2["stats"]["M"]]}
+        x = None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xb = make_input(cfg, args.seed) if x is None else x
+        cb = time_oracle(cfg, xb, steps=2, warmup=0)
+        cpu = {k2: cb[k2] for k2 in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        st = res["stats"]
+        line = {
+            "metric": "top-k G elem/s and achieved HBM GB/s vs ~8 TB/s peak, 1xGB300",
+            "value": round(res["value"], 3), "unit": "G elem/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if cfg["kind"].endswith("_bf16") else "f32",
+            "data": "synthetic (seeded numpy: %s)" % cfg["kind"],
+            "config": {"workload": args.workload, "rows": cfg["rows"], "n": cfg["n"], "k": cfg["k"],
+                       "eps": cfg["eps"], "mode": cfg["mode"], "path": res["path"],
+                       "S": st["S"], "t": st["t"], "M": st["M"], "R": st["R"],
+                       "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "hbm_gbs_whole_step": round(res["hbm_gbs_whole_step"], 1),
+            "frac_of_8tbs_whole_step": round(res["hbm_gbs_whole_step"] / NORTH_STAR_GBS, 4),
+            "roofline": res["roofline"], "stages": res["stages"], "cpu_baseline": cpu, "e2e": res["e2e"],
+            "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "secondary": secondary,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,209 @@
+/*
+ * topk.h -- C ABI of the GB300 Prof-K top-k selection engine (libtopk_gb300.so).
+ *
+ * The method is Prof-K ("Prof-K: Probabilistic One-Pass Filtering for
+ * Efficient Top-k Selection", sections 3-4 and Algorithm 1): draw S uniform
+ * positions, take the t-th largest sampled element as a threshold tau, stream
+ * the input once keeping every element that ranks at or above tau in a buffer
+ * of capacity M, then select the exact top-k of the buffer.  When fewer than k
+ * elements survive, or more than M do, the engine falls back to an exact
+ * selection over the whole input, so every result is exact.
+ *
+ * Conventions shared by every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller.  x is
+ *     row-major and contiguous, rows x n elements of the given dtype.
+ *   - out_vals has the dtype of x and holds the input's own bits at the chosen
+ *     positions; out_idx is int64.
+ *   - Order: each output row lists the k winners by (value descending, index
+ *     ascending) -- equal values go to the lower index, as in "Rank by
+ *     Counting" (top-k task 1).  With largest == 0 the value order is reversed
+ *     (smallest first) and ties still go to the lower index.  NaN ranks above
+ *     every number (so it comes last when largest == 0), all NaNs are equal,
+ *     -0 equals +0.
+ *   - The call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream) and does no host synchronisation, except that
+ *     topk_select_ex synchronises the stream when `stats` is non-NULL.
+ *   - The library keeps a per-(device, stream) workspace for the sample, the
+ *     threshold, the candidate buffer and counters; it grows on demand with
+ *     stream-ordered allocation and is never shrunk.  Calls that share a
+ *     stream are ordered; calls on different streams use different workspaces.
+ *   - Errors are returned as topk_status_t codes; nothing is thrown across the
+ *     ABI and no message is printed.
+ */
+#ifndef TOPK_GB300_H
+#define TOPK_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { TOPK_F32 = 0, TOPK_BF16 = 1 } topk_dtype_t;
+
+typedef enum {
+  TOPK_OK = 0,
+  TOPK_EINVAL = -1,        /* bad argument: null pointer, k < 1, k > n, eps outside [0,1), ... */
+  TOPK_ENOMEM = -2,        /* workspace allocation failed */
+  TOPK_ECUDA = -3,         /* a CUDA runtime call or kernel launch failed */
+  TOPK_EUNSUPPORTED = -4,  /* valid request outside the engine's limits (see topk_select) */
+  TOPK_ETIMEOUT = -5       /* a bounded device-side wait gave up (reported with stats only) */
+} topk_status_t;
+
+/* Parameter rule for (t, M).  Both use Algorithm 1's sample size S.
+ *   TOPK_RULE_EXACT (default): t and M from the exact binomial tails of the
+ *     with-replacement sampler, eps/2 for recall failure and eps/2 for
+ *     overflow (Theorem 3's split without the normal approximation).
+ *   TOPK_RULE_ALG1: t and M as Algorithm 1 prints them (Eq. 6, Eq. 12 and
+ *     the t = 1 sparse rule).  Results stay exact; only the miss rate differs. */
+typedef enum { TOPK_RULE_EXACT = 0, TOPK_RULE_ALG1 = 1 } topk_rule_t;
+
+/* Which pipeline ran (or is forced).
+ *   TOPK_PATH_DIRECT: exact radix select straight over each row (small rows, or
+ *     when the sample would be at least half the row).
+ *   TOPK_PATH_PROFK:  sample -> threshold -> one-pass filter -> exact refine,
+ *     with the full-input fallback on a miss.
+ *   TOPK_PATH_EXACT:  the full-input radix select of the fallback, used for
+ *     large rows when eps == 0. */
+typedef enum {
+  TOPK_PATH_AUTO = 0,
+  TOPK_PATH_DIRECT = 1,
+  TOPK_PATH_PROFK = 2,
+  TOPK_PATH_EXACT = 3
+} topk_path_t;
+
+/* Tuning and test knobs.  Initialise with topk_options_init(). */
+typedef struct {
+  int64_t s_min;       /* Algorithm 1 S_min (default 32768) */
+  int64_t s_max;       /* Algorithm 1 S_max (default 131072) */
+  double cost_ratio;   /* tau_B / tau_A of Eq. 13 (default 1) */
+  int rule;            /* topk_rule_t (default TOPK_RULE_EXACT) */
+  int path;            /* topk_path_t; TOPK_PATH_AUTO lets the engine choose */
+  uint64_t seed;       /* Philox key for the sampler (default fixed) */
+  int64_t counter;     /* Philox call counter; -1 = next value of a per-process counter */
+  int force_miss;      /* non-zero: every row takes the fallback (fault injection on the host) */
+  int64_t m_override;  /* > 0: use this buffer capacity M instead of the rule's */
+  int64_t t_override;  /* > 0: use this threshold rank t instead of the rule's */
+  /* Optional cudaEvent_t handles (NULL = none) recorded on `stream` at the
+   * stage boundaries of the Prof-K path: [0] before the sample kernel, [1]
+   * after it, [2] after the threshold selection, [3] after the filter, [4]
+   * after the fallback check, [5] after the final selection.  The caller owns
+   * the events; they are only recorded, never created or destroyed here. */
+  void* events[6];
+} topk_options_t;
+
+/* Per-call report (row 0 for the per-row fields). */
+typedef struct {
+  int path;            /* topk_path_t that ran */
+  int index_bits;      /* b of the composite key format below */
+  int64_t S, t, M;     /* sample size, threshold rank, buffer capacity (0 on the direct path) */
+  int64_t R;           /* row 0: elements that passed the filter (before any fallback) */
+  int64_t misses;      /* rows whose filter result missed k <= R <= M and took the fallback */
+  uint64_t tau;        /* row 0: composite key of the sampled threshold */
+  int64_t tau_index;   /* row 0: position of the element tau was taken from */
+  uint64_t seed;       /* Philox key and counter the sampler used */
+  int64_t counter;
+  int cluster;         /* CTAs per thread-block cluster in the final selection */
+} topk_stats_t;
+
+/* Parameters the engine would use for a selection of k out of n (host only). */
+typedef struct {
+  int path;            /* topk_path_t the automatic choice resolves to */
+  int64_t S, t, M;
+  double p_recall_fail;  /* P[R < k] for these (S, t) under the with-replacement sampler */
+  double p_overflow;     /* P[R > M] */
+} topk_plan_t;
+
+/* Fills *opt with the defaults above. */
+void topk_options_init(topk_options_t* opt);
+
+/*
+ * Per-row top-k (section 3: "for batched inputs ... applied in parallel to each
+ * batch element").  For each of `rows` rows of n elements, writes the k
+ * winners to out_vals[r*k + j] and their row-local positions to
+ * out_idx[r*k + j].  eps in [0, 1) is the target probability that a row takes
+ * the fallback (Theorem 3); eps == 0 selects exactly without sampling.  The
+ * result never depends on eps or on the sampler.
+ *   Limits: n < 2^31; k <= 180224 (EUNSUPPORTED beyond); rows == 0 is a no-op.
+ *   EINVAL: null pointer (with rows > 0), rows < 0, n < 1, k < 1, k > n,
+ *           eps outside [0, 1), unknown dtype.
+ */
+int topk_select(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,
+                double eps, void* out_vals, int64_t* out_idx, void* stream);
+
+/*
+ * Batch-global top-k (BatchTopK, section 5: the B x d_dict activations are
+ * flattened into one vector of N = B*d_dict and the K = B*k largest are kept).
+ * Treats the rows*n elements as one vector: out_vals[j], out_idx_flat[j] for
+ * j < k, with flat positions r*n + c.
+ *   Limits: rows*n <= 2^32 for F32 and <= 2^48 for BF16; k <= 180224.
+ *   EINVAL as topk_select, with k > rows*n in place of k > n.
+ */
+int topk_select_global(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,
+                       double eps, void* out_vals, int64_t* out_idx_flat, void* stream);
+
+/*
+ * topk_select (global == 0) or topk_select_global (global != 0) with options
+ * (NULL = defaults) and an optional report.  When stats is non-NULL the call
+ * synchronises `stream` before returning and can return TOPK_ETIMEOUT.
+ */
+int topk_select_ex(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,
+                   double eps, void* out_vals, int64_t* out_idx, void* stream, int global,
+                   const topk_options_t* opt, topk_stats_t* stats);
+
+/* Host-only: the path and (S, t, M) the engine uses for one selection of k out
+ * of n elements (n = rows*n for the global variant).  Algorithm 1 and the rule
+ * in opt (NULL = defaults).  EINVAL on bad arguments. */
+int topk_plan(int64_t n, int64_t k, double eps, const topk_options_t* opt, topk_plan_t* plan);
+
+/* Static text for a status code. */
+const char* topk_status_str(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int topk_version(void);
+
+/* ------------------------------------------------------------------------
+ * Stage entry points: the individual steps of the Prof-K pipeline, for tests
+ * and for callers that want the pieces.
+ *
+ * Composite key format.  Every element is identified by a 64-bit key whose
+ * unsigned order is the selection order:
+ *     key = (v << b) | (2^b - 1 - i)
+ * where i is the element's position in its selection (row-local, or flat for
+ * the global variant), b = topk_index_bits(length of the selection), and v is
+ * the order-preserving image of the value: for F32 bits u (BF16 likewise on 16
+ * bits), NaN -> all ones, -0 -> +0, then v = u | signbit if u is non-negative,
+ * else ~u; with largest == 0, v is complemented.  Larger key = better rank;
+ * keys are distinct, so "ranks at or above tau" is simply key >= tau.
+ * ------------------------------------------------------------------------ */
+
+/* b for a selection over `len` elements: the bits needed for positions 0..len-1 (at least 1). */
+int topk_index_bits(int64_t len);
+
+/*
+ * Stage 1 (section 3, sampling): for each selection r, draws S positions with
+ * Philox4x32-10 -- draw j uses counter (j/2, r, counter_lo, counter_hi) and key
+ * (seed_lo, seed_hi); the even draw takes the 64-bit word (w1<<32 | w0), the
+ * odd one (w3<<32 | w2); the position is floor(word * len / 2^64) -- and writes
+ * the composite keys of the drawn elements to out_keys[r*S + j].
+ * global != 0 treats x as one selection of rows*n elements.
+ */
+int topk_prof_sample(const void* x, int dtype, int64_t rows, int64_t n, int global, int largest,
+                     int64_t S, uint64_t seed, int64_t counter, uint64_t* out_keys, void* stream);
+
+/*
+ * Stage 3 (section 3, filtering): for each selection r, streams its elements
+ * once and appends the composite key of every element with key >= tau[r] to
+ * buf[r*M ...]; counts[r] receives the number R of such elements (it keeps
+ * counting past M; only the first M found are stored, in no particular order).
+ * tau (device, one key per selection) uses the key format above.
+ */
+int topk_prof_filter(const void* x, int dtype, int64_t rows, int64_t n, int global, int largest,
+                     const uint64_t* tau, int64_t M, uint64_t* buf, uint64_t* counts,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOPK_GB300_H */

@@ -1,0 +1,131 @@
+"""Parity of the CUDA path with the CPU oracle: bit-exact values and indices.
+
+Sizes are chosen so the oracle finishes in seconds while spanning many filter
+tiles and ragged tails.  Every case goes through the C ABI via the binding.
+"""
+import zlib
+
+import pytest
+
+from oracle import plain
+from top_selection_prof_gb300 import workloads
+
+from .gpu_util import assert_same, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _tk():
+    import top_selection_prof_gb300 as tk
+    return tk
+
+
+def _check(x, k, largest=True, eps=1e-3, global_=False, expect_path=None, **opts):
+    tk = _tk()
+    xd = to_device(x)
+    v, i, st = tk.select_ex(xd, k, largest=largest, eps=eps, global_=global_, **opts)
+    ov, oi = plain.topk(x, k, largest=largest, global_=global_)
+    assert_same(v, i, ov, oi, "k=%d largest=%s path=%s" % (k, largest, st["path_name"]))
+    if expect_path is not None:
+        assert st["path_name"] == expect_path, st
+    return st
+
+
+# (kind, rows, n, k, eps, global, expected path)
+CASES = [
+    ("int20", 1, 65536, 10, 1e-3, False, "direct"),             # the exercise's own shape
+    ("normal", 64, 32768, 64, 1e-3, False, "direct"),
+    ("normal", 3, 100_003, 37, 1e-3, False, "profk"),            # ragged rows -> scalar loads
+    ("pareto15", 1, 1 << 22, 1024, 1e-6, False, "profk"),
+    ("ties1000", 1, 1 << 22, 10000, 1e-3, False, "profk"),
+    ("ties1000_sorted", 1, 1 << 22, 10000, 1e-3, False, "profk"),
+    ("relu_normal_bf16", 256, 65536, 8192, 1e-3, True, "profk"),
+    ("relu_normal_bf16", 256, 65536, 100000, 1e-3, True, "profk"),  # 16-CTA cluster sort
+    ("uniform", 1, 1_000_003, 777, 1e-3, False, "profk"),
+    ("pareto15", 4, 1 << 21, 100, 1e-3, False, "profk"),          # per-row Prof-K
+    ("normal", 1, 1 << 20, 1, 1e-3, False, "profk"),
+    ("specials", 1, 1 << 20, 3000, 1e-3, False, "profk"),
+    ("specials", 5, 4099, 50, 1e-3, False, "direct"),
+    ("constant", 1, 1 << 21, 500, 1e-3, False, "profk"),
+    ("relu_normal_bf16", 7, 33_333, 20, 1e-3, False, None),
+]
+
+
+@pytest.mark.parametrize("kind,rows,n,k,eps,global_,path", CASES)
+@pytest.mark.parametrize("largest", [True, False])
+def test_parity(kind, rows, n, k, eps, global_, path, largest):
+    x = workloads.make(kind, rows, n, seed=zlib.crc32(("%s/%d/%d/%d" % (kind, rows, n, k)).encode()) % 1000)
+    _check(x, k, largest=largest, eps=eps, global_=global_, expect_path=path)
+
+
+@pytest.mark.parametrize("path", [1, 2, 3])   # direct, Prof-K, grid-wide exact
+def test_every_path_on_the_same_input(path):
+    x = workloads.make("ties1000", 1, 1 << 21, seed=3)
+    _check(x, 2500, eps=1e-3 if path == 2 else 0.0, path=path)
+    x = workloads.make("relu_normal_bf16", 32, 65536, seed=4)
+    _check(x, 3000, eps=1e-3 if path == 2 else 0.0, global_=True, path=path)
+
+
+def test_forced_miss_takes_the_fallback_and_stays_exact():
+    x = workloads.make("pareto15", 1, 1 << 22, seed=5)
+    st = _check(x, 1024, eps=1e-3, force_miss=1)
+    assert st["misses"] == 1 and st["path_name"] == "profk"
+
+
+@pytest.mark.parametrize("m_override,t_override", [(1100, 0), (0, 1), (0, 400)])
+def test_overflow_and_recall_misses_are_repaired(m_override, t_override):
+    # a tiny buffer overflows; t = 1 tends to miss recall; a huge t overflows the buffer
+    x = workloads.make("normal", 1, 1 << 22, seed=6)
+    st = _check(x, 1000, eps=1e-3, m_override=m_override, t_override=t_override)
+    if st["misses"]:
+        assert st["R"] < 1000 or st["R"] > st["M"]
+    else:
+        assert 1000 <= st["R"] <= st["M"]
+
+
+def test_k_equals_n_and_k_one_direct():
+    x = workloads.make("ties1000", 3, 5000, seed=7)
+    _check(x, 5000)
+    _check(x, 1)
+
+
+def test_unaligned_input_pointer():
+    tk = _tk()
+    base = workloads.make("normal", 1, (1 << 21) + 1, seed=8)
+    flat = to_device(base.reshape(-1))[1:]         # 4-byte offset: no 16-byte vectors
+    assert flat.data_ptr() % 16 != 0
+    v, i, st = tk.select_ex(flat, 300, eps=1e-3)
+    ov, oi = plain.topk(base.reshape(-1)[1:][None, :], 300)
+    assert_same(v[None, :], i[None, :], ov, oi, "unaligned")
+    assert st["path_name"] == "profk"
+
+
+def test_rows_zero_is_a_noop():
+    import torch
+    tk = _tk()
+    x = torch.empty((0, 100), device="cuda")
+    v, i = tk.select(x, 5)
+    assert v.shape == (0, 5) and i.shape == (0, 5)
+
+
+def test_maximum_k_cluster_sort():
+    tk = _tk()
+    kmax = 16 * 11264
+    x = workloads.make("normal", 1, 1 << 20, seed=9)
+    _check(x, kmax, eps=1e-3)
+    with pytest.raises(tk.TopkError):
+        tk.select(to_device(x), kmax + 1)
+
+
+def test_repeated_calls_and_streams():
+    import torch
+    tk = _tk()
+    x = workloads.make("pareto15", 1, 1 << 22, seed=10)
+    xd = to_device(x)
+    ov, oi = plain.topk(x, 512)
+    s = torch.cuda.Stream()
+    for rep in range(3):
+        with torch.cuda.stream(s):
+            v, i = tk.select(xd, 512)
+        s.synchronize()
+        assert_same(v, i, ov, oi, "rep %d" % rep)

@@ -1,0 +1,135 @@
+// Device-side building blocks shared by the engine's kernels: the composite
+// key, Philox4x32-10, PTX wrappers and the bounded device wait.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tk {
+
+constexpr int kF32 = 0;
+constexpr int kBF16 = 1;
+
+// ---------------------------------------------------------------------------
+// Order-preserving keys.  Unsigned order of the key == the selection order of
+// the value: NaN above everything (all NaNs equal), -0 == +0.  The composite
+// key appends the complemented position so that, among equal values, the lower
+// position has the larger key -- the index tie-break of "Rank by Counting".
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ uint32_t order_key_f32(uint32_t u) {
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0xffffffffu;  // NaN
+  if (u == 0x80000000u) u = 0u;                              // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__host__ __device__ __forceinline__ uint32_t order_key_bf16(uint32_t h) {
+  if ((h & 0x7fffu) > 0x7f80u) return 0xffffu;
+  if (h == 0x8000u) h = 0u;
+  return (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
+}
+
+// Inverse of order_key_* for keys that are neither NaN nor zero (those two do
+// not determine the input bits; the caller reads the input instead).
+__host__ __device__ __forceinline__ uint32_t value_bits_f32(uint32_t key) {
+  return (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+}
+__host__ __device__ __forceinline__ uint32_t value_bits_bf16(uint32_t key) {
+  return (key & 0x8000u) ? (key & 0x7fffu) : (~key & 0xffffu);
+}
+
+template <int DT>
+struct Dt;
+
+template <>
+struct Dt<kF32> {
+  using storage = uint32_t;
+  static constexpr int kKeyBits = 32;
+  static constexpr uint32_t kKeyMask = 0xffffffffu;
+  static constexpr int kVec = 4;  // elements per 16-byte vector
+  __device__ __forceinline__ static uint32_t key(uint32_t u) { return order_key_f32(u); }
+  __device__ __forceinline__ static uint32_t bits(uint32_t key) { return value_bits_f32(key); }
+  __device__ __forceinline__ static float to_float(uint32_t u) { return __uint_as_float(u); }
+  static constexpr uint32_t kZeroKey = 0x80000000u;
+  static constexpr uint32_t kNanKey = 0xffffffffu;
+};
+
+template <>
+struct Dt<kBF16> {
+  using storage = uint16_t;
+  static constexpr int kKeyBits = 16;
+  static constexpr uint32_t kKeyMask = 0xffffu;
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static uint32_t key(uint32_t h) { return order_key_bf16(h); }
+  __device__ __forceinline__ static uint32_t bits(uint32_t key) { return value_bits_bf16(key); }
+  __device__ __forceinline__ static float to_float(uint32_t h) { return __uint_as_float(h << 16); }
+  static constexpr uint32_t kZeroKey = 0x8000u;
+  static constexpr uint32_t kNanKey = 0xffffu;
+};
+
+// Composite key: (value key << b) | (2^b - 1 - position).
+__host__ __device__ __forceinline__ uint64_t compose(uint32_t vkey, uint64_t pos, int b) {
+  const uint64_t mask = (b >= 64) ? ~0ull : ((1ull << b) - 1ull);
+  return (static_cast<uint64_t>(vkey) << b) | (mask - pos);
+}
+__host__ __device__ __forceinline__ uint64_t position_of(uint64_t ck, int b) {
+  const uint64_t mask = (1ull << b) - 1ull;
+  return mask - (ck & mask);
+}
+__host__ __device__ __forceinline__ uint32_t vkey_of(uint64_t ck, int b) {
+  return static_cast<uint32_t>(ck >> b);
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon et al., SC'11): 10 rounds of two 32x32->64 multiplies,
+// key bumped by the Weyl constants between rounds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    k.x += 0x9E3779B9u;
+    k.y += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Device status codes written to the workspace status word.
+constexpr int kDevOk = 0;
+constexpr int kDevTimeout = 1;
+constexpr int kDevBadState = 2;
+
+// Upper bound of every device-side spin wait.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+}  // namespace tk

@@ -1,0 +1,88 @@
+// Internal interface between the C ABI (topk_api.cu) and the kernel
+// translation units.  Host code only; no torch types anywhere.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tk {
+
+// One "selection problem" is a row (per-row variant) or the whole flattened
+// input (global variant).  `len` elements each, problems laid out back to back.
+struct Problem {
+  const void* x;
+  int dtype;       // kF32 / kBF16
+  int64_t nsel;    // number of selections
+  int64_t len;     // elements per selection
+  int ib;          // index bits of the composite key
+  uint32_t flip;   // 0 for largest, value-key mask for smallest
+  bool vec_ok;     // 16-byte vector loads are legal (alignment and len % vec)
+};
+
+// ---- parameters (params.cpp) -------------------------------------------------
+struct ParamRule {
+  int64_t s_min = 32768, s_max = 131072;
+  double cost_ratio = 1.0;
+  int rule = 0;  // 0 exact tails, 1 Algorithm 1 as printed
+};
+double inv_normal_upper(double q);  // x with P[Z > x] = q
+double binom_upper_tail(int64_t s, double p, int64_t t);  // P[Bin(s,p) >= t]
+double binom_lower_tail(int64_t s, double p, int64_t t);  // P[Bin(s,p) <= t]
+int64_t alg1_sample_size(int64_t n, int64_t k, double eps, const ParamRule& pr);
+// Returns false when no valid t exists (the caller takes an exact path).
+bool choose_params(int64_t n, int64_t k, double eps, const ParamRule& pr, int64_t* S, int64_t* t,
+                   int64_t* M);
+
+// Per-call device words shared by the pipeline's kernels.
+struct DevHeader {
+  unsigned barrier[2];         // grid barrier of the fallback: arrivals, generation
+  int status;                  // kDevOk / kDevTimeout / kDevBadState
+  int pad;
+  unsigned long long misses;   // selections that took the fallback
+};
+
+// ---- sample (kernels_sample.cu) ----------------------------------------------
+// Also resets counts[0..nsel) and the header (arrivals, status, misses) when
+// those pointers are non-null, so the filter and fallback start clean.
+cudaError_t launch_sample(const Problem& p, int64_t S, uint64_t seed, uint64_t counter,
+                          uint64_t* keys, unsigned long long* counts_to_zero, DevHeader* hdr,
+                          cudaStream_t st);
+
+// ---- filter and fallback (kernels_filter.cu) ---------------------------------
+cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
+                          unsigned long long* counts, cudaStream_t st);
+
+struct FallbackScratch {
+  unsigned* ghist;        // 8 passes x 256 counters
+  unsigned* tile_counts;  // ceil(len / kFallbackTile) counters
+  unsigned* barrier;      // [0] arrivals, [1] generation
+  int* status;
+  unsigned long long* r_seen;  // per selection: R as the filter left it
+  unsigned long long* misses;  // number of selections that fell back
+  uint64_t* tau_exact;         // per selection: exact k-th key written on a miss
+};
+constexpr int64_t kFallbackTile = 4096;
+// force: 0 = only rows that missed, 1 = every row (fault injection / exact path).
+cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,
+                            unsigned long long* counts, const FallbackScratch& fs, int force,
+                            cudaStream_t st);
+
+// ---- final selection (kernels_select.cu) -------------------------------------
+struct SelectJob {
+  // source: either composite keys (keys != nullptr) or the raw input (p.x)
+  const uint64_t* keys;
+  int64_t key_stride;                  // keys per selection in `keys`
+  const unsigned long long* counts;    // valid keys per selection (clamped to key_stride); may be null
+  int64_t r;                           // rank to find (1-based)
+  bool want_topk;                      // true: sort and write the r winners; false: write tau
+  uint64_t* tau_out;                   // per selection (want_topk == false)
+  void* out_vals;                      // want_topk
+  int64_t* out_idx;
+  int* status;                         // device status word (kDevBadState on inconsistency)
+};
+// Returns the cluster size used via *cluster (may be null).
+cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source_bound, int* cluster,
+                          cudaStream_t st);
+int64_t select_max_k();
+
+}  // namespace tk

@@ -1,0 +1,481 @@
+// Stage 3 of Prof-K (section 3, "Filtering") and the exact fallback
+// (section 3, stage 4, and Appendix D "Fallback as a Safety Mechanism").
+//
+// filter_kernel streams every selection once and appends the composite key of
+// each element ranking at or above tau to the candidate buffer.  It is the
+// HBM-bound hot loop: a persistent grid walks 16 KB tiles with 16-byte
+// read-only loads; a float compare against tau's value is the common-path
+// test, and only when some lane of a warp sees a candidate does the warp build
+// exact composite keys.  Survivors are ranked with __ballot_sync/__popc
+// (the warp flag ranks of "One Bit at a Time") into a per-warp shared-memory
+// stage, which is flushed with one global atomicAdd per 256 survivors.  The
+// counter keeps counting past the capacity M so R is exact; only slots < M are
+// written.
+//
+// fallback_kernel is a cooperative launch.  For every selection whose filter
+// result missed k <= R <= M (or every selection when forced) it finds the
+// k-th largest element exactly by radix select on the value key (8-bit digits,
+// one grid-wide histogram per digit), resolves ties at that value by index --
+// per-tile counts of the tied value, a scan and a lower bound over the running
+// count ("Find It in log n"), then an ordered scan of one tile -- and re-runs
+// the filter with that exact threshold, which keeps exactly k elements.
+// Grid-wide steps use a bounded barrier that reports a timeout instead of
+// hanging.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "engine.h"
+
+namespace tk {
+
+namespace {
+
+constexpr int kFilterBlock = 256;
+constexpr int kFilterUnroll = 4;
+constexpr int kWarpStage = 256;  // survivors staged per warp before a flush
+constexpr unsigned kFull = 0xffffffffu;
+
+struct FilterParams {
+  const void* x;
+  int64_t nsel, len;
+  int ib;
+  uint32_t flip;
+  const uint64_t* tau;
+  int64_t cap;
+  uint64_t* buf;
+  unsigned long long* counts;
+};
+
+// Element e of a packed group of raw words (VEC elements).
+template <int DT, int VEC>
+__device__ __forceinline__ uint32_t elem(const uint32_t (&w)[4], int e) {
+  if (DT == kF32) return VEC == 1 ? w[0] : w[e];
+  if (VEC == 1) return w[0] & 0xffffu;
+  return (w[e >> 1] >> ((e & 1) * 16)) & 0xffffu;
+}
+
+template <int DT, int VEC>
+__device__ __forceinline__ void load_group(const typename Dt<DT>::storage* p, uint32_t (&w)[4]) {
+  if (VEC == 1) {
+    w[0] = static_cast<uint32_t>(__ldg(p));
+  } else {
+    const uint4 v = ld_stream_v4(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  }
+}
+
+// Float value of tau for the cheap superset test.  NaN (test passes for all)
+// when tau's value is NaN.
+template <int DT>
+__device__ __forceinline__ float tau_value(uint64_t tau, int ib, uint32_t flip) {
+  const uint32_t k = vkey_of(tau, ib) ^ flip;
+  if (k == Dt<DT>::kNanKey) return __uint_as_float(0x7fc00000u);
+  if (k == Dt<DT>::kZeroKey) return 0.0f;
+  return Dt<DT>::to_float(Dt<DT>::bits(k));
+}
+
+struct WarpStage {
+  uint64_t* s;   // this warp's staging slots
+  uint32_t n;    // warp-uniform fill
+};
+
+__device__ __forceinline__ void warp_flush(WarpStage& st, int64_t row, int64_t cap, uint64_t* buf,
+                                           unsigned long long* counts) {
+  if (st.n == 0) return;
+  const int lane = threadIdx.x & 31;
+  unsigned long long base = 0;
+  if (lane == 0) base = atomicAdd(counts + row, static_cast<unsigned long long>(st.n));
+  base = __shfl_sync(kFull, base, 0);
+  __syncwarp();
+  uint64_t* dst = buf + row * cap;
+  for (uint32_t j = lane; j < st.n; j += 32) {
+    const unsigned long long pos = base + j;
+    if (pos < static_cast<unsigned long long>(cap)) dst[pos] = st.s[j];
+  }
+  __syncwarp();
+  st.n = 0;
+}
+
+// One group of VEC consecutive elements per lane: superset test, then the
+// exact composite-key test and ballot ranking for warps that saw a candidate.
+template <int DT, bool LARGEST, int VEC>
+__device__ __forceinline__ void filter_group(const uint32_t (&w)[4], int64_t pos, bool ok, float tv,
+                                             uint64_t tau, int ib, uint32_t flip, WarpStage& st,
+                                             int64_t row, const FilterParams& fp) {
+  bool cand = false;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) {
+    const float f = Dt<DT>::to_float(elem<DT, VEC>(w, e));
+    cand |= LARGEST ? !(f < tv) : !(f > tv);
+  }
+  cand &= ok;
+  if (!__any_sync(kFull, cand)) return;
+  const unsigned lt = lanemask_lt();
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) {
+    uint64_t ck = 0;
+    bool pass = false;
+    if (cand) {
+      ck = compose(Dt<DT>::key(elem<DT, VEC>(w, e)) ^ flip, static_cast<uint64_t>(pos + e), ib);
+      pass = ck >= tau;
+    }
+    const unsigned m = __ballot_sync(kFull, pass);
+    if (m) {
+      if (st.n + 32 > kWarpStage) warp_flush(st, row, fp.cap, fp.buf, fp.counts);
+      if (pass) st.s[st.n + __popc(m & lt)] = ck;
+      st.n += __popc(m);
+    }
+  }
+}
+
+// Filter the tiles [tile_begin, tile_end) (stride tile_step) of the flattened
+// tile space (selection-major).  Used by the filter kernel and the fallback.
+template <int DT, bool LARGEST, int VEC>
+__device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t tile_end,
+                             int64_t tile_step, WarpStage& st) {
+  using T = typename Dt<DT>::storage;
+  constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
+  const int64_t tiles_per_row = (fp.len + kTile - 1) / kTile;
+  int64_t cur_row = -1;
+  uint64_t tau = 0;
+  float tv = 0.0f;
+  for (int64_t tile = tile_begin; tile < tile_end; tile += tile_step) {
+    const int64_t row = tile / tiles_per_row;
+    const int64_t base = (tile - row * tiles_per_row) * kTile;
+    if (row != cur_row) {
+      if (cur_row >= 0) warp_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
+      cur_row = row;
+      tau = __ldcg(fp.tau + row);
+      tv = tau_value<DT>(tau, fp.ib, fp.flip);
+    }
+    const T* xr = static_cast<const T*>(fp.x) + row * fp.len;
+    uint32_t w[kFilterUnroll][4];
+    bool ok[kFilterUnroll];
+    int64_t pos[kFilterUnroll];
+#pragma unroll
+    for (int u = 0; u < kFilterUnroll; ++u) {
+      pos[u] = base + (static_cast<int64_t>(u) * kFilterBlock + threadIdx.x) * VEC;
+      ok[u] = pos[u] < fp.len;
+      if (ok[u]) load_group<DT, VEC>(xr + pos[u], w[u]);
+      else w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kFilterUnroll; ++u)
+      filter_group<DT, LARGEST, VEC>(w[u], pos[u], ok[u], tv, tau, fp.ib, fp.flip, st, row, fp);
+  }
+  if (cur_row >= 0) warp_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
+}
+
+template <int DT, bool LARGEST, int VEC>
+__global__ void __launch_bounds__(kFilterBlock) filter_kernel(FilterParams fp) {
+  __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
+  WarpStage st{stage[threadIdx.x >> 5], 0u};
+  constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
+  const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
+  filter_tiles<DT, LARGEST, VEC>(fp, blockIdx.x, ntiles, gridDim.x, st);
+}
+
+// ---------------------------------------------------------------------------
+// Fallback
+// ---------------------------------------------------------------------------
+
+struct FallbackParams {
+  FilterParams fp;
+  int64_t k;
+  int force;
+  FallbackScratch fs;
+};
+
+// Grid-wide barrier for a cooperative launch.  Gives up after kWaitLimitNs and
+// records kDevTimeout in the status word; returns false then (and when another
+// block already reported an error).
+__device__ bool grid_barrier(unsigned* bar, int* status) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const unsigned gen = ld_acquire_u32(bar + 1);
+    __threadfence();
+    const unsigned arrived = atomicAdd(bar, 1u) + 1u;
+    if (arrived == gridDim.x) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u32(bar + 1) == gen) {
+        if (*reinterpret_cast<volatile int*>(status) != kDevOk ||
+            globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicCAS(status, kDevOk, kDevTimeout);
+          ok = 0;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// Block-wide exclusive scan of one unsigned per thread (blockDim.x <= 1024).
+__device__ unsigned block_exclusive_scan(unsigned v, unsigned* warp_sums, unsigned* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  unsigned inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(kFull, inc, o);
+    if (lane >= o) inc += y;
+  }
+  __syncthreads();
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned s = lane < nwarps ? warp_sums[lane] : 0u;
+    unsigned si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(kFull, si, o);
+      if (lane >= o) si += y;
+    }
+    if (lane < nwarps) warp_sums[lane] = si - s;
+    if (lane == 31) *total = si;
+  }
+  __syncthreads();
+  return inc - v + warp_sums[warp];
+}
+
+template <int DT, bool LARGEST, int VEC>
+__global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a) {
+  using T = typename Dt<DT>::storage;
+  constexpr int kVKB = Dt<DT>::kKeyBits;
+  __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
+  __shared__ unsigned shist[kFilterBlock / 32][256];
+  __shared__ unsigned scan_tmp[32];
+  __shared__ unsigned s_total;
+  __shared__ unsigned long long s_bucket_info[2];
+  __shared__ int s_tile_found;
+  __shared__ unsigned long long s_found_pos;
+
+  const FilterParams& fp = a.fp;
+  const FallbackScratch& fs = a.fs;
+  WarpStage st{stage[threadIdx.x >> 5], 0u};
+  const int warp = threadIdx.x >> 5;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+
+  for (int64_t row = 0; row < fp.nsel; ++row) {
+    const unsigned long long R = __ldcg(fp.counts + row);
+    const bool miss = a.force || R < static_cast<unsigned long long>(a.k) ||
+                      R > static_cast<unsigned long long>(fp.cap);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      fs.r_seen[row] = R;
+      if (miss) atomicAdd(fs.misses, 1ull);
+    }
+    if (!miss) continue;
+    const T* xr = static_cast<const T*>(fp.x) + row * fp.len;
+
+    // -- zero the per-digit histograms
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) fs.ghist[i] = 0u;
+    if (!grid_barrier(fs.barrier, fs.status)) return;
+
+    // -- phase A: radix select of the k-th largest value key
+    uint32_t vprefix = 0, vmask = 0;
+    unsigned long long rank = static_cast<unsigned long long>(a.k);
+    int pass = 0;
+    for (int shift = kVKB - 8; shift >= 0; shift -= 8, ++pass) {
+      for (int i = threadIdx.x; i < (kFilterBlock / 32) * 256; i += blockDim.x) (&shist[0][0])[i] = 0u;
+      __syncthreads();
+      for (int64_t i = gtid; i < fp.len; i += nthreads) {
+        const uint32_t vk = Dt<DT>::key(static_cast<uint32_t>(xr[i])) ^ fp.flip;
+        if ((vk & vmask) == vprefix) atomicAdd(&shist[warp][(vk >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      for (int d = threadIdx.x; d < 256; d += blockDim.x) {
+        unsigned s = 0;
+        for (int wv = 0; wv < kFilterBlock / 32; ++wv) s += shist[wv][d];
+        if (s) atomicAdd(&fs.ghist[pass * 256 + d], s);
+      }
+      if (!grid_barrier(fs.barrier, fs.status)) return;
+      // every block finds the digit holding the rank-th largest (same answer
+      // everywhere); thread j looks at digit 255 - j (kFilterBlock == 256)
+      {
+        const int d = 255 - static_cast<int>(threadIdx.x);
+        const unsigned c = ld_acquire_u32(&fs.ghist[pass * 256 + d]);
+        unsigned v = c;
+        const int lane = threadIdx.x & 31, wv = threadIdx.x >> 5;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_up_sync(kFull, v, o);
+          if (lane >= o) v += y;
+        }
+        if (lane == 31) scan_tmp[wv] = v;
+        __syncthreads();
+        unsigned before = 0;
+        for (int q = 0; q < wv; ++q) before += scan_tmp[q];
+        const unsigned long long incl = static_cast<unsigned long long>(before) + v;
+        const unsigned long long excl = incl - c;
+        if (excl < rank && rank <= incl) {
+          s_bucket_info[0] = static_cast<unsigned long long>(d);
+          s_bucket_info[1] = excl;
+        }
+      }
+      __syncthreads();
+      vprefix |= static_cast<uint32_t>(s_bucket_info[0]) << shift;
+      vmask |= 255u << shift;
+      rank -= s_bucket_info[1];
+      __syncthreads();
+    }
+    // vprefix is the k-th largest value key; `rank` is its place (1-based)
+    // among the elements holding that value, in index order.
+
+    // -- phase B: count the tied value per tile
+    const int64_t ntile = (fp.len + kFallbackTile - 1) / kFallbackTile;
+    for (int64_t tile = blockIdx.x; tile < ntile; tile += gridDim.x) {
+      unsigned c = 0;
+      const int64_t end = (tile + 1) * kFallbackTile < fp.len ? (tile + 1) * kFallbackTile : fp.len;
+      for (int64_t i = tile * kFallbackTile + threadIdx.x; i < end; i += blockDim.x)
+        c += ((Dt<DT>::key(static_cast<uint32_t>(xr[i])) ^ fp.flip) == vprefix) ? 1u : 0u;
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+      if ((threadIdx.x & 31) == 0) scan_tmp[warp] = c;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        unsigned s = 0;
+        for (int q = 0; q < kFilterBlock / 32; ++q) s += scan_tmp[q];
+        fs.tile_counts[tile] = s;
+      }
+      __syncthreads();
+    }
+    if (!grid_barrier(fs.barrier, fs.status)) return;
+
+    if (blockIdx.x == 0) {
+      // lower bound over the running count of the tied value: the first tile
+      // whose inclusive count reaches `rank`.
+      const int64_t per = (ntile + blockDim.x - 1) / blockDim.x;
+      const int64_t lo = threadIdx.x * per, hi = lo + per < ntile ? lo + per : ntile;
+      unsigned mine = 0;
+      for (int64_t j = lo; j < hi; ++j) mine += ld_acquire_u32(&fs.tile_counts[j]);
+      const unsigned before = block_exclusive_scan(mine, scan_tmp, &s_total);
+      if (threadIdx.x == 0) s_tile_found = -1;
+      __syncthreads();
+      if (before < rank && rank <= static_cast<unsigned long long>(before) + mine) {
+        unsigned run = before;
+        for (int64_t j = lo; j < hi; ++j) {
+          const unsigned c = ld_acquire_u32(&fs.tile_counts[j]);
+          if (rank <= static_cast<unsigned long long>(run) + c) {
+            s_found_pos = static_cast<unsigned long long>(j);
+            s_bucket_info[1] = run;  // tied elements before this tile
+            s_tile_found = 1;
+            break;
+          }
+          run += c;
+        }
+      }
+      __syncthreads();
+      if (s_tile_found != 1) {
+        if (threadIdx.x == 0) atomicCAS(fs.status, kDevOk, kDevBadState);
+      } else {
+        // ordered scan inside the tile: the (rank - before)-th tied element
+        const int64_t tile = static_cast<int64_t>(s_found_pos);
+        unsigned long long need = rank - s_bucket_info[1];
+        const int64_t end = (tile + 1) * kFallbackTile < fp.len ? (tile + 1) * kFallbackTile : fp.len;
+        for (int64_t start = tile * kFallbackTile; start < end; start += blockDim.x) {
+          const int64_t i = start + threadIdx.x;
+          const unsigned f = (i < end && ((Dt<DT>::key(static_cast<uint32_t>(xr[i])) ^ fp.flip) == vprefix))
+                                 ? 1u : 0u;
+          const unsigned ex = block_exclusive_scan(f, scan_tmp, &s_total);
+          if (f && ex + 1 == need) s_found_pos = static_cast<unsigned long long>(i);
+          __syncthreads();
+          if (s_total >= need) break;   // block-uniform
+          need -= s_total;
+          __syncthreads();
+        }
+        if (threadIdx.x == 0) {
+          fs.tau_exact[row] = compose(vprefix, s_found_pos, fp.ib);
+          fp.counts[row] = 0ull;
+        }
+      }
+    }
+    if (!grid_barrier(fs.barrier, fs.status)) return;
+    if (*reinterpret_cast<volatile int*>(fs.status) != kDevOk) return;
+
+    // -- phase C: filter the selection again with the exact threshold
+    constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
+    const int64_t tiles_per_row = (fp.len + kTile - 1) / kTile;
+    filter_tiles<DT, LARGEST, VEC>(fp, row * tiles_per_row + blockIdx.x, (row + 1) * tiles_per_row,
+                                   gridDim.x, st);
+  }
+}
+
+template <int DT, bool LARGEST, int VEC>
+int filter_grid_size() {
+  static int cached = 0;
+  if (cached) return cached;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, filter_kernel<DT, LARGEST, VEC>, kFilterBlock, 0);
+  if (per_sm < 1) per_sm = 1;
+  cached = sms * per_sm;
+  return cached;
+}
+
+template <int DT, bool LARGEST, int VEC>
+cudaError_t launch_filter_t(const FilterParams& fp, cudaStream_t st) {
+  constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
+  const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
+  int64_t grid = filter_grid_size<DT, LARGEST, VEC>();
+  if (grid > ntiles) grid = ntiles;
+  if (grid < 1) grid = 1;
+  filter_kernel<DT, LARGEST, VEC><<<static_cast<unsigned>(grid), kFilterBlock, 0, st>>>(fp);
+  return cudaGetLastError();
+}
+
+template <int DT, bool LARGEST, int VEC>
+cudaError_t launch_fallback_t(const FallbackParams& a, cudaStream_t st) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, fallback_kernel<DT, LARGEST, VEC>, kFilterBlock, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const unsigned grid = static_cast<unsigned>(sms * per_sm);
+  FallbackParams args = a;
+  void* kargs[] = {&args};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(fallback_kernel<DT, LARGEST, VEC>), grid,
+                                     kFilterBlock, kargs, 0, st);
+}
+
+}  // namespace
+
+cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
+                          unsigned long long* counts, cudaStream_t st) {
+  FilterParams fp{p.x, p.nsel, p.len, p.ib, p.flip, tau, cap, buf, counts};
+  const bool largest = p.flip == 0;
+  if (p.dtype == kF32) {
+    if (p.vec_ok) return largest ? launch_filter_t<kF32, true, 4>(fp, st) : launch_filter_t<kF32, false, 4>(fp, st);
+    return largest ? launch_filter_t<kF32, true, 1>(fp, st) : launch_filter_t<kF32, false, 1>(fp, st);
+  }
+  if (p.vec_ok) return largest ? launch_filter_t<kBF16, true, 8>(fp, st) : launch_filter_t<kBF16, false, 8>(fp, st);
+  return largest ? launch_filter_t<kBF16, true, 1>(fp, st) : launch_filter_t<kBF16, false, 1>(fp, st);
+}
+
+cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,
+                            unsigned long long* counts, const FallbackScratch& fs, int force,
+                            cudaStream_t st) {
+  // the re-filter reads the exact threshold the fallback itself writes
+  FallbackParams a{{p.x, p.nsel, p.len, p.ib, p.flip, fs.tau_exact, cap, buf, counts}, k, force, fs};
+  const bool largest = p.flip == 0;
+  if (p.dtype == kF32) {
+    if (p.vec_ok) return largest ? launch_fallback_t<kF32, true, 4>(a, st) : launch_fallback_t<kF32, false, 4>(a, st);
+    return largest ? launch_fallback_t<kF32, true, 1>(a, st) : launch_fallback_t<kF32, false, 1>(a, st);
+  }
+  if (p.vec_ok) return largest ? launch_fallback_t<kBF16, true, 8>(a, st) : launch_fallback_t<kBF16, false, 8>(a, st);
+  return largest ? launch_fallback_t<kBF16, true, 1>(a, st) : launch_fallback_t<kBF16, false, 1>(a, st);
+}
+
+}  // namespace tk

@@ -1,0 +1,63 @@
+// Stage 1 of Prof-K (section 3, "Sampling"): S uniform positions per selection,
+// drawn with Philox4x32-10, and the composite keys of the drawn elements.
+//
+// The draws are independent (with replacement); the parameter rule accounts
+// for that exactly (see params.cpp).  Each thread makes one Philox call and
+// turns its four 32-bit words into two 64-bit uniforms, i.e. two positions.
+// The gathers are random 2- or 4-byte reads -- latency bound, so the grid is
+// spread over every SM and each thread has both loads in flight at once.
+#include "common.cuh"
+#include "engine.h"
+
+namespace tk {
+
+template <int DT>
+__global__ void __launch_bounds__(256) sample_kernel(const void* __restrict__ x, int64_t len, int64_t S,
+                                                     int ib, uint32_t flip, uint2 key, uint2 ctr_hi,
+                                                     uint64_t* __restrict__ keys,
+                                                     unsigned long long* __restrict__ counts,
+                                                     DevHeader* __restrict__ hdr) {
+  using T = typename Dt<DT>::storage;
+  const uint32_t row = blockIdx.y;
+  const int64_t pair = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (pair == 0) {
+    if (counts) counts[row] = 0ull;  // survivor counter of the filter that follows
+    if (hdr && row == 0) {
+      hdr->barrier[0] = 0u;  // arrival count of the fallback's grid barrier
+      hdr->status = kDevOk;
+      hdr->misses = 0ull;
+    }
+  }
+  if (2 * pair >= S) return;
+  const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(pair), row, ctr_hi.x, ctr_hi.y), key);
+  const uint64_t u0 = (static_cast<uint64_t>(w.y) << 32) | w.x;
+  const uint64_t u1 = (static_cast<uint64_t>(w.w) << 32) | w.z;
+  const uint64_t p0 = __umul64hi(u0, static_cast<uint64_t>(len));
+  const uint64_t p1 = __umul64hi(u1, static_cast<uint64_t>(len));
+  const T* xr = static_cast<const T*>(x) + static_cast<int64_t>(row) * len;
+  const bool two = 2 * pair + 1 < S;
+  const uint32_t v0 = __ldg(xr + p0);
+  const uint32_t v1 = two ? static_cast<uint32_t>(__ldg(xr + p1)) : 0u;
+  uint64_t* out = keys + static_cast<int64_t>(row) * S + 2 * pair;
+  out[0] = compose(Dt<DT>::key(v0) ^ flip, p0, ib);
+  if (two) out[1] = compose(Dt<DT>::key(v1) ^ flip, p1, ib);
+}
+
+cudaError_t launch_sample(const Problem& p, int64_t S, uint64_t seed, uint64_t counter,
+                          uint64_t* keys, unsigned long long* counts_to_zero, DevHeader* hdr,
+                          cudaStream_t st) {
+  const int64_t pairs = (S + 1) / 2;
+  const dim3 block(256);
+  const dim3 grid(static_cast<unsigned>((pairs + 255) / 256), static_cast<unsigned>(p.nsel));
+  const uint2 key = make_uint2(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  const uint2 ctr = make_uint2(static_cast<uint32_t>(counter), static_cast<uint32_t>(counter >> 32));
+  if (p.dtype == kF32)
+    sample_kernel<kF32><<<grid, block, 0, st>>>(p.x, p.len, S, p.ib, p.flip, key, ctr, keys,
+                                                counts_to_zero, hdr);
+  else
+    sample_kernel<kBF16><<<grid, block, 0, st>>>(p.x, p.len, S, p.ib, p.flip, key, ctr, keys,
+                                                 counts_to_zero, hdr);
+  return cudaGetLastError();
+}
+
+}  // namespace tk

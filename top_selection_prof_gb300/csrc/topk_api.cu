@@ -1,0 +1,421 @@
+// C ABI of the engine (declared in include/topk.h): argument checks, the
+// choice of path, the per-(device, stream) workspace and the launch sequence.
+//
+// Prof-K path (section 3 of "Prof-K: Probabilistic One-Pass Filtering for
+// Efficient Top-k Selection"), all on the caller's stream, no host sync:
+//   sample_kernel    S Philox draws per selection -> composite keys
+//   select_kernel    t-th largest sampled key -> tau             (stage 2)
+//   filter_kernel    one pass over x, keys >= tau -> buffer, R    (stage 3)
+//   fallback_kernel  exits at once unless R < k or R > M; then exact (stage 4)
+//   select_kernel    exact top-k of the buffer, sorted -> outputs (stage 4)
+// The miss decision is made on the device by the fallback kernel itself.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/topk.h"
+#include "common.cuh"
+#include "engine.h"
+
+namespace tk {
+namespace {
+
+constexpr uint64_t kDefaultSeed = 0x243F6A8885A308D3ull;
+constexpr int64_t kDirectMaxLen = int64_t(1) << 22;  // larger single rows use the grid-wide exact path
+std::atomic<uint64_t> g_counter{0};
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+// Returns a device block of at least `bytes` for this (device, stream); grows
+// with stream-ordered allocation (the old block is released in stream order).
+cudaError_t workspace(cudaStream_t st, size_t bytes, void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  Workspace& w = g_ws[std::make_pair(dev, st)];
+  if (w.bytes < bytes) {
+    size_t grow = bytes + bytes / 4;
+    grow = (grow + 0xFFFFF) & ~size_t(0xFFFFF);
+    void* p = nullptr;
+    e = cudaMallocAsync(&p, grow, st);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(p, 0, grow, st);
+    if (e != cudaSuccess) return e;
+    if (w.ptr) cudaFreeAsync(w.ptr, st);
+    w.ptr = p;
+    w.bytes = grow;
+  }
+  *out = w.ptr;
+  return cudaSuccess;
+}
+
+size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
+
+int index_bits(int64_t len) {
+  int b = 1;
+  while (b < 63 && (int64_t(1) << b) < len) ++b;
+  return b;
+}
+
+struct Plan {
+  int path;
+  int64_t S, t, M;
+};
+
+ParamRule rule_of(const topk_options_t* o) {
+  ParamRule pr;
+  if (o) {
+    pr.s_min = o->s_min;
+    pr.s_max = o->s_max;
+    pr.cost_ratio = o->cost_ratio;
+    pr.rule = o->rule;
+  }
+  return pr;
+}
+
+// Path choice for one selection of k out of len (nsel selections).
+int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
+              const topk_options_t* o, Plan* plan) {
+  plan->S = plan->t = plan->M = 0;
+  const int forced = o ? o->path : TOPK_PATH_AUTO;
+  bool profk_ok = false;
+  if (eps > 0.0) {
+    const ParamRule pr = rule_of(o);
+    if (pr.s_min < 1 || pr.s_max < pr.s_min || !(pr.cost_ratio > 0.0) || (pr.rule != 0 && pr.rule != 1))
+      return TOPK_EINVAL;
+    int64_t S = 0, t = 0, M = 0;
+    if (choose_params(len, k, eps, pr, &S, &t, &M)) {
+      if (o && o->t_override > 0) t = o->t_override;
+      if (o && o->m_override > 0) M = o->m_override;
+      plan->S = S;
+      plan->t = t;
+      plan->M = M;
+      profk_ok = t >= 1 && t <= S && 2 * S < len && 2 * M <= len && M >= k && nsel <= 65535;
+    }
+  }
+  switch (forced) {
+    case TOPK_PATH_AUTO:
+      if (profk_ok) plan->path = TOPK_PATH_PROFK;
+      else if (len <= kDirectMaxLen || many_rows) plan->path = TOPK_PATH_DIRECT;
+      else plan->path = TOPK_PATH_EXACT;
+      break;
+    case TOPK_PATH_PROFK:
+      if (eps <= 0.0 || plan->t < 1 || plan->t > plan->S || plan->M < k || plan->S >= len ||
+          nsel > 65535)
+        return TOPK_EUNSUPPORTED;
+      plan->path = TOPK_PATH_PROFK;
+      break;
+    case TOPK_PATH_DIRECT:
+    case TOPK_PATH_EXACT:
+      plan->path = forced;
+      break;
+    default:
+      return TOPK_EINVAL;
+  }
+  if (plan->path != TOPK_PATH_PROFK) plan->S = plan->t = plan->M = 0;
+  return TOPK_OK;
+}
+
+int sm_count_host() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return sms;
+}
+
+int check_common(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, double eps,
+                 const void* out_vals, const void* out_idx, bool global) {
+  if (dtype != TOPK_F32 && dtype != TOPK_BF16) return TOPK_EINVAL;
+  if (rows < 0 || n < 1 || k < 1) return TOPK_EINVAL;
+  if (!(eps >= 0.0 && eps < 1.0)) return TOPK_EINVAL;
+  if (rows == 0) return TOPK_OK;
+  if (!x || !out_vals || !out_idx) return TOPK_EINVAL;
+  if (!global) {
+    if (k > n) return TOPK_EINVAL;
+    if (n >= (int64_t(1) << 31)) return TOPK_EUNSUPPORTED;
+  } else {
+    if (rows > INT64_MAX / n) return TOPK_EUNSUPPORTED;
+    const int64_t len = rows * n;
+    if (k > len) return TOPK_EINVAL;
+    const int64_t lim = dtype == TOPK_F32 ? (int64_t(1) << 32) : (int64_t(1) << 48);
+    if (len > lim) return TOPK_EUNSUPPORTED;
+  }
+  if (k > select_max_k()) return TOPK_EUNSUPPORTED;
+  return TOPK_OK;
+}
+
+Problem make_problem(const void* x, int dtype, int64_t rows, int64_t n, int largest, bool global) {
+  Problem p;
+  p.x = x;
+  p.dtype = dtype;
+  p.nsel = global ? 1 : rows;
+  p.len = global ? rows * n : n;
+  p.ib = index_bits(p.len);
+  p.flip = largest ? 0u : (dtype == TOPK_F32 ? 0xffffffffu : 0xffffu);
+  const int vec = dtype == TOPK_F32 ? 4 : 8;
+  p.vec_ok = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (p.len % vec == 0);
+  return p;
+}
+
+int status_of(cudaError_t e) {
+  if (e == cudaSuccess) return TOPK_OK;
+  if (e == cudaErrorMemoryAllocation) return TOPK_ENOMEM;
+  return TOPK_ECUDA;
+}
+
+#define TK_TRY(expr)                         \
+  do {                                       \
+    const cudaError_t _e = (expr);           \
+    if (_e != cudaSuccess) return status_of(_e); \
+  } while (0)
+
+int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest, double eps,
+        void* out_vals, int64_t* out_idx, cudaStream_t st, bool global, const topk_options_t* o,
+        topk_stats_t* stats) {
+  int rc = check_common(x, dtype, rows, n, k, eps, out_vals, out_idx, global);
+  if (rc != TOPK_OK) return rc;
+  if (stats) std::memset(stats, 0, sizeof(*stats));
+  if (rows == 0) return TOPK_OK;
+  const Problem p = make_problem(x, dtype, rows, n, largest, global);
+  const bool many = p.nsel >= sm_count_host();
+  Plan plan;
+  rc = make_plan(p.len, k, eps, p.nsel, many, o, &plan);
+  if (rc != TOPK_OK) return rc;
+  if (stats) {
+    stats->path = plan.path;
+    stats->index_bits = p.ib;
+    stats->S = plan.S;
+    stats->t = plan.t;
+    stats->M = plan.M;
+  }
+
+  int cluster = 0;
+  if (plan.path == TOPK_PATH_DIRECT) {
+    // one small header for the status word only
+    void* ws = nullptr;
+    TK_TRY(workspace(st, 256, &ws));
+    DevHeader* hdr = static_cast<DevHeader*>(ws);
+    TK_TRY(cudaMemsetAsync(&hdr->status, 0, sizeof(int), st));
+    SelectJob job{};
+    job.keys = nullptr;
+    job.r = k;
+    job.want_topk = true;
+    job.out_vals = out_vals;
+    job.out_idx = out_idx;
+    job.status = &hdr->status;
+    TK_TRY(launch_select(p, job, p.len, &cluster, st));
+    if (stats) {
+      stats->cluster = cluster;
+      stats->R = p.len;
+      int dstat = 0;
+      TK_TRY(cudaMemcpyAsync(&dstat, &hdr->status, sizeof(int), cudaMemcpyDeviceToHost, st));
+      TK_TRY(cudaStreamSynchronize(st));
+      if (dstat != kDevOk) return dstat == kDevTimeout ? TOPK_ETIMEOUT : TOPK_ECUDA;
+    }
+    return TOPK_OK;
+  }
+
+  // workspace layout
+  const int64_t nsel = p.nsel;
+  const int64_t M = plan.path == TOPK_PATH_PROFK ? plan.M : k;
+  const int64_t S = plan.S;
+  const int64_t ntile = (p.len + kFallbackTile - 1) / kFallbackTile;
+  size_t off = 0;
+  const size_t o_hdr = off; off = align_up(off + sizeof(DevHeader));
+  const size_t o_counts = off; off = align_up(off + sizeof(unsigned long long) * nsel);
+  const size_t o_rseen = off; off = align_up(off + sizeof(unsigned long long) * nsel);
+  const size_t o_tau = off; off = align_up(off + sizeof(uint64_t) * nsel);
+  const size_t o_taux = off; off = align_up(off + sizeof(uint64_t) * nsel);
+  const size_t o_ghist = off; off = align_up(off + sizeof(unsigned) * 8 * 256);
+  const size_t o_tiles = off; off = align_up(off + sizeof(unsigned) * ntile);
+  const size_t o_samples = off; off = align_up(off + sizeof(uint64_t) * nsel * S);
+  const size_t o_buf = off; off = align_up(off + sizeof(uint64_t) * nsel * M);
+  void* ws = nullptr;
+  TK_TRY(workspace(st, off, &ws));
+  char* base = static_cast<char*>(ws);
+  DevHeader* hdr = reinterpret_cast<DevHeader*>(base + o_hdr);
+  auto* counts = reinterpret_cast<unsigned long long*>(base + o_counts);
+  auto* r_seen = reinterpret_cast<unsigned long long*>(base + o_rseen);
+  auto* tau = reinterpret_cast<uint64_t*>(base + o_tau);
+  auto* tau_x = reinterpret_cast<uint64_t*>(base + o_taux);
+  auto* ghist = reinterpret_cast<unsigned*>(base + o_ghist);
+  auto* tiles = reinterpret_cast<unsigned*>(base + o_tiles);
+  auto* samples = reinterpret_cast<uint64_t*>(base + o_samples);
+  auto* buf = reinterpret_cast<uint64_t*>(base + o_buf);
+
+  FallbackScratch fs{ghist, tiles, hdr->barrier, &hdr->status, r_seen, &hdr->misses, tau_x};
+  const uint64_t seed = (o && o->seed) ? o->seed : kDefaultSeed;
+  const uint64_t counter = (o && o->counter >= 0) ? static_cast<uint64_t>(o->counter)
+                                                  : g_counter.fetch_add(1);
+  const int force = (o && o->force_miss) ? 1 : 0;
+
+  auto mark = [&](int i) -> cudaError_t {
+    if (!o || !o->events[i]) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(o->events[i]), st);
+  };
+  if (plan.path == TOPK_PATH_PROFK) {
+    TK_TRY(mark(0));
+    TK_TRY(launch_sample(p, S, seed, counter, samples, counts, hdr, st));
+    TK_TRY(mark(1));
+    SelectJob tj{};
+    tj.keys = samples;
+    tj.key_stride = S;
+    tj.counts = nullptr;
+    tj.r = plan.t;
+    tj.want_topk = false;
+    tj.tau_out = tau;
+    tj.status = &hdr->status;
+    TK_TRY(launch_select(p, tj, S, nullptr, st));
+    TK_TRY(mark(2));
+    TK_TRY(launch_filter(p, tau, M, buf, counts, st));
+    TK_TRY(mark(3));
+    TK_TRY(launch_fallback(p, k, M, buf, counts, fs, force, st));
+    TK_TRY(mark(4));
+  } else {  // TOPK_PATH_EXACT
+    TK_TRY(cudaMemsetAsync(base, 0, o_tau, st));  // header, counts, r_seen
+    TK_TRY(launch_fallback(p, k, M, buf, counts, fs, 1, st));
+  }
+  SelectJob rj{};
+  rj.keys = buf;
+  rj.key_stride = M;
+  rj.counts = counts;
+  rj.r = k;
+  rj.want_topk = true;
+  rj.out_vals = out_vals;
+  rj.out_idx = out_idx;
+  rj.status = &hdr->status;
+  TK_TRY(launch_select(p, rj, M, &cluster, st));
+  if (plan.path == TOPK_PATH_PROFK) TK_TRY(mark(5));
+
+  if (stats) {
+    DevHeader h;
+    unsigned long long r0 = 0;
+    uint64_t tau0 = 0;
+    TK_TRY(cudaMemcpyAsync(&h, hdr, sizeof(h), cudaMemcpyDeviceToHost, st));
+    TK_TRY(cudaMemcpyAsync(&r0, r_seen, sizeof(r0), cudaMemcpyDeviceToHost, st));
+    if (plan.path == TOPK_PATH_PROFK)
+      TK_TRY(cudaMemcpyAsync(&tau0, tau, sizeof(tau0), cudaMemcpyDeviceToHost, st));
+    TK_TRY(cudaStreamSynchronize(st));
+    stats->R = static_cast<int64_t>(r0);
+    stats->misses = static_cast<int64_t>(h.misses);
+    stats->tau = tau0;
+    stats->tau_index = plan.path == TOPK_PATH_PROFK ? static_cast<int64_t>(position_of(tau0, p.ib)) : -1;
+    stats->seed = seed;
+    stats->counter = static_cast<int64_t>(counter);
+    stats->cluster = cluster;
+    if (h.status != kDevOk) return h.status == kDevTimeout ? TOPK_ETIMEOUT : TOPK_ECUDA;
+  }
+  return TOPK_OK;
+}
+
+}  // namespace
+}  // namespace tk
+
+using namespace tk;
+
+extern "C" {
+
+void topk_options_init(topk_options_t* opt) {
+  if (!opt) return;
+  std::memset(opt, 0, sizeof(*opt));
+  opt->s_min = 32768;
+  opt->s_max = 131072;
+  opt->cost_ratio = 1.0;
+  opt->rule = TOPK_RULE_EXACT;
+  opt->path = TOPK_PATH_AUTO;
+  opt->seed = kDefaultSeed;
+  opt->counter = -1;
+}
+
+int topk_select(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest, double eps,
+                void* out_vals, int64_t* out_idx, void* stream) {
+  return run(x, dtype, rows, n, k, largest, eps, out_vals, out_idx,
+             static_cast<cudaStream_t>(stream), false, nullptr, nullptr);
+}
+
+int topk_select_global(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,
+                       double eps, void* out_vals, int64_t* out_idx_flat, void* stream) {
+  return run(x, dtype, rows, n, k, largest, eps, out_vals, out_idx_flat,
+             static_cast<cudaStream_t>(stream), true, nullptr, nullptr);
+}
+
+int topk_select_ex(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,
+                   double eps, void* out_vals, int64_t* out_idx, void* stream, int global,
+                   const topk_options_t* opt, topk_stats_t* stats) {
+  return run(x, dtype, rows, n, k, largest, eps, out_vals, out_idx,
+             static_cast<cudaStream_t>(stream), global != 0, opt, stats);
+}
+
+int topk_plan(int64_t n, int64_t k, double eps, const topk_options_t* opt, topk_plan_t* plan) {
+  if (!plan || n < 1 || k < 1 || k > n || !(eps >= 0.0 && eps < 1.0)) return TOPK_EINVAL;
+  Plan pl;
+  const int rc = make_plan(n, k, eps, 1, false, opt, &pl);
+  if (rc != TOPK_OK) return rc;
+  plan->path = pl.path;
+  plan->S = pl.S;
+  plan->t = pl.t;
+  plan->M = pl.M;
+  plan->p_recall_fail = 0.0;
+  plan->p_overflow = 0.0;
+  if (pl.path == TOPK_PATH_PROFK) {
+    const double nd = static_cast<double>(n);
+    plan->p_recall_fail = binom_upper_tail(pl.S, (static_cast<double>(k) - 1.0) / nd, pl.t);
+    plan->p_overflow = binom_lower_tail(pl.S, static_cast<double>(pl.M) / nd, pl.t - 1);
+  }
+  return TOPK_OK;
+}
+
+const char* topk_status_str(int status) {
+  switch (status) {
+    case TOPK_OK: return "ok";
+    case TOPK_EINVAL: return "invalid argument";
+    case TOPK_ENOMEM: return "out of device memory";
+    case TOPK_ECUDA: return "CUDA error";
+    case TOPK_EUNSUPPORTED: return "unsupported size";
+    case TOPK_ETIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int topk_version(void) { return 100; }
+
+int topk_index_bits(int64_t len) { return len < 1 ? 1 : index_bits(len); }
+
+int topk_prof_sample(const void* x, int dtype, int64_t rows, int64_t n, int global, int largest,
+                     int64_t S, uint64_t seed, int64_t counter, uint64_t* out_keys, void* stream) {
+  if (dtype != TOPK_F32 && dtype != TOPK_BF16) return TOPK_EINVAL;
+  if (rows < 0 || n < 1 || S < 1 || counter < 0) return TOPK_EINVAL;
+  if (rows == 0) return TOPK_OK;
+  if (!x || !out_keys) return TOPK_EINVAL;
+  const Problem p = make_problem(x, dtype, rows, n, largest, global != 0);
+  if (p.nsel > 65535) return TOPK_EUNSUPPORTED;
+  const cudaError_t e = launch_sample(p, S, seed, static_cast<uint64_t>(counter), out_keys, nullptr,
+                                      nullptr, static_cast<cudaStream_t>(stream));
+  return status_of(e);
+}
+
+int topk_prof_filter(const void* x, int dtype, int64_t rows, int64_t n, int global, int largest,
+                     const uint64_t* tau, int64_t M, uint64_t* buf, uint64_t* counts, void* stream) {
+  if (dtype != TOPK_F32 && dtype != TOPK_BF16) return TOPK_EINVAL;
+  if (rows < 0 || n < 1 || M < 1) return TOPK_EINVAL;
+  if (rows == 0) return TOPK_OK;
+  if (!x || !tau || !buf || !counts) return TOPK_EINVAL;
+  const Problem p = make_problem(x, dtype, rows, n, largest, global != 0);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(uint64_t) * p.nsel, st);
+  if (e != cudaSuccess) return status_of(e);
+  e = launch_filter(p, tau, M, buf, reinterpret_cast<unsigned long long*>(counts), st);
+  return status_of(e);
+}
+
+}  // extern "C"
