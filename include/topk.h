@@ -202,6 +202,33 @@ int topk_prof_filter(const void* x, int dtype, int64_t rows, int64_t n, int glob
                      const uint64_t* tau, int64_t M, uint64_t* buf, uint64_t* counts,
                      void* stream);
 
+/*
+ * topk_select_noalloc -- the selection of topk_select (global == 0) or
+ * topk_select_global (global != 0) without any device allocation.  The paper
+ * has no counterpart of this entry point.
+ *
+ * For callers that cannot allocate while they run: a process whose device
+ * memory belongs to another allocator (a framework caching allocator holding
+ * nearly all of HBM, where a hidden cudaMalloc can fail or fragment it), or
+ * latency-critical loops that cannot take cudaMalloc's implicit device
+ * synchronisation.  All scratch comes from one static device array of 8 MiB
+ * inside the library, held by every GPU that loads the library until exit.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the array and it keeps the last call's
+ *     contents; the library clears the words that must start at zero.  Calls
+ *     that overlap on the GPU (e.g. unordered streams of one device) race on
+ *     the array: order them on one stream.
+ *   - A request whose scratch would exceed 8 MiB (roughly: sample plus buffer
+ *     plus per-4096-element counters of all selections) returns
+ *     TOPK_EUNSUPPORTED before anything is launched; use topk_select then.
+ * Arguments, outputs, limits and the other error codes are those of
+ * topk_select / topk_select_global.
+ */
+int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,
+                        double eps, void* out_vals, int64_t* out_idx, int global, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,7 +15,8 @@ PATH_NAMES = {TOPK_PATH_DIRECT: "direct", TOPK_PATH_PROFK: "profk", TOPK_PATH_EX
 
 # Every symbol include/topk.h declares.
 EXPORTS = ("topk_options_init", "topk_select", "topk_select_global", "topk_select_ex", "topk_plan",
-           "topk_status_str", "topk_version", "topk_index_bits", "topk_prof_sample", "topk_prof_filter")
+           "topk_status_str", "topk_version", "topk_index_bits", "topk_prof_sample", "topk_prof_filter",
+           "topk_select_noalloc")
 
 
 class TopkOptions(ctypes.Structure):
