@@ -46,6 +46,10 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true", help="skip the BatchTopK side measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--scale-down", type=int, default=0,
+                    help="divide the workload by 2^s (row length, or rows for global mode); for profiling")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -66,11 +70,18 @@ def load_peaks():
     return 6800.0, "fallback (6.8 TB/s)"
 
 
-def workload(name):
+def workload(name, scale_down=0):
     from top_selection_prof_gb300 import workloads
     if name not in workloads.WORKLOADS:
         raise SystemExit("unknown workload %r; choose from %s" % (name, sorted(workloads.WORKLOADS)))
-    return workloads.WORKLOADS[name]
+    cfg = dict(workloads.WORKLOADS[name])
+    if scale_down:
+        if cfg["mode"] == "global" or cfg["rows"] > 1:
+            cfg["rows"] = max(1, cfg["rows"] >> scale_down)
+        else:
+            cfg["n"] = max(cfg["k"] * 4, cfg["n"] >> scale_down)
+        cfg["k"] = min(cfg["k"], cfg["n"] * (cfg["rows"] if cfg["mode"] == "global" else 1))
+    return cfg
 
 
 def make_input(cfg, seed):
@@ -255,11 +266,6 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
                 call()
             torch.cuda.synchronize()
 
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
-    for evs in stage_ev:
-        for e in evs:
-            e.record(stream)
-    handles = [[ctypes.c_void_p(e.cuda_event).value for e in evs] for evs in stage_ev]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -267,14 +273,28 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
         dist.barrier()
     torch.cuda.synchronize()
     start.record(stream)
-    for s in range(steps):
-        call(handles[s] if path == "profk" else None)
+    for _ in range(steps):
+        call()
     end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     ms_total = start.elapsed_time(end)
     clock_info = clocks.stop() if clocks else None
+
+    # Profiled pass: the same K steps again with CUDA events recorded on the
+    # launching stream at every stage boundary (recording events between the
+    # kernels stops them from overlapping their launches, so this pass is kept
+    # out of the throughput number above).
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for evs in stage_ev:
+        for e in evs:
+            e.record(stream)
+    handles = [[ctypes.c_void_p(e.cuda_event).value for e in evs] for evs in stage_ev]
+    torch.cuda.synchronize()
+    for s_ in range(steps):
+        call(handles[s_] if path == "profk" else None)
+    torch.cuda.synchronize()
 
     if world > 1:
         t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
@@ -287,6 +307,7 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
     filt_ms = None
     if path == "profk":
         names = ["sample", "threshold", "filter", "fallback_check", "refine_sort"]
+        # stage boundaries come from the profiled pass
         per = {nm: [] for nm in names}
         for evs in stage_ev:
             for j, nm in enumerate(names):
@@ -346,7 +367,7 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
 def main():
     args = parse_args()
     world, rank, local = dist_env()
-    cfg = workload(args.workload)
+    cfg = workload(args.workload, args.scale_down)
 
     if args.impl == "reference":
         if rank != 0:
@@ -378,11 +399,12 @@ def main():
     tk._lib.get()   # fails loudly if the engine is not built
 
     x = make_input(cfg, args.seed + rank)
-    res = run_ours(cfg, args.workload, x, args.steps, args.warmup, world, rank)
+    res = run_ours(cfg, args.workload, x, args.steps, args.warmup, world, rank,
+                   with_clocks=not args.no_clocks, with_e2e=not args.no_e2e)
 
     secondary = None
     if not args.no_secondary and args.workload != SECONDARY_WORKLOAD:
-        c2 = workload(SECONDARY_WORKLOAD)
+        c2 = workload(SECONDARY_WORKLOAD, args.scale_down)
         del x
         x2 = make_input(c2, args.seed + rank)
         r2 = run_ours(c2, SECONDARY_WORKLOAD, x2, args.steps, args.warmup, world, rank, with_clocks=False,
@@ -410,7 +432,8 @@ def main():
             "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if cfg["kind"].endswith("_bf16") else "f32",
             "data": "synthetic (seeded numpy: %s)" % cfg["kind"],
-            "config": {"workload": args.workload, "rows": cfg["rows"], "n": cfg["n"], "k": cfg["k"],
+            "config": {"workload": args.workload + ("/2^%d" % args.scale_down if args.scale_down else ""),
+                       "rows": cfg["rows"], "n": cfg["n"], "k": cfg["k"],
                        "eps": cfg["eps"], "mode": cfg["mode"], "path": res["path"],
                        "S": st["S"], "t": st["t"], "M": st["M"], "R": st["R"],
                        "l2": "inputs larger than L2 (no flush)",

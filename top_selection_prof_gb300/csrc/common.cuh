@@ -95,9 +95,27 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
   return c;
 }
 
+// Stage-1 draws j = 2*pair and 2*pair + 1 of selection `row`: counter
+// (pair, row, call_lo, call_hi), key (seed_lo, seed_hi); the even draw takes
+// the 64-bit word (w1 << 32 | w0), the odd one (w3 << 32 | w2); the position
+// is floor(word * len / 2^64).
+__device__ __forceinline__ void sample_pair(uint2 key, uint2 call, uint32_t row, uint32_t pair, uint64_t len,
+                                            uint64_t* p0, uint64_t* p1) {
+  const uint4 w = philox4x32_10(make_uint4(pair, row, call.x, call.y), key);
+  *p0 = __umul64hi((static_cast<uint64_t>(w.y) << 32) | w.x, len);
+  *p1 = __umul64hi((static_cast<uint64_t>(w.w) << 32) | w.z, len);
+}
+
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: wait for the preceding grid (and its memory),
+// and let the next grid start launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -20,6 +20,9 @@ struct Problem {
 };
 
 // ---- parameters (params.cpp) -------------------------------------------------
+// Programmatic dependent launch between the pipeline's kernels; off unless
+// TOPK_ENABLE_PDL=1 (measured slower on the single-row pipeline).
+bool pdl_enabled();
 struct ParamRule {
   int64_t s_min = 32768, s_max = 131072;
   double cost_ratio = 1.0;
@@ -79,10 +82,14 @@ struct SelectJob {
   void* out_vals;                      // want_topk
   int64_t* out_idx;
   int* status;                         // device status word (kDevBadState on inconsistency)
+  uint64_t* xbuf = nullptr;            // want_topk across CTAs: 2*r keys per selection (L2 exchange)
 };
 // Returns the cluster size used via *cluster (may be null).
 cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source_bound, int* cluster,
                           cudaStream_t st);
 int64_t select_max_k();
+#ifdef TK_PHASE_TIMING
+int debug_phase_ns(unsigned long long* out);  // debug builds: per-phase timer stamps
+#endif
 
 }  // namespace tk

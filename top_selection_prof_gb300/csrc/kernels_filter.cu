@@ -48,131 +48,213 @@ struct FilterParams {
 
 // Element e of a packed group of raw words (VEC elements).
 template <int DT, int VEC>
-__device__ __forceinline__ uint32_t elem(const uint32_t (&w)[4], int e) {
-  if (DT == kF32) return VEC == 1 ? w[0] : w[e];
-  if (VEC == 1) return w[0] & 0xffffu;
-  return (w[e >> 1] >> ((e & 1) * 16)) & 0xffffu;
+__device__ __forceinline__ uint32_t elem(const uint4& v, int e) {
+  const uint32_t w = (e >> (DT == kF32 ? 0 : 1)) == 0 ? v.x
+                     : (e >> (DT == kF32 ? 0 : 1)) == 1 ? v.y
+                     : (e >> (DT == kF32 ? 0 : 1)) == 2 ? v.z : v.w;
+  if (DT == kF32) return w;
+  return (VEC == 1) ? (w & 0xffffu) : ((w >> ((e & 1) * 16)) & 0xffffu);
 }
 
 template <int DT, int VEC>
-__device__ __forceinline__ void load_group(const typename Dt<DT>::storage* p, uint32_t (&w)[4]) {
-  if (VEC == 1) {
-    w[0] = static_cast<uint32_t>(__ldg(p));
+__device__ __forceinline__ uint4 load_group(const typename Dt<DT>::storage* p) {
+  if (VEC == 1) return make_uint4(static_cast<uint32_t>(__ldg(p)), 0u, 0u, 0u);
+  return ld_stream_v4(p);
+}
+
+// NaN-propagating max / min (PTX max.NaN / min.NaN).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bmin2_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Superset test for a group: does any element rank at or above tau's value?
+// One NaN-propagating max (largest) or min (smallest) over the group and one
+// compare; NaN elements always pass here (the exact test sorts them out).
+template <int DT, bool LARGEST, int VEC>
+__device__ __forceinline__ bool group_candidate(const uint4& v, float tv) {
+  float m;
+  if (DT == kF32) {
+    if (VEC == 1) {
+      m = __uint_as_float(v.x);
+    } else if (LARGEST) {
+      m = fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                   fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+    } else {
+      m = fmin_nan(fmin_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                   fmin_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
   } else {
-    const uint4 v = ld_stream_v4(p);
-    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    if (VEC == 1) {
+      m = __uint_as_float(v.x << 16);
+    } else {
+      const uint32_t c = LARGEST ? bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w))
+                                 : bmin2_nan(bmin2_nan(v.x, v.y), bmin2_nan(v.z, v.w));
+      const float lo = __uint_as_float(c << 16), hi = __uint_as_float(c & 0xffff0000u);
+      m = LARGEST ? fmax_nan(lo, hi) : fmin_nan(lo, hi);
+    }
   }
+  return LARGEST ? !(m < tv) : !(m > tv);
 }
 
-// Float value of tau for the cheap superset test.  NaN (test passes for all)
-// when tau's value is NaN.
-template <int DT>
-__device__ __forceinline__ float tau_value(uint64_t tau, int ib, uint32_t flip) {
-  const uint32_t k = vkey_of(tau, ib) ^ flip;
-  if (k == Dt<DT>::kNanKey) return __uint_as_float(0x7fc00000u);
-  if (k == Dt<DT>::kZeroKey) return 0.0f;
-  return Dt<DT>::to_float(Dt<DT>::bits(k));
-}
-
-struct WarpStage {
-  uint64_t* s;   // this warp's staging slots
-  uint32_t n;    // warp-uniform fill
+// Per-row threshold in the forms the filter tests against.
+struct RowTau {
+  uint64_t key;   // composite key
+  uint64_t pos;   // position of the element it came from
+  float value;    // its value (0 for the zero key)
+  bool nan;       // tau's value is NaN: fall back to composite-key compares
 };
 
-__device__ __forceinline__ void warp_flush(WarpStage& st, int64_t row, int64_t cap, uint64_t* buf,
-                                           unsigned long long* counts) {
-  if (st.n == 0) return;
+template <int DT>
+__device__ __forceinline__ RowTau row_tau(uint64_t tau, int ib, uint32_t flip) {
+  RowTau r;
+  r.key = tau;
+  r.pos = position_of(tau, ib);
+  const uint32_t k = vkey_of(tau, ib) ^ flip;
+  r.nan = (k == Dt<DT>::kNanKey);
+  r.value = (k == Dt<DT>::kZeroKey || r.nan) ? 0.0f : Dt<DT>::to_float(Dt<DT>::bits(k));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t warp_flush(uint64_t* s, uint32_t n, int64_t row, int64_t cap,
+                                               uint64_t* buf, unsigned long long* counts) {
+  if (n == 0) return 0;
   const int lane = threadIdx.x & 31;
   unsigned long long base = 0;
-  if (lane == 0) base = atomicAdd(counts + row, static_cast<unsigned long long>(st.n));
+  if (lane == 0) base = atomicAdd(counts + row, static_cast<unsigned long long>(n));
   base = __shfl_sync(kFull, base, 0);
   __syncwarp();
   uint64_t* dst = buf + row * cap;
-  for (uint32_t j = lane; j < st.n; j += 32) {
+  for (uint32_t j = lane; j < n; j += 32) {
     const unsigned long long pos = base + j;
-    if (pos < static_cast<unsigned long long>(cap)) dst[pos] = st.s[j];
+    if (pos < static_cast<unsigned long long>(cap)) dst[pos] = s[j];
   }
   __syncwarp();
-  st.n = 0;
+  return 0;
 }
 
-// One group of VEC consecutive elements per lane: superset test, then the
-// exact composite-key test and ballot ranking for warps that saw a candidate.
+// Exact test of one group for a warp that saw a candidate (rare, kept out of
+// line so the streaming loop stays small).  In the value domain an element
+// passes when it ranks strictly above tau's value, or ties with it at a
+// position <= tau's (the composite-key order).  Each lane counts its
+// survivors, a warp prefix sum gives every lane its slots in the warp's stage.
+// Returns the stage's new fill.
 template <int DT, bool LARGEST, int VEC>
-__device__ __forceinline__ void filter_group(const uint32_t (&w)[4], int64_t pos, bool ok, float tv,
-                                             uint64_t tau, int ib, uint32_t flip, WarpStage& st,
-                                             int64_t row, const FilterParams& fp) {
-  bool cand = false;
+__device__ __noinline__ uint32_t group_exact(uint4 v, int64_t pos, bool cand, RowTau t, int ib, uint32_t flip,
+                                             uint64_t* s, uint32_t n, int64_t row, int64_t cap, uint64_t* buf,
+                                             unsigned long long* counts) {
+  uint32_t mask = 0;
+  if (cand) {
 #pragma unroll
-  for (int e = 0; e < VEC; ++e) {
-    const float f = Dt<DT>::to_float(elem<DT, VEC>(w, e));
-    cand |= LARGEST ? !(f < tv) : !(f > tv);
-  }
-  cand &= ok;
-  if (!__any_sync(kFull, cand)) return;
-  const unsigned lt = lanemask_lt();
-#pragma unroll
-  for (int e = 0; e < VEC; ++e) {
-    uint64_t ck = 0;
-    bool pass = false;
-    if (cand) {
-      ck = compose(Dt<DT>::key(elem<DT, VEC>(w, e)) ^ flip, static_cast<uint64_t>(pos + e), ib);
-      pass = ck >= tau;
-    }
-    const unsigned m = __ballot_sync(kFull, pass);
-    if (m) {
-      if (st.n + 32 > kWarpStage) warp_flush(st, row, fp.cap, fp.buf, fp.counts);
-      if (pass) st.s[st.n + __popc(m & lt)] = ck;
-      st.n += __popc(m);
+    for (int e = 0; e < VEC; ++e) {
+      const uint32_t raw = elem<DT, VEC>(v, e);
+      const float f = Dt<DT>::to_float(raw);
+      const uint64_t p = static_cast<uint64_t>(pos + e);
+      bool pass;
+      if (t.nan) {
+        pass = compose(Dt<DT>::key(raw) ^ flip, p, ib) >= t.key;
+      } else if (LARGEST) {
+        pass = (f > t.value) || (f != f) || (f == t.value && p <= t.pos);
+      } else {
+        pass = (f < t.value) || (f == t.value && p <= t.pos);
+      }
+      mask |= static_cast<uint32_t>(pass) << e;
     }
   }
+  const int lane = threadIdx.x & 31;
+  const uint32_t cnt = __popc(mask);
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t total = __shfl_sync(kFull, incl, 31);
+  if (total == 0) return n;
+  if (n + total > static_cast<uint32_t>(kWarpStage)) n = warp_flush(s, n, row, cap, buf, counts);
+  uint32_t off = n + incl - cnt;
+  while (mask) {
+    const int e = __ffs(mask) - 1;
+    mask &= mask - 1;
+    s[off++] = compose(Dt<DT>::key(elem<DT, VEC>(v, e)) ^ flip, static_cast<uint64_t>(pos + e), ib);
+  }
+  __syncwarp();
+  return n + total;
 }
 
 // Filter the tiles [tile_begin, tile_end) (stride tile_step) of the flattened
 // tile space (selection-major).  Used by the filter kernel and the fallback.
 template <int DT, bool LARGEST, int VEC>
 __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t tile_end,
-                             int64_t tile_step, WarpStage& st) {
+                             int64_t tile_step, uint64_t* stage) {
   using T = typename Dt<DT>::storage;
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   const int64_t tiles_per_row = (fp.len + kTile - 1) / kTile;
   int64_t cur_row = -1;
-  uint64_t tau = 0;
-  float tv = 0.0f;
+  RowTau t{};
+  uint32_t n = 0;
   for (int64_t tile = tile_begin; tile < tile_end; tile += tile_step) {
     const int64_t row = tile / tiles_per_row;
     const int64_t base = (tile - row * tiles_per_row) * kTile;
     if (row != cur_row) {
-      if (cur_row >= 0) warp_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
+      if (cur_row >= 0) n = warp_flush(stage, n, cur_row, fp.cap, fp.buf, fp.counts);
       cur_row = row;
-      tau = __ldcg(fp.tau + row);
-      tv = tau_value<DT>(tau, fp.ib, fp.flip);
+      t = row_tau<DT>(__ldcg(fp.tau + row), fp.ib, fp.flip);
     }
     const T* xr = static_cast<const T*>(fp.x) + row * fp.len;
-    uint32_t w[kFilterUnroll][4];
-    bool ok[kFilterUnroll];
-    int64_t pos[kFilterUnroll];
+    uint4 v[kFilterUnroll];
+    if (base + kTile <= fp.len) {
 #pragma unroll
-    for (int u = 0; u < kFilterUnroll; ++u) {
-      pos[u] = base + (static_cast<int64_t>(u) * kFilterBlock + threadIdx.x) * VEC;
-      ok[u] = pos[u] < fp.len;
-      if (ok[u]) load_group<DT, VEC>(xr + pos[u], w[u]);
-      else w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0u;
+      for (int u = 0; u < kFilterUnroll; ++u)
+        v[u] = load_group<DT, VEC>(xr + base + (u * kFilterBlock + threadIdx.x) * VEC);
+#pragma unroll
+      for (int u = 0; u < kFilterUnroll; ++u) {
+        const bool c = group_candidate<DT, LARGEST, VEC>(v[u], t.value) || t.nan;
+        if (__any_sync(kFull, c)) {
+          const int64_t pos = base + (u * kFilterBlock + threadIdx.x) * VEC;
+          n = group_exact<DT, LARGEST, VEC>(v[u], pos, c, t, fp.ib, fp.flip, stage, n, row, fp.cap, fp.buf,
+                                            fp.counts);
+        }
+      }
+    } else {  // the last, partial tile of a selection
+#pragma unroll
+      for (int u = 0; u < kFilterUnroll; ++u) {
+        const int64_t pos = base + (u * kFilterBlock + threadIdx.x) * VEC;
+        const bool ok = pos < fp.len;
+        v[u] = ok ? load_group<DT, VEC>(xr + pos) : make_uint4(0u, 0u, 0u, 0u);
+        const bool c = ok && (group_candidate<DT, LARGEST, VEC>(v[u], t.value) || t.nan);
+        if (__any_sync(kFull, c))
+          n = group_exact<DT, LARGEST, VEC>(v[u], pos, c, t, fp.ib, fp.flip, stage, n, row, fp.cap, fp.buf,
+                                            fp.counts);
+      }
     }
-#pragma unroll
-    for (int u = 0; u < kFilterUnroll; ++u)
-      filter_group<DT, LARGEST, VEC>(w[u], pos[u], ok[u], tv, tau, fp.ib, fp.flip, st, row, fp);
   }
-  if (cur_row >= 0) warp_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
+  if (cur_row >= 0) warp_flush(stage, n, cur_row, fp.cap, fp.buf, fp.counts);
 }
 
 template <int DT, bool LARGEST, int VEC>
 __global__ void __launch_bounds__(kFilterBlock) filter_kernel(FilterParams fp) {
   __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
-  WarpStage st{stage[threadIdx.x >> 5], 0u};
+  grid_dependency_wait();  // tau and the zeroed counters come from the previous grid
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
-  filter_tiles<DT, LARGEST, VEC>(fp, blockIdx.x, ntiles, gridDim.x, st);
+  filter_tiles<DT, LARGEST, VEC>(fp, blockIdx.x, ntiles, gridDim.x, stage[threadIdx.x >> 5]);
 }
 
 // ---------------------------------------------------------------------------
@@ -261,7 +343,7 @@ __global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a
 
   const FilterParams& fp = a.fp;
   const FallbackScratch& fs = a.fs;
-  WarpStage st{stage[threadIdx.x >> 5], 0u};
+  grid_launch_dependents();  // the final selection may start launching
   const int warp = threadIdx.x >> 5;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -406,7 +488,7 @@ __global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a
     constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
     const int64_t tiles_per_row = (fp.len + kTile - 1) / kTile;
     filter_tiles<DT, LARGEST, VEC>(fp, row * tiles_per_row + blockIdx.x, (row + 1) * tiles_per_row,
-                                   gridDim.x, st);
+                                   gridDim.x, stage[threadIdx.x >> 5]);
   }
 }
 
@@ -430,20 +512,32 @@ cudaError_t launch_filter_t(const FilterParams& fp, cudaStream_t st) {
   int64_t grid = filter_grid_size<DT, LARGEST, VEC>();
   if (grid > ntiles) grid = ntiles;
   if (grid < 1) grid = 1;
-  filter_kernel<DT, LARGEST, VEC><<<static_cast<unsigned>(grid), kFilterBlock, 0, st>>>(fp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kFilterBlock, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, filter_kernel<DT, LARGEST, VEC>, fp);
 }
 
 template <int DT, bool LARGEST, int VEC>
 cudaError_t launch_fallback_t(const FallbackParams& a, cudaStream_t st) {
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, fallback_kernel<DT, LARGEST, VEC>, kFilterBlock, 0);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const unsigned grid = static_cast<unsigned>(sms * per_sm);
+  static unsigned grid = 0;  // co-resident blocks: one full wave of the device
+  if (!grid) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, fallback_kernel<DT, LARGEST, VEC>, kFilterBlock, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (per_sm > 2) per_sm = 2;  // enough for the rare full passes, cheap when nothing missed
+    grid = static_cast<unsigned>(sms * per_sm);
+  }
   FallbackParams args = a;
   void* kargs[] = {&args};
   return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(fallback_kernel<DT, LARGEST, VEC>), grid,

@@ -29,11 +29,8 @@ __global__ void __launch_bounds__(256) sample_kernel(const void* __restrict__ x,
     }
   }
   if (2 * pair >= S) return;
-  const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(pair), row, ctr_hi.x, ctr_hi.y), key);
-  const uint64_t u0 = (static_cast<uint64_t>(w.y) << 32) | w.x;
-  const uint64_t u1 = (static_cast<uint64_t>(w.w) << 32) | w.z;
-  const uint64_t p0 = __umul64hi(u0, static_cast<uint64_t>(len));
-  const uint64_t p1 = __umul64hi(u1, static_cast<uint64_t>(len));
+  uint64_t p0, p1;
+  sample_pair(key, ctr_hi, row, static_cast<uint32_t>(pair), static_cast<uint64_t>(len), &p0, &p1);
   const T* xr = static_cast<const T*>(x) + static_cast<int64_t>(row) * len;
   const bool two = 2 * pair + 1 < S;
   const uint32_t v0 = __ldg(xr + p0);

@@ -9,19 +9,26 @@
 // Select: radix select from the most significant 8-bit digit of the composite
 // key ("count elements into buckets and recurse into the bucket that contains
 // the boundary", Find the Cutoff Instead).  Each CTA histograms its slice of
-// the source into per-warp shared-memory counters; the cluster's CTAs read one
-// another's histograms through distributed shared memory, so every CTA finds
-// the same boundary digit without touching global memory.  Once a CTA's
-// elements at or above the current prefix fit in shared memory it caches them
-// and stops re-reading the source.
+// the source into per-warp shared-memory counters (warp-aggregated with
+// __match_any_sync, so equal digits never serialise on one address); the
+// cluster's CTAs read one another's histograms through distributed shared
+// memory, so every CTA finds the same boundary digit without global memory.
+// Slices are read with 16-byte loads, eight keys per thread in flight.  Once a
+// CTA's elements at or above the current prefix fit in shared memory it caches
+// them and stops re-reading the source.  When the boundary bucket holds at
+// most kGather keys, they are gathered into CTA 0 and ranked by counting
+// ("Rank by Counting": rank = number of larger keys, ties by position), which
+// ends the select without further digit passes.
 //
 // Sort (top-k only): the k winners (keys >= the k-th key; keys are distinct)
-// are first spread evenly over the cluster, then sorted by a stable LSD radix
-// sort, descending, one 8-bit digit per pass, skipping digits on which all
-// winners agree.  Each pass ranks a CTA's items stably with __match_any_sync
-// per warp, exchanges per-digit counts over DSMEM, and scatters every key
-// straight into its destination CTA's shared memory.  The result is the order
-// (value descending, index ascending), since the composite key encodes it.
+// are sorted by a stable LSD radix sort, descending, one 8-bit digit per pass,
+// skipping digits on which all winners agree.  If the winners fit in one CTA
+// they are gathered into CTA 0 and sorted there with block barriers only;
+// otherwise they are spread evenly over the cluster and every pass ranks a
+// CTA's items stably per warp, exchanges per-digit counts over DSMEM and
+// scatters each key straight into its destination CTA's shared memory.  The
+// composite key encodes (value descending, index ascending), so that is the
+// output order.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -34,6 +41,20 @@ namespace tk {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned kGather = 256;  // bucket size at which the select finishes by ranking
+
+#ifdef TK_PHASE_TIMING
+// Debug builds only: globaltimer stamps of the first cluster's CTA 0.
+__device__ unsigned long long g_phase_ns[2][32];
+#define TK_STAMP(i)                                                                         \
+  do {                                                                                      \
+    if (blockIdx.x == 0 && threadIdx.x == 0) g_phase_ns[a.want_topk][(i)] = globaltimer_ns(); \
+  } while (0)
+#else
+#define TK_STAMP(i) \
+  do {              \
+  } while (0)
+#endif
 
 struct SelParams {
   const uint64_t* keys;               // key source (SRC == 0)
@@ -44,38 +65,154 @@ struct SelParams {
   int ib;
   uint32_t flip;
   int key_bits;                       // value-key bits (32 or 16)
+  int key_vec;                        // key rows allow 16-byte loads
+  int src_vec;                        // x rows allow 16-byte loads
   int64_t r;                          // rank sought (1-based)
   int want_topk;
   uint64_t* tau_out;
   void* out_vals;
   int64_t* out_idx;
   int* status;
+  uint64_t* xbuf;                     // 2*r keys per selection: the L2 exchange of the sort
 };
 
 template <int BLOCK, int P, int CB>
 struct Layout {
   static constexpr int kWarps = BLOCK / 32;
   static constexpr int kItems = (P + BLOCK - 1) / BLOCK;
+  static constexpr int kQuarters = BLOCK / 256;          // thread groups of 256 (one per digit)
+  static constexpr int kWarpsPerQuarter = kWarps / kQuarters;
   static constexpr size_t kBufA = 0;
   static constexpr size_t kBufB = kBufA + sizeof(uint64_t) * P;
   static constexpr size_t kWhist = kBufB + sizeof(uint64_t) * CB;
   static constexpr size_t kHist = kWhist + sizeof(unsigned) * kWarps * 256;
   static constexpr size_t kGbase = kHist + sizeof(unsigned) * 256;
-  static constexpr size_t kXch = kGbase + sizeof(unsigned) * 256;
+  static constexpr size_t kPart = kGbase + sizeof(unsigned) * 256;
+  static constexpr size_t kXch = kPart + sizeof(unsigned) * kQuarters * 256;
   static constexpr size_t kBytes = kXch + sizeof(unsigned long long) * 4;
   static_assert(CB >= P, "cache buffer doubles as the second sort buffer");
-  static_assert(BLOCK >= 256, "one thread per digit");
+  static_assert(BLOCK % 256 == 0, "one thread per digit in each group of 256");
+  static_assert(kWarps * 256 * sizeof(unsigned) >= kGather * sizeof(uint64_t), "gather buffer");
 };
 
+// Eight consecutive source elements i0 .. i0+7 (i0 a multiple of 8) as
+// composite keys.  Only elements in [lo, hi) are meaningful; vector loads may
+// also read neighbours that lie inside the same row.
 template <int SRC>
-__device__ __forceinline__ uint64_t source_key(const SelParams& a, int64_t row, int64_t i) {
-  if (SRC == 0) return __ldcg(a.keys + row * a.key_stride + i);
-  if (SRC == 1) {
-    const uint32_t u = __ldg(static_cast<const uint32_t*>(a.x) + row * a.len + i);
-    return compose(order_key_f32(u) ^ a.flip, static_cast<uint64_t>(i), a.ib);
+__device__ __forceinline__ void load8(const SelParams& a, int64_t row, int64_t i0, int64_t lo, int64_t hi,
+                                      uint64_t (&k)[8]) {
+  if (SRC == 0) {
+    const uint64_t* base = a.keys + row * a.key_stride;
+    if (a.key_vec && i0 + 8 <= a.key_stride) {
+      const uint4* p = reinterpret_cast<const uint4*>(base + i0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = __ldcg(p + q);
+        k[2 * q] = (static_cast<uint64_t>(v.y) << 32) | v.x;
+        k[2 * q + 1] = (static_cast<uint64_t>(v.w) << 32) | v.z;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) k[j] = (i0 + j >= lo && i0 + j < hi) ? __ldcg(base + i0 + j) : 0ull;
+    }
+  } else {
+    uint32_t u[8];
+    if (SRC == 1) {
+      const uint32_t* xr = static_cast<const uint32_t*>(a.x) + row * a.len;
+      if (a.src_vec && i0 + 8 <= a.len) {
+        const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(xr + i0));
+        const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(xr + i0) + 1);
+        u[0] = v0.x; u[1] = v0.y; u[2] = v0.z; u[3] = v0.w;
+        u[4] = v1.x; u[5] = v1.y; u[6] = v1.z; u[7] = v1.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) u[j] = (i0 + j >= lo && i0 + j < hi) ? __ldg(xr + i0 + j) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        k[j] = compose(order_key_f32(u[j]) ^ a.flip, static_cast<uint64_t>(i0 + j), a.ib);
+    } else {
+      const uint16_t* xr = static_cast<const uint16_t*>(a.x) + row * a.len;
+      if (a.src_vec && i0 + 8 <= a.len) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + i0));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) u[j] = (w[j >> 1] >> ((j & 1) * 16)) & 0xffffu;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) u[j] = (i0 + j >= lo && i0 + j < hi) ? __ldg(xr + i0 + j) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        k[j] = compose(order_key_bf16(u[j]) ^ a.flip, static_cast<uint64_t>(i0 + j), a.ib);
+    }
   }
-  const uint32_t h = __ldg(static_cast<const uint16_t*>(a.x) + row * a.len + i);
-  return compose(order_key_bf16(h) ^ a.flip, static_cast<uint64_t>(i), a.ib);
+}
+
+// Calls f(key, in_range) for every element of the 8-aligned chunks covering
+// [lo, hi) of this row, eight keys per thread and iteration.  The trip count
+// is the same for the 32 lanes of a warp, so f may use full-warp intrinsics.
+template <int SRC, int BLOCK, typename F>
+__device__ __forceinline__ void for_slice(const SelParams& a, int64_t row, int64_t lo, int64_t hi, F&& f) {
+  const int64_t c0 = lo >> 3, c1 = (hi + 7) >> 3;
+  const int lane = threadIdx.x & 31;
+  for (int64_t cw = c0 + (threadIdx.x & ~31u); cw < c1; cw += BLOCK) {
+    const int64_t c = cw + lane;
+    uint64_t k[8];
+    if (c < c1) {
+      load8<SRC>(a, row, c << 3, lo, hi, k);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) k[j] = 0ull;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t i = (c << 3) + j;
+      f(k[j], c < c1 && i >= lo && i < hi);
+    }
+  }
+}
+
+// Calls f(cache[i], valid) for i < n, with a warp-uniform trip count.
+template <int BLOCK, typename F>
+__device__ __forceinline__ void for_cache(const uint64_t* cache, unsigned n, F&& f) {
+  const unsigned lane = threadIdx.x & 31;
+  for (unsigned iw = threadIdx.x & ~31u; iw < n; iw += BLOCK) {
+    const unsigned i = iw + lane;
+    f(i < n ? cache[i] : 0ull, i < n);
+  }
+}
+
+// Adds one to this warp's counter for `digit` (256 = nothing to count).
+// Lanes holding the same digit are merged with __match_any_sync and only the
+// lowest of them writes, so there is no atomic and no same-address conflict.
+// Called by all 32 lanes of the warp.
+__device__ __forceinline__ void warp_hist_add(unsigned* wh, unsigned digit) {
+  const unsigned peers = __match_any_sync(kFull, digit);
+  if (digit < 256u && (peers & lanemask_lt()) == 0) wh[digit] += __popc(peers);
+  __syncwarp();
+}
+
+// Appends key to dst[*counter ...] for lanes with want set: one shared atomic
+// per warp.  Returns the slot of this lane's key (meaningless when !want).
+// Called by all 32 lanes of the warp.
+__device__ __forceinline__ unsigned warp_append_slot(unsigned* counter, bool want) {
+  const unsigned m = __ballot_sync(kFull, want);
+  if (m == 0) return 0u;
+  const int leader = __ffs(m) - 1;
+  unsigned base = 0;
+  if (static_cast<int>(threadIdx.x & 31) == leader) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(kFull, base, leader);
+  return base + __popc(m & lanemask_lt());
+}
+
+// 16-byte global -> shared copies that bypass registers (cp.async, L2 only).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 // Block-wide inclusive scan of one 64-bit value per thread.  `tmp` holds 32
@@ -117,8 +254,11 @@ __device__ __forceinline__ unsigned long long block_sum(unsigned long long v, un
   return r;
 }
 
+template <int BLOCK>
+constexpr int min_blocks() { return BLOCK >= 1024 ? 1 : 4; }
+
 template <int BLOCK, int P, int CB, int SRC>
-__global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
+__global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelParams a) {
   using L = Layout<BLOCK, P, CB>;
   extern __shared__ __align__(16) unsigned char smem[];
   uint64_t* bufA = reinterpret_cast<uint64_t*>(smem + L::kBufA);
@@ -126,10 +266,12 @@ __global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
   unsigned* whist = reinterpret_cast<unsigned*>(smem + L::kWhist);
   unsigned* hist = reinterpret_cast<unsigned*>(smem + L::kHist);
   unsigned* gbase = reinterpret_cast<unsigned*>(smem + L::kGbase);
+  unsigned* part = reinterpret_cast<unsigned*>(smem + L::kPart);
   unsigned long long* xch = reinterpret_cast<unsigned long long*>(smem + L::kXch);
   __shared__ unsigned long long s_tmp[32];
-  __shared__ unsigned long long s_info[4];
+  __shared__ unsigned long long s_info[5];
   __shared__ unsigned s_cnt;
+  __shared__ unsigned s_gcount;
   __shared__ int s_over;
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -138,75 +280,164 @@ __global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
   const int64_t row = blockIdx.x / G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+  // programmatic dependent launch: everything below may read what earlier
+  // grids wrote, so wait for them; the next grid may begin launching now
+  grid_dependency_wait();
+  grid_launch_dependents();
+
   int64_t valid = (SRC == 0) ? a.key_stride : a.len;
   if (SRC == 0 && a.counts) {
     const unsigned long long c = __ldcg(a.counts + row);
     if (c < static_cast<unsigned long long>(valid)) valid = static_cast<int64_t>(c);
   }
-  const int64_t sb = valid * crank / G, se = valid * (crank + 1) / G;
+  // slices start at even positions so key slices can be copied in 16-byte units
+  const int64_t sb = (valid * crank / G) & ~int64_t(1);
+  const int64_t se = (crank + 1 == G) ? valid : ((valid * (crank + 1) / G) & ~int64_t(1));
+  if (tid == 0) s_gcount = 0u;
+  TK_STAMP(0);
+
+  // The cache: the whole buffer when only tau is wanted, else the second
+  // buffer (the first one receives the winners for the sort).
+  uint64_t* cache = a.want_topk ? bufB : bufA;
+  const unsigned long long cache_cap = a.want_topk ? CB : (P + CB);
+  bool cached = false;
+  unsigned cache_n = 0;
+  if (SRC == 0 && static_cast<unsigned long long>(se - sb) <= cache_cap) {
+    // the whole slice fits: copy it in with cp.async, no registers involved
+    const uint64_t* from = a.keys + row * a.key_stride + sb;
+    const unsigned n = static_cast<unsigned>(se - sb);
+    if (a.key_vec) {
+      for (unsigned i = 2 * tid; i + 1 < n; i += 2 * BLOCK) cp_async16(cache + i, from + i);
+      if ((n & 1u) && tid == 0) cache[n - 1] = __ldcg(from + n - 1);
+      cp_async_wait_all();
+    } else {
+      for (unsigned i = tid; i < n; i += BLOCK) cache[i] = __ldcg(from + i);
+    }
+    cached = true;
+    cache_n = n;
+    __syncthreads();
+  }
+  TK_STAMP(1);
 
   // ------------------------------------------------------------------ select
   const int kb = a.key_bits + a.ib;
   uint64_t prefix = 0, pmask = 0;
   unsigned long long rank = static_cast<unsigned long long>(a.r);
-  bool cached = false;
-  unsigned cache_n = 0;
   unsigned long long local_above = 0, local_bucket = static_cast<unsigned long long>(se - sb);
   bool failed = false;
   for (int shift = ((kb - 1) / 8) * 8; shift >= 0; shift -= 8) {
-    const bool will_cache = !cached && (local_above + local_bucket) <= static_cast<unsigned long long>(CB);
+    const bool will_cache = !cached && (local_above + local_bucket) <= cache_cap;
     for (int i = tid; i < L::kWarps * 256; i += BLOCK) whist[i] = 0u;
     if (tid == 0) s_cnt = 0u;
     __syncthreads();
     unsigned* wh = whist + warp * 256;
     if (cached) {
-      for (unsigned i = tid; i < cache_n; i += BLOCK) {
-        const uint64_t k = bufB[i];
-        if ((k & pmask) == prefix) atomicAdd(&wh[(k >> shift) & 255u], 1u);
+      for (unsigned i = 2 * tid; i < cache_n; i += 2 * BLOCK) {
+        const uint64_t k0 = cache[i];
+        if ((k0 & pmask) == prefix) atomicAdd(&wh[(k0 >> shift) & 255u], 1u);
+        if (i + 1 < cache_n) {
+          const uint64_t k1 = cache[i + 1];
+          if ((k1 & pmask) == prefix) atomicAdd(&wh[(k1 >> shift) & 255u], 1u);
+        }
       }
     } else {
-      for (int64_t i = sb + tid; i < se; i += BLOCK) {
-        const uint64_t k = source_key<SRC>(a, row, i);
-        if ((k & pmask) == prefix) atomicAdd(&wh[(k >> shift) & 255u], 1u);
-        if (will_cache && k >= prefix) bufB[atomicAdd(&s_cnt, 1u)] = k;
-      }
+      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t k, bool in) {
+        warp_hist_add(wh, (in && (k & pmask) == prefix) ? static_cast<unsigned>((k >> shift) & 255u) : 256u);
+        if (will_cache) {
+          const bool want = in && k >= prefix;
+          const unsigned slot = warp_append_slot(&s_cnt, want);
+          if (want) cache[slot] = k;
+        }
+      });
     }
     __syncthreads();
-    for (int d = tid; d < 256; d += BLOCK) {
-      unsigned s = 0;
-      for (int w = 0; w < L::kWarps; ++w) s += whist[w * 256 + d];
-      hist[d] = s;
+    if (shift == ((kb - 1) / 8) * 8) TK_STAMP(25);
+    {
+      // per-digit sum over the warps' counters: each group of 256 threads
+      // sums a quarter of the warps, then the quarters are added
+      const int dq = tid & 255, q = tid >> 8;
+      unsigned sq = 0;
+      for (int w = q * L::kWarpsPerQuarter; w < (q + 1) * L::kWarpsPerQuarter; ++w) sq += whist[w * 256 + dq];
+      part[q * 256 + dq] = sq;
+      __syncthreads();
+      if (tid < 256) {
+        unsigned sd = 0;
+        for (int q2 = 0; q2 < L::kQuarters; ++q2) sd += part[q2 * 256 + tid];
+        hist[tid] = sd;
+      }
     }
     if (will_cache) {
       cache_n = s_cnt;
       cached = true;
     }
     if (tid == 0) s_info[0] = ~0ull;
+    if (shift == ((kb - 1) / 8) * 8) TK_STAMP(26);
     cluster.sync();
-    // digit 255 - tid; inclusive scan from the top digit downwards
-    unsigned long long tot = 0;
+    if (shift == ((kb - 1) / 8) * 8) TK_STAMP(27);
+    // digit 255 - tid; inclusive scans from the top digit downwards of the
+    // cluster totals and of this CTA's own counts
+    unsigned long long tot = 0, mine = 0;
     const int d = 255 - tid;
-    if (tid < 256)
+    if (tid < 256) {
       for (unsigned c = 0; c < G; ++c) tot += cluster.map_shared_rank(hist, c)[d];
+      mine = hist[d];
+    }
     const unsigned long long incl = block_scan_incl(tot, s_tmp);
+    const unsigned long long mine_incl = block_scan_incl(mine, s_tmp);
+    if (shift == ((kb - 1) / 8) * 8) TK_STAMP(28);
     if (tid < 256) {
       const unsigned long long excl = incl - tot;
       if (excl < rank && rank <= incl) {
         s_info[0] = static_cast<unsigned long long>(d);
         s_info[1] = excl;
-        s_info[2] = hist[d];
-        unsigned long long above = 0;
-        for (int q = d + 1; q < 256; ++q) above += hist[q];
-        s_info[3] = above;
+        s_info[2] = mine;
+        s_info[3] = mine_incl - mine;  // this CTA's keys in digits above d
+        s_info[4] = tot;
       }
     }
     cluster.sync();
+    TK_STAMP(2 + (shift >> 3));
     if (s_info[0] == ~0ull) { failed = true; break; }
     prefix |= s_info[0] << shift;
     pmask |= 0xffull << shift;
     rank -= s_info[1];
     local_above += s_info[3];
     local_bucket = s_info[2];
+    if (shift > 0 && s_info[4] <= kGather) {
+      // Gather the boundary bucket into CTA 0 and rank it by counting.
+      unsigned* g_cnt = cluster.map_shared_rank(&s_gcount, 0);
+      uint64_t* g_buf = cluster.map_shared_rank(reinterpret_cast<uint64_t*>(whist), 0);
+      if (cached) {
+        for (unsigned i = tid; i < cache_n; i += BLOCK) {
+          const uint64_t k = cache[i];
+          if ((k & pmask) == prefix) g_buf[atomicAdd(g_cnt, 1u)] = k;
+        }
+      } else {
+        for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t k, bool in) {
+          if (in && (k & pmask) == prefix) g_buf[atomicAdd(g_cnt, 1u)] = k;
+        });
+      }
+      cluster.sync();
+      if (crank == 0) {
+        const unsigned n = s_gcount;
+        const uint64_t* g = reinterpret_cast<const uint64_t*>(whist);
+        if (static_cast<unsigned>(tid) < n) {
+          const uint64_t mine = g[tid];
+          unsigned long long above = 0;
+          for (unsigned j = 0; j < n; ++j) {
+            const uint64_t o = g[j];
+            above += (o > mine || (o == mine && j < static_cast<unsigned>(tid))) ? 1ull : 0ull;
+          }
+          if (above == rank - 1)
+            for (unsigned c = 0; c < G; ++c) cluster.map_shared_rank(xch, c)[3] = mine;
+        }
+      }
+      cluster.sync();
+      TK_STAMP(12);
+      prefix = xch[3];
+      pmask = ~0ull;
+      break;
+    }
   }
   if (failed) {
     if (tid == 0 && crank == 0) atomicCAS(a.status, kDevOk, kDevBadState);
@@ -219,8 +450,10 @@ __global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
   }
 
   // ------------------------------------------------------------------ winners
+  TK_STAMP(13);
   const int64_t k = a.r;
-  const int64_t pe = (k + G - 1) / G;  // positions per CTA
+  const unsigned sortG = (k <= P) ? 1u : G;               // CTAs taking part in the sort
+  const int64_t pe = (sortG == 1) ? k : (k + G - 1) / G;  // sort positions per CTA
   {
     unsigned long long cnt = 0, orm = 0, andm = ~0ull;
     if (tid == 0) {
@@ -232,21 +465,21 @@ __global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
     __syncthreads();
     if (cached) {
       for (unsigned i = tid; i < cache_n; i += BLOCK) {
-        const uint64_t key = bufB[i];
+        const uint64_t key = cache[i];
         if (key >= tau) { ++cnt; orm |= key; andm &= key; }
       }
     } else {
-      for (int64_t i = sb + tid; i < se; i += BLOCK) {
-        const uint64_t key = source_key<SRC>(a, row, i);
-        if (key >= tau) {
-          ++cnt; orm |= key; andm &= key;
-          const unsigned slot = atomicAdd(&s_cnt, 1u);
+      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t key, bool in) {
+        const bool w = in && key >= tau;
+        if (w) { ++cnt; orm |= key; andm &= key; }
+        const unsigned slot = warp_append_slot(&s_cnt, w);
+        if (w) {
           if (slot < static_cast<unsigned>(CB)) bufB[slot] = key; else s_over = 1;
         }
-      }
+      });
     }
-    // count / or / and over the block; published in xch for the cluster
     const unsigned long long total = block_sum(cnt, s_tmp);
+    TK_STAMP(15);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       orm |= __shfl_xor_sync(kFull, orm, o);
@@ -272,32 +505,88 @@ __global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
     cluster.sync();
     return;
   }
-  // place the winners evenly: position base + local sequence -> CTA pos / pe
+  TK_STAMP(29);
+  // Place the winners: position base + local sequence.  With several CTAs the
+  // keys go through an L2-resident exchange buffer (plain global stores, then
+  // each CTA reads back its own contiguous range), which costs far less than
+  // scattering single keys into other CTAs' shared memory.
+  uint64_t* xb = a.xbuf + row * 2 * k;
+  int xsel = 0;  // which half of the exchange buffer the next exchange uses
   {
     if (tid == 0) s_cnt = 0u;
     __syncthreads();
+    auto place = [&](uint64_t key, bool want) {
+      const unsigned slot = warp_append_slot(&s_cnt, want);
+      if (want) {
+        const unsigned pos = static_cast<unsigned>(base) + slot;
+        if (G == 1) bufA[pos] = key; else xb[pos] = key;
+      }
+    };
     if (cached || !s_over) {
       const unsigned n = cached ? cache_n : static_cast<unsigned>(xch[0]);
-      for (unsigned i = tid; i < n; i += BLOCK) {
-        const uint64_t key = bufB[i];
-        if (cached && key < tau) continue;
-        const unsigned long long pos = base + atomicAdd(&s_cnt, 1u);
-        cluster.map_shared_rank(bufA, static_cast<unsigned>(pos / pe))[pos % pe] = key;
-      }
+      const uint64_t* from = cached ? cache : bufB;
+      for_cache<BLOCK>(from, n, [&](uint64_t key, bool in) { place(key, in && (!cached || key >= tau)); });
     } else {
-      for (int64_t i = sb + tid; i < se; i += BLOCK) {
-        const uint64_t key = source_key<SRC>(a, row, i);
-        if (key < tau) continue;
-        const unsigned long long pos = base + atomicAdd(&s_cnt, 1u);
-        cluster.map_shared_rank(bufA, static_cast<unsigned>(pos / pe))[pos % pe] = key;
-      }
+      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t key, bool in) { place(key, in && key >= tau); });
     }
   }
+  TK_STAMP(30);
   cluster.sync();
-
-  // ------------------------------------------------------------------ sort
+  TK_STAMP(14);
+  if (sortG == 1 && crank != 0) return;  // CTA 0 sorts alone
   const int64_t my0 = static_cast<int64_t>(crank) * pe;
   const int n_c = static_cast<int>(my0 >= k ? 0 : (k - my0 < pe ? k - my0 : pe));
+  if (G > 1) {
+    for (int i = tid; i < n_c; i += BLOCK) bufA[i] = __ldcg(xb + my0 + i);
+    xsel = 1;
+    __syncthreads();
+  }
+
+  // ------------------------------------------------------------------ sort
+  if (sortG == 1 && k <= BLOCK) {
+    // Bitonic sort, one key per thread of CTA 0, descending; strides below a
+    // warp use shuffles, larger ones a shared-memory exchange.  Padding keys
+    // are 0: a real key 0 can only be the smallest winner and is bit-identical
+    // to a pad, so either may land at position k-1.
+    int n2 = 1;
+    while (n2 < k) n2 <<= 1;
+    uint64_t v = (tid < k) ? bufA[tid] : 0ull;
+    for (int size = 2; size <= n2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        uint64_t o;
+        if (stride >= 32) {
+          bufB[tid] = v;
+          __syncthreads();
+          o = bufB[tid ^ stride];
+          __syncthreads();
+        } else {
+          o = __shfl_xor_sync(kFull, v, stride);
+        }
+        const bool lower = (tid & stride) == 0;
+        const bool desc = (tid & size) == 0;
+        v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
+      }
+    }
+    TK_STAMP(24);
+    if (tid < k) {
+      const int64_t oi = row * k + tid;
+      const uint64_t pos = position_of(v, a.ib);
+      a.out_idx[oi] = static_cast<int64_t>(pos);
+      const uint32_t vk = vkey_of(v, a.ib) ^ a.flip;
+      if (a.key_bits == 32) {
+        static_cast<uint32_t*>(a.out_vals)[oi] =
+            (vk == Dt<kF32>::kZeroKey || vk == Dt<kF32>::kNanKey)
+                ? __ldg(static_cast<const uint32_t*>(a.x) + row * a.len + pos)
+                : value_bits_f32(vk);
+      } else {
+        static_cast<uint16_t*>(a.out_vals)[oi] =
+            (vk == Dt<kBF16>::kZeroKey || vk == Dt<kBF16>::kNanKey)
+                ? __ldg(static_cast<const uint16_t*>(a.x) + row * a.len + pos)
+                : static_cast<uint16_t>(value_bits_bf16(vk));
+      }
+    }
+    return;
+  }
   const unsigned long long vary = all_or ^ all_and;
   uint64_t* src = bufA;
   uint64_t* dst = bufB;
@@ -305,15 +594,20 @@ __global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
   const int seg0 = warp * ipw;
   const int seg1 = (seg0 + ipw < n_c) ? seg0 + ipw : n_c;
   const unsigned lt = lanemask_lt();
+  auto gsync = [&]() {
+    if (sortG > 1) cluster.sync(); else __syncthreads();
+  };
   for (int shift = 0; shift < 64; shift += 8) {
-    if (((vary >> shift) & 0xffull) == 0) continue;  // cluster-uniform
+    if (((vary >> shift) & 0xffull) == 0) continue;  // uniform over the sorting CTAs
     for (int i = tid; i < L::kWarps * 256; i += BLOCK) whist[i] = 0u;
     __syncthreads();
     unsigned* wh = whist + warp * 256;
     uint64_t key[L::kItems];
     unsigned dig[L::kItems], wr[L::kItems];
+    const int nj = (seg1 - seg0 + 31) >> 5;  // items per lane, uniform in the warp
 #pragma unroll
     for (int j = 0; j < L::kItems; ++j) {
+      if (j >= nj) break;
       const int i = seg0 + j * 32 + lane;
       const bool v = i < seg1;
       key[j] = v ? src[i] : 0ull;
@@ -327,19 +621,31 @@ __global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
       wr[j] = b + before;
     }
     __syncthreads();
-    for (int d = tid; d < 256; d += BLOCK) {
+    TK_STAMP(10);
+    // exclusive prefix of the per-warp counts over warps, per digit, in two
+    // steps: within groups of warps, then across groups
+    {
+      const int d = tid & 255, q = tid >> 8;
       unsigned run = 0;
-      for (int w = 0; w < L::kWarps; ++w) {
+      for (int w = q * L::kWarpsPerQuarter; w < (q + 1) * L::kWarpsPerQuarter; ++w) {
         const unsigned t = whist[w * 256 + d];
         whist[w * 256 + d] = run;
         run += t;
       }
-      hist[d] = run;
+      part[q * 256 + d] = run;
+      __syncthreads();
+      unsigned qbase = 0;
+      for (int q2 = 0; q2 < q; ++q2) qbase += part[q2 * 256 + d];
+      if (qbase)
+        for (int w = q * L::kWarpsPerQuarter; w < (q + 1) * L::kWarpsPerQuarter; ++w) whist[w * 256 + d] += qbase;
+      if (q == L::kQuarters - 1) hist[d] = qbase + run;
     }
-    cluster.sync();
+    TK_STAMP(11);
+    gsync();
+    TK_STAMP(31);
     unsigned long long tot = 0, before_me = 0;
     if (tid < 256) {
-      for (unsigned c = 0; c < G; ++c) {
+      for (unsigned c = 0; c < sortG; ++c) {
         const unsigned h = cluster.map_shared_rank(hist, c)[tid];
         tot += h;
         if (c < crank) before_me += h;
@@ -347,21 +653,35 @@ __global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
     }
     const unsigned long long incl = block_scan_incl(tot, s_tmp);
     if (tid < 256) gbase[tid] = static_cast<unsigned>(incl - tot + before_me);
-    cluster.sync();
+    gsync();
+    TK_STAMP(23);
 #pragma unroll
     for (int j = 0; j < L::kItems; ++j) {
+      if (j >= nj) break;
       const int i = seg0 + j * 32 + lane;
       if (i < seg1) {
-        const unsigned long long pos =
-            static_cast<unsigned long long>(gbase[dig[j]]) + wh[dig[j]] + wr[j];
-        cluster.map_shared_rank(dst, static_cast<unsigned>(pos / pe))[pos % pe] = key[j];
+        const unsigned pos = gbase[dig[j]] + wh[dig[j]] + wr[j];
+        if (sortG == 1) dst[pos] = key[j]; else xb[xsel * k + pos] = key[j];
       }
     }
-    cluster.sync();
-    uint64_t* t = src; src = dst; dst = t;
+    TK_STAMP(22);
+    gsync();
+    TK_STAMP(21);
+    if (sortG == 1) {
+      uint64_t* t = src; src = dst; dst = t;
+    } else {
+      // read back this CTA's range; the next exchange uses the other half, so
+      // no CTA can overwrite what another is still reading
+      const uint64_t* from = xb + xsel * k + my0;
+      for (int i = tid; i < n_c; i += BLOCK) src[i] = __ldcg(from + i);
+      xsel ^= 1;
+      __syncthreads();
+    }
+    TK_STAMP(16 + (shift >> 3));
   }
 
   // ------------------------------------------------------------------ output
+  TK_STAMP(24);
   const int64_t obase = row * k + my0;
   for (int i = tid; i < n_c; i += BLOCK) {
     const uint64_t key = src[i];
@@ -383,8 +703,8 @@ __global__ void __launch_bounds__(BLOCK, 1) select_kernel(SelParams a) {
 }
 
 // Kernel variants: (block, sort positions per CTA, cache/second buffer).
-constexpr int kSmallBlock = 256, kSmallP = 512, kSmallCB = 2048;
-constexpr int kBigBlock = 1024, kBigP = 11264, kBigCB = 11264;
+constexpr int kSmallBlock = 256, kSmallP = 1024, kSmallCB = 2048;
+constexpr int kBigBlock = 1024, kBigP = 8192, kBigCB = 14336;
 constexpr int kMaxCluster = 16;
 
 template <int BLOCK, int P, int CB, int SRC>
@@ -430,19 +750,22 @@ cudaError_t launch_variant(const SelParams& a, int64_t nsel, int G, int* used, c
   if (G > max_g) G = max_g;
   const int64_t sort_k = a.want_topk ? a.r : 1;
   if (sort_k > static_cast<int64_t>(G) * P) return cudaErrorInvalidConfiguration;
+  if (a.want_topk && G > 1 && a.xbuf == nullptr) return cudaErrorInvalidValue;
   *used = G;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nsel * G), 1, 1);
   cfg.blockDim = dim3(BLOCK, 1, 1);
   cfg.dynamicSmemBytes = L::kBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(G);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, select_kernel<BLOCK, P, CB, SRC>, a);
 }
 
@@ -452,6 +775,7 @@ cudaError_t launch_src(const SelParams& a, int src, int64_t nsel, int G, int* us
   if (src == 1) return launch_variant<BLOCK, P, CB, 1>(a, nsel, G, used, st);
   return launch_variant<BLOCK, P, CB, 2>(a, nsel, G, used, st);
 }
+
 
 int pow2_at_least(int64_t v) {
   int g = 1;
@@ -473,7 +797,13 @@ int sm_count() {
 
 int64_t select_max_k() { return static_cast<int64_t>(kMaxCluster) * kBigP; }
 
-cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source_bound, int* cluster,
+#ifdef TK_PHASE_TIMING
+int debug_phase_ns(unsigned long long* out) {
+  return cudaMemcpyFromSymbol(out, g_phase_ns, sizeof(g_phase_ns)) == cudaSuccess ? 0 : -3;
+}
+#endif
+
+cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source_hint, int* cluster,
                           cudaStream_t st) {
   SelParams a{};
   a.keys = job.keys;
@@ -484,25 +814,32 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   a.ib = p.ib;
   a.flip = p.flip;
   a.key_bits = p.dtype == kF32 ? 32 : 16;
+  a.key_vec = job.keys && (reinterpret_cast<uintptr_t>(job.keys) % 16 == 0) &&
+              (job.key_stride % 2 == 0 || p.nsel == 1);
+  a.src_vec = p.vec_ok;
   a.r = job.r;
   a.want_topk = job.want_topk ? 1 : 0;
   a.tau_out = job.tau_out;
   a.out_vals = job.out_vals;
   a.out_idx = job.out_idx;
   a.status = job.status;
+  a.xbuf = job.xbuf;
   const int src = job.keys ? 0 : (p.dtype == kF32 ? 1 : 2);
   const bool many = p.nsel >= sm_count();
-  const int64_t sort_k = job.want_topk ? job.r : 1;
-  const bool small = sort_k <= static_cast<int64_t>(kMaxCluster) * kSmallP;
   int G;
-  if (small) {
-    const int64_t g_min = (sort_k + kSmallP - 1) / kSmallP;
-    const int64_t g_par = many ? 1 : (source_bound + kSmallBlock * 64 - 1) / (kSmallBlock * 64);
-    G = pow2_at_least(g_min > g_par ? g_min : g_par);
+  bool small;
+  if (!job.want_topk) {
+    // tau: cache every key of the slice; the whole buffer is the cache
+    small = false;
+    G = pow2_at_least((source_hint + kBigP + kBigCB - 1) / (kBigP + kBigCB));
+  } else if (many && job.r <= kSmallP) {
+    small = true;
+    G = 1;
   } else {
-    const int64_t g_min = (sort_k + kBigP - 1) / kBigP;
-    const int64_t g_par = many ? 1 : (source_bound + kBigBlock * 16 - 1) / (kBigBlock * 16);
-    G = pow2_at_least(g_min > g_par ? g_min : g_par);
+    small = false;
+    const int64_t g_min = (job.r + kBigP - 1) / kBigP;
+    const int64_t g_cache = (source_hint + kBigCB - 1) / kBigCB;
+    G = many ? pow2_at_least(g_min) : pow2_at_least(g_min > g_cache ? g_min : g_cache);
   }
   int used = G;
   const cudaError_t e = small ? launch_src<kSmallBlock, kSmallP, kSmallCB>(a, src, p.nsel, G, &used, st)

@@ -21,6 +21,8 @@
 // lgamma/log1p for the first term and the term ratio for the rest.
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include "engine.h"
 
@@ -45,7 +47,7 @@ double sum_up(int64_t s, double p, int64_t t) {
   const double ratio_scale = p / (1.0 - p);
   for (int64_t j = t; j <= s; ++j) {
     sum += term;
-    if (term < sum * 1e-18 && static_cast<double>(j) > static_cast<double>(s) * p) break;
+    if (term <= sum * 1e-18 && static_cast<double>(j) > static_cast<double>(s) * p) break;
     term *= static_cast<double>(s - j) / static_cast<double>(j + 1) * ratio_scale;
   }
   return sum;
@@ -58,7 +60,7 @@ double sum_down(int64_t s, double p, int64_t t) {
   const double ratio_scale = (1.0 - p) / p;
   for (int64_t j = t; j >= 0; --j) {
     sum += term;
-    if (term < sum * 1e-18 && static_cast<double>(j) < static_cast<double>(s) * p) break;
+    if (term <= sum * 1e-18 && static_cast<double>(j) < static_cast<double>(s) * p) break;
     term *= static_cast<double>(j) / static_cast<double>(s - j + 1) * ratio_scale;
   }
   return sum;
@@ -157,6 +159,14 @@ bool choose_params(int64_t n, int64_t k, double eps, const ParamRule& pr, int64_
   *t_out = t;
   *M_out = M;
   return true;
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("TOPK_ENABLE_PDL");
+    return v && std::strcmp(v, "1") == 0;
+  }();
+  return on;
 }
 
 }  // namespace tk

@@ -83,6 +83,55 @@ ParamRule rule_of(const topk_options_t* o) {
   return pr;
 }
 
+// Parameters of recent (len, k, eps, rule) requests: the tail searches cost
+// tens of microseconds, a lookup well under one.
+struct PlanKey {
+  int64_t len, k;
+  double eps;
+  int64_t s_min, s_max;
+  double ratio;
+  int rule;
+  bool operator<(const PlanKey& o) const {
+    if (len != o.len) return len < o.len;
+    if (k != o.k) return k < o.k;
+    if (eps != o.eps) return eps < o.eps;
+    if (s_min != o.s_min) return s_min < o.s_min;
+    if (s_max != o.s_max) return s_max < o.s_max;
+    if (ratio != o.ratio) return ratio < o.ratio;
+    return rule < o.rule;
+  }
+};
+struct PlanVal {
+  bool ok;
+  int64_t S, t, M;
+};
+std::mutex g_plan_mu;
+std::map<PlanKey, PlanVal> g_plans;
+
+bool cached_params(int64_t len, int64_t k, double eps, const ParamRule& pr, int64_t* S, int64_t* t,
+                   int64_t* M) {
+  const PlanKey key{len, k, eps, pr.s_min, pr.s_max, pr.cost_ratio, pr.rule};
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) {
+      *S = it->second.S;
+      *t = it->second.t;
+      *M = it->second.M;
+      return it->second.ok;
+    }
+  }
+  PlanVal v{};
+  v.ok = choose_params(len, k, eps, pr, &v.S, &v.t, &v.M);
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  if (g_plans.size() > 4096) g_plans.clear();
+  g_plans[key] = v;
+  *S = v.S;
+  *t = v.t;
+  *M = v.M;
+  return v.ok;
+}
+
 // Path choice for one selection of k out of len (nsel selections).
 int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
               const topk_options_t* o, Plan* plan) {
@@ -94,7 +143,7 @@ int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
     if (pr.s_min < 1 || pr.s_max < pr.s_min || !(pr.cost_ratio > 0.0) || (pr.rule != 0 && pr.rule != 1))
       return TOPK_EINVAL;
     int64_t S = 0, t = 0, M = 0;
-    if (choose_params(len, k, eps, pr, &S, &t, &M)) {
+    if (cached_params(len, k, eps, pr, &S, &t, &M)) {
       if (o && o->t_override > 0) t = o->t_override;
       if (o && o->m_override > 0) M = o->m_override;
       plan->S = S;
@@ -127,9 +176,12 @@ int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
 }
 
 int sm_count_host() {
-  int dev = 0, sms = 0;
+  static int sms = 0;
+  if (sms) return sms;
+  int dev = 0, v = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  sms = v;
   return sms;
 }
 
@@ -201,9 +253,9 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
 
   int cluster = 0;
   if (plan.path == TOPK_PATH_DIRECT) {
-    // one small header for the status word only
+    // the status word and the sort's exchange buffer
     void* ws = nullptr;
-    TK_TRY(workspace(st, 256, &ws));
+    TK_TRY(workspace(st, 256 + sizeof(uint64_t) * 2 * p.nsel * k, &ws));
     DevHeader* hdr = static_cast<DevHeader*>(ws);
     TK_TRY(cudaMemsetAsync(&hdr->status, 0, sizeof(int), st));
     SelectJob job{};
@@ -213,6 +265,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     job.out_vals = out_vals;
     job.out_idx = out_idx;
     job.status = &hdr->status;
+    job.xbuf = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + 256);
     TK_TRY(launch_select(p, job, p.len, &cluster, st));
     if (stats) {
       stats->cluster = cluster;
@@ -240,6 +293,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   const size_t o_tiles = off; off = align_up(off + sizeof(unsigned) * ntile);
   const size_t o_samples = off; off = align_up(off + sizeof(uint64_t) * nsel * S);
   const size_t o_buf = off; off = align_up(off + sizeof(uint64_t) * nsel * M);
+  const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * 2 * nsel * k);
   void* ws = nullptr;
   TK_TRY(workspace(st, off, &ws));
   char* base = static_cast<char*>(ws);
@@ -252,6 +306,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   auto* tiles = reinterpret_cast<unsigned*>(base + o_tiles);
   auto* samples = reinterpret_cast<uint64_t*>(base + o_samples);
   auto* buf = reinterpret_cast<uint64_t*>(base + o_buf);
+  auto* xbuf = reinterpret_cast<uint64_t*>(base + o_xbuf);
 
   FallbackScratch fs{ghist, tiles, hdr->barrier, &hdr->status, r_seen, &hdr->misses, tau_x};
   const uint64_t seed = (o && o->seed) ? o->seed : kDefaultSeed;
@@ -270,7 +325,6 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     SelectJob tj{};
     tj.keys = samples;
     tj.key_stride = S;
-    tj.counts = nullptr;
     tj.r = plan.t;
     tj.want_topk = false;
     tj.tau_out = tau;
@@ -294,7 +348,16 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.out_vals = out_vals;
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
-  TK_TRY(launch_select(p, rj, M, &cluster, st));
+  rj.xbuf = xbuf;
+  // expected survivors: E[R] = t (N+1)/(S+1) (Lemma 1, Eq. 2), with headroom
+  int64_t hint = M;
+  if (plan.path == TOPK_PATH_PROFK) {
+    const double er = static_cast<double>(plan.t) * (static_cast<double>(p.len) + 1.0) /
+                      (static_cast<double>(S) + 1.0);
+    if (1.5 * er < static_cast<double>(M)) hint = static_cast<int64_t>(1.5 * er);
+    if (hint < k) hint = k;
+  }
+  TK_TRY(launch_select(p, rj, hint, &cluster, st));
   if (plan.path == TOPK_PATH_PROFK) TK_TRY(mark(5));
 
   if (stats) {
@@ -388,6 +451,10 @@ const char* topk_status_str(int status) {
 }
 
 int topk_version(void) { return 100; }
+
+#ifdef TK_PHASE_TIMING
+int topk_debug_phase_ns(unsigned long long* out) { return tk::debug_phase_ns(out); }
+#endif
 
 int topk_index_bits(int64_t len) { return len < 1 ? 1 : index_bits(len); }
 

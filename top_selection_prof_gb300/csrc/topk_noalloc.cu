@@ -132,7 +132,14 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
   const size_t o_tiles = off; off = up256(off + sizeof(unsigned) * ((len + kFallbackTile - 1) / kFallbackTile));
   const size_t o_samples = off; off = up256(off + sizeof(uint64_t) * nsel * S);
   const size_t o_buf = off; off = up256(off + sizeof(uint64_t) * nsel * cap);
-  if (path != TOPK_PATH_DIRECT && off > kNoAllocScratchBytes) return TOPK_EUNSUPPORTED;
+  const size_t o_xbuf = off; off = up256(off + sizeof(uint64_t) * 2 * nsel * k);
+  if (path == TOPK_PATH_DIRECT) {
+    // the direct path needs only the header and the sort's exchange buffer
+    if (up256(sizeof(DevHeader)) + sizeof(uint64_t) * 2 * nsel * k > kNoAllocScratchBytes)
+      return TOPK_EUNSUPPORTED;
+  } else if (off > kNoAllocScratchBytes) {
+    return TOPK_EUNSUPPORTED;
+  }
 
   void* scratch = nullptr;
   cudaError_t e = scratch_address(&scratch);
@@ -154,6 +161,7 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
     job.out_vals = out_vals;
     job.out_idx = out_idx;
     job.status = &hdr->status;
+    job.xbuf = reinterpret_cast<uint64_t*>(base + up256(sizeof(DevHeader)));
     NA_TRY(launch_select(p, job, len, nullptr, st));
     return TOPK_OK;
   }
@@ -191,6 +199,7 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
   rj.out_vals = out_vals;
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
+  rj.xbuf = reinterpret_cast<uint64_t*>(base + o_xbuf);
   NA_TRY(launch_select(p, rj, cap, nullptr, st));
 #undef NA_TRY
   return TOPK_OK;
