@@ -42,17 +42,26 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned kGather = 256;  // bucket size at which the select finishes by ranking
+constexpr int64_t kRankMax = 4096;  // winners sorted by counting ranks instead of radix passes
 
 #ifdef TK_PHASE_TIMING
 // Debug builds only: globaltimer stamps of the first cluster's CTA 0.
 __device__ unsigned long long g_phase_ns[2][32];
+__device__ unsigned long long g_cta_ns[2][16][8];  // per CTA of the first cluster: debug stamps
 #define TK_STAMP(i)                                                                         \
   do {                                                                                      \
     if (blockIdx.x == 0 && threadIdx.x == 0) g_phase_ns[a.want_topk][(i)] = globaltimer_ns(); \
   } while (0)
+#define TK_CTA(slot, v)                                                                    \
+  do {                                                                                     \
+    if (blockIdx.x < 16 && threadIdx.x == 0) g_cta_ns[a.want_topk][blockIdx.x][(slot)] = (v); \
+  } while (0)
 #else
 #define TK_STAMP(i) \
   do {              \
+  } while (0)
+#define TK_CTA(slot, v) \
+  do {                  \
   } while (0)
 #endif
 
@@ -257,6 +266,120 @@ __device__ __forceinline__ unsigned long long block_sum(unsigned long long v, un
 template <int BLOCK>
 constexpr int min_blocks() { return BLOCK >= 1024 ? 1 : 4; }
 
+// Writes out_vals / out_idx for one winner key at output place `place`.
+__device__ __forceinline__ void write_out(const SelParams& a, int64_t row, int64_t k, int64_t place,
+                                          uint64_t key) {
+  const int64_t oi = row * k + place;
+  const uint64_t pos = position_of(key, a.ib);
+  a.out_idx[oi] = static_cast<int64_t>(pos);
+  const uint32_t vk = vkey_of(key, a.ib) ^ a.flip;
+  if (a.key_bits == 32) {
+    static_cast<uint32_t*>(a.out_vals)[oi] =
+        (vk == Dt<kF32>::kZeroKey || vk == Dt<kF32>::kNanKey)
+            ? __ldg(static_cast<const uint32_t*>(a.x) + row * a.len + pos)
+            : value_bits_f32(vk);
+  } else {
+    static_cast<uint16_t*>(a.out_vals)[oi] =
+        (vk == Dt<kBF16>::kZeroKey || vk == Dt<kBF16>::kNanKey)
+            ? __ldg(static_cast<const uint16_t*>(a.x) + row * a.len + pos)
+            : static_cast<uint16_t>(value_bits_bf16(vk));
+  }
+}
+
+// Places keys by counting ("Rank by Counting": a key's place is the number
+// of keys that outrank it; the keys are distinct, so places form a
+// permutation).  The n keys of src are first grouped, largest group first, by
+// the NB-bucket digit of their most significant varying bits, so a key only
+// compares against its own group.  The keys are then ranked in grouped order,
+// so the lanes of a warp mostly share a group: they read each group member
+// once (a broadcast) and run the same number of steps.  Only groups starting
+// in [split0, split1) are ranked here (how CTAs share the work); keys whose
+// place base_place + rank lies in [w0, w1) are written out.  Returns false
+// without writing when the largest group exceeds max_group.
+template <int BLOCK, int NB>
+__device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long vary, unsigned split0,
+                                unsigned split1, uint64_t* grp, unsigned* gcount, unsigned* gstart,
+                                unsigned* gcur, unsigned long long* s_tmp, unsigned max_group,
+                                const SelParams& a, int64_t row, int64_t kout, int64_t base_place, int64_t w0,
+                                int64_t w1) {
+  static_assert(NB % BLOCK == 0, "whole groups per thread");
+  constexpr int kBits = NB == 2048 ? 11 : 8;
+  constexpr int kPer = NB / BLOCK;
+  __shared__ unsigned s_gmax;
+  const int tid = threadIdx.x;
+  const int hb = vary ? 63 - __clzll(static_cast<long long>(vary)) : 0;
+  const int dsh = hb >= kBits - 1 ? hb - (kBits - 1) : 0;
+  const unsigned mask = NB - 1;
+  for (int i = tid; i < NB; i += BLOCK) { gcount[i] = 0u; gcur[i] = 0u; }
+  if (tid == 0) s_gmax = 0u;
+  __syncthreads();
+  for (int i = tid; i < n; i += BLOCK) atomicAdd(&gcount[mask - static_cast<unsigned>((src[i] >> dsh) & mask)], 1u);
+  __syncthreads();
+  unsigned c[kPer];
+  unsigned long long sum = 0;
+  unsigned mx = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    c[q] = gcount[tid * kPer + q];
+    sum += c[q];
+    mx = c[q] > mx ? c[q] : mx;
+  }
+  const unsigned long long incl = block_scan_incl(sum, s_tmp);
+  unsigned run = static_cast<unsigned>(incl - sum);
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    gstart[tid * kPer + q] = run;
+    run += c[q];
+  }
+  atomicMax(&s_gmax, mx);
+  __syncthreads();
+  if (s_gmax > max_group) return false;
+  for (int i = tid; i < n; i += BLOCK) {
+    const uint64_t key = src[i];
+    const unsigned g = mask - static_cast<unsigned>((key >> dsh) & mask);
+    grp[gstart[g] + atomicAdd(&gcur[g], 1u)] = key;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += BLOCK) {
+    const uint64_t v = grp[i];
+    const unsigned g = mask - static_cast<unsigned>((v >> dsh) & mask);
+    const unsigned g0 = gstart[g];
+    if (g0 < split0 || g0 >= split1) continue;
+    const unsigned g1 = g0 + gcount[g];
+    unsigned r0 = 0, r1 = 0;
+    unsigned j = g0;
+    for (; j + 1 < g1; j += 2) {
+      r0 += grp[j] > v ? 1u : 0u;
+      r1 += grp[j + 1] > v ? 1u : 0u;
+    }
+    if (j < g1) r0 += grp[j] > v ? 1u : 0u;
+    const int64_t place = base_place + g0 + r0 + r1;
+    if (place >= w0 && place < w1) write_out(a, row, kout, place, v);
+  }
+  return true;
+}
+
+// OR and AND of src[0..n) over the block.
+template <int BLOCK>
+__device__ void block_or_and(const uint64_t* src, int n, unsigned long long* out_or, unsigned long long* out_and) {
+  __shared__ unsigned long long s_or[32], s_and[32];
+  unsigned long long o = 0, d = ~0ull;
+  for (int i = threadIdx.x; i < n; i += BLOCK) { o |= src[i]; d &= src[i]; }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) {
+    o |= __shfl_xor_sync(kFull, o, m);
+    d &= __shfl_xor_sync(kFull, d, m);
+  }
+  if ((threadIdx.x & 31) == 0) { s_or[threadIdx.x >> 5] = o; s_and[threadIdx.x >> 5] = d; }
+  __syncthreads();
+  o = 0;
+  d = ~0ull;
+  for (int w = 0; w < BLOCK / 32; ++w) { o |= s_or[w]; d &= s_and[w]; }
+  *out_or = o;
+  *out_and = d;
+  __syncthreads();
+}
+
 template <int BLOCK, int P, int CB, int SRC>
 __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelParams a) {
   using L = Layout<BLOCK, P, CB>;
@@ -295,11 +418,12 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   const int64_t se = (crank + 1 == G) ? valid : ((valid * (crank + 1) / G) & ~int64_t(1));
   if (tid == 0) s_gcount = 0u;
   TK_STAMP(0);
+  TK_CTA(0, globaltimer_ns());
 
-  // The cache: the whole buffer when only tau is wanted, else the second
-  // buffer (the first one receives the winners for the sort).
-  uint64_t* cache = a.want_topk ? bufB : bufA;
-  const unsigned long long cache_cap = a.want_topk ? CB : (P + CB);
+  // The cache is the whole buffer (both halves): the winners later leave
+  // through the L2 exchange buffer, so nothing else is written here meanwhile.
+  uint64_t* cache = bufA;
+  const unsigned long long cache_cap = P + CB;
   bool cached = false;
   unsigned cache_n = 0;
   if (SRC == 0 && static_cast<unsigned long long>(se - sb) <= cache_cap) {
@@ -452,8 +576,6 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   // ------------------------------------------------------------------ winners
   TK_STAMP(13);
   const int64_t k = a.r;
-  const unsigned sortG = (k <= P) ? 1u : G;               // CTAs taking part in the sort
-  const int64_t pe = (sortG == 1) ? k : (k + G - 1) / G;  // sort positions per CTA
   {
     unsigned long long cnt = 0, orm = 0, andm = ~0ull;
     if (tid == 0) {
@@ -506,10 +628,10 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
     return;
   }
   TK_STAMP(29);
-  // Place the winners: position base + local sequence.  With several CTAs the
-  // keys go through an L2-resident exchange buffer (plain global stores, then
-  // each CTA reads back its own contiguous range), which costs far less than
-  // scattering single keys into other CTAs' shared memory.
+  // Place the winners: position base + local sequence, in an L2-resident
+  // exchange buffer (plain global stores; each CTA then reads back what it
+  // needs), which costs far less than scattering single keys into other CTAs'
+  // shared memory.
   uint64_t* xb = a.xbuf + row * 2 * k;
   int xsel = 0;  // which half of the exchange buffer the next exchange uses
   {
@@ -518,8 +640,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
     auto place = [&](uint64_t key, bool want) {
       const unsigned slot = warp_append_slot(&s_cnt, want);
       if (want) {
-        const unsigned pos = static_cast<unsigned>(base) + slot;
-        if (G == 1) bufA[pos] = key; else xb[pos] = key;
+        xb[static_cast<unsigned>(base) + slot] = key;
       }
     };
     if (cached || !s_over) {
@@ -533,61 +654,138 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   TK_STAMP(30);
   cluster.sync();
   TK_STAMP(14);
-  if (sortG == 1 && crank != 0) return;  // CTA 0 sorts alone
-  const int64_t my0 = static_cast<int64_t>(crank) * pe;
-  const int n_c = static_cast<int>(my0 >= k ? 0 : (k - my0 < pe ? k - my0 : pe));
-  if (G > 1) {
-    for (int i = tid; i < n_c; i += BLOCK) bufA[i] = __ldcg(xb + my0 + i);
-    xsel = 1;
-    __syncthreads();
-  }
-
-  // ------------------------------------------------------------------ sort
-  if (sortG == 1 && k <= BLOCK) {
-    // Bitonic sort, one key per thread of CTA 0, descending; strides below a
-    // warp use shuffles, larger ones a shared-memory exchange.  Padding keys
-    // are 0: a real key 0 can only be the smallest winner and is bit-identical
-    // to a pad, so either may land at position k-1.
-    int n2 = 1;
-    while (n2 < k) n2 <<= 1;
-    uint64_t v = (tid < k) ? bufA[tid] : 0ull;
-    for (int size = 2; size <= n2; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        uint64_t o;
-        if (stride >= 32) {
-          bufB[tid] = v;
-          __syncthreads();
-          o = bufB[tid ^ stride];
-          __syncthreads();
-        } else {
-          o = __shfl_xor_sync(kFull, v, stride);
-        }
-        const bool lower = (tid & stride) == 0;
-        const bool desc = (tid & size) == 0;
-        v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
-      }
-    }
+  if (k <= kRankMax) {
+    // Every CTA holds all k winners (read from the exchange buffer, in the
+    // same order everywhere) and places its 1/G share of them.
+    for (int i = tid; i < k; i += BLOCK) bufA[i] = __ldcg(xb + i);
+    // CTA c ranks the groups that start in its 1/G of the places
+    const unsigned kc = static_cast<unsigned>((k + G - 1) / G);
+    const unsigned lo = crank * kc, hi = crank + 1 == G ? static_cast<unsigned>(k) : lo + kc;
+    if constexpr (BLOCK >= 1024)
+      place_by_groups<BLOCK, 2048>(bufA, static_cast<int>(k), all_or ^ all_and, lo, hi, bufB, whist,
+                                   whist + 2048, whist + 4096, s_tmp, ~0u, a, row, k, 0, 0, k);
+    else
+      place_by_groups<BLOCK, 256>(bufA, static_cast<int>(k), all_or ^ all_and, lo, hi, bufB, hist, gbase,
+                                  part, s_tmp, ~0u, a, row, k, 0, 0, k);
     TK_STAMP(24);
-    if (tid < k) {
-      const int64_t oi = row * k + tid;
-      const uint64_t pos = position_of(v, a.ib);
-      a.out_idx[oi] = static_cast<int64_t>(pos);
-      const uint32_t vk = vkey_of(v, a.ib) ^ a.flip;
-      if (a.key_bits == 32) {
-        static_cast<uint32_t*>(a.out_vals)[oi] =
-            (vk == Dt<kF32>::kZeroKey || vk == Dt<kF32>::kNanKey)
-                ? __ldg(static_cast<const uint32_t*>(a.x) + row * a.len + pos)
-                : value_bits_f32(vk);
-      } else {
-        static_cast<uint16_t*>(a.out_vals)[oi] =
-            (vk == Dt<kBF16>::kZeroKey || vk == Dt<kBF16>::kNanKey)
-                ? __ldg(static_cast<const uint16_t*>(a.x) + row * a.len + pos)
-                : static_cast<uint16_t>(value_bits_bf16(vk));
-      }
-    }
     return;
   }
+
+  // ------------------------------------------------------------------ large k
+  // Each CTA owns the output places [my0, my0 + n_mine).  The winners are
+  // partitioned once by their 11 most significant varying bits: exact bin
+  // counts are exchanged over DSMEM, every key is written to its bin's
+  // segment of the exchange buffer, and each CTA then sorts only the bins
+  // that overlap its places, locally.  If some CTA's bins do not fit in its
+  // shared memory (a pathological bin), the cluster falls back to an LSD
+  // radix sort over evenly split chunks.
   const unsigned long long vary = all_or ^ all_and;
+  const int hb = vary ? 63 - __clzll(static_cast<long long>(vary)) : 0;
+  const int64_t pe = (k + G - 1) / G;
+  const int64_t my0 = static_cast<int64_t>(crank) * pe;
+  const int n_mine = static_cast<int>(my0 >= k ? 0 : (k - my0 < pe ? k - my0 : pe));
+  for (int i = tid; i < n_mine; i += BLOCK) bufA[i] = __ldcg(xb + my0 + i);
+  __syncthreads();
+  bool local_sort = (G == 1);
+  int64_t ext0 = my0;
+  int n_c = n_mine;
+  if (G > 1 && BLOCK == 1024) {
+    const int psh = hb >= 10 ? hb - 10 : 0;
+    unsigned* lh = whist;           // local count per bin (read by the other CTAs)
+    unsigned* bst = whist + 2048;   // first place of each bin (the end of the last one is k)
+    unsigned* off = whist + 4096;   // this CTA's first place inside each bin
+    unsigned* cur = whist + 6144;   // fill cursors
+    for (int i = tid; i < 2048; i += BLOCK) { lh[i] = 0u; cur[i] = 0u; }
+    __syncthreads();
+    for (int i = tid; i < n_mine; i += BLOCK) atomicAdd(&lh[2047u - ((bufA[i] >> psh) & 2047u)], 1u);
+    cluster.sync();
+    {
+      unsigned tt[2], bm[2];
+      unsigned long long tsum = 0;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int b = tid * 2 + q;
+        unsigned t = 0, before = 0;
+        for (unsigned c = 0; c < G; ++c) {
+          const unsigned h = cluster.map_shared_rank(lh, c)[b];
+          t += h;
+          if (c < crank) before += h;
+        }
+        tt[q] = t;
+        bm[q] = before;
+        tsum += t;
+      }
+      const unsigned long long incl = block_scan_incl(tsum, s_tmp);
+      unsigned run = static_cast<unsigned>(incl - tsum);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int b = tid * 2 + q;
+        bst[b] = run;
+        off[b] = run + bm[q];
+        run += tt[q];
+      }
+    }
+    cluster.sync();  // every CTA has read the others' counts
+    uint64_t* xb1 = xb + k;
+    for (int i = tid; i < n_mine; i += BLOCK) {
+      const uint64_t key = bufA[i];
+      const unsigned bi = 2047u - static_cast<unsigned>((key >> psh) & 2047u);
+      xb1[off[bi] + atomicAdd(&cur[bi], 1u)] = key;
+    }
+    // extended range of every CTA: from the start of the bin holding its
+    // first place to the end of the bin holding its last place
+    __shared__ unsigned s_ext[2 * 16];
+    __shared__ int s_fit;
+    if (tid == 0) s_fit = 1;
+    __syncthreads();
+    if (tid < static_cast<int>(G)) {
+      const int64_t c0 = static_cast<int64_t>(tid) * pe;
+      const int64_t c1 = c0 + pe < k ? c0 + pe : k;
+      unsigned e0 = 0, e1 = 0;
+      if (c0 < k) {
+        // bin holding place p: the last b with bst[b] <= p (empty bins have
+        // no place, so the first b with bst[b] > p follows the right one)
+        auto bin_of = [&](unsigned p) {
+          int lo2 = 0, hi2 = 2048;
+          while (lo2 < hi2) {
+            const int mid = (lo2 + hi2) >> 1;
+            if (bst[mid] <= p) lo2 = mid + 1; else hi2 = mid;
+          }
+          return lo2 - 1;
+        };
+        e0 = bst[bin_of(static_cast<unsigned>(c0))];
+        const int b1 = bin_of(static_cast<unsigned>(c1 - 1)) + 1;
+        e1 = b1 < 2048 ? bst[b1] : static_cast<unsigned>(k);
+      }
+      s_ext[2 * tid] = e0;
+      s_ext[2 * tid + 1] = e1;
+      if (e1 - e0 > static_cast<unsigned>(P)) atomicAnd(&s_fit, 0);
+    }
+    cluster.sync();  // the bins are complete in the exchange buffer
+    if (s_fit) {
+      local_sort = true;
+      ext0 = s_ext[2 * crank];
+      n_c = static_cast<int>(s_ext[2 * crank + 1] - s_ext[2 * crank]);
+      for (int i = tid; i < n_c; i += BLOCK) bufA[i] = __ldcg(xb1 + ext0 + i);
+      __syncthreads();
+    }
+  }
+  TK_STAMP(15);
+  TK_CTA(1, globaltimer_ns());
+  if constexpr (BLOCK >= 1024) if (local_sort) {
+    unsigned long long lo_or, lo_and;
+    block_or_and<BLOCK>(bufA, n_c, &lo_or, &lo_and);
+    if (place_by_groups<BLOCK, 2048>(bufA, n_c, lo_or ^ lo_and, 0u, ~0u, bufB, whist, whist + 2048,
+                                     whist + 4096, s_tmp, 512u, a, row, k, ext0, my0, my0 + n_mine)) {
+      TK_STAMP(24);
+      TK_CTA(2, globaltimer_ns());
+      TK_CTA(3, 1ull);
+      return;
+    }
+  }
+  const unsigned sortG = local_sort ? 1u : G;  // CTAs taking part in each sort pass
+
+  // ------------------------------------------------------------------ sort
   uint64_t* src = bufA;
   uint64_t* dst = bufB;
   const int ipw = (n_c + L::kWarps - 1) / L::kWarps;  // items per warp segment
@@ -645,10 +843,14 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
     TK_STAMP(31);
     unsigned long long tot = 0, before_me = 0;
     if (tid < 256) {
-      for (unsigned c = 0; c < sortG; ++c) {
-        const unsigned h = cluster.map_shared_rank(hist, c)[tid];
-        tot += h;
-        if (c < crank) before_me += h;
+      if (sortG == 1) {
+        tot = hist[tid];  // this CTA sorts alone
+      } else {
+        for (unsigned c = 0; c < sortG; ++c) {
+          const unsigned h = cluster.map_shared_rank(hist, c)[tid];
+          tot += h;
+          if (c < crank) before_me += h;
+        }
       }
     }
     const unsigned long long incl = block_scan_incl(tot, s_tmp);
@@ -682,29 +884,18 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
 
   // ------------------------------------------------------------------ output
   TK_STAMP(24);
-  const int64_t obase = row * k + my0;
+  // local index i holds place ext0 + i; this CTA writes the places it owns
   for (int i = tid; i < n_c; i += BLOCK) {
-    const uint64_t key = src[i];
-    const uint64_t pos = position_of(key, a.ib);
-    a.out_idx[obase + i] = static_cast<int64_t>(pos);
-    const uint32_t vk = vkey_of(key, a.ib) ^ a.flip;
-    if (a.key_bits == 32) {
-      const uint32_t bits = (vk == Dt<kF32>::kZeroKey || vk == Dt<kF32>::kNanKey)
-                                ? __ldg(static_cast<const uint32_t*>(a.x) + row * a.len + pos)
-                                : value_bits_f32(vk);
-      static_cast<uint32_t*>(a.out_vals)[obase + i] = bits;
-    } else {
-      const uint16_t bits = (vk == Dt<kBF16>::kZeroKey || vk == Dt<kBF16>::kNanKey)
-                                ? __ldg(static_cast<const uint16_t*>(a.x) + row * a.len + pos)
-                                : static_cast<uint16_t>(value_bits_bf16(vk));
-      static_cast<uint16_t*>(a.out_vals)[obase + i] = bits;
-    }
+    const int64_t place = ext0 + i;
+    if (place >= my0 && place < my0 + n_mine) write_out(a, row, k, place, src[i]);
   }
+  TK_CTA(2, globaltimer_ns());
+  TK_CTA(3, 2ull + static_cast<unsigned long long>(n_c));
 }
 
 // Kernel variants: (block, sort positions per CTA, cache/second buffer).
 constexpr int kSmallBlock = 256, kSmallP = 1024, kSmallCB = 2048;
-constexpr int kBigBlock = 1024, kBigP = 8192, kBigCB = 14336;
+constexpr int kBigBlock = 1024, kBigP = 12000, kBigCB = 12000;
 constexpr int kMaxCluster = 16;
 
 template <int BLOCK, int P, int CB, int SRC>
@@ -799,7 +990,8 @@ int64_t select_max_k() { return static_cast<int64_t>(kMaxCluster) * kBigP; }
 
 #ifdef TK_PHASE_TIMING
 int debug_phase_ns(unsigned long long* out) {
-  return cudaMemcpyFromSymbol(out, g_phase_ns, sizeof(g_phase_ns)) == cudaSuccess ? 0 : -3;
+  if (cudaMemcpyFromSymbol(out, g_phase_ns, sizeof(g_phase_ns)) != cudaSuccess) return -3;
+  return cudaMemcpyFromSymbol(out + 64, g_cta_ns, sizeof(g_cta_ns)) == cudaSuccess ? 0 : -3;  // 2*16*8
 }
 #endif
 
