@@ -4,11 +4,11 @@
 // filter_kernel streams every selection once and appends the composite key of
 // each element ranking at or above tau to the candidate buffer.  It is the
 // HBM-bound hot loop: a persistent grid walks 16 KB tiles with 16-byte
-// read-only loads; a float compare against tau's value is the common-path
-// test, and only when some lane of a warp sees a candidate does the warp build
-// exact composite keys.  Survivors are ranked with __ballot_sync/__popc
-// (the warp flag ranks of "One Bit at a Time") into a per-warp shared-memory
-// stage, which is flushed with one global atomicAdd per 256 survivors.  The
+// read-only loads; one NaN-propagating max (min) per 16 bytes and a float
+// compare against tau's value is the common-path test.  Only a lane whose
+// group holds a candidate builds exact composite keys, and it appends its
+// survivors to its warp's shared-memory stage with one shared atomic; the
+// stage is flushed at tile ends with one global atomicAdd per flush.  The
 // counter keeps counting past the capacity M so R is exact; only slots < M are
 // written.
 //
@@ -35,6 +35,29 @@ constexpr int kFilterUnroll = 4;
 constexpr int kWarpStage = 256;  // survivors staged per warp before a flush
 constexpr unsigned kFull = 0xffffffffu;
 
+// Division by the invariant tiles-per-row count without a divide instruction
+// (Granlund and Montgomery, "Division by Invariant Integers using
+// Multiplication", the round-up multiplier of their section 4): with
+// l = ceil(log2 d) and m = floor(2^64 (2^l - d) / d) + 1,
+// n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0) where t = mulhi(m, n).
+struct Divider {
+  uint64_t m;
+  uint32_t s1, s2;
+};
+
+Divider make_divider(uint64_t d) {
+  int l = 0;
+  while (l < 63 && (1ull << l) < d) ++l;
+  const unsigned __int128 two64 = static_cast<unsigned __int128>(1) << 64;
+  const uint64_t m = static_cast<uint64_t>(two64 * ((1ull << l) - d) / d + 1);
+  return Divider{m, static_cast<uint32_t>(l < 1 ? l : 1), static_cast<uint32_t>(l > 1 ? l - 1 : 0)};
+}
+
+__device__ __forceinline__ uint64_t divide(uint64_t n, const Divider& dv) {
+  const uint64_t t = __umul64hi(dv.m, n);
+  return (t + ((n - t) >> dv.s1)) >> dv.s2;
+}
+
 struct FilterParams {
   const void* x;
   int64_t nsel, len;
@@ -44,6 +67,7 @@ struct FilterParams {
   int64_t cap;
   uint64_t* buf;
   unsigned long long* counts;
+  Divider tiles_per_row;  // set by the launcher for its tile size
 };
 
 // Element e of a packed group of raw words (VEC elements).
@@ -84,6 +108,35 @@ __device__ __forceinline__ uint32_t bmin2_nan(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Packed bf16x2 compares: each 16-bit half of the result is all ones where the
+// compare holds.  gtu holds for NaN too; lt and eq do not.
+__device__ __forceinline__ uint32_t bset_gtu(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("set.gtu.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bset_lt(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("set.lt.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bset_eq(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("set.eq.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Eight per-element compare results of a bf16 group (four packed words, each
+// half 0xffff or 0) -> an 8-bit mask, bit e for element e.
+__device__ __forceinline__ uint32_t halves_to_mask(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+  // one byte per element (0xff or 0): the high byte of each half
+  const uint32_t lo = __byte_perm(a0, a1, 0x7531);  // elements 0..3
+  const uint32_t hi = __byte_perm(a2, a3, 0x7531);  // elements 4..7
+  // keep bit e in byte e of lo and bit e+4 in byte e of hi, then add the bytes
+  const uint32_t b = (lo & 0x08040201u) | (hi & 0x80402010u);
+  return (b * 0x01010101u) >> 24;
+}
+
 // Superset test for a group: does any element rank at or above tau's value?
 // One NaN-propagating max (largest) or min (smallest) over the group and one
 // compare; NaN elements always pass here (the exact test sorts them out).
@@ -118,6 +171,7 @@ struct RowTau {
   uint64_t key;   // composite key
   uint64_t pos;   // position of the element it came from
   float value;    // its value (0 for the zero key)
+  uint32_t v2;    // bf16: the value's bits in both halves of a word
   bool nan;       // tau's value is NaN: fall back to composite-key compares
 };
 
@@ -129,91 +183,130 @@ __device__ __forceinline__ RowTau row_tau(uint64_t tau, int ib, uint32_t flip) {
   const uint32_t k = vkey_of(tau, ib) ^ flip;
   r.nan = (k == Dt<DT>::kNanKey);
   r.value = (k == Dt<DT>::kZeroKey || r.nan) ? 0.0f : Dt<DT>::to_float(Dt<DT>::bits(k));
+  const uint32_t b16 = __float_as_uint(r.value) >> 16;  // exact for a bf16 value
+  r.v2 = (b16 << 16) | b16;
   return r;
 }
 
-__device__ __forceinline__ uint32_t warp_flush(uint64_t* s, uint32_t n, int64_t row, int64_t cap,
-                                               uint64_t* buf, unsigned long long* counts) {
-  if (n == 0) return 0;
-  const int lane = threadIdx.x & 31;
-  unsigned long long base = 0;
-  if (lane == 0) base = atomicAdd(counts + row, static_cast<unsigned long long>(n));
-  base = __shfl_sync(kFull, base, 0);
-  __syncwarp();
-  uint64_t* dst = buf + row * cap;
-  for (uint32_t j = lane; j < n; j += 32) {
-    const unsigned long long pos = base + j;
-    if (pos < static_cast<unsigned long long>(cap)) dst[pos] = s[j];
-  }
-  __syncwarp();
-  return 0;
-}
+// A warp's survivor stage: slots in shared memory and a fill counter that the
+// warp's lanes advance with shared atomics.
+struct Stage {
+  uint64_t* s;
+  unsigned* n;
+};
 
-// Exact test of one group for a warp that saw a candidate (rare, kept out of
-// line so the streaming loop stays small).  In the value domain an element
-// passes when it ranks strictly above tau's value, or ties with it at a
-// position <= tau's (the composite-key order).  Each lane counts its
-// survivors, a warp prefix sum gives every lane its slots in the warp's stage.
-// Returns the stage's new fill.
-template <int DT, bool LARGEST, int VEC>
-__device__ __noinline__ uint32_t group_exact(uint4 v, int64_t pos, bool cand, RowTau t, int ib, uint32_t flip,
-                                             uint64_t* s, uint32_t n, int64_t row, int64_t cap, uint64_t* buf,
-                                             unsigned long long* counts) {
-  uint32_t mask = 0;
-  if (cand) {
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      const uint32_t raw = elem<DT, VEC>(v, e);
-      const float f = Dt<DT>::to_float(raw);
-      const uint64_t p = static_cast<uint64_t>(pos + e);
-      bool pass;
-      if (t.nan) {
-        pass = compose(Dt<DT>::key(raw) ^ flip, p, ib) >= t.key;
-      } else if (LARGEST) {
-        pass = (f > t.value) || (f != f) || (f == t.value && p <= t.pos);
-      } else {
-        pass = (f < t.value) || (f == t.value && p <= t.pos);
-      }
-      mask |= static_cast<uint32_t>(pass) << e;
+// Moves the stage to the candidate buffer: one global atomic reserves the
+// slots (the counter keeps counting past the capacity, so R stays exact; only
+// slots below the capacity are written).  Called by the whole warp.
+__device__ __forceinline__ void stage_flush(const Stage& st, int64_t row, int64_t cap, uint64_t* buf,
+                                            unsigned long long* counts) {
+  __syncwarp();
+  const unsigned filled = *st.n;
+  const unsigned n = filled < static_cast<unsigned>(kWarpStage) ? filled : static_cast<unsigned>(kWarpStage);
+  if (n) {
+    const int lane = threadIdx.x & 31;
+    unsigned long long base = 0;
+    if (lane == 0) base = atomicAdd(counts + row, static_cast<unsigned long long>(n));
+    base = __shfl_sync(kFull, base, 0);
+    uint64_t* dst = buf + row * cap;
+    for (unsigned j = lane; j < n; j += 32) {
+      const unsigned long long pos = base + j;
+      if (pos < static_cast<unsigned long long>(cap)) dst[pos] = st.s[j];
     }
   }
-  const int lane = threadIdx.x & 31;
-  const uint32_t cnt = __popc(mask);
-  uint32_t incl = cnt;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) *st.n = 0u;
+  __syncwarp();
+}
+
+// Exact test of one group: bit e is set when element e ranks at or above
+// tau, i.e. its value ranks strictly above tau's value, or equals it at a
+// position <= tau's (the composite-key order).  Packed compares give the
+// "above" and "equal" masks; the position test runs only for ties.
+template <int DT, bool LARGEST, int VEC>
+__device__ __forceinline__ uint32_t exact_mask(const uint4& v, int64_t pos, const RowTau& t, int ib,
+                                               uint32_t flip) {
+  uint32_t above = 0, equal = 0;
+  if (t.nan) {  // only NaN keys tie with tau: compare composite keys
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
+    for (int e = 0; e < VEC; ++e)
+      above |= static_cast<uint32_t>(compose(Dt<DT>::key(elem<DT, VEC>(v, e)) ^ flip,
+                                             static_cast<uint64_t>(pos + e), ib) >= t.key) << e;
+    return above;
   }
-  const uint32_t total = __shfl_sync(kFull, incl, 31);
-  if (total == 0) return n;
-  if (n + total > static_cast<uint32_t>(kWarpStage)) n = warp_flush(s, n, row, cap, buf, counts);
-  uint32_t off = n + incl - cnt;
+  if (DT == kBF16 && VEC == 8) {
+    const uint32_t tv = t.v2;
+    above = LARGEST ? halves_to_mask(bset_gtu(v.x, tv), bset_gtu(v.y, tv), bset_gtu(v.z, tv), bset_gtu(v.w, tv))
+                    : halves_to_mask(bset_lt(v.x, tv), bset_lt(v.y, tv), bset_lt(v.z, tv), bset_lt(v.w, tv));
+    equal = halves_to_mask(bset_eq(v.x, tv), bset_eq(v.y, tv), bset_eq(v.z, tv), bset_eq(v.w, tv));
+  } else {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const float f = Dt<DT>::to_float(elem<DT, VEC>(v, e));
+      above |= static_cast<uint32_t>(LARGEST ? !(f <= t.value) : (f < t.value)) << e;
+      equal |= static_cast<uint32_t>(f == t.value) << e;
+    }
+  }
+  while (equal) {  // ties with tau's value: the lower position ranks higher
+    const int e = __ffs(equal) - 1;
+    equal &= equal - 1;
+    if (static_cast<uint64_t>(pos + e) <= t.pos) above |= 1u << e;
+  }
+  return above;
+}
+
+// Appends the elements of `mask` to the warp's stage with one shared atomic;
+// what does not fit is appended to the buffer directly.
+template <int DT, int VEC>
+__device__ __forceinline__ void lane_append(uint32_t mask, const uint4& v, int64_t pos, int ib, uint32_t flip,
+                                            const Stage& st, int64_t row, int64_t cap, uint64_t* buf,
+                                            unsigned long long* counts) {
+  const unsigned n = __popc(mask);
+  const unsigned slot = atomicAdd(st.n, n);
+  const unsigned fit = slot >= static_cast<unsigned>(kWarpStage)
+                           ? 0u
+                           : (slot + n <= static_cast<unsigned>(kWarpStage) ? n : kWarpStage - slot);
+  unsigned long long gbase = 0;
+  if (fit < n) gbase = atomicAdd(counts + row, static_cast<unsigned long long>(n - fit));
+  unsigned j = 0;
   while (mask) {
     const int e = __ffs(mask) - 1;
     mask &= mask - 1;
-    s[off++] = compose(Dt<DT>::key(elem<DT, VEC>(v, e)) ^ flip, static_cast<uint64_t>(pos + e), ib);
+    const uint64_t key = compose(Dt<DT>::key(elem<DT, VEC>(v, e)) ^ flip, static_cast<uint64_t>(pos + e), ib);
+    if (j < fit) {
+      st.s[slot + j] = key;
+    } else {
+      const unsigned long long q = gbase + (j - fit);
+      if (q < static_cast<unsigned long long>(cap)) buf[row * cap + q] = key;
+    }
+    ++j;
   }
-  __syncwarp();
-  return n + total;
+}
+
+template <int DT, bool LARGEST, int VEC>
+__device__ __forceinline__ void test_group(const uint4& v, int64_t pos, const RowTau& t, const FilterParams& fp,
+                                           const Stage& st, int64_t row) {
+  if (group_candidate<DT, LARGEST, VEC>(v, t.value) || t.nan) {
+    const uint32_t mask = exact_mask<DT, LARGEST, VEC>(v, pos, t, fp.ib, fp.flip);
+    if (mask) lane_append<DT, VEC>(mask, v, pos, fp.ib, fp.flip, st, row, fp.cap, fp.buf, fp.counts);
+  }
 }
 
 // Filter the tiles [tile_begin, tile_end) (stride tile_step) of the flattened
 // tile space (selection-major).  Used by the filter kernel and the fallback.
 template <int DT, bool LARGEST, int VEC>
 __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t tile_end,
-                             int64_t tile_step, uint64_t* stage) {
+                             int64_t tile_step, const Stage& st) {
   using T = typename Dt<DT>::storage;
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   const int64_t tiles_per_row = (fp.len + kTile - 1) / kTile;
   int64_t cur_row = -1;
   RowTau t{};
-  uint32_t n = 0;
   for (int64_t tile = tile_begin; tile < tile_end; tile += tile_step) {
-    const int64_t row = tile / tiles_per_row;
+    const int64_t row = static_cast<int64_t>(divide(static_cast<uint64_t>(tile), fp.tiles_per_row));
     const int64_t base = (tile - row * tiles_per_row) * kTile;
     if (row != cur_row) {
-      if (cur_row >= 0) n = warp_flush(stage, n, cur_row, fp.cap, fp.buf, fp.counts);
+      if (cur_row >= 0) stage_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
       cur_row = row;
       t = row_tau<DT>(__ldcg(fp.tau + row), fp.ib, fp.flip);
     }
@@ -224,37 +317,37 @@ __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t
       for (int u = 0; u < kFilterUnroll; ++u)
         v[u] = load_group<DT, VEC>(xr + base + (u * kFilterBlock + threadIdx.x) * VEC);
 #pragma unroll
-      for (int u = 0; u < kFilterUnroll; ++u) {
-        const bool c = group_candidate<DT, LARGEST, VEC>(v[u], t.value) || t.nan;
-        if (__any_sync(kFull, c)) {
-          const int64_t pos = base + (u * kFilterBlock + threadIdx.x) * VEC;
-          n = group_exact<DT, LARGEST, VEC>(v[u], pos, c, t, fp.ib, fp.flip, stage, n, row, fp.cap, fp.buf,
-                                            fp.counts);
-        }
-      }
+      for (int u = 0; u < kFilterUnroll; ++u)
+        test_group<DT, LARGEST, VEC>(v[u], base + (u * kFilterBlock + threadIdx.x) * VEC, t, fp, st, row);
     } else {  // the last, partial tile of a selection
 #pragma unroll
       for (int u = 0; u < kFilterUnroll; ++u) {
         const int64_t pos = base + (u * kFilterBlock + threadIdx.x) * VEC;
-        const bool ok = pos < fp.len;
-        v[u] = ok ? load_group<DT, VEC>(xr + pos) : make_uint4(0u, 0u, 0u, 0u);
-        const bool c = ok && (group_candidate<DT, LARGEST, VEC>(v[u], t.value) || t.nan);
-        if (__any_sync(kFull, c))
-          n = group_exact<DT, LARGEST, VEC>(v[u], pos, c, t, fp.ib, fp.flip, stage, n, row, fp.cap, fp.buf,
-                                            fp.counts);
+        if (pos < fp.len) {
+          v[u] = load_group<DT, VEC>(xr + pos);
+          test_group<DT, LARGEST, VEC>(v[u], pos, t, fp, st, row);
+        }
       }
     }
+    // a warp-uniform point: move the stage out once it is half full
+    __syncwarp();
+    if (__shfl_sync(kFull, *st.n, 0) >= static_cast<unsigned>(kWarpStage / 2))
+      stage_flush(st, row, fp.cap, fp.buf, fp.counts);
   }
-  if (cur_row >= 0) warp_flush(stage, n, cur_row, fp.cap, fp.buf, fp.counts);
+  if (cur_row >= 0) stage_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
 }
 
 template <int DT, bool LARGEST, int VEC>
 __global__ void __launch_bounds__(kFilterBlock) filter_kernel(FilterParams fp) {
   __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
+  __shared__ unsigned stage_n[kFilterBlock / 32];
   grid_dependency_wait();  // tau and the zeroed counters come from the previous grid
+  if ((threadIdx.x & 31) == 0) stage_n[threadIdx.x >> 5] = 0u;
+  __syncwarp();
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
-  filter_tiles<DT, LARGEST, VEC>(fp, blockIdx.x, ntiles, gridDim.x, stage[threadIdx.x >> 5]);
+  const Stage st{stage[threadIdx.x >> 5], &stage_n[threadIdx.x >> 5]};
+  filter_tiles<DT, LARGEST, VEC>(fp, blockIdx.x, ntiles, gridDim.x, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -334,6 +427,7 @@ __global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a
   using T = typename Dt<DT>::storage;
   constexpr int kVKB = Dt<DT>::kKeyBits;
   __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
+  __shared__ unsigned stage_n[kFilterBlock / 32];
   __shared__ unsigned shist[kFilterBlock / 32][256];
   __shared__ unsigned scan_tmp[32];
   __shared__ unsigned s_total;
@@ -487,8 +581,11 @@ __global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a
     // -- phase C: filter the selection again with the exact threshold
     constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
     const int64_t tiles_per_row = (fp.len + kTile - 1) / kTile;
+    if ((threadIdx.x & 31) == 0) stage_n[threadIdx.x >> 5] = 0u;
+    __syncwarp();
+    const Stage st{stage[threadIdx.x >> 5], &stage_n[threadIdx.x >> 5]};
     filter_tiles<DT, LARGEST, VEC>(fp, row * tiles_per_row + blockIdx.x, (row + 1) * tiles_per_row,
-                                   gridDim.x, stage[threadIdx.x >> 5]);
+                                   gridDim.x, st);
   }
 }
 
@@ -509,6 +606,8 @@ template <int DT, bool LARGEST, int VEC>
 cudaError_t launch_filter_t(const FilterParams& fp, cudaStream_t st) {
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
+  FilterParams args = fp;
+  args.tiles_per_row = make_divider(static_cast<uint64_t>((fp.len + kTile - 1) / kTile));
   int64_t grid = filter_grid_size<DT, LARGEST, VEC>();
   if (grid > ntiles) grid = ntiles;
   if (grid < 1) grid = 1;
@@ -521,7 +620,7 @@ cudaError_t launch_filter_t(const FilterParams& fp, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, filter_kernel<DT, LARGEST, VEC>, fp);
+  return cudaLaunchKernelEx(&cfg, filter_kernel<DT, LARGEST, VEC>, args);
 }
 
 template <int DT, bool LARGEST, int VEC>
@@ -539,6 +638,8 @@ cudaError_t launch_fallback_t(const FallbackParams& a, cudaStream_t st) {
     grid = static_cast<unsigned>(sms * per_sm);
   }
   FallbackParams args = a;
+  constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
+  args.fp.tiles_per_row = make_divider(static_cast<uint64_t>((a.fp.len + kTile - 1) / kTile));
   void* kargs[] = {&args};
   return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(fallback_kernel<DT, LARGEST, VEC>), grid,
                                      kFilterBlock, kargs, 0, st);
@@ -548,7 +649,7 @@ cudaError_t launch_fallback_t(const FallbackParams& a, cudaStream_t st) {
 
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
                           unsigned long long* counts, cudaStream_t st) {
-  FilterParams fp{p.x, p.nsel, p.len, p.ib, p.flip, tau, cap, buf, counts};
+  FilterParams fp{p.x, p.nsel, p.len, p.ib, p.flip, tau, cap, buf, counts, Divider{}};
   const bool largest = p.flip == 0;
   if (p.dtype == kF32) {
     if (p.vec_ok) return largest ? launch_filter_t<kF32, true, 4>(fp, st) : launch_filter_t<kF32, false, 4>(fp, st);
@@ -562,7 +663,7 @@ cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* 
                             unsigned long long* counts, const FallbackScratch& fs, int force,
                             cudaStream_t st) {
   // the re-filter reads the exact threshold the fallback itself writes
-  FallbackParams a{{p.x, p.nsel, p.len, p.ib, p.flip, fs.tau_exact, cap, buf, counts}, k, force, fs};
+  FallbackParams a{{p.x, p.nsel, p.len, p.ib, p.flip, fs.tau_exact, cap, buf, counts, Divider{}}, k, force, fs};
   const bool largest = p.flip == 0;
   if (p.dtype == kF32) {
     if (p.vec_ok) return largest ? launch_fallback_t<kF32, true, 4>(a, st) : launch_fallback_t<kF32, false, 4>(a, st);
