@@ -124,7 +124,7 @@ void topk_options_init(topk_options_t* opt);
  * out_idx[r*k + j].  eps in [0, 1) is the target probability that a row takes
  * the fallback (Theorem 3); eps == 0 selects exactly without sampling.  The
  * result never depends on eps or on the sampler.
- *   Limits: n < 2^31; k <= 192000 (EUNSUPPORTED beyond); rows == 0 is a no-op.
+ *   Limits: n < 2^31; k <= 188416 (EUNSUPPORTED beyond); rows == 0 is a no-op.
  *   EINVAL: null pointer (with rows > 0), rows < 0, n < 1, k < 1, k > n,
  *           eps outside [0, 1), unknown dtype.
  */
@@ -136,7 +136,7 @@ int topk_select(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, in
  * flattened into one vector of N = B*d_dict and the K = B*k largest are kept).
  * Treats the rows*n elements as one vector: out_vals[j], out_idx_flat[j] for
  * j < k, with flat positions r*n + c.
- *   Limits: rows*n <= 2^32 for F32 and <= 2^48 for BF16; k <= 192000.
+ *   Limits: rows*n <= 2^32 for F32 and <= 2^48 for BF16; k <= 188416.
  *   EINVAL as topk_select, with k > rows*n in place of k > n.
  */
 int topk_select_global(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,

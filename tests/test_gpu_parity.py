@@ -110,7 +110,7 @@ def test_rows_zero_is_a_noop():
 
 def test_maximum_k_cluster_sort():
     tk = _tk()
-    kmax = 16 * 12000
+    kmax = 16 * 11776
     x = workloads.make("normal", 1, 1 << 20, seed=9)
     _check(x, kmax, eps=1e-3)
     with pytest.raises(tk.TopkError):

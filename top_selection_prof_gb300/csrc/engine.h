@@ -20,9 +20,9 @@ struct Problem {
 };
 
 // ---- parameters (params.cpp) -------------------------------------------------
-// Programmatic dependent launch between the pipeline's kernels; off unless
-// TOPK_ENABLE_PDL=1 (measured slower on the single-row pipeline).
-bool pdl_enabled();
+// Programmatic dependent launch for one pipeline edge (see params.cpp).
+constexpr unsigned kPdlTau = 1, kPdlFilter = 2, kPdlFallback = 4, kPdlRefine = 8;
+bool pdl_edge(unsigned bit);
 struct ParamRule {
   int64_t s_min = 32768, s_max = 131072;
   double cost_ratio = 1.0;
@@ -52,8 +52,17 @@ cudaError_t launch_sample(const Problem& p, int64_t S, uint64_t seed, uint64_t c
                           cudaStream_t st);
 
 // ---- filter and fallback (kernels_filter.cu) ---------------------------------
+// SMs a threshold select of nsel clusters of G blocks holds while the filter
+// launches, or -1 when it spans too many SMs to overlap.
+inline int overlap_sms(int G, int64_t nsel) {
+  const int64_t held = static_cast<int64_t>(G) * nsel;
+  return held <= 16 ? static_cast<int>(held) : -1;
+}
+
+// reserved_sms: SMs the preceding grid (the threshold select) holds; the
+// launch may overlap that grid only when it is >= 0.
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
-                          unsigned long long* counts, cudaStream_t st);
+                          unsigned long long* counts, int reserved_sms, cudaStream_t st);
 
 struct FallbackScratch {
   unsigned* ghist;        // 8 passes x 256 counters

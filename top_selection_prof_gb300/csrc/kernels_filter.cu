@@ -437,6 +437,7 @@ __global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a
 
   const FilterParams& fp = a.fp;
   const FallbackScratch& fs = a.fs;
+  grid_dependency_wait();    // the survivor counts come from the filter
   grid_launch_dependents();  // the final selection may start launching
   const int warp = threadIdx.x >> 5;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -589,26 +590,32 @@ __global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a
   }
 }
 
+// One full wave: SMs x resident blocks per SM, less the SMs held by the
+// preceding grid when this launch may overlap it (programmatic dependent
+// launch): the tiles are dealt out by block index, so every block must start
+// at once.
 template <int DT, bool LARGEST, int VEC>
-int filter_grid_size() {
-  static int cached = 0;
-  if (cached) return cached;
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, filter_kernel<DT, LARGEST, VEC>, kFilterBlock, 0);
-  if (per_sm < 1) per_sm = 1;
-  cached = sms * per_sm;
-  return cached;
+int filter_grid_size(int reserved_sms) {
+  static int sms = 0, per_sm = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, filter_kernel<DT, LARGEST, VEC>, kFilterBlock, 0);
+    if (per_sm < 1) per_sm = 1;
+  }
+  const int usable = sms - reserved_sms > sms / 2 ? sms - reserved_sms : sms / 2;
+  return usable * per_sm;
 }
 
 template <int DT, bool LARGEST, int VEC>
-cudaError_t launch_filter_t(const FilterParams& fp, cudaStream_t st) {
+cudaError_t launch_filter_t(const FilterParams& fp, int reserved_sms, cudaStream_t st) {
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
   FilterParams args = fp;
   args.tiles_per_row = make_divider(static_cast<uint64_t>((fp.len + kTile - 1) / kTile));
-  int64_t grid = filter_grid_size<DT, LARGEST, VEC>();
+  const bool pdl = reserved_sms >= 0 && pdl_edge(kPdlFilter);
+  int64_t grid = filter_grid_size<DT, LARGEST, VEC>(pdl ? reserved_sms : 0);
   if (grid > ntiles) grid = ntiles;
   if (grid < 1) grid = 1;
   cudaLaunchConfig_t cfg = {};
@@ -619,7 +626,7 @@ cudaError_t launch_filter_t(const FilterParams& fp, cudaStream_t st) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, filter_kernel<DT, LARGEST, VEC>, args);
 }
 
@@ -640,23 +647,32 @@ cudaError_t launch_fallback_t(const FallbackParams& a, cudaStream_t st) {
   FallbackParams args = a;
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   args.fp.tiles_per_row = make_divider(static_cast<uint64_t>((a.fp.len + kTile - 1) / kTile));
-  void* kargs[] = {&args};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(fallback_kernel<DT, LARGEST, VEC>), grid,
-                                     kFilterBlock, kargs, 0, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kFilterBlock, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the grid barrier needs every block resident
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_edge(kPdlFallback) ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, fallback_kernel<DT, LARGEST, VEC>, args);
 }
 
 }  // namespace
 
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
-                          unsigned long long* counts, cudaStream_t st) {
+                          unsigned long long* counts, int reserved_sms, cudaStream_t st) {
   FilterParams fp{p.x, p.nsel, p.len, p.ib, p.flip, tau, cap, buf, counts, Divider{}};
   const bool largest = p.flip == 0;
   if (p.dtype == kF32) {
-    if (p.vec_ok) return largest ? launch_filter_t<kF32, true, 4>(fp, st) : launch_filter_t<kF32, false, 4>(fp, st);
-    return largest ? launch_filter_t<kF32, true, 1>(fp, st) : launch_filter_t<kF32, false, 1>(fp, st);
+    if (p.vec_ok) return largest ? launch_filter_t<kF32, true, 4>(fp, reserved_sms, st) : launch_filter_t<kF32, false, 4>(fp, reserved_sms, st);
+    return largest ? launch_filter_t<kF32, true, 1>(fp, reserved_sms, st) : launch_filter_t<kF32, false, 1>(fp, reserved_sms, st);
   }
-  if (p.vec_ok) return largest ? launch_filter_t<kBF16, true, 8>(fp, st) : launch_filter_t<kBF16, false, 8>(fp, st);
-  return largest ? launch_filter_t<kBF16, true, 1>(fp, st) : launch_filter_t<kBF16, false, 1>(fp, st);
+  if (p.vec_ok) return largest ? launch_filter_t<kBF16, true, 8>(fp, reserved_sms, st) : launch_filter_t<kBF16, false, 8>(fp, reserved_sms, st);
+  return largest ? launch_filter_t<kBF16, true, 1>(fp, reserved_sms, st) : launch_filter_t<kBF16, false, 1>(fp, reserved_sms, st);
 }
 
 cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,

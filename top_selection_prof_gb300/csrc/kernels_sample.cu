@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(256) sample_kernel(const void* __restrict__ x,
                                                      unsigned long long* __restrict__ counts,
                                                      DevHeader* __restrict__ hdr) {
   using T = typename Dt<DT>::storage;
+  grid_launch_dependents();  // the threshold select may start launching
   const uint32_t row = blockIdx.y;
   const int64_t pair = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (pair == 0) {

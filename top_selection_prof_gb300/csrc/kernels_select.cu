@@ -4,31 +4,29 @@
 //   * threshold estimation (section 3, stage 2): the t-th largest of the S
 //     sampled composite keys -> tau;
 //   * refinement (section 3, stage 4): the exact top-k of the candidate buffer;
-//   * the direct path for small rows: the exact top-k of the row itself.
+//   * the direct path: the exact top-k of the row itself.
 //
-// Select: radix select from the most significant 8-bit digit of the composite
-// key ("count elements into buckets and recurse into the bucket that contains
-// the boundary", Find the Cutoff Instead).  Each CTA histograms its slice of
-// the source into per-warp shared-memory counters (warp-aggregated with
-// __match_any_sync, so equal digits never serialise on one address); the
-// cluster's CTAs read one another's histograms through distributed shared
-// memory, so every CTA finds the same boundary digit without global memory.
-// Slices are read with 16-byte loads, eight keys per thread in flight.  Once a
-// CTA's elements at or above the current prefix fit in shared memory it caches
-// them and stops re-reading the source.  When the boundary bucket holds at
-// most kGather keys, they are gathered into CTA 0 and ranked by counting
-// ("Rank by Counting": rank = number of larger keys, ties by position), which
-// ends the select without further digit passes.
+// Select: radix select ("count elements into buckets and recurse into the
+// bucket that contains the boundary", Find the Cutoff Instead) with 11-bit
+// digits (2048 bins; 8-bit in the 256-thread variant), starting below the
+// most significant bit on which the keys differ.  Each CTA histograms its
+// slice of the source into shared memory; the cluster's CTAs read one
+// another's counters through distributed shared memory, so every CTA finds
+// the same boundary bin with one cluster barrier per digit (the counters are
+// double-buffered).  Slices are cached in shared memory when they fit.  When
+// the boundary bucket is small it is gathered into CTA 0 and ranked by
+// counting ("Rank by Counting": rank = number of larger keys; the composite
+// keys are distinct, ties by position being built into them).
 //
-// Sort (top-k only): the k winners (keys >= the k-th key; keys are distinct)
-// are sorted by a stable LSD radix sort, descending, one 8-bit digit per pass,
-// skipping digits on which all winners agree.  If the winners fit in one CTA
-// they are gathered into CTA 0 and sorted there with block barriers only;
-// otherwise they are spread evenly over the cluster and every pass ranks a
-// CTA's items stably per warp, exchanges per-digit counts over DSMEM and
-// scatters each key straight into its destination CTA's shared memory.  The
-// composite key encodes (value descending, index ascending), so that is the
-// output order.
+// Sort (top-k only): the first digit's bins partition the k winners.  Every
+// CTA writes its winners into their bins' segments of an L2-resident
+// exchange buffer (offsets from the exchanged counts), then owns k/G output
+// places.  It reads the bins that overlap its places; a bin at either end
+// that would overflow shared memory is cut down, by further digits, to the
+// sub-bin holding the boundary place.  The keys in between are ranked by
+// counting inside groups of equal leading bits (a stable LSD radix sort if a
+// group is too large) and written to their places.  The composite key encodes
+// (value descending, index ascending), so that is the output order.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -41,8 +39,8 @@ namespace tk {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr unsigned kGather = 256;  // bucket size at which the select finishes by ranking
-constexpr int64_t kRankMax = 4096;  // winners sorted by counting ranks instead of radix passes
+constexpr int kMaxCluster = 16;
+constexpr bool kMergeFirstPass = false;  // warp-merged counting of the first digit
 
 #ifdef TK_PHASE_TIMING
 // Debug builds only: globaltimer stamps of the first cluster's CTA 0.
@@ -83,25 +81,6 @@ struct SelParams {
   int64_t* out_idx;
   int* status;
   uint64_t* xbuf;                     // 2*r keys per selection: the L2 exchange of the sort
-};
-
-template <int BLOCK, int P, int CB>
-struct Layout {
-  static constexpr int kWarps = BLOCK / 32;
-  static constexpr int kItems = (P + BLOCK - 1) / BLOCK;
-  static constexpr int kQuarters = BLOCK / 256;          // thread groups of 256 (one per digit)
-  static constexpr int kWarpsPerQuarter = kWarps / kQuarters;
-  static constexpr size_t kBufA = 0;
-  static constexpr size_t kBufB = kBufA + sizeof(uint64_t) * P;
-  static constexpr size_t kWhist = kBufB + sizeof(uint64_t) * CB;
-  static constexpr size_t kHist = kWhist + sizeof(unsigned) * kWarps * 256;
-  static constexpr size_t kGbase = kHist + sizeof(unsigned) * 256;
-  static constexpr size_t kPart = kGbase + sizeof(unsigned) * 256;
-  static constexpr size_t kXch = kPart + sizeof(unsigned) * kQuarters * 256;
-  static constexpr size_t kBytes = kXch + sizeof(unsigned long long) * 4;
-  static_assert(CB >= P, "cache buffer doubles as the second sort buffer");
-  static_assert(BLOCK % 256 == 0, "one thread per digit in each group of 256");
-  static_assert(kWarps * 256 * sizeof(unsigned) >= kGather * sizeof(uint64_t), "gather buffer");
 };
 
 // Eight consecutive source elements i0 .. i0+7 (i0 a multiple of 8) as
@@ -192,16 +171,6 @@ __device__ __forceinline__ void for_cache(const uint64_t* cache, unsigned n, F&&
   }
 }
 
-// Adds one to this warp's counter for `digit` (256 = nothing to count).
-// Lanes holding the same digit are merged with __match_any_sync and only the
-// lowest of them writes, so there is no atomic and no same-address conflict.
-// Called by all 32 lanes of the warp.
-__device__ __forceinline__ void warp_hist_add(unsigned* wh, unsigned digit) {
-  const unsigned peers = __match_any_sync(kFull, digit);
-  if (digit < 256u && (peers & lanemask_lt()) == 0) wh[digit] += __popc(peers);
-  __syncwarp();
-}
-
 // Appends key to dst[*counter ...] for lanes with want set: one shared atomic
 // per warp.  Returns the slot of this lane's key (meaningless when !want).
 // Called by all 32 lanes of the warp.
@@ -251,16 +220,6 @@ __device__ __forceinline__ unsigned long long block_scan_incl(unsigned long long
   v += tmp[warp];
   __syncthreads();
   return v;
-}
-
-__device__ __forceinline__ unsigned long long block_sum(unsigned long long v, unsigned long long* tmp) {
-  __shared__ unsigned long long s_tot;
-  const unsigned long long inc = block_scan_incl(v, tmp);
-  if (threadIdx.x == blockDim.x - 1) s_tot = inc;
-  __syncthreads();
-  const unsigned long long r = s_tot;
-  __syncthreads();
-  return r;
 }
 
 template <int BLOCK>
@@ -380,431 +339,38 @@ __device__ void block_or_and(const uint64_t* src, int n, unsigned long long* out
   __syncthreads();
 }
 
-template <int BLOCK, int P, int CB, int SRC>
-__global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelParams a) {
-  using L = Layout<BLOCK, P, CB>;
-  extern __shared__ __align__(16) unsigned char smem[];
-  uint64_t* bufA = reinterpret_cast<uint64_t*>(smem + L::kBufA);
-  uint64_t* bufB = reinterpret_cast<uint64_t*>(smem + L::kBufB);
-  unsigned* whist = reinterpret_cast<unsigned*>(smem + L::kWhist);
-  unsigned* hist = reinterpret_cast<unsigned*>(smem + L::kHist);
-  unsigned* gbase = reinterpret_cast<unsigned*>(smem + L::kGbase);
-  unsigned* part = reinterpret_cast<unsigned*>(smem + L::kPart);
-  unsigned long long* xch = reinterpret_cast<unsigned long long*>(smem + L::kXch);
-  __shared__ unsigned long long s_tmp[32];
-  __shared__ unsigned long long s_info[5];
-  __shared__ unsigned s_cnt;
-  __shared__ unsigned s_gcount;
-  __shared__ int s_over;
-
-  cg::cluster_group cluster = cg::this_cluster();
-  const unsigned G = cluster.num_blocks();
-  const unsigned crank = cluster.block_rank();
-  const int64_t row = blockIdx.x / G;
+// Stable LSD radix sort of src[0..n) into descending key order, one 8-bit
+// digit per pass, skipping digits on which all keys agree (bits of `vary`
+// clear).  Each warp ranks a contiguous segment stably (__match_any_sync
+// peers), per-warp counts are scanned per digit, and keys are scattered to
+// the other buffer.  `scratch` holds kWarps*256 + 2*256 + kQuarters*256
+// counters.  Returns the buffer holding the result.
+template <int BLOCK, int P>
+__device__ __noinline__ uint64_t* lsd_sort(uint64_t* src, uint64_t* dst, int n, unsigned long long vary, unsigned* scratch) {
+  constexpr int kWarps = BLOCK / 32;
+  constexpr int kQuarters = BLOCK / 256;
+  constexpr int kWarpsPerQuarter = kWarps / kQuarters;
+  constexpr int kItems = (P + BLOCK - 1) / BLOCK;
+  __shared__ unsigned long long s_scan[32];
+  unsigned* whist = scratch;
+  unsigned* hist = whist + kWarps * 256;
+  unsigned* gbase = hist + 256;
+  unsigned* part = gbase + 256;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  // programmatic dependent launch: everything below may read what earlier
-  // grids wrote, so wait for them; the next grid may begin launching now
-  grid_dependency_wait();
-  grid_launch_dependents();
-
-  int64_t valid = (SRC == 0) ? a.key_stride : a.len;
-  if (SRC == 0 && a.counts) {
-    const unsigned long long c = __ldcg(a.counts + row);
-    if (c < static_cast<unsigned long long>(valid)) valid = static_cast<int64_t>(c);
-  }
-  // slices start at even positions so key slices can be copied in 16-byte units
-  const int64_t sb = (valid * crank / G) & ~int64_t(1);
-  const int64_t se = (crank + 1 == G) ? valid : ((valid * (crank + 1) / G) & ~int64_t(1));
-  if (tid == 0) s_gcount = 0u;
-  TK_STAMP(0);
-  TK_CTA(0, globaltimer_ns());
-
-  // The cache is the whole buffer (both halves): the winners later leave
-  // through the L2 exchange buffer, so nothing else is written here meanwhile.
-  uint64_t* cache = bufA;
-  const unsigned long long cache_cap = P + CB;
-  bool cached = false;
-  unsigned cache_n = 0;
-  if (SRC == 0 && static_cast<unsigned long long>(se - sb) <= cache_cap) {
-    // the whole slice fits: copy it in with cp.async, no registers involved
-    const uint64_t* from = a.keys + row * a.key_stride + sb;
-    const unsigned n = static_cast<unsigned>(se - sb);
-    if (a.key_vec) {
-      for (unsigned i = 2 * tid; i + 1 < n; i += 2 * BLOCK) cp_async16(cache + i, from + i);
-      if ((n & 1u) && tid == 0) cache[n - 1] = __ldcg(from + n - 1);
-      cp_async_wait_all();
-    } else {
-      for (unsigned i = tid; i < n; i += BLOCK) cache[i] = __ldcg(from + i);
-    }
-    cached = true;
-    cache_n = n;
-    __syncthreads();
-  }
-  TK_STAMP(1);
-
-  // ------------------------------------------------------------------ select
-  const int kb = a.key_bits + a.ib;
-  uint64_t prefix = 0, pmask = 0;
-  unsigned long long rank = static_cast<unsigned long long>(a.r);
-  unsigned long long local_above = 0, local_bucket = static_cast<unsigned long long>(se - sb);
-  bool failed = false;
-  for (int shift = ((kb - 1) / 8) * 8; shift >= 0; shift -= 8) {
-    const bool will_cache = !cached && (local_above + local_bucket) <= cache_cap;
-    for (int i = tid; i < L::kWarps * 256; i += BLOCK) whist[i] = 0u;
-    if (tid == 0) s_cnt = 0u;
-    __syncthreads();
-    unsigned* wh = whist + warp * 256;
-    if (cached) {
-      for (unsigned i = 2 * tid; i < cache_n; i += 2 * BLOCK) {
-        const uint64_t k0 = cache[i];
-        if ((k0 & pmask) == prefix) atomicAdd(&wh[(k0 >> shift) & 255u], 1u);
-        if (i + 1 < cache_n) {
-          const uint64_t k1 = cache[i + 1];
-          if ((k1 & pmask) == prefix) atomicAdd(&wh[(k1 >> shift) & 255u], 1u);
-        }
-      }
-    } else {
-      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t k, bool in) {
-        warp_hist_add(wh, (in && (k & pmask) == prefix) ? static_cast<unsigned>((k >> shift) & 255u) : 256u);
-        if (will_cache) {
-          const bool want = in && k >= prefix;
-          const unsigned slot = warp_append_slot(&s_cnt, want);
-          if (want) cache[slot] = k;
-        }
-      });
-    }
-    __syncthreads();
-    if (shift == ((kb - 1) / 8) * 8) TK_STAMP(25);
-    {
-      // per-digit sum over the warps' counters: each group of 256 threads
-      // sums a quarter of the warps, then the quarters are added
-      const int dq = tid & 255, q = tid >> 8;
-      unsigned sq = 0;
-      for (int w = q * L::kWarpsPerQuarter; w < (q + 1) * L::kWarpsPerQuarter; ++w) sq += whist[w * 256 + dq];
-      part[q * 256 + dq] = sq;
-      __syncthreads();
-      if (tid < 256) {
-        unsigned sd = 0;
-        for (int q2 = 0; q2 < L::kQuarters; ++q2) sd += part[q2 * 256 + tid];
-        hist[tid] = sd;
-      }
-    }
-    if (will_cache) {
-      cache_n = s_cnt;
-      cached = true;
-    }
-    if (tid == 0) s_info[0] = ~0ull;
-    if (shift == ((kb - 1) / 8) * 8) TK_STAMP(26);
-    cluster.sync();
-    if (shift == ((kb - 1) / 8) * 8) TK_STAMP(27);
-    // digit 255 - tid; inclusive scans from the top digit downwards of the
-    // cluster totals and of this CTA's own counts
-    unsigned long long tot = 0, mine = 0;
-    const int d = 255 - tid;
-    if (tid < 256) {
-      for (unsigned c = 0; c < G; ++c) tot += cluster.map_shared_rank(hist, c)[d];
-      mine = hist[d];
-    }
-    const unsigned long long incl = block_scan_incl(tot, s_tmp);
-    const unsigned long long mine_incl = block_scan_incl(mine, s_tmp);
-    if (shift == ((kb - 1) / 8) * 8) TK_STAMP(28);
-    if (tid < 256) {
-      const unsigned long long excl = incl - tot;
-      if (excl < rank && rank <= incl) {
-        s_info[0] = static_cast<unsigned long long>(d);
-        s_info[1] = excl;
-        s_info[2] = mine;
-        s_info[3] = mine_incl - mine;  // this CTA's keys in digits above d
-        s_info[4] = tot;
-      }
-    }
-    cluster.sync();
-    TK_STAMP(2 + (shift >> 3));
-    if (s_info[0] == ~0ull) { failed = true; break; }
-    prefix |= s_info[0] << shift;
-    pmask |= 0xffull << shift;
-    rank -= s_info[1];
-    local_above += s_info[3];
-    local_bucket = s_info[2];
-    if (shift > 0 && s_info[4] <= kGather) {
-      // Gather the boundary bucket into CTA 0 and rank it by counting.
-      unsigned* g_cnt = cluster.map_shared_rank(&s_gcount, 0);
-      uint64_t* g_buf = cluster.map_shared_rank(reinterpret_cast<uint64_t*>(whist), 0);
-      if (cached) {
-        for (unsigned i = tid; i < cache_n; i += BLOCK) {
-          const uint64_t k = cache[i];
-          if ((k & pmask) == prefix) g_buf[atomicAdd(g_cnt, 1u)] = k;
-        }
-      } else {
-        for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t k, bool in) {
-          if (in && (k & pmask) == prefix) g_buf[atomicAdd(g_cnt, 1u)] = k;
-        });
-      }
-      cluster.sync();
-      if (crank == 0) {
-        const unsigned n = s_gcount;
-        const uint64_t* g = reinterpret_cast<const uint64_t*>(whist);
-        if (static_cast<unsigned>(tid) < n) {
-          const uint64_t mine = g[tid];
-          unsigned long long above = 0;
-          for (unsigned j = 0; j < n; ++j) {
-            const uint64_t o = g[j];
-            above += (o > mine || (o == mine && j < static_cast<unsigned>(tid))) ? 1ull : 0ull;
-          }
-          if (above == rank - 1)
-            for (unsigned c = 0; c < G; ++c) cluster.map_shared_rank(xch, c)[3] = mine;
-        }
-      }
-      cluster.sync();
-      TK_STAMP(12);
-      prefix = xch[3];
-      pmask = ~0ull;
-      break;
-    }
-  }
-  if (failed) {
-    if (tid == 0 && crank == 0) atomicCAS(a.status, kDevOk, kDevBadState);
-    return;
-  }
-  const uint64_t tau = prefix;  // the r-th largest key
-  if (!a.want_topk) {
-    if (tid == 0 && crank == 0) a.tau_out[row] = tau;
-    return;
-  }
-
-  // ------------------------------------------------------------------ winners
-  TK_STAMP(13);
-  const int64_t k = a.r;
-  {
-    unsigned long long cnt = 0, orm = 0, andm = ~0ull;
-    if (tid == 0) {
-      s_cnt = 0u;
-      s_over = 0;
-      xch[1] = 0ull;
-      xch[2] = ~0ull;
-    }
-    __syncthreads();
-    if (cached) {
-      for (unsigned i = tid; i < cache_n; i += BLOCK) {
-        const uint64_t key = cache[i];
-        if (key >= tau) { ++cnt; orm |= key; andm &= key; }
-      }
-    } else {
-      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t key, bool in) {
-        const bool w = in && key >= tau;
-        if (w) { ++cnt; orm |= key; andm &= key; }
-        const unsigned slot = warp_append_slot(&s_cnt, w);
-        if (w) {
-          if (slot < static_cast<unsigned>(CB)) bufB[slot] = key; else s_over = 1;
-        }
-      });
-    }
-    const unsigned long long total = block_sum(cnt, s_tmp);
-    TK_STAMP(15);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      orm |= __shfl_xor_sync(kFull, orm, o);
-      andm &= __shfl_xor_sync(kFull, andm, o);
-    }
-    if (lane == 0) {
-      atomicOr(&xch[1], orm);
-      atomicAnd(&xch[2], andm);
-    }
-    if (tid == 0) xch[0] = total;
-  }
-  cluster.sync();
-  unsigned long long base = 0, all_or = 0, all_and = ~0ull, all_cnt = 0;
-  for (unsigned c = 0; c < G; ++c) {
-    const unsigned long long* rx = cluster.map_shared_rank(xch, c);
-    if (c < crank) base += rx[0];
-    all_cnt += rx[0];
-    all_or |= rx[1];
-    all_and &= rx[2];
-  }
-  if (all_cnt != static_cast<unsigned long long>(k)) {
-    if (tid == 0 && crank == 0) atomicCAS(a.status, kDevOk, kDevBadState);
-    cluster.sync();
-    return;
-  }
-  TK_STAMP(29);
-  // Place the winners: position base + local sequence, in an L2-resident
-  // exchange buffer (plain global stores; each CTA then reads back what it
-  // needs), which costs far less than scattering single keys into other CTAs'
-  // shared memory.
-  uint64_t* xb = a.xbuf + row * 2 * k;
-  int xsel = 0;  // which half of the exchange buffer the next exchange uses
-  {
-    if (tid == 0) s_cnt = 0u;
-    __syncthreads();
-    auto place = [&](uint64_t key, bool want) {
-      const unsigned slot = warp_append_slot(&s_cnt, want);
-      if (want) {
-        xb[static_cast<unsigned>(base) + slot] = key;
-      }
-    };
-    if (cached || !s_over) {
-      const unsigned n = cached ? cache_n : static_cast<unsigned>(xch[0]);
-      const uint64_t* from = cached ? cache : bufB;
-      for_cache<BLOCK>(from, n, [&](uint64_t key, bool in) { place(key, in && (!cached || key >= tau)); });
-    } else {
-      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t key, bool in) { place(key, in && key >= tau); });
-    }
-  }
-  TK_STAMP(30);
-  cluster.sync();
-  TK_STAMP(14);
-  if (k <= kRankMax) {
-    // Every CTA holds all k winners (read from the exchange buffer, in the
-    // same order everywhere) and places its 1/G share of them.
-    for (int i = tid; i < k; i += BLOCK) bufA[i] = __ldcg(xb + i);
-    // CTA c ranks the groups that start in its 1/G of the places
-    const unsigned kc = static_cast<unsigned>((k + G - 1) / G);
-    const unsigned lo = crank * kc, hi = crank + 1 == G ? static_cast<unsigned>(k) : lo + kc;
-    if constexpr (BLOCK >= 1024)
-      place_by_groups<BLOCK, 2048>(bufA, static_cast<int>(k), all_or ^ all_and, lo, hi, bufB, whist,
-                                   whist + 2048, whist + 4096, s_tmp, ~0u, a, row, k, 0, 0, k);
-    else
-      place_by_groups<BLOCK, 256>(bufA, static_cast<int>(k), all_or ^ all_and, lo, hi, bufB, hist, gbase,
-                                  part, s_tmp, ~0u, a, row, k, 0, 0, k);
-    TK_STAMP(24);
-    return;
-  }
-
-  // ------------------------------------------------------------------ large k
-  // Each CTA owns the output places [my0, my0 + n_mine).  The winners are
-  // partitioned once by their 11 most significant varying bits: exact bin
-  // counts are exchanged over DSMEM, every key is written to its bin's
-  // segment of the exchange buffer, and each CTA then sorts only the bins
-  // that overlap its places, locally.  If some CTA's bins do not fit in its
-  // shared memory (a pathological bin), the cluster falls back to an LSD
-  // radix sort over evenly split chunks.
-  const unsigned long long vary = all_or ^ all_and;
-  const int hb = vary ? 63 - __clzll(static_cast<long long>(vary)) : 0;
-  const int64_t pe = (k + G - 1) / G;
-  const int64_t my0 = static_cast<int64_t>(crank) * pe;
-  const int n_mine = static_cast<int>(my0 >= k ? 0 : (k - my0 < pe ? k - my0 : pe));
-  for (int i = tid; i < n_mine; i += BLOCK) bufA[i] = __ldcg(xb + my0 + i);
-  __syncthreads();
-  bool local_sort = (G == 1);
-  int64_t ext0 = my0;
-  int n_c = n_mine;
-  if (G > 1 && BLOCK == 1024) {
-    const int psh = hb >= 10 ? hb - 10 : 0;
-    unsigned* lh = whist;           // local count per bin (read by the other CTAs)
-    unsigned* bst = whist + 2048;   // first place of each bin (the end of the last one is k)
-    unsigned* off = whist + 4096;   // this CTA's first place inside each bin
-    unsigned* cur = whist + 6144;   // fill cursors
-    for (int i = tid; i < 2048; i += BLOCK) { lh[i] = 0u; cur[i] = 0u; }
-    __syncthreads();
-    for (int i = tid; i < n_mine; i += BLOCK) atomicAdd(&lh[2047u - ((bufA[i] >> psh) & 2047u)], 1u);
-    cluster.sync();
-    {
-      unsigned tt[2], bm[2];
-      unsigned long long tsum = 0;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int b = tid * 2 + q;
-        unsigned t = 0, before = 0;
-        for (unsigned c = 0; c < G; ++c) {
-          const unsigned h = cluster.map_shared_rank(lh, c)[b];
-          t += h;
-          if (c < crank) before += h;
-        }
-        tt[q] = t;
-        bm[q] = before;
-        tsum += t;
-      }
-      const unsigned long long incl = block_scan_incl(tsum, s_tmp);
-      unsigned run = static_cast<unsigned>(incl - tsum);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int b = tid * 2 + q;
-        bst[b] = run;
-        off[b] = run + bm[q];
-        run += tt[q];
-      }
-    }
-    cluster.sync();  // every CTA has read the others' counts
-    uint64_t* xb1 = xb + k;
-    for (int i = tid; i < n_mine; i += BLOCK) {
-      const uint64_t key = bufA[i];
-      const unsigned bi = 2047u - static_cast<unsigned>((key >> psh) & 2047u);
-      xb1[off[bi] + atomicAdd(&cur[bi], 1u)] = key;
-    }
-    // extended range of every CTA: from the start of the bin holding its
-    // first place to the end of the bin holding its last place
-    __shared__ unsigned s_ext[2 * 16];
-    __shared__ int s_fit;
-    if (tid == 0) s_fit = 1;
-    __syncthreads();
-    if (tid < static_cast<int>(G)) {
-      const int64_t c0 = static_cast<int64_t>(tid) * pe;
-      const int64_t c1 = c0 + pe < k ? c0 + pe : k;
-      unsigned e0 = 0, e1 = 0;
-      if (c0 < k) {
-        // bin holding place p: the last b with bst[b] <= p (empty bins have
-        // no place, so the first b with bst[b] > p follows the right one)
-        auto bin_of = [&](unsigned p) {
-          int lo2 = 0, hi2 = 2048;
-          while (lo2 < hi2) {
-            const int mid = (lo2 + hi2) >> 1;
-            if (bst[mid] <= p) lo2 = mid + 1; else hi2 = mid;
-          }
-          return lo2 - 1;
-        };
-        e0 = bst[bin_of(static_cast<unsigned>(c0))];
-        const int b1 = bin_of(static_cast<unsigned>(c1 - 1)) + 1;
-        e1 = b1 < 2048 ? bst[b1] : static_cast<unsigned>(k);
-      }
-      s_ext[2 * tid] = e0;
-      s_ext[2 * tid + 1] = e1;
-      if (e1 - e0 > static_cast<unsigned>(P)) atomicAnd(&s_fit, 0);
-    }
-    cluster.sync();  // the bins are complete in the exchange buffer
-    if (s_fit) {
-      local_sort = true;
-      ext0 = s_ext[2 * crank];
-      n_c = static_cast<int>(s_ext[2 * crank + 1] - s_ext[2 * crank]);
-      for (int i = tid; i < n_c; i += BLOCK) bufA[i] = __ldcg(xb1 + ext0 + i);
-      __syncthreads();
-    }
-  }
-  TK_STAMP(15);
-  TK_CTA(1, globaltimer_ns());
-  if constexpr (BLOCK >= 1024) if (local_sort) {
-    unsigned long long lo_or, lo_and;
-    block_or_and<BLOCK>(bufA, n_c, &lo_or, &lo_and);
-    if (place_by_groups<BLOCK, 2048>(bufA, n_c, lo_or ^ lo_and, 0u, ~0u, bufB, whist, whist + 2048,
-                                     whist + 4096, s_tmp, 512u, a, row, k, ext0, my0, my0 + n_mine)) {
-      TK_STAMP(24);
-      TK_CTA(2, globaltimer_ns());
-      TK_CTA(3, 1ull);
-      return;
-    }
-  }
-  const unsigned sortG = local_sort ? 1u : G;  // CTAs taking part in each sort pass
-
-  // ------------------------------------------------------------------ sort
-  uint64_t* src = bufA;
-  uint64_t* dst = bufB;
-  const int ipw = (n_c + L::kWarps - 1) / L::kWarps;  // items per warp segment
+  const int ipw = (n + kWarps - 1) / kWarps;  // items per warp segment
   const int seg0 = warp * ipw;
-  const int seg1 = (seg0 + ipw < n_c) ? seg0 + ipw : n_c;
+  const int seg1 = (seg0 + ipw < n) ? seg0 + ipw : n;
   const unsigned lt = lanemask_lt();
-  auto gsync = [&]() {
-    if (sortG > 1) cluster.sync(); else __syncthreads();
-  };
   for (int shift = 0; shift < 64; shift += 8) {
-    if (((vary >> shift) & 0xffull) == 0) continue;  // uniform over the sorting CTAs
-    for (int i = tid; i < L::kWarps * 256; i += BLOCK) whist[i] = 0u;
+    if (((vary >> shift) & 0xffull) == 0) continue;  // uniform over the block
+    for (int i = tid; i < kWarps * 256; i += BLOCK) whist[i] = 0u;
     __syncthreads();
     unsigned* wh = whist + warp * 256;
-    uint64_t key[L::kItems];
-    unsigned dig[L::kItems], wr[L::kItems];
+    uint64_t key[kItems];
+    unsigned dig[kItems], wr[kItems];
     const int nj = (seg1 - seg0 + 31) >> 5;  // items per lane, uniform in the warp
 #pragma unroll
-    for (int j = 0; j < L::kItems; ++j) {
+    for (int j = 0; j < kItems; ++j) {
       if (j >= nj) break;
       const int i = seg0 + j * 32 + lane;
       const bool v = i < seg1;
@@ -819,13 +385,12 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
       wr[j] = b + before;
     }
     __syncthreads();
-    TK_STAMP(10);
-    // exclusive prefix of the per-warp counts over warps, per digit, in two
-    // steps: within groups of warps, then across groups
+    // exclusive prefix of the per-warp counts over warps, per digit, within
+    // groups of warps and then across groups
     {
       const int d = tid & 255, q = tid >> 8;
       unsigned run = 0;
-      for (int w = q * L::kWarpsPerQuarter; w < (q + 1) * L::kWarpsPerQuarter; ++w) {
+      for (int w = q * kWarpsPerQuarter; w < (q + 1) * kWarpsPerQuarter; ++w) {
         const unsigned t = whist[w * 256 + d];
         whist[w * 256 + d] = run;
         run += t;
@@ -835,73 +400,569 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
       unsigned qbase = 0;
       for (int q2 = 0; q2 < q; ++q2) qbase += part[q2 * 256 + d];
       if (qbase)
-        for (int w = q * L::kWarpsPerQuarter; w < (q + 1) * L::kWarpsPerQuarter; ++w) whist[w * 256 + d] += qbase;
-      if (q == L::kQuarters - 1) hist[d] = qbase + run;
+        for (int w = q * kWarpsPerQuarter; w < (q + 1) * kWarpsPerQuarter; ++w) whist[w * 256 + d] += qbase;
+      if (q == kQuarters - 1) hist[d] = qbase + run;
     }
-    TK_STAMP(11);
-    gsync();
-    TK_STAMP(31);
-    unsigned long long tot = 0, before_me = 0;
-    if (tid < 256) {
-      if (sortG == 1) {
-        tot = hist[tid];  // this CTA sorts alone
+    __syncthreads();
+    const unsigned long long tot = tid < 256 ? hist[tid] : 0ull;
+    const unsigned long long incl = block_scan_incl(tot, s_scan);
+    if (tid < 256) gbase[tid] = static_cast<unsigned>(incl - tot);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+      if (j >= nj) break;
+      const int i = seg0 + j * 32 + lane;
+      if (i < seg1) dst[gbase[dig[j]] + wh[dig[j]] + wr[j]] = key[j];
+    }
+    __syncthreads();
+    uint64_t* t = src;
+    src = dst;
+    dst = t;
+  }
+  return src;
+}
+
+template <int BLOCK, int P, int CB, int NB>
+struct Layout {
+  static constexpr int kWarps = BLOCK / 32;
+  static constexpr int kQuarters = BLOCK / 256;          // thread groups of 256 (one per 8-bit digit)
+  static constexpr int kDigitBits = NB == 2048 ? 11 : 8;
+  static constexpr int kPer = NB / BLOCK;                // bins per thread in the scans
+  // scratch of the local LSD sort: per-warp counters, totals, bases, partials
+  static constexpr int kLsdWords = kWarps * 256 + 2 * 256 + kQuarters * 256;
+  static constexpr int kWorkWords = (3 * NB > kLsdWords - 2 * NB) ? 3 * NB : kLsdWords - 2 * NB;
+  static constexpr unsigned kGather = NB / 2 < 512 ? NB / 2 : 512;  // keys gathered into CTA 0
+  static constexpr size_t kBufA = 0;
+  static constexpr size_t kBufB = kBufA + sizeof(uint64_t) * P;
+  static constexpr size_t kH2 = kBufB + sizeof(uint64_t) * CB;     // 2 x NB counters (cluster-visible)
+  static constexpr size_t kWork = kH2 + sizeof(unsigned) * 2 * NB;  // kWorkWords counters
+  static constexpr size_t kGorg = kWork + sizeof(unsigned) * kWorkWords;
+  static constexpr size_t kXch = (kGorg + kGather + 15) / 16 * 16;
+  // exchange words: 0-1 this CTA's OR / AND, 3 tau, 4 winner offset,
+  // 8.. per-CTA counts (in CTA 0), 24.. every CTA's OR / AND (pushed)
+  static constexpr int kXchWords = 24 + 2 * kMaxCluster;
+  static constexpr size_t kBytes = kXch + sizeof(unsigned long long) * kXchWords;
+  static_assert(CB >= P, "the second buffer holds a full local set");
+  static_assert(BLOCK % 256 == 0, "one thread per 8-bit digit in each group of 256");
+  static_assert(NB % BLOCK == 0, "whole bins per thread");
+};
+
+template <int BLOCK, int P, int CB, int NB, int SRC>
+__global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelParams a) {
+  using L = Layout<BLOCK, P, CB, NB>;
+  constexpr int DB = L::kDigitBits;
+  constexpr unsigned DM = NB - 1;
+  constexpr int kPer = L::kPer;
+  constexpr unsigned kGatherMax = L::kGather;
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint64_t* bufA = reinterpret_cast<uint64_t*>(smem + L::kBufA);
+  uint64_t* bufB = reinterpret_cast<uint64_t*>(smem + L::kBufB);
+  unsigned* h2 = reinterpret_cast<unsigned*>(smem + L::kH2);
+  unsigned* work = reinterpret_cast<unsigned*>(smem + L::kWork);
+  unsigned char* gorg = smem + L::kGorg;
+  unsigned long long* xch = reinterpret_cast<unsigned long long*>(smem + L::kXch);
+  __shared__ unsigned long long s_tmp[32];
+  __shared__ unsigned long long s_info[5];
+  __shared__ unsigned s_cnt;
+  __shared__ unsigned s_gcount;
+  __shared__ unsigned s_wcnt[kMaxCluster];
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned G = cluster.num_blocks();
+  const unsigned crank = cluster.block_rank();
+  const int64_t row = blockIdx.x / G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // programmatic dependent launch: everything below may read what earlier
+  // grids wrote, so wait for them; the next grid may begin launching now
+  grid_dependency_wait();
+  grid_launch_dependents();
+  // Shared memory of another CTA may be used only once that CTA runs: arrive
+  // now, wait before the first remote access.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  bool cluster_started = false;
+  auto await_cluster = [&]() {
+    if (!cluster_started) {
+      asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+      cluster_started = true;
+    }
+  };
+  auto gsync = [&]() {
+    await_cluster();
+    if (G > 1) cluster.sync(); else __syncthreads();
+  };
+
+  int64_t valid = (SRC == 0) ? a.key_stride : a.len;
+  if (SRC == 0 && a.counts) {
+    const unsigned long long c = __ldcg(a.counts + row);
+    if (c < static_cast<unsigned long long>(valid)) valid = static_cast<int64_t>(c);
+  }
+  // slices start at even positions so key slices can be copied in 16-byte units
+  const int64_t sb = (valid * crank / G) & ~int64_t(1);
+  const int64_t se = (crank + 1 == G) ? valid : ((valid * (crank + 1) / G) & ~int64_t(1));
+  if (tid == 0) { s_gcount = 0u; s_cnt = 0u; }
+  if (tid < kMaxCluster) s_wcnt[tid] = 0u;
+  TK_STAMP(0);
+  TK_CTA(4, globaltimer_ns());
+
+  // ------------------------------------------------------------------ load
+  // The cache is the whole key buffer (both halves).  Whether the slices fit
+  // is decided from sizes every CTA of the cluster sees alike.
+  uint64_t* cache = bufA;
+  const int64_t cache_cap = P + CB;
+  const bool fits = (valid + G - 1) / G + 2 <= cache_cap;
+  bool cached = false;
+  unsigned cache_n = 0;
+  __syncthreads();
+  if (fits) {
+    const unsigned n = static_cast<unsigned>(se - sb);
+    if (SRC == 0) {
+      const uint64_t* from = a.keys + row * a.key_stride + sb;
+      if (a.key_vec) {
+        for (unsigned i = 2 * tid; i + 1 < n; i += 2 * BLOCK) cp_async16(cache + i, from + i);
+        if ((n & 1u) && tid == 0) cache[n - 1] = __ldcg(from + n - 1);
+        cp_async_wait_all();
       } else {
-        for (unsigned c = 0; c < sortG; ++c) {
-          const unsigned h = cluster.map_shared_rank(hist, c)[tid];
-          tot += h;
-          if (c < crank) before_me += h;
+        for (unsigned i = tid; i < n; i += BLOCK) cache[i] = __ldcg(from + i);
+      }
+    } else {
+      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t k, bool in) {
+        const unsigned slot = warp_append_slot(&s_cnt, in);
+        if (in) cache[slot] = k;
+      });
+    }
+    cached = true;
+    cache_n = n;
+    __syncthreads();
+  }
+  TK_STAMP(1);
+  TK_CTA(0, globaltimer_ns());
+
+  // ------------------------------------------------------------------ varying bits
+  // Bits on which all keys agree are skipped: the first digit is the 11 (or
+  // 8) bits below the most significant varying bit.  Streamed slices skip
+  // this exchange and start at the top of the key.
+  const int kb = a.key_bits + a.ib;
+  unsigned long long all_or = (kb >= 64) ? ~0ull : ((1ull << kb) - 1ull), all_and = 0ull;
+  if (fits) {
+    // warp-reduce, then one shared atomic per warp; the CTA's result is
+    // published in xch[0..1] and read by every CTA of the cluster
+    if (tid == 0) { xch[0] = 0ull; xch[1] = ~0ull; }
+    unsigned long long o = 0, d = ~0ull;
+    for (unsigned i = tid; i < cache_n; i += BLOCK) { o |= cache[i]; d &= cache[i]; }
+    TK_STAMP(19);
+    TK_CTA(1, globaltimer_ns());
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+      o |= __shfl_xor_sync(kFull, o, m);
+      d &= __shfl_xor_sync(kFull, d, m);
+    }
+    __syncthreads();
+    if (lane == 0 && static_cast<unsigned>(tid) < cache_n) {  // the warp holds keys
+      atomicOr(&xch[0], o);
+      atomicAnd(&xch[1], d);
+    }
+    __syncthreads();
+    await_cluster();
+    // push this CTA's result into every CTA (remote stores need no reply)
+    if (warp == 0 && static_cast<unsigned>(lane) < G) {
+      unsigned long long* rx = cluster.map_shared_rank(xch, static_cast<unsigned>(lane));
+      rx[24 + 2 * crank] = xch[0];
+      rx[25 + 2 * crank] = xch[1];
+    }
+    TK_STAMP(20);
+    gsync();  // every CTA's OR / AND has arrived
+    TK_STAMP(21);
+    TK_CTA(2, globaltimer_ns());
+    all_or = 0ull;
+    all_and = ~0ull;
+    for (unsigned c = 0; c < G; ++c) {
+      all_or |= xch[24 + 2 * c];
+      all_and &= xch[25 + 2 * c];
+    }
+  }
+  TK_STAMP(2);
+
+  // ------------------------------------------------------------------ select
+  // Radix select of the r-th largest key with NB-bin digits.  Bins are
+  // indexed in descending key order (bin = DM - digit), so places run with
+  // the bin index.  The first pass's per-bin totals and this CTA's offsets
+  // inside each bin are kept: they partition the winners later.
+  const unsigned long long vary = all_or ^ all_and;
+  const int hb = vary ? 63 - __clzll(static_cast<long long>(vary)) : 0;
+  uint64_t pmask = (hb >= 63) ? 0ull : (~0ull << (hb + 1));
+  uint64_t prefix = all_and & pmask;
+  int shift = hb >= DB - 1 ? hb - (DB - 1) : 0;
+  const int shift1 = shift;
+  const uint64_t prefix1 = prefix, pmask1 = pmask;
+  unsigned long long rank = static_cast<unsigned long long>(a.r);
+  unsigned long long above_b1 = 0;   // this CTA's keys of the first-pass bin above the bucket
+  unsigned long long above_all = 0;  // this CTA's keys above the bucket
+  unsigned long long bucket_tot = 0, bucket_mine = static_cast<unsigned long long>(se - sb);
+  unsigned b1 = 0;
+  unsigned* bst = work;           // first place of each first-pass bin
+  unsigned* off = work + NB;      // this CTA's first place inside each first-pass bin
+  unsigned* cur = work + 2 * NB;  // fill cursors
+  int pass = 0;
+  bool failed = false;
+  for (;; ++pass) {
+    unsigned* hc = h2 + (pass & 1) * NB;
+    const bool will_cache = !cached && (above_all + bucket_mine) <= static_cast<unsigned long long>(cache_cap);
+    for (int i = tid; i < NB; i += BLOCK) hc[i] = 0u;
+    if (tid == 0) s_cnt = 0u;
+    __syncthreads();
+    // The first digit (leading exponent bits, typically) is skewed: lanes of
+    // a warp holding the same bin are merged with __match_any_sync so a hot
+    // bin takes one atomic per warp.  Later digits are close to uniform.
+    const bool merge = kMergeFirstPass && pass == 0;
+    auto count = [&](uint64_t k, bool in) {  // called by all 32 lanes
+      const bool take = in && (k & pmask) == prefix;
+      const unsigned bin = DM - static_cast<unsigned>((k >> shift) & DM);
+      if (merge) {
+        const unsigned peers = __match_any_sync(kFull, take ? bin : 0xffffffffu);
+        if (take && (peers & lanemask_lt()) == 0) atomicAdd(&hc[bin], __popc(peers));
+      } else if (take) {
+        atomicAdd(&hc[bin], 1u);
+      }
+    };
+    if (cached) {
+      for_cache<BLOCK>(cache, cache_n, count);
+    } else {
+      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t k, bool in) {
+        count(k, in);
+        if (will_cache) {
+          const bool want = in && k >= prefix;
+          const unsigned slot = warp_append_slot(&s_cnt, want);
+          if (want && slot < static_cast<unsigned>(cache_cap)) cache[slot] = k;
+        }
+      });
+    }
+    if (tid == 0) s_info[0] = ~0ull;
+    if (pass == 0) TK_STAMP(15);
+    if (pass == 0) TK_CTA(3, globaltimer_ns());
+    gsync();  // every CTA's counts of this pass are complete
+    if (pass == 0) TK_STAMP(16);
+    if (will_cache) {
+      cached = true;
+      cache_n = s_cnt;
+    }
+    // totals over the cluster, this CTA's counts, and the counts of the CTAs
+    // before it, for this thread's kPer consecutive bins
+    // (remote loads are issued eight CTAs at a time, before any is used)
+    unsigned tt[kPer], mm[kPer], bf[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) { tt[q] = 0u; bf[q] = 0u; mm[q] = hc[tid * kPer + q]; }
+#pragma unroll
+    for (int c0 = 0; c0 < kMaxCluster; c0 += 8) {
+      if (c0 < static_cast<int>(G)) {
+        unsigned rv[8][kPer];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 + j;
+          if (c < static_cast<int>(G)) {
+            // CTAs start at different ranks so no CTA's counters are read by all at once
+            const unsigned src = (crank + static_cast<unsigned>(c)) % G;
+            const unsigned* r = cluster.map_shared_rank(hc, src) + tid * kPer;
+            if constexpr (kPer == 2) {
+              const uint2 v = *reinterpret_cast<const uint2*>(r);
+              rv[j][0] = v.x;
+              rv[j][1] = v.y;
+            } else {
+#pragma unroll
+              for (int q = 0; q < kPer; ++q) rv[j][q] = r[q];
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 + j;
+          if (c < static_cast<int>(G)) {
+#pragma unroll
+            const unsigned src = (crank + static_cast<unsigned>(c)) % G;
+#pragma unroll
+            for (int q = 0; q < kPer; ++q) {
+              tt[q] += rv[j][q];
+              if (src < crank) bf[q] += rv[j][q];
+            }
+          }
         }
       }
     }
-    const unsigned long long incl = block_scan_incl(tot, s_tmp);
-    if (tid < 256) gbase[tid] = static_cast<unsigned>(incl - tot + before_me);
-    gsync();
-    TK_STAMP(23);
+    if (pass == 0) TK_STAMP(17);
+    unsigned long long tsum = 0, msum = 0;
 #pragma unroll
-    for (int j = 0; j < L::kItems; ++j) {
-      if (j >= nj) break;
-      const int i = seg0 + j * 32 + lane;
-      if (i < seg1) {
-        const unsigned pos = gbase[dig[j]] + wh[dig[j]] + wr[j];
-        if (sortG == 1) dst[pos] = key[j]; else xb[xsel * k + pos] = key[j];
+    for (int q = 0; q < kPer; ++q) { tsum += tt[q]; msum += mm[q]; }
+    const unsigned long long tincl = block_scan_incl(tsum, s_tmp);
+    const unsigned long long mincl = block_scan_incl(msum, s_tmp);
+    unsigned long long trun = tincl - tsum, mrun = mincl - msum;
+    if (pass == 0) TK_STAMP(18);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int b = tid * kPer + q;
+      if (pass == 0 && a.want_topk) {
+        bst[b] = static_cast<unsigned>(trun);
+        off[b] = static_cast<unsigned>(trun) + bf[q];
+        cur[b] = 0u;
       }
+      if (trun < rank && rank <= trun + tt[q]) {
+        s_info[0] = static_cast<unsigned long long>(b);
+        s_info[1] = trun;
+        s_info[2] = tt[q];
+        s_info[3] = mrun;   // this CTA's keys in the bins above
+        s_info[4] = mm[q];
+      }
+      trun += tt[q];
+      mrun += mm[q];
     }
-    TK_STAMP(22);
-    gsync();
-    TK_STAMP(21);
-    if (sortG == 1) {
-      uint64_t* t = src; src = dst; dst = t;
-    } else {
-      // read back this CTA's range; the next exchange uses the other half, so
-      // no CTA can overwrite what another is still reading
-      const uint64_t* from = xb + xsel * k + my0;
-      for (int i = tid; i < n_c; i += BLOCK) src[i] = __ldcg(from + i);
-      xsel ^= 1;
-      __syncthreads();
-    }
-    TK_STAMP(16 + (shift >> 3));
+    __syncthreads();
+    if (s_info[0] == ~0ull) { failed = true; break; }
+    const unsigned bin = static_cast<unsigned>(s_info[0]);
+    prefix |= static_cast<uint64_t>(DM - bin) << shift;
+    pmask |= static_cast<uint64_t>(DM) << shift;
+    rank -= s_info[1];
+    bucket_tot = s_info[2];
+    above_all += s_info[3];
+    if (pass == 0) b1 = bin; else above_b1 += s_info[3];
+    bucket_mine = s_info[4];
+    TK_STAMP(3 + (pass < 6 ? pass : 6));
+    __syncthreads();  // s_info is rewritten by the next pass
+    if (bucket_tot <= kGatherMax || shift == 0) break;
+    shift = shift >= DB ? shift - DB : 0;
+  }
+  if (failed) {
+    if (tid == 0 && crank == 0) atomicCAS(a.status, kDevOk, kDevBadState);
+    gsync();  // no CTA leaves while another may still read its counters
+    return;
   }
 
-  // ------------------------------------------------------------------ output
-  TK_STAMP(24);
-  // local index i holds place ext0 + i; this CTA writes the places it owns
-  for (int i = tid; i < n_c; i += BLOCK) {
-    const int64_t place = ext0 + i;
-    if (place >= my0 && place < my0 + n_mine) write_out(a, row, k, place, src[i]);
+  // ------------------------------------------------------------------ gather
+  // The boundary bucket (at most kGather keys) is gathered into CTA 0, in the
+  // half of its counter area the last pass did not use, and ranked by
+  // counting ("Rank by Counting").  Each key carries the CTA it came from,
+  // so CTA 0 also counts every CTA's winners inside the first-pass bin.
+  {
+    uint64_t* gb0 = cluster.map_shared_rank(reinterpret_cast<uint64_t*>(h2 + ((pass + 1) & 1) * NB), 0);
+    unsigned* gc0 = cluster.map_shared_rank(&s_gcount, 0);
+    unsigned char* go0 = cluster.map_shared_rank(gorg, 0);
+    auto give = [&](uint64_t k, bool in) {  // all 32 lanes; one remote atomic per warp
+      const bool want = in && (k & pmask) == prefix;
+      const unsigned slot = warp_append_slot(gc0, want);
+      if (want && slot < kGatherMax) {
+        gb0[slot] = k;
+        go0[slot] = static_cast<unsigned char>(crank);
+      }
+    };
+    if (cached) {
+      for_cache<BLOCK>(cache, cache_n, give);
+    } else {
+      for_slice<SRC, BLOCK>(a, row, sb, se, give);
+    }
+    if (tid == 0) cluster.map_shared_rank(xch, 0)[8 + crank] = above_b1;
   }
-  TK_CTA(2, globaltimer_ns());
-  TK_CTA(3, 2ull + static_cast<unsigned long long>(n_c));
+  gsync();  // the bucket is in CTA 0
+  if (crank == 0) {
+    const uint64_t* g = reinterpret_cast<const uint64_t*>(h2 + ((pass + 1) & 1) * NB);
+    const unsigned n = s_gcount < kGatherMax ? s_gcount : kGatherMax;
+    if (tid == 0) xch[3] = 0ull;
+    if (tid == 0 && s_gcount > kGatherMax) atomicCAS(a.status, kDevOk, kDevBadState);
+    __syncthreads();
+    for (unsigned i = tid; i < n; i += BLOCK) {
+      const uint64_t mine = g[i];
+      unsigned long long above = 0;
+      for (unsigned j = 0; j < n; ++j) above += g[j] > mine ? 1ull : 0ull;
+      if (above == rank - 1) xch[3] = mine;
+    }
+    __syncthreads();
+    const uint64_t tau = xch[3];
+    if (!a.want_topk) {
+      if (tid == 0) a.tau_out[row] = tau;
+    } else {
+      for (unsigned i = tid; i < n; i += BLOCK)
+        if (g[i] >= tau) atomicAdd(&s_wcnt[gorg[i]], 1u);
+      __syncthreads();
+      if (tid == 0) {
+        unsigned long long run = 0;
+        for (unsigned c = 0; c < G; ++c) {
+          unsigned long long* rx = cluster.map_shared_rank(xch, c);
+          rx[3] = tau;
+          rx[4] = run;  // winners of the first-pass bin held by the CTAs before c
+          run += xch[8 + c] + s_wcnt[c];
+        }
+      }
+    }
+  }
+  TK_STAMP(10);
+  if (!a.want_topk) return;  // nothing reads another CTA's shared memory any more
+  gsync();  // tau and the offsets are delivered
+  const uint64_t tau = xch[3];
+  const int64_t k = a.r;
+
+  // ------------------------------------------------------------------ partition
+  // Every winner (key >= tau) goes to its first-pass bin's segment of the
+  // exchange buffer (bins in descending order: the bins' places).  Inside
+  // the first-pass bin of the boundary, this CTA's winners start after those
+  // of the CTAs before it.
+  uint64_t* xb = a.xbuf + row * k;
+  if (tid == 0) off[b1] = bst[b1] + static_cast<unsigned>(xch[4]);
+  __syncthreads();
+  {
+    auto put = [&](uint64_t key) {
+      const unsigned b = DM - static_cast<unsigned>((key >> shift1) & DM);
+      const unsigned pos = off[b] + atomicAdd(&cur[b], 1u);
+      if (pos < static_cast<unsigned long long>(k)) xb[pos] = key;
+    };
+    if (cached) {
+      for (unsigned i = tid; i < cache_n; i += BLOCK)
+        if (cache[i] >= tau) put(cache[i]);
+    } else {
+      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t key, bool in) {
+        if (in && key >= tau) put(key);
+      });
+    }
+  }
+  gsync();  // all winners are in the exchange buffer
+  TK_STAMP(11);
+
+  // ------------------------------------------------------------------ local sort
+  // CTA c owns the places [my0, my1).  It takes the first-pass bins that
+  // overlap them; a bin at either end that would overflow shared memory is
+  // cut, by further digits read from the exchange buffer, down to the
+  // sub-bin holding the boundary place.  The keys between the two cuts are a
+  // contiguous key range, sorted here.
+  const int64_t pe = (k + G - 1) / G;
+  const int64_t my0 = static_cast<int64_t>(crank) * pe;
+  if (my0 >= k) return;
+  const int64_t my1 = my0 + pe < k ? my0 + pe : k;
+  auto bin_end = [&](unsigned b) -> int64_t {
+    const int64_t e = (b + 1 < static_cast<unsigned>(NB)) ? static_cast<int64_t>(bst[b + 1]) : k;
+    return e < k ? e : k;
+  };
+  // bins holding places my0 and my1 - 1
+  if (tid == 0) { s_info[0] = 0; s_info[1] = 0; }
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const unsigned b = tid * kPer + q;
+    const int64_t s = bst[b], e = bin_end(b);
+    if (s <= my0 && my0 < e) s_info[0] = b;
+    if (s <= my1 - 1 && my1 - 1 < e) s_info[1] = b;
+  }
+  __syncthreads();
+  const unsigned bfirst = static_cast<unsigned>(s_info[0]), blast = static_cast<unsigned>(s_info[1]);
+  __syncthreads();
+  const int64_t r0 = bst[bfirst], r1 = bin_end(blast);  // the exchange-buffer range to read
+  uint64_t hi_key = ~0ull, lo_key = 0ull;               // key range of the local set
+  int64_t place0 = r0, place1 = r1;                     // its places
+  if (r1 - r0 > P) {
+    const int64_t lim = (P - (my1 - my0)) / 2;
+    unsigned* lh = h2;  // free now: no CTA reads counters any more
+    // cut bin b down to the sub-bin holding place p; returns its key prefix,
+    // mask and place range
+    auto cut = [&](unsigned b, int64_t p, uint64_t& pre, uint64_t& msk, int64_t& s0, int64_t& s1) -> bool {
+      pre = prefix1 | (static_cast<uint64_t>(DM - b) << shift1);
+      msk = pmask1 | (static_cast<uint64_t>(DM) << shift1);
+      const int64_t s = bst[b], e = bin_end(b);
+      s0 = s;
+      s1 = e;
+      int sh = shift1;
+      while (s1 - s0 > lim && sh > 0) {
+        const int sh2 = sh >= DB ? sh - DB : 0;
+        for (int i = tid; i < NB; i += BLOCK) lh[i] = 0u;
+        if (tid == 0) s_info[2] = ~0ull;
+        __syncthreads();
+        for (int64_t i = s + tid; i < e; i += BLOCK) {
+          const uint64_t key = __ldcg(xb + i);
+          if ((key & msk) == pre) atomicAdd(&lh[DM - static_cast<unsigned>((key >> sh2) & DM)], 1u);
+        }
+        __syncthreads();
+        unsigned cc[kPer];
+        unsigned long long csum = 0;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) { cc[q] = lh[tid * kPer + q]; csum += cc[q]; }
+        const unsigned long long cincl = block_scan_incl(csum, s_tmp);
+        unsigned long long crun = static_cast<unsigned long long>(s0) + cincl - csum;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+          if (crun <= static_cast<unsigned long long>(p) && static_cast<unsigned long long>(p) < crun + cc[q]) {
+            s_info[2] = static_cast<unsigned long long>(tid * kPer + q);
+            s_info[3] = crun;
+            s_info[4] = cc[q];
+          }
+          crun += cc[q];
+        }
+        __syncthreads();
+        if (s_info[2] == ~0ull) return false;
+        pre |= static_cast<uint64_t>(DM - static_cast<unsigned>(s_info[2])) << sh2;
+        msk |= static_cast<uint64_t>(DM) << sh2;
+        s0 = static_cast<int64_t>(s_info[3]);
+        s1 = s0 + static_cast<int64_t>(s_info[4]);
+        sh = sh2;
+        __syncthreads();
+      }
+      return true;
+    };
+    uint64_t pre, msk;
+    int64_t s0, s1;
+    bool ok = cut(bfirst, my0, pre, msk, s0, s1);
+    hi_key = pre | ~msk;
+    place0 = s0;
+    ok = ok && cut(blast, my1 - 1, pre, msk, s0, s1);
+    lo_key = pre;
+    place1 = s1;
+    if (!ok || place1 - place0 > P) {
+      if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
+      return;
+    }
+  }
+  const int n_c = static_cast<int>(place1 - place0);
+  if (r1 - r0 <= P) {
+    for (int i = tid; i < n_c; i += BLOCK) bufA[i] = __ldcg(xb + r0 + i);
+  } else {
+    if (tid == 0) s_cnt = 0u;
+    __syncthreads();
+    const unsigned lane_u = static_cast<unsigned>(lane);
+    for (int64_t iw = r0 + (tid & ~31); iw < r1; iw += BLOCK) {
+      const int64_t i = iw + lane_u;
+      const uint64_t key = i < r1 ? __ldcg(xb + i) : 0ull;
+      const bool want = i < r1 && key <= hi_key && key >= lo_key;
+      const unsigned slot = warp_append_slot(&s_cnt, want);
+      if (want && slot < static_cast<unsigned>(P)) bufA[slot] = key;
+    }
+    __syncthreads();
+    if (s_cnt != static_cast<unsigned>(n_c)) {
+      if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
+      return;
+    }
+  }
+  __syncthreads();
+  TK_STAMP(12);
+  {
+    unsigned long long lo_or, lo_and;
+    block_or_and<BLOCK>(bufA, n_c, &lo_or, &lo_and);
+    if (place_by_groups<BLOCK, NB>(bufA, n_c, lo_or ^ lo_and, 0u, ~0u, bufB, work, work + NB, work + 2 * NB,
+                                   s_tmp, 512u, a, row, k, place0, my0, my1)) {
+      TK_STAMP(13);
+      return;
+    }
+    // a group too large to rank by counting: stable LSD radix sort, one
+    // 8-bit digit per pass, of the digits on which the local keys differ
+    const uint64_t* sorted = lsd_sort<BLOCK, P>(bufA, bufB, n_c, lo_or ^ lo_and, h2);
+    for (int i = tid; i < n_c; i += BLOCK) {
+      const int64_t place = place0 + i;
+      if (place >= my0 && place < my1) write_out(a, row, k, place, sorted[i]);
+    }
+    TK_STAMP(14);
+  }
 }
 
 // Kernel variants: (block, sort positions per CTA, cache/second buffer).
-constexpr int kSmallBlock = 256, kSmallP = 1024, kSmallCB = 2048;
-constexpr int kBigBlock = 1024, kBigP = 12000, kBigCB = 12000;
-constexpr int kMaxCluster = 16;
+constexpr int kSmallBlock = 256, kSmallP = 1024, kSmallCB = 2048, kSmallNB = 256;
+constexpr int kBigBlock = 1024, kBigP = 11776, kBigCB = 11776, kBigNB = 2048;
 
-template <int BLOCK, int P, int CB, int SRC>
+template <int BLOCK, int P, int CB, int NB, int SRC>
 cudaError_t configure(int* max_g) {
-  using L = Layout<BLOCK, P, CB>;
-  auto kern = select_kernel<BLOCK, P, CB, SRC>;
+  using L = Layout<BLOCK, P, CB, NB>;
+  auto kern = select_kernel<BLOCK, P, CB, NB, SRC>;
   static int cached = 0;  // largest cluster size the device can schedule for this variant
   if (!cached) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -932,16 +993,16 @@ cudaError_t configure(int* max_g) {
   return cudaSuccess;
 }
 
-template <int BLOCK, int P, int CB, int SRC>
+template <int BLOCK, int P, int CB, int NB, int SRC>
 cudaError_t launch_variant(const SelParams& a, int64_t nsel, int G, int* used, cudaStream_t st) {
-  using L = Layout<BLOCK, P, CB>;
+  using L = Layout<BLOCK, P, CB, NB>;
   int max_g = 1;
-  cudaError_t e = configure<BLOCK, P, CB, SRC>(&max_g);
+  cudaError_t e = configure<BLOCK, P, CB, NB, SRC>(&max_g);
   if (e != cudaSuccess) return e;
   if (G > max_g) G = max_g;
   const int64_t sort_k = a.want_topk ? a.r : 1;
   if (sort_k > static_cast<int64_t>(G) * P) return cudaErrorInvalidConfiguration;
-  if (a.want_topk && G > 1 && a.xbuf == nullptr) return cudaErrorInvalidValue;
+  if (a.want_topk && a.xbuf == nullptr) return cudaErrorInvalidValue;
   *used = G;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nsel * G), 1, 1);
@@ -956,15 +1017,15 @@ cudaError_t launch_variant(const SelParams& a, int64_t nsel, int G, int* used, c
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, select_kernel<BLOCK, P, CB, SRC>, a);
+  cfg.numAttrs = pdl_edge(a.want_topk ? (a.keys ? kPdlRefine : 0u) : kPdlTau) ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, select_kernel<BLOCK, P, CB, NB, SRC>, a);
 }
 
-template <int BLOCK, int P, int CB>
+template <int BLOCK, int P, int CB, int NB>
 cudaError_t launch_src(const SelParams& a, int src, int64_t nsel, int G, int* used, cudaStream_t st) {
-  if (src == 0) return launch_variant<BLOCK, P, CB, 0>(a, nsel, G, used, st);
-  if (src == 1) return launch_variant<BLOCK, P, CB, 1>(a, nsel, G, used, st);
-  return launch_variant<BLOCK, P, CB, 2>(a, nsel, G, used, st);
+  if (src == 0) return launch_variant<BLOCK, P, CB, NB, 0>(a, nsel, G, used, st);
+  if (src == 1) return launch_variant<BLOCK, P, CB, NB, 1>(a, nsel, G, used, st);
+  return launch_variant<BLOCK, P, CB, NB, 2>(a, nsel, G, used, st);
 }
 
 
@@ -1018,24 +1079,26 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   a.xbuf = job.xbuf;
   const int src = job.keys ? 0 : (p.dtype == kF32 ? 1 : 2);
   const bool many = p.nsel >= sm_count();
+  constexpr int64_t kBigCache = kBigP + kBigCB;
   int G;
   bool small;
   if (!job.want_topk) {
-    // tau: cache every key of the slice; the whole buffer is the cache
+    // tau: every CTA caches its whole slice of the samples
     small = false;
-    G = pow2_at_least((source_hint + kBigP + kBigCB - 1) / (kBigP + kBigCB));
+    G = pow2_at_least((source_hint + kBigCache - 1) / kBigCache);
   } else if (many && job.r <= kSmallP) {
     small = true;
     G = 1;
   } else {
+    // each CTA sorts at most P places; prefer slices that fit the cache
     small = false;
     const int64_t g_min = (job.r + kBigP - 1) / kBigP;
-    const int64_t g_cache = (source_hint + kBigCB - 1) / kBigCB;
+    const int64_t g_cache = (source_hint + kBigCache - 1) / kBigCache;
     G = many ? pow2_at_least(g_min) : pow2_at_least(g_min > g_cache ? g_min : g_cache);
   }
   int used = G;
-  const cudaError_t e = small ? launch_src<kSmallBlock, kSmallP, kSmallCB>(a, src, p.nsel, G, &used, st)
-                              : launch_src<kBigBlock, kBigP, kBigCB>(a, src, p.nsel, G, &used, st);
+  const cudaError_t e = small ? launch_src<kSmallBlock, kSmallP, kSmallCB, kSmallNB>(a, src, p.nsel, G, &used, st)
+                              : launch_src<kBigBlock, kBigP, kBigCB, kBigNB>(a, src, p.nsel, G, &used, st);
   if (cluster) *cluster = used;
   return e;
 }

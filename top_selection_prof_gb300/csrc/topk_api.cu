@@ -329,9 +329,10 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     tj.want_topk = false;
     tj.tau_out = tau;
     tj.status = &hdr->status;
-    TK_TRY(launch_select(p, tj, S, nullptr, st));
+    int tau_cluster = 0;
+    TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
     TK_TRY(mark(2));
-    TK_TRY(launch_filter(p, tau, M, buf, counts, st));
+    TK_TRY(launch_filter(p, tau, M, buf, counts, overlap_sms(tau_cluster, nsel), st));
     TK_TRY(mark(3));
     TK_TRY(launch_fallback(p, k, M, buf, counts, fs, force, st));
     TK_TRY(mark(4));
@@ -481,7 +482,7 @@ int topk_prof_filter(const void* x, int dtype, int64_t rows, int64_t n, int glob
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(uint64_t) * p.nsel, st);
   if (e != cudaSuccess) return status_of(e);
-  e = launch_filter(p, tau, M, buf, reinterpret_cast<unsigned long long*>(counts), st);
+  e = launch_filter(p, tau, M, buf, reinterpret_cast<unsigned long long*>(counts), 0, st);
   return status_of(e);
 }
 

@@ -183,8 +183,9 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
     tj.r = t;
     tj.tau_out = tau;
     tj.status = &hdr->status;
-    NA_TRY(launch_select(p, tj, S, nullptr, st));
-    NA_TRY(launch_filter(p, tau, cap, buf, counts, st));
+    int tau_cluster = 0;
+    NA_TRY(launch_select(p, tj, S, &tau_cluster, st));
+    NA_TRY(launch_filter(p, tau, cap, buf, counts, overlap_sms(tau_cluster, nsel), st));
     NA_TRY(launch_fallback(p, k, cap, buf, counts, fs, 0, st));
   } else {
     NA_TRY(cudaMemsetAsync(base, 0, o_tau, st));  // header, counts, r_seen
