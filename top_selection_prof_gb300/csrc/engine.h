@@ -47,9 +47,17 @@ struct DevHeader {
 // ---- sample (kernels_sample.cu) ----------------------------------------------
 // Also resets counts[0..nsel) and the header (arrivals, status, misses) when
 // those pointers are non-null, so the filter and fallback start clean.
+// hist_add / hist_zero (nullable, kSampleHistBins counters per selection):
+// the sampled keys are counted by their leading kSampleHistBits bits into
+// hist_add (bin = kSampleHistBins - 1 - digit, largest keys first), and
+// hist_zero is cleared for the next call.  Both must be zero-initialised
+// once; they then alternate between calls.
+constexpr int kSampleHistBits = 11;
+constexpr int kSampleHistBins = 1 << kSampleHistBits;
+constexpr int64_t kSampleHistMaxRows = 16;  // selections with a sample histogram
 cudaError_t launch_sample(const Problem& p, int64_t S, uint64_t seed, uint64_t counter,
                           uint64_t* keys, unsigned long long* counts_to_zero, DevHeader* hdr,
-                          cudaStream_t st);
+                          unsigned* hist_add, unsigned* hist_zero, cudaStream_t st);
 
 // ---- filter and fallback (kernels_filter.cu) ---------------------------------
 // SMs a threshold select of nsel clusters of G blocks holds while the filter
@@ -58,11 +66,6 @@ inline int overlap_sms(int G, int64_t nsel) {
   const int64_t held = static_cast<int64_t>(G) * nsel;
   return held <= 16 ? static_cast<int>(held) : -1;
 }
-
-// reserved_sms: SMs the preceding grid (the threshold select) holds; the
-// launch may overlap that grid only when it is >= 0.
-cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
-                          unsigned long long* counts, int reserved_sms, cudaStream_t st);
 
 struct FallbackScratch {
   unsigned* ghist;        // 8 passes x 256 counters
@@ -74,6 +77,10 @@ struct FallbackScratch {
   uint64_t* tau_exact;         // per selection: exact k-th key written on a miss
 };
 constexpr int64_t kFallbackTile = 4096;
+// reserved_sms: SMs the preceding grid (the threshold select) holds; the
+// launch may overlap that grid only when it is >= 0.
+cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
+                          unsigned long long* counts, int reserved_sms, cudaStream_t st);
 // force: 0 = only rows that missed, 1 = every row (fault injection / exact path).
 cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,
                             unsigned long long* counts, const FallbackScratch& fs, int force,
@@ -92,6 +99,7 @@ struct SelectJob {
   int64_t* out_idx;
   int* status;                         // device status word (kDevBadState on inconsistency)
   uint64_t* xbuf = nullptr;            // want_topk across CTAs: 2*r keys per selection (L2 exchange)
+  const unsigned* sample_hist = nullptr;  // !want_topk: counts of the keys' leading bits (launch_sample)
 };
 // Returns the cluster size used via *cluster (may be null).
 cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source_bound, int* cluster,

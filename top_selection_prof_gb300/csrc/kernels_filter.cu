@@ -80,9 +80,14 @@ __device__ __forceinline__ uint32_t elem(const uint4& v, int e) {
   return (VEC == 1) ? (w & 0xffffu) : ((w >> ((e & 1) * 16)) & 0xffffu);
 }
 
+// The input is read exactly once: its L2 lines are marked evict-first, so
+// the stream leaves the next kernels' code, keys and buffers in L2.
+constexpr bool kStreamEvictFirst = true;
+
 template <int DT, int VEC>
-__device__ __forceinline__ uint4 load_group(const typename Dt<DT>::storage* p) {
+__device__ __forceinline__ uint4 load_group(const typename Dt<DT>::storage* p, uint64_t policy) {
   if (VEC == 1) return make_uint4(static_cast<uint32_t>(__ldg(p)), 0u, 0u, 0u);
+  if (kStreamEvictFirst) return ld_stream_v4(p, policy);
   return ld_stream_v4(p);
 }
 
@@ -300,6 +305,7 @@ __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t
   using T = typename Dt<DT>::storage;
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   const int64_t tiles_per_row = (fp.len + kTile - 1) / kTile;
+  const uint64_t pol = l2_evict_first_policy();
   int64_t cur_row = -1;
   RowTau t{};
   for (int64_t tile = tile_begin; tile < tile_end; tile += tile_step) {
@@ -315,7 +321,7 @@ __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t
     if (base + kTile <= fp.len) {
 #pragma unroll
       for (int u = 0; u < kFilterUnroll; ++u)
-        v[u] = load_group<DT, VEC>(xr + base + (u * kFilterBlock + threadIdx.x) * VEC);
+        v[u] = load_group<DT, VEC>(xr + base + (u * kFilterBlock + threadIdx.x) * VEC, pol);
 #pragma unroll
       for (int u = 0; u < kFilterUnroll; ++u)
         test_group<DT, LARGEST, VEC>(v[u], base + (u * kFilterBlock + threadIdx.x) * VEC, t, fp, st, row);
@@ -324,7 +330,7 @@ __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t
       for (int u = 0; u < kFilterUnroll; ++u) {
         const int64_t pos = base + (u * kFilterBlock + threadIdx.x) * VEC;
         if (pos < fp.len) {
-          v[u] = load_group<DT, VEC>(xr + pos);
+          v[u] = load_group<DT, VEC>(xr + pos, pol);
           test_group<DT, LARGEST, VEC>(v[u], pos, t, fp, st, row);
         }
       }
@@ -335,19 +341,6 @@ __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t
       stage_flush(st, row, fp.cap, fp.buf, fp.counts);
   }
   if (cur_row >= 0) stage_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
-}
-
-template <int DT, bool LARGEST, int VEC>
-__global__ void __launch_bounds__(kFilterBlock) filter_kernel(FilterParams fp) {
-  __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
-  __shared__ unsigned stage_n[kFilterBlock / 32];
-  grid_dependency_wait();  // tau and the zeroed counters come from the previous grid
-  if ((threadIdx.x & 31) == 0) stage_n[threadIdx.x >> 5] = 0u;
-  __syncwarp();
-  constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
-  const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
-  const Stage st{stage[threadIdx.x >> 5], &stage_n[threadIdx.x >> 5]};
-  filter_tiles<DT, LARGEST, VEC>(fp, blockIdx.x, ntiles, gridDim.x, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -422,12 +415,14 @@ __device__ unsigned block_exclusive_scan(unsigned v, unsigned* warp_sums, unsign
   return inc - v + warp_sums[warp];
 }
 
+// The miss check and the exact fallback (section 4): every block of a
+// cooperative grid runs this after the survivor counts are final.  `stage`
+// and `stage_n` are the caller's per-warp survivor stages.
 template <int DT, bool LARGEST, int VEC>
-__global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a) {
+__device__ void fallback_body(const FallbackParams& a, uint64_t (*stage)[kWarpStage],
+                                           unsigned* stage_n) {
   using T = typename Dt<DT>::storage;
   constexpr int kVKB = Dt<DT>::kKeyBits;
-  __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
-  __shared__ unsigned stage_n[kFilterBlock / 32];
   __shared__ unsigned shist[kFilterBlock / 32][256];
   __shared__ unsigned scan_tmp[32];
   __shared__ unsigned s_total;
@@ -435,10 +430,10 @@ __global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a
   __shared__ int s_tile_found;
   __shared__ unsigned long long s_found_pos;
 
-  const FilterParams& fp = a.fp;
+  // the re-filter compares against the exact threshold found here
+  FilterParams fp = a.fp;
+  fp.tau = a.fs.tau_exact;
   const FallbackScratch& fs = a.fs;
-  grid_dependency_wait();    // the survivor counts come from the filter
-  grid_launch_dependents();  // the final selection may start launching
   const int warp = threadIdx.x >> 5;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -590,6 +585,28 @@ __global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a
   }
 }
 
+template <int DT, bool LARGEST, int VEC>
+__global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a) {
+  __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
+  __shared__ unsigned stage_n[kFilterBlock / 32];
+  grid_dependency_wait();    // the survivor counts come from the filter
+  grid_launch_dependents();  // the final selection may start launching
+  fallback_body<DT, LARGEST, VEC>(a, stage, stage_n);
+}
+
+template <int DT, bool LARGEST, int VEC>
+__global__ void __launch_bounds__(kFilterBlock) filter_kernel(FilterParams fp) {
+  __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
+  __shared__ unsigned stage_n[kFilterBlock / 32];
+  grid_dependency_wait();  // tau and the zeroed counters come from the previous grid
+  if ((threadIdx.x & 31) == 0) stage_n[threadIdx.x >> 5] = 0u;
+  __syncwarp();
+  constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
+  const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
+  const Stage st{stage[threadIdx.x >> 5], &stage_n[threadIdx.x >> 5]};
+  filter_tiles<DT, LARGEST, VEC>(fp, blockIdx.x, ntiles, gridDim.x, st);
+}
+
 // One full wave: SMs x resident blocks per SM, less the SMs held by the
 // preceding grid when this launch may overlap it (programmatic dependent
 // launch): the tiles are dealt out by block index, so every block must start
@@ -665,14 +682,18 @@ cudaError_t launch_fallback_t(const FallbackParams& a, cudaStream_t st) {
 
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
                           unsigned long long* counts, int reserved_sms, cudaStream_t st) {
-  FilterParams fp{p.x, p.nsel, p.len, p.ib, p.flip, tau, cap, buf, counts, Divider{}};
+  const FilterParams fp{p.x, p.nsel, p.len, p.ib, p.flip, tau, cap, buf, counts, Divider{}};
   const bool largest = p.flip == 0;
   if (p.dtype == kF32) {
-    if (p.vec_ok) return largest ? launch_filter_t<kF32, true, 4>(fp, reserved_sms, st) : launch_filter_t<kF32, false, 4>(fp, reserved_sms, st);
-    return largest ? launch_filter_t<kF32, true, 1>(fp, reserved_sms, st) : launch_filter_t<kF32, false, 1>(fp, reserved_sms, st);
+    if (p.vec_ok) return largest ? launch_filter_t<kF32, true, 4>(fp, reserved_sms, st)
+                                 : launch_filter_t<kF32, false, 4>(fp, reserved_sms, st);
+    return largest ? launch_filter_t<kF32, true, 1>(fp, reserved_sms, st)
+                   : launch_filter_t<kF32, false, 1>(fp, reserved_sms, st);
   }
-  if (p.vec_ok) return largest ? launch_filter_t<kBF16, true, 8>(fp, reserved_sms, st) : launch_filter_t<kBF16, false, 8>(fp, reserved_sms, st);
-  return largest ? launch_filter_t<kBF16, true, 1>(fp, reserved_sms, st) : launch_filter_t<kBF16, false, 1>(fp, reserved_sms, st);
+  if (p.vec_ok) return largest ? launch_filter_t<kBF16, true, 8>(fp, reserved_sms, st)
+                               : launch_filter_t<kBF16, false, 8>(fp, reserved_sms, st);
+  return largest ? launch_filter_t<kBF16, true, 1>(fp, reserved_sms, st)
+                 : launch_filter_t<kBF16, false, 1>(fp, reserved_sms, st);
 }
 
 cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,

@@ -40,7 +40,6 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxCluster = 16;
-constexpr bool kMergeFirstPass = false;  // warp-merged counting of the first digit
 
 #ifdef TK_PHASE_TIMING
 // Debug builds only: globaltimer stamps of the first cluster's CTA 0.
@@ -54,7 +53,11 @@ __device__ unsigned long long g_cta_ns[2][16][8];  // per CTA of the first clust
   do {                                                                                     \
     if (blockIdx.x < 16 && threadIdx.x == 0) g_cta_ns[a.want_topk][blockIdx.x][(slot)] = (v); \
   } while (0)
+#define TK_DBG(slot, v) (g_cta_ns[1][15][(slot)] = (v))
 #else
+#define TK_DBG(slot, v) \
+  do {                  \
+  } while (0)
 #define TK_STAMP(i) \
   do {              \
   } while (0)
@@ -80,7 +83,8 @@ struct SelParams {
   void* out_vals;
   int64_t* out_idx;
   int* status;
-  uint64_t* xbuf;                     // 2*r keys per selection: the L2 exchange of the sort
+  uint64_t* xbuf;                     // r keys per selection: the L2 exchange of the sort
+  const unsigned* shist;              // tau only: first-digit counts of the samples (nullable)
 };
 
 // Eight consecutive source elements i0 .. i0+7 (i0 a multiple of 8) as
@@ -245,6 +249,23 @@ __device__ __forceinline__ void write_out(const SelParams& a, int64_t row, int64
   }
 }
 
+// Number of keys in src[j0, j1) greater than v.  Eight independent loads are
+// in flight per step: the loop is bound by shared-memory latency, not by the
+// compares.
+__device__ __forceinline__ unsigned count_above(const uint64_t* src, unsigned j0, unsigned j1, uint64_t v) {
+  unsigned r = 0;
+  unsigned j = j0;
+  for (; j + 8 <= j1; j += 8) {
+    uint64_t t[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) t[q] = src[j + q];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) r += t[q] > v ? 1u : 0u;
+  }
+  for (; j < j1; ++j) r += src[j] > v ? 1u : 0u;
+  return r;
+}
+
 // Places keys by counting ("Rank by Counting": a key's place is the number
 // of keys that outrank it; the keys are distinct, so places form a
 // permutation).  The n keys of src are first grouped, largest group first, by
@@ -274,6 +295,7 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
   __syncthreads();
   for (int i = tid; i < n; i += BLOCK) atomicAdd(&gcount[mask - static_cast<unsigned>((src[i] >> dsh) & mask)], 1u);
   __syncthreads();
+  TK_STAMP(22);
   unsigned c[kPer];
   unsigned long long sum = 0;
   unsigned mx = 0;
@@ -292,6 +314,8 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
   }
   atomicMax(&s_gmax, mx);
   __syncthreads();
+  TK_STAMP(23);
+  if (blockIdx.x == 0 && threadIdx.x == 0) TK_DBG(0, s_gmax);
   if (s_gmax > max_group) return false;
   for (int i = tid; i < n; i += BLOCK) {
     const uint64_t key = src[i];
@@ -299,20 +323,15 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
     grp[gstart[g] + atomicAdd(&gcur[g], 1u)] = key;
   }
   __syncthreads();
+  TK_STAMP(25);
   for (int i = tid; i < n; i += BLOCK) {
     const uint64_t v = grp[i];
     const unsigned g = mask - static_cast<unsigned>((v >> dsh) & mask);
     const unsigned g0 = gstart[g];
     if (g0 < split0 || g0 >= split1) continue;
     const unsigned g1 = g0 + gcount[g];
-    unsigned r0 = 0, r1 = 0;
-    unsigned j = g0;
-    for (; j + 1 < g1; j += 2) {
-      r0 += grp[j] > v ? 1u : 0u;
-      r1 += grp[j + 1] > v ? 1u : 0u;
-    }
-    if (j < g1) r0 += grp[j] > v ? 1u : 0u;
-    const int64_t place = base_place + g0 + r0 + r1;
+    const unsigned r = count_above(grp, g0, g1, v);
+    const int64_t place = base_place + g0 + r;
     if (place >= w0 && place < w1) write_out(a, row, kout, place, v);
   }
   return true;
@@ -510,7 +529,10 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   // is decided from sizes every CTA of the cluster sees alike.
   uint64_t* cache = bufA;
   const int64_t cache_cap = P + CB;
-  const bool fits = (valid + G - 1) / G + 2 <= cache_cap;
+  // tau from the sample histogram: the first digit is already counted, and
+  // only the boundary bucket's keys are read (streamed; cached if small)
+  const bool from_hist = NB == 2048 && !a.want_topk && a.shist != nullptr;
+  const bool fits = !from_hist && (valid + G - 1) / G + 2 <= cache_cap;
   bool cached = false;
   unsigned cache_n = 0;
   __syncthreads();
@@ -605,25 +627,58 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   unsigned* cur = work + 2 * NB;  // fill cursors
   int pass = 0;
   bool failed = false;
-  for (;; ++pass) {
+  // keys a CTA would cache for the remaining passes: in tau mode the bucket
+  // only, otherwise the bucket and everything above it
+  unsigned long long cache_need = bucket_mine;
+  bool run_passes = true;
+  if (from_hist) {
+    // The sample kernel counted the keys by their leading DB bits (bins in
+    // descending order); every CTA finds the same boundary bin from them.
+    shift = kb - DB;
+    pmask = (kb >= 64) ? 0ull : (~0ull << kb);
+    prefix = 0ull;
+    const unsigned* h = a.shist + row * NB;
+    unsigned tt[kPer];
+    unsigned long long tsum = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) { tt[q] = __ldcg(h + tid * kPer + q); tsum += tt[q]; }
+    if (tid == 0) s_info[0] = ~0ull;
+    const unsigned long long tincl = block_scan_incl(tsum, s_tmp);
+    unsigned long long trun = tincl - tsum;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      if (trun < rank && rank <= trun + tt[q]) {
+        s_info[0] = static_cast<unsigned long long>(tid * kPer + q);
+        s_info[1] = trun;
+        s_info[2] = tt[q];
+      }
+      trun += tt[q];
+    }
+    __syncthreads();
+    if (s_info[0] == ~0ull) {
+      failed = true;
+      run_passes = false;
+    } else {
+      prefix |= static_cast<uint64_t>(DM - static_cast<unsigned>(s_info[0])) << shift;
+      pmask |= static_cast<uint64_t>(DM) << shift;
+      rank -= s_info[1];
+      bucket_tot = s_info[2];
+      cache_need = bucket_tot;  // an upper bound of every CTA's share
+      run_passes = bucket_tot > kGatherMax && shift > 0;
+      if (run_passes) shift = shift >= DB ? shift - DB : 0;
+    }
+    __syncthreads();
+  }
+  for (; run_passes; ++pass) {
     unsigned* hc = h2 + (pass & 1) * NB;
-    const bool will_cache = !cached && (above_all + bucket_mine) <= static_cast<unsigned long long>(cache_cap);
+    const bool will_cache = !cached && cache_need <= static_cast<unsigned long long>(cache_cap);
     for (int i = tid; i < NB; i += BLOCK) hc[i] = 0u;
     if (tid == 0) s_cnt = 0u;
     __syncthreads();
-    // The first digit (leading exponent bits, typically) is skewed: lanes of
-    // a warp holding the same bin are merged with __match_any_sync so a hot
-    // bin takes one atomic per warp.  Later digits are close to uniform.
-    const bool merge = kMergeFirstPass && pass == 0;
-    auto count = [&](uint64_t k, bool in) {  // called by all 32 lanes
-      const bool take = in && (k & pmask) == prefix;
-      const unsigned bin = DM - static_cast<unsigned>((k >> shift) & DM);
-      if (merge) {
-        const unsigned peers = __match_any_sync(kFull, take ? bin : 0xffffffffu);
-        if (take && (peers & lanemask_lt()) == 0) atomicAdd(&hc[bin], __popc(peers));
-      } else if (take) {
-        atomicAdd(&hc[bin], 1u);
-      }
+    // (plain shared atomics: merging equal bins of a warp with
+    // __match_any_sync first measured several times slower)
+    auto count = [&](uint64_t k, bool in) {
+      if (in && (k & pmask) == prefix) atomicAdd(&hc[DM - static_cast<unsigned>((k >> shift) & DM)], 1u);
     };
     if (cached) {
       for_cache<BLOCK>(cache, cache_n, count);
@@ -631,7 +686,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
       for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t k, bool in) {
         count(k, in);
         if (will_cache) {
-          const bool want = in && k >= prefix;
+          const bool want = in && (a.want_topk ? k >= prefix : (k & pmask) == prefix);
           const unsigned slot = warp_append_slot(&s_cnt, want);
           if (want && slot < static_cast<unsigned>(cache_cap)) cache[slot] = k;
         }
@@ -648,43 +703,43 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
     }
     // totals over the cluster, this CTA's counts, and the counts of the CTAs
     // before it, for this thread's kPer consecutive bins
-    // (remote loads are issued eight CTAs at a time, before any is used)
+    // (remote loads are issued eight CTAs at a time, before any is used;
+    // CTAs start at different ranks so no CTA's counters are read by all at
+    // once; the loops run to G, not to the largest cluster)
     unsigned tt[kPer], mm[kPer], bf[kPer];
 #pragma unroll
     for (int q = 0; q < kPer; ++q) { tt[q] = 0u; bf[q] = 0u; mm[q] = hc[tid * kPer + q]; }
+    for (unsigned c0 = 0; c0 < G; c0 += 8) {
+      const unsigned nb = G - c0 < 8u ? G - c0 : 8u;
+      unsigned rv[8][kPer];
+      unsigned src = crank + c0;
+      if (src >= G) src -= G;
 #pragma unroll
-    for (int c0 = 0; c0 < kMaxCluster; c0 += 8) {
-      if (c0 < static_cast<int>(G)) {
-        unsigned rv[8][kPer];
+      for (unsigned j = 0; j < 8; ++j) {
+        if (j < nb) {
+          const unsigned* r = cluster.map_shared_rank(hc, src) + tid * kPer;
+          if constexpr (kPer == 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(r);
+            rv[j][0] = v.x;
+            rv[j][1] = v.y;
+          } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = c0 + j;
-          if (c < static_cast<int>(G)) {
-            // CTAs start at different ranks so no CTA's counters are read by all at once
-            const unsigned src = (crank + static_cast<unsigned>(c)) % G;
-            const unsigned* r = cluster.map_shared_rank(hc, src) + tid * kPer;
-            if constexpr (kPer == 2) {
-              const uint2 v = *reinterpret_cast<const uint2*>(r);
-              rv[j][0] = v.x;
-              rv[j][1] = v.y;
-            } else {
-#pragma unroll
-              for (int q = 0; q < kPer; ++q) rv[j][q] = r[q];
-            }
+            for (int q = 0; q < kPer; ++q) rv[j][q] = r[q];
           }
+          if (++src == G) src = 0;
         }
+      }
+      src = crank + c0;
+      if (src >= G) src -= G;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = c0 + j;
-          if (c < static_cast<int>(G)) {
+      for (unsigned j = 0; j < 8; ++j) {
+        if (j < nb) {
 #pragma unroll
-            const unsigned src = (crank + static_cast<unsigned>(c)) % G;
-#pragma unroll
-            for (int q = 0; q < kPer; ++q) {
-              tt[q] += rv[j][q];
-              if (src < crank) bf[q] += rv[j][q];
-            }
+          for (int q = 0; q < kPer; ++q) {
+            tt[q] += rv[j][q];
+            if (src < crank) bf[q] += rv[j][q];
           }
+          if (++src == G) src = 0;
         }
       }
     }
@@ -699,7 +754,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
       const int b = tid * kPer + q;
-      if (pass == 0 && a.want_topk) {
+      if (pass == 0 && a.want_topk && G > 1) {
         bst[b] = static_cast<unsigned>(trun);
         off[b] = static_cast<unsigned>(trun) + bf[q];
         cur[b] = 0u;
@@ -724,6 +779,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
     above_all += s_info[3];
     if (pass == 0) b1 = bin; else above_b1 += s_info[3];
     bucket_mine = s_info[4];
+    cache_need = a.want_topk ? above_all + bucket_mine : bucket_mine;
     TK_STAMP(3 + (pass < 6 ? pass : 6));
     __syncthreads();  // s_info is rewritten by the next pass
     if (bucket_tot <= kGatherMax || shift == 0) break;
@@ -740,6 +796,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   // half of its counter area the last pass did not use, and ranked by
   // counting ("Rank by Counting").  Each key carries the CTA it came from,
   // so CTA 0 also counts every CTA's winners inside the first-pass bin.
+  await_cluster();  // (when no pass ran) CTA 0 must be running before it is written
   {
     uint64_t* gb0 = cluster.map_shared_rank(reinterpret_cast<uint64_t*>(h2 + ((pass + 1) & 1) * NB), 0);
     unsigned* gc0 = cluster.map_shared_rank(&s_gcount, 0);
@@ -759,7 +816,9 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
     }
     if (tid == 0) cluster.map_shared_rank(xch, 0)[8 + crank] = above_b1;
   }
+  TK_CTA(5, globaltimer_ns());
   gsync();  // the bucket is in CTA 0
+  TK_CTA(6, globaltimer_ns());
   if (crank == 0) {
     const uint64_t* g = reinterpret_cast<const uint64_t*>(h2 + ((pass + 1) & 1) * NB);
     const unsigned n = s_gcount < kGatherMax ? s_gcount : kGatherMax;
@@ -768,9 +827,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
     __syncthreads();
     for (unsigned i = tid; i < n; i += BLOCK) {
       const uint64_t mine = g[i];
-      unsigned long long above = 0;
-      for (unsigned j = 0; j < n; ++j) above += g[j] > mine ? 1ull : 0ull;
-      if (above == rank - 1) xch[3] = mine;
+      if (count_above(g, 0u, n, mine) == rank - 1) xch[3] = mine;
     }
     __syncthreads();
     const uint64_t tau = xch[3];
@@ -797,141 +854,196 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   const uint64_t tau = xch[3];
   const int64_t k = a.r;
 
-  // ------------------------------------------------------------------ partition
-  // Every winner (key >= tau) goes to its first-pass bin's segment of the
-  // exchange buffer (bins in descending order: the bins' places).  Inside
-  // the first-pass bin of the boundary, this CTA's winners start after those
-  // of the CTAs before it.
-  uint64_t* xb = a.xbuf + row * k;
-  if (tid == 0) off[b1] = bst[b1] + static_cast<unsigned>(xch[4]);
-  __syncthreads();
-  {
-    auto put = [&](uint64_t key) {
-      const unsigned b = DM - static_cast<unsigned>((key >> shift1) & DM);
-      const unsigned pos = off[b] + atomicAdd(&cur[b], 1u);
-      if (pos < static_cast<unsigned long long>(k)) xb[pos] = key;
-    };
-    if (cached) {
-      for (unsigned i = tid; i < cache_n; i += BLOCK)
-        if (cache[i] >= tau) put(cache[i]);
-    } else {
-      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t key, bool in) {
-        if (in && key >= tau) put(key);
-      });
-    }
-  }
-  gsync();  // all winners are in the exchange buffer
-  TK_STAMP(11);
-
-  // ------------------------------------------------------------------ local sort
-  // CTA c owns the places [my0, my1).  It takes the first-pass bins that
-  // overlap them; a bin at either end that would overflow shared memory is
-  // cut, by further digits read from the exchange buffer, down to the
-  // sub-bin holding the boundary place.  The keys between the two cuts are a
-  // contiguous key range, sorted here.
-  const int64_t pe = (k + G - 1) / G;
-  const int64_t my0 = static_cast<int64_t>(crank) * pe;
-  if (my0 >= k) return;
-  const int64_t my1 = my0 + pe < k ? my0 + pe : k;
-  auto bin_end = [&](unsigned b) -> int64_t {
-    const int64_t e = (b + 1 < static_cast<unsigned>(NB)) ? static_cast<int64_t>(bst[b + 1]) : k;
-    return e < k ? e : k;
-  };
-  // bins holding places my0 and my1 - 1
-  if (tid == 0) { s_info[0] = 0; s_info[1] = 0; }
-  __syncthreads();
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const unsigned b = tid * kPer + q;
-    const int64_t s = bst[b], e = bin_end(b);
-    if (s <= my0 && my0 < e) s_info[0] = b;
-    if (s <= my1 - 1 && my1 - 1 < e) s_info[1] = b;
-  }
-  __syncthreads();
-  const unsigned bfirst = static_cast<unsigned>(s_info[0]), blast = static_cast<unsigned>(s_info[1]);
-  __syncthreads();
-  const int64_t r0 = bst[bfirst], r1 = bin_end(blast);  // the exchange-buffer range to read
-  uint64_t hi_key = ~0ull, lo_key = 0ull;               // key range of the local set
-  int64_t place0 = r0, place1 = r1;                     // its places
-  if (r1 - r0 > P) {
-    const int64_t lim = (P - (my1 - my0)) / 2;
-    unsigned* lh = h2;  // free now: no CTA reads counters any more
-    // cut bin b down to the sub-bin holding place p; returns its key prefix,
-    // mask and place range
-    auto cut = [&](unsigned b, int64_t p, uint64_t& pre, uint64_t& msk, int64_t& s0, int64_t& s1) -> bool {
-      pre = prefix1 | (static_cast<uint64_t>(DM - b) << shift1);
-      msk = pmask1 | (static_cast<uint64_t>(DM) << shift1);
-      const int64_t s = bst[b], e = bin_end(b);
-      s0 = s;
-      s1 = e;
-      int sh = shift1;
-      while (s1 - s0 > lim && sh > 0) {
-        const int sh2 = sh >= DB ? sh - DB : 0;
-        for (int i = tid; i < NB; i += BLOCK) lh[i] = 0u;
-        if (tid == 0) s_info[2] = ~0ull;
-        __syncthreads();
-        for (int64_t i = s + tid; i < e; i += BLOCK) {
-          const uint64_t key = __ldcg(xb + i);
-          if ((key & msk) == pre) atomicAdd(&lh[DM - static_cast<unsigned>((key >> sh2) & DM)], 1u);
-        }
-        __syncthreads();
-        unsigned cc[kPer];
-        unsigned long long csum = 0;
-#pragma unroll
-        for (int q = 0; q < kPer; ++q) { cc[q] = lh[tid * kPer + q]; csum += cc[q]; }
-        const unsigned long long cincl = block_scan_incl(csum, s_tmp);
-        unsigned long long crun = static_cast<unsigned long long>(s0) + cincl - csum;
-#pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-          if (crun <= static_cast<unsigned long long>(p) && static_cast<unsigned long long>(p) < crun + cc[q]) {
-            s_info[2] = static_cast<unsigned long long>(tid * kPer + q);
-            s_info[3] = crun;
-            s_info[4] = cc[q];
-          }
-          crun += cc[q];
-        }
-        __syncthreads();
-        if (s_info[2] == ~0ull) return false;
-        pre |= static_cast<uint64_t>(DM - static_cast<unsigned>(s_info[2])) << sh2;
-        msk |= static_cast<uint64_t>(DM) << sh2;
-        s0 = static_cast<int64_t>(s_info[3]);
-        s1 = s0 + static_cast<int64_t>(s_info[4]);
-        sh = sh2;
-        __syncthreads();
-      }
-      return true;
-    };
-    uint64_t pre, msk;
-    int64_t s0, s1;
-    bool ok = cut(bfirst, my0, pre, msk, s0, s1);
-    hi_key = pre | ~msk;
-    place0 = s0;
-    ok = ok && cut(blast, my1 - 1, pre, msk, s0, s1);
-    lo_key = pre;
-    place1 = s1;
-    if (!ok || place1 - place0 > P) {
-      if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
-      return;
-    }
-  }
-  const int n_c = static_cast<int>(place1 - place0);
-  if (r1 - r0 <= P) {
-    for (int i = tid; i < n_c; i += BLOCK) bufA[i] = __ldcg(xb + r0 + i);
-  } else {
+  int n_c = 0;
+  int64_t place0 = 0, my0 = 0, my1 = k;
+  if (G == 1) {
+    // One CTA holds every winner: compact them to the front of the cache
+    // (each chunk is read into registers before any of it is overwritten).
     if (tid == 0) s_cnt = 0u;
     __syncthreads();
-    const unsigned lane_u = static_cast<unsigned>(lane);
-    for (int64_t iw = r0 + (tid & ~31); iw < r1; iw += BLOCK) {
-      const int64_t i = iw + lane_u;
-      const uint64_t key = i < r1 ? __ldcg(xb + i) : 0ull;
-      const bool want = i < r1 && key <= hi_key && key >= lo_key;
-      const unsigned slot = warp_append_slot(&s_cnt, want);
-      if (want && slot < static_cast<unsigned>(P)) bufA[slot] = key;
+    if (cached) {
+      for (unsigned base = 0; base < cache_n; base += 8 * BLOCK) {
+        uint64_t kk[8];
+        unsigned wm = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const unsigned i = base + j * BLOCK + tid;
+          kk[j] = i < cache_n ? cache[i] : 0ull;
+          wm |= (i < cache_n && kk[j] >= tau ? 1u : 0u) << j;
+        }
+        // this thread's winners go to consecutive slots: a warp scan of the
+        // counts and one shared atomic per warp
+        const unsigned c = __popc(wm);
+        unsigned incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += y;
+        }
+        unsigned wbase = 0;
+        if (lane == 31 && incl) wbase = atomicAdd(&s_cnt, incl);
+        wbase = __shfl_sync(kFull, wbase, 31);
+        __syncthreads();  // the whole chunk is in registers before any slot is written
+        unsigned slot = wbase + incl - c;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if ((wm >> j) & 1u) {
+            if (slot < static_cast<unsigned>(P)) bufA[slot] = kk[j];
+            ++slot;
+          }
+        __syncthreads();
+      }
+    } else {
+      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t key, bool in) {
+        const bool w = in && key >= tau;
+        const unsigned slot = warp_append_slot(&s_cnt, w);
+        if (w && slot < static_cast<unsigned>(P)) bufA[slot] = key;
+      });
     }
     __syncthreads();
-    if (s_cnt != static_cast<unsigned>(n_c)) {
+    if (s_cnt != static_cast<unsigned>(k)) {
       if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
       return;
+    }
+    n_c = static_cast<int>(k);
+  } else {
+    // ------------------------------------------------------------------ partition
+    // Every winner (key >= tau) goes to its first-pass bin's segment of the
+    // exchange buffer (bins in descending order: the bins' places).  Inside
+    // the first-pass bin of the boundary, this CTA's winners start after those
+    // of the CTAs before it.
+    uint64_t* xb = a.xbuf + row * k;
+    if (tid == 0) off[b1] = bst[b1] + static_cast<unsigned>(xch[4]);
+    __syncthreads();
+    {
+      auto put = [&](uint64_t key) {
+        const unsigned b = DM - static_cast<unsigned>((key >> shift1) & DM);
+        const unsigned pos = off[b] + atomicAdd(&cur[b], 1u);
+        if (pos < static_cast<unsigned long long>(k)) xb[pos] = key;
+      };
+      if (cached) {
+        for (unsigned i = tid; i < cache_n; i += BLOCK)
+          if (cache[i] >= tau) put(cache[i]);
+      } else {
+        for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t key, bool in) {
+          if (in && key >= tau) put(key);
+        });
+      }
+    }
+    gsync();  // all winners are in the exchange buffer
+    TK_STAMP(11);
+
+    // ------------------------------------------------------------------ local sort
+    // CTA c owns the places [my0, my1).  It takes the first-pass bins that
+    // overlap them; a bin at either end that would overflow shared memory is
+    // cut, by further digits read from the exchange buffer, down to the
+    // sub-bin holding the boundary place.  The keys between the two cuts are a
+    // contiguous key range, sorted here.
+    const int64_t pe = (k + G - 1) / G;
+    my0 = static_cast<int64_t>(crank) * pe;
+    if (my0 >= k) return;
+    my1 = my0 + pe < k ? my0 + pe : k;
+    auto bin_end = [&](unsigned b) -> int64_t {
+      const int64_t e = (b + 1 < static_cast<unsigned>(NB)) ? static_cast<int64_t>(bst[b + 1]) : k;
+      return e < k ? e : k;
+    };
+    // bins holding places my0 and my1 - 1
+    if (tid == 0) { s_info[0] = 0; s_info[1] = 0; }
+    __syncthreads();
+  #pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const unsigned b = tid * kPer + q;
+      const int64_t s = bst[b], e = bin_end(b);
+      if (s <= my0 && my0 < e) s_info[0] = b;
+      if (s <= my1 - 1 && my1 - 1 < e) s_info[1] = b;
+    }
+    __syncthreads();
+    const unsigned bfirst = static_cast<unsigned>(s_info[0]), blast = static_cast<unsigned>(s_info[1]);
+    __syncthreads();
+    const int64_t r0 = bst[bfirst], r1 = bin_end(blast);  // the exchange-buffer range to read
+    uint64_t hi_key = ~0ull, lo_key = 0ull;               // key range of the local set
+    place0 = r0;                                          // its places
+    int64_t place1 = r1;
+    if (r1 - r0 > P) {
+      const int64_t lim = (P - (my1 - my0)) / 2;
+      unsigned* lh = h2;  // free now: no CTA reads counters any more
+      // cut bin b down to the sub-bin holding place p; returns its key prefix,
+      // mask and place range
+      auto cut = [&](unsigned b, int64_t p, uint64_t& pre, uint64_t& msk, int64_t& s0, int64_t& s1) -> bool {
+        pre = prefix1 | (static_cast<uint64_t>(DM - b) << shift1);
+        msk = pmask1 | (static_cast<uint64_t>(DM) << shift1);
+        const int64_t s = bst[b], e = bin_end(b);
+        s0 = s;
+        s1 = e;
+        int sh = shift1;
+        while (s1 - s0 > lim && sh > 0) {
+          const int sh2 = sh >= DB ? sh - DB : 0;
+          for (int i = tid; i < NB; i += BLOCK) lh[i] = 0u;
+          if (tid == 0) s_info[2] = ~0ull;
+          __syncthreads();
+          for (int64_t i = s + tid; i < e; i += BLOCK) {
+            const uint64_t key = __ldcg(xb + i);
+            if ((key & msk) == pre) atomicAdd(&lh[DM - static_cast<unsigned>((key >> sh2) & DM)], 1u);
+          }
+          __syncthreads();
+          unsigned cc[kPer];
+          unsigned long long csum = 0;
+  #pragma unroll
+          for (int q = 0; q < kPer; ++q) { cc[q] = lh[tid * kPer + q]; csum += cc[q]; }
+          const unsigned long long cincl = block_scan_incl(csum, s_tmp);
+          unsigned long long crun = static_cast<unsigned long long>(s0) + cincl - csum;
+  #pragma unroll
+          for (int q = 0; q < kPer; ++q) {
+            if (crun <= static_cast<unsigned long long>(p) && static_cast<unsigned long long>(p) < crun + cc[q]) {
+              s_info[2] = static_cast<unsigned long long>(tid * kPer + q);
+              s_info[3] = crun;
+              s_info[4] = cc[q];
+            }
+            crun += cc[q];
+          }
+          __syncthreads();
+          if (s_info[2] == ~0ull) return false;
+          pre |= static_cast<uint64_t>(DM - static_cast<unsigned>(s_info[2])) << sh2;
+          msk |= static_cast<uint64_t>(DM) << sh2;
+          s0 = static_cast<int64_t>(s_info[3]);
+          s1 = s0 + static_cast<int64_t>(s_info[4]);
+          sh = sh2;
+          __syncthreads();
+        }
+        return true;
+      };
+      uint64_t pre, msk;
+      int64_t s0, s1;
+      bool ok = cut(bfirst, my0, pre, msk, s0, s1);
+      hi_key = pre | ~msk;
+      place0 = s0;
+      ok = ok && cut(blast, my1 - 1, pre, msk, s0, s1);
+      lo_key = pre;
+      place1 = s1;
+      if (!ok || place1 - place0 > P) {
+        if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
+        return;
+      }
+    }
+    n_c = static_cast<int>(place1 - place0);
+    if (r1 - r0 <= P) {
+      for (int i = tid; i < n_c; i += BLOCK) bufA[i] = __ldcg(xb + r0 + i);
+    } else {
+      if (tid == 0) s_cnt = 0u;
+      __syncthreads();
+      const unsigned lane_u = static_cast<unsigned>(lane);
+      for (int64_t iw = r0 + (tid & ~31); iw < r1; iw += BLOCK) {
+        const int64_t i = iw + lane_u;
+        const uint64_t key = i < r1 ? __ldcg(xb + i) : 0ull;
+        const bool want = i < r1 && key <= hi_key && key >= lo_key;
+        const unsigned slot = warp_append_slot(&s_cnt, want);
+        if (want && slot < static_cast<unsigned>(P)) bufA[slot] = key;
+      }
+      __syncthreads();
+      if (s_cnt != static_cast<unsigned>(n_c)) {
+        if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
+        return;
+      }
     }
   }
   __syncthreads();
@@ -958,6 +1070,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
 // Kernel variants: (block, sort positions per CTA, cache/second buffer).
 constexpr int kSmallBlock = 256, kSmallP = 1024, kSmallCB = 2048, kSmallNB = 256;
 constexpr int kBigBlock = 1024, kBigP = 11776, kBigCB = 11776, kBigNB = 2048;
+constexpr int64_t kTauSlice = 8192;  // samples streamed per CTA when tau starts from the histogram
 
 template <int BLOCK, int P, int CB, int NB, int SRC>
 cudaError_t configure(int* max_g) {
@@ -1077,12 +1190,17 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   a.out_idx = job.out_idx;
   a.status = job.status;
   a.xbuf = job.xbuf;
+  a.shist = job.want_topk ? nullptr : job.sample_hist;
   const int src = job.keys ? 0 : (p.dtype == kF32 ? 1 : 2);
   const bool many = p.nsel >= sm_count();
   constexpr int64_t kBigCache = kBigP + kBigCB;
   int G;
   bool small;
-  if (!job.want_topk) {
+  if (!job.want_topk && job.sample_hist) {
+    // tau from the sample histogram: one streaming pass for the bucket
+    small = false;
+    G = pow2_at_least((source_hint + kTauSlice - 1) / kTauSlice);
+  } else if (!job.want_topk) {
     // tau: every CTA caches its whole slice of the samples
     small = false;
     G = pow2_at_least((source_hint + kBigCache - 1) / kBigCache);

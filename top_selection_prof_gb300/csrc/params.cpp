@@ -164,11 +164,11 @@ bool choose_params(int64_t n, int64_t k, double eps, const ParamRule& pr, int64_
 bool pdl_edge(unsigned bit) {
   // Programmatic dependent launch per pipeline edge (bits: 1 threshold
   // select, 2 filter, 4 fallback, 8 refinement).  On by default for the
-  // edges where it shortens the pipeline (1, 2, 8); TOPK_PDL_MASK overrides
+  // edges where it shortens the pipeline (1, 8); TOPK_PDL_MASK overrides
   // (0 turns it off).
   static const unsigned mask = [] {
     const char* m = std::getenv("TOPK_PDL_MASK");
-    return m ? static_cast<unsigned>(std::strtoul(m, nullptr, 0)) : (kPdlTau | kPdlFilter | kPdlRefine);
+    return m ? static_cast<unsigned>(std::strtoul(m, nullptr, 0)) : (kPdlTau | kPdlRefine);
   }();
   return (mask & bit) != 0;
 }

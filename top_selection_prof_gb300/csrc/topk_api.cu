@@ -12,6 +12,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -31,13 +32,14 @@ std::atomic<uint64_t> g_counter{0};
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
+  uint64_t sample_calls = 0;  // calls whose sample kernel launched: picks the histogram half
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
 // Returns a device block of at least `bytes` for this (device, stream); grows
 // with stream-ordered allocation (the old block is released in stream order).
-cudaError_t workspace(cudaStream_t st, size_t bytes, void** out) {
+cudaError_t workspace(cudaStream_t st, size_t bytes, void** out, Workspace** entry = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -56,8 +58,19 @@ cudaError_t workspace(cudaStream_t st, size_t bytes, void** out) {
     w.bytes = grow;
   }
   *out = w.ptr;
+  if (entry) *entry = &w;
   return cudaSuccess;
 }
+
+// Every workspace starts with the same prefix, whatever the call's layout:
+// the device header, then two halves of the sample histograms.  The halves
+// alternate between Prof-K calls: a call's sample kernel counts into one and
+// clears the other for the next call, so they stay zero between calls
+// without a memset (the block is zeroed once when it is allocated).
+size_t align_up(size_t v);
+constexpr size_t kHistHalfBytes = sizeof(unsigned) * kSampleHistBins * kSampleHistMaxRows;
+size_t ws_hist_offset() { return align_up(sizeof(DevHeader)); }
+size_t ws_prefix() { return ws_hist_offset() + 2 * kHistHalfBytes; }
 
 size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -255,7 +268,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   if (plan.path == TOPK_PATH_DIRECT) {
     // the status word and the sort's exchange buffer
     void* ws = nullptr;
-    TK_TRY(workspace(st, 256 + sizeof(uint64_t) * 2 * p.nsel * k, &ws));
+    TK_TRY(workspace(st, ws_prefix() + sizeof(uint64_t) * p.nsel * k, &ws));
     DevHeader* hdr = static_cast<DevHeader*>(ws);
     TK_TRY(cudaMemsetAsync(&hdr->status, 0, sizeof(int), st));
     SelectJob job{};
@@ -265,7 +278,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     job.out_vals = out_vals;
     job.out_idx = out_idx;
     job.status = &hdr->status;
-    job.xbuf = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + 256);
+    job.xbuf = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + ws_prefix());
     TK_TRY(launch_select(p, job, p.len, &cluster, st));
     if (stats) {
       stats->cluster = cluster;
@@ -283,8 +296,8 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   const int64_t M = plan.path == TOPK_PATH_PROFK ? plan.M : k;
   const int64_t S = plan.S;
   const int64_t ntile = (p.len + kFallbackTile - 1) / kFallbackTile;
-  size_t off = 0;
-  const size_t o_hdr = off; off = align_up(off + sizeof(DevHeader));
+  const size_t o_hdr = 0;
+  size_t off = ws_prefix();
   const size_t o_counts = off; off = align_up(off + sizeof(unsigned long long) * nsel);
   const size_t o_rseen = off; off = align_up(off + sizeof(unsigned long long) * nsel);
   const size_t o_tau = off; off = align_up(off + sizeof(uint64_t) * nsel);
@@ -293,9 +306,10 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   const size_t o_tiles = off; off = align_up(off + sizeof(unsigned) * ntile);
   const size_t o_samples = off; off = align_up(off + sizeof(uint64_t) * nsel * S);
   const size_t o_buf = off; off = align_up(off + sizeof(uint64_t) * nsel * M);
-  const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * 2 * nsel * k);
+  const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * nsel * k);
   void* ws = nullptr;
-  TK_TRY(workspace(st, off, &ws));
+  Workspace* wentry = nullptr;
+  TK_TRY(workspace(st, off, &ws, &wentry));
   char* base = static_cast<char*>(ws);
   DevHeader* hdr = reinterpret_cast<DevHeader*>(base + o_hdr);
   auto* counts = reinterpret_cast<unsigned long long*>(base + o_counts);
@@ -320,7 +334,19 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   };
   if (plan.path == TOPK_PATH_PROFK) {
     TK_TRY(mark(0));
-    TK_TRY(launch_sample(p, S, seed, counter, samples, counts, hdr, st));
+    unsigned* hist_add = nullptr;
+    unsigned* hist_zero = nullptr;
+    if (nsel <= kSampleHistMaxRows) {
+      char* halves = base + ws_hist_offset();
+      const uint64_t parity = wentry->sample_calls & 1u;
+      hist_add = reinterpret_cast<unsigned*>(halves + parity * kHistHalfBytes);
+      hist_zero = reinterpret_cast<unsigned*>(halves + (parity ^ 1u) * kHistHalfBytes);
+    }
+    TK_TRY(launch_sample(p, S, seed, counter, samples, counts, hdr, hist_add, hist_zero, st));
+    if (hist_add) {
+      std::lock_guard<std::mutex> lock(g_ws_mu);
+      ++wentry->sample_calls;
+    }
     TK_TRY(mark(1));
     SelectJob tj{};
     tj.keys = samples;
@@ -328,16 +354,23 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     tj.r = plan.t;
     tj.want_topk = false;
     tj.tau_out = tau;
+    tj.sample_hist = hist_add;
     tj.status = &hdr->status;
     int tau_cluster = 0;
     TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
+#ifdef TK_PHASE_TIMING
+    if (std::getenv("TK_DEBUG_TWICE")) TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
+#endif
     TK_TRY(mark(2));
+    // the filter grid also checks for misses and falls back in place; a
+    // forced miss uses the separate fallback launch
     TK_TRY(launch_filter(p, tau, M, buf, counts, overlap_sms(tau_cluster, nsel), st));
     TK_TRY(mark(3));
     TK_TRY(launch_fallback(p, k, M, buf, counts, fs, force, st));
     TK_TRY(mark(4));
   } else {  // TOPK_PATH_EXACT
-    TK_TRY(cudaMemsetAsync(base, 0, o_tau, st));  // header, counts, r_seen
+    TK_TRY(cudaMemsetAsync(base, 0, sizeof(DevHeader), st));
+    TK_TRY(cudaMemsetAsync(base + o_counts, 0, o_tau - o_counts, st));  // counts, r_seen
     TK_TRY(launch_fallback(p, k, M, buf, counts, fs, 1, st));
   }
   SelectJob rj{};
@@ -350,7 +383,9 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
   rj.xbuf = xbuf;
-  // expected survivors: E[R] = t (N+1)/(S+1) (Lemma 1, Eq. 2), with headroom
+  // expected survivors: E[R] = t (N+1)/(S+1) (Lemma 1, Eq. 2), with
+  // headroom.  Only the cluster size depends on it; survivors beyond what the
+  // cluster caches are streamed from L2, which a single CTA does slowly.
   int64_t hint = M;
   if (plan.path == TOPK_PATH_PROFK) {
     const double er = static_cast<double>(plan.t) * (static_cast<double>(p.len) + 1.0) /
@@ -359,6 +394,9 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     if (hint < k) hint = k;
   }
   TK_TRY(launch_select(p, rj, hint, &cluster, st));
+#ifdef TK_PHASE_TIMING
+  if (std::getenv("TK_DEBUG_TWICE")) TK_TRY(launch_select(p, rj, hint, &cluster, st));
+#endif
   if (plan.path == TOPK_PATH_PROFK) TK_TRY(mark(5));
 
   if (stats) {
@@ -468,7 +506,7 @@ int topk_prof_sample(const void* x, int dtype, int64_t rows, int64_t n, int glob
   const Problem p = make_problem(x, dtype, rows, n, largest, global != 0);
   if (p.nsel > 65535) return TOPK_EUNSUPPORTED;
   const cudaError_t e = launch_sample(p, S, seed, static_cast<uint64_t>(counter), out_keys, nullptr,
-                                      nullptr, static_cast<cudaStream_t>(stream));
+                                      nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
   return status_of(e);
 }
 

@@ -176,7 +176,7 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
     static uint64_t calls = 0;  // Philox call counter of this entry point
     const uint64_t counter = __atomic_fetch_add(&calls, 1, __ATOMIC_RELAXED);
     auto* samples = reinterpret_cast<uint64_t*>(base + o_samples);
-    NA_TRY(launch_sample(p, S, 0x243F6A8885A308D3ull, counter, samples, counts, hdr, st));
+    NA_TRY(launch_sample(p, S, 0x243F6A8885A308D3ull, counter, samples, counts, hdr, nullptr, nullptr, st));
     SelectJob tj{};
     tj.keys = samples;
     tj.key_stride = S;
