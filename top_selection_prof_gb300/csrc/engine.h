@@ -100,6 +100,12 @@ struct SelectJob {
   int* status;                         // device status word (kDevBadState on inconsistency)
   uint64_t* xbuf = nullptr;            // want_topk across CTAs: 2*r keys per selection (L2 exchange)
   const unsigned* sample_hist = nullptr;  // !want_topk: counts of the keys' leading bits (launch_sample)
+  // refinement of the Prof-K buffer: check for a miss (counts[row] < r or >
+  // key_stride, or force_miss) and then select from the whole row of x
+  bool check_miss = false;
+  bool force_miss = false;
+  unsigned long long* r_seen = nullptr;   // per selection: R as the filter left it
+  unsigned long long* misses = nullptr;   // incremented once per missed selection
 };
 // Returns the cluster size used via *cluster (may be null).
 cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source_bound, int* cluster,

@@ -67,10 +67,10 @@ __device__ unsigned long long g_cta_ns[2][16][8];  // per CTA of the first clust
 #endif
 
 struct SelParams {
-  const uint64_t* keys;               // key source (SRC == 0)
+  const uint64_t* keys;               // key source (SRC 0, or 3 unless the selection missed)
   int64_t key_stride;
   const unsigned long long* counts;   // valid keys per selection (nullable)
-  const void* x;                      // the input (SRC != 0, and for output values)
+  const void* x;                      // the input (SRC 1 / 2, after a miss, and for output values)
   int64_t len;                        // elements per selection of x
   int ib;
   uint32_t flip;
@@ -85,14 +85,35 @@ struct SelParams {
   int* status;
   uint64_t* xbuf;                     // r keys per selection: the L2 exchange of the sort
   const unsigned* shist;              // tau only: first-digit counts of the samples (nullable)
+  // refinement of a candidate buffer: when R < r or R > key_stride (a miss;
+  // or force), select from x instead (source 1 = f32, 2 = bf16; 0 = no check)
+  int miss_src;
+  int force;
+  unsigned long long* r_seen;         // per selection: R as the filter left it
+  unsigned long long* misses;         // selections that missed
 };
+
+// Source of the refinement kernel (template source 3), chosen at run time:
+// 0 = the candidate buffer, or after a miss 1 / 2 = x as f32 / bf16.
+__shared__ int s_source;
 
 // Eight consecutive source elements i0 .. i0+7 (i0 a multiple of 8) as
 // composite keys.  Only elements in [lo, hi) are meaningful; vector loads may
 // also read neighbours that lie inside the same row.
 template <int SRC>
 __device__ __forceinline__ void load8(const SelParams& a, int64_t row, int64_t i0, int64_t lo, int64_t hi,
+                                      uint64_t (&k)[8]);
+
+template <int SRC>
+__device__ __forceinline__ void load8(const SelParams& a, int64_t row, int64_t i0, int64_t lo, int64_t hi,
                                       uint64_t (&k)[8]) {
+  if (SRC == 3) {
+    const int src = s_source;
+    if (src == 0) load8<0>(a, row, i0, lo, hi, k);
+    else if (src == 1) load8<1>(a, row, i0, lo, hi, k);
+    else load8<2>(a, row, i0, lo, hi, k);
+    return;
+  }
   if (SRC == 0) {
     const uint64_t* base = a.keys + row * a.key_stride;
     if (a.key_vec && i0 + 8 <= a.key_stride) {
@@ -467,7 +488,7 @@ struct Layout {
 };
 
 template <int BLOCK, int P, int CB, int NB, int SRC>
-__global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelParams a) {
+__device__ __forceinline__ void select_body(const SelParams& a) {
   using L = Layout<BLOCK, P, CB, NB>;
   constexpr int DB = L::kDigitBits;
   constexpr unsigned DM = NB - 1;
@@ -492,10 +513,6 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   const int64_t row = blockIdx.x / G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // programmatic dependent launch: everything below may read what earlier
-  // grids wrote, so wait for them; the next grid may begin launching now
-  grid_dependency_wait();
-  grid_launch_dependents();
   // Shared memory of another CTA may be used only once that CTA runs: arrive
   // now, wait before the first remote access.
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -511,8 +528,9 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
     if (G > 1) cluster.sync(); else __syncthreads();
   };
 
-  int64_t valid = (SRC == 0) ? a.key_stride : a.len;
-  if (SRC == 0 && a.counts) {
+  const bool from_buf = SRC == 0 || (SRC == 3 && s_source == 0);
+  int64_t valid = from_buf ? a.key_stride : a.len;
+  if (from_buf && a.counts) {
     const unsigned long long c = __ldcg(a.counts + row);
     if (c < static_cast<unsigned long long>(valid)) valid = static_cast<int64_t>(c);
   }
@@ -538,7 +556,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   __syncthreads();
   if (fits) {
     const unsigned n = static_cast<unsigned>(se - sb);
-    if (SRC == 0) {
+    if (from_buf) {
       const uint64_t* from = a.keys + row * a.key_stride + sb;
       if (a.key_vec) {
         for (unsigned i = 2 * tid; i + 1 < n; i += 2 * BLOCK) cp_async16(cache + i, from + i);
@@ -1067,6 +1085,34 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   }
 }
 
+template <int BLOCK, int P, int CB, int NB, int SRC>
+__global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelParams a) {
+  // programmatic dependent launch: everything below may read what earlier
+  // grids wrote, so wait for them; the next grid may begin launching now
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if constexpr (SRC == 3) {
+    // The miss check of the refinement (section 4): with fewer than r
+    // survivors, or more than the buffer holds, the candidates cannot give
+    // the exact answer, and the whole row of x is the source instead.  Every
+    // CTA of the cluster reads the same count, so all take the same branch.
+    cg::cluster_group cluster = cg::this_cluster();
+    const int64_t row = blockIdx.x / cluster.num_blocks();
+    if (threadIdx.x == 0) {
+      const unsigned long long R = __ldcg(a.counts + row);
+      const bool miss = a.force || R < static_cast<unsigned long long>(a.r) ||
+                        R > static_cast<unsigned long long>(a.key_stride);
+      s_source = miss ? a.miss_src : 0;
+      if (cluster.block_rank() == 0) {
+        a.r_seen[row] = R;
+        if (miss) atomicAdd(a.misses, 1ull);
+      }
+    }
+    __syncthreads();
+  }
+  select_body<BLOCK, P, CB, NB, SRC>(a);
+}
+
 // Kernel variants: (block, sort positions per CTA, cache/second buffer).
 constexpr int kSmallBlock = 256, kSmallP = 1024, kSmallCB = 2048, kSmallNB = 256;
 constexpr int kBigBlock = 1024, kBigP = 11776, kBigCB = 11776, kBigNB = 2048;
@@ -1138,7 +1184,8 @@ template <int BLOCK, int P, int CB, int NB>
 cudaError_t launch_src(const SelParams& a, int src, int64_t nsel, int G, int* used, cudaStream_t st) {
   if (src == 0) return launch_variant<BLOCK, P, CB, NB, 0>(a, nsel, G, used, st);
   if (src == 1) return launch_variant<BLOCK, P, CB, NB, 1>(a, nsel, G, used, st);
-  return launch_variant<BLOCK, P, CB, NB, 2>(a, nsel, G, used, st);
+  if (src == 2) return launch_variant<BLOCK, P, CB, NB, 2>(a, nsel, G, used, st);
+  return launch_variant<BLOCK, P, CB, NB, 3>(a, nsel, G, used, st);
 }
 
 
@@ -1191,7 +1238,13 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   a.status = job.status;
   a.xbuf = job.xbuf;
   a.shist = job.want_topk ? nullptr : job.sample_hist;
-  const int src = job.keys ? 0 : (p.dtype == kF32 ? 1 : 2);
+  if (job.want_topk && job.keys && job.check_miss) {
+    a.miss_src = p.dtype == kF32 ? 1 : 2;
+    a.force = job.force_miss ? 1 : 0;
+    a.r_seen = job.r_seen;
+    a.misses = job.misses;
+  }
+  const int src = job.keys ? (a.miss_src ? 3 : 0) : (p.dtype == kF32 ? 1 : 2);
   const bool many = p.nsel >= sm_count();
   constexpr int64_t kBigCache = kBigP + kBigCB;
   int G;

@@ -6,9 +6,11 @@
 //   sample_kernel    S Philox draws per selection -> composite keys
 //   select_kernel    t-th largest sampled key -> tau             (stage 2)
 //   filter_kernel    one pass over x, keys >= tau -> buffer, R    (stage 3)
-//   fallback_kernel  exits at once unless R < k or R > M; then exact (stage 4)
-//   select_kernel    exact top-k of the buffer, sorted -> outputs (stage 4)
-// The miss decision is made on the device by the fallback kernel itself.
+//   select_kernel    exact top-k of the buffer, sorted -> outputs (stage 4);
+//                    on a miss (R < k or R > M) it selects from x instead
+// The miss decision is made on the device by the refinement kernel itself.
+// The exact path (no Prof-K) runs the grid-wide fallback_kernel and then the
+// same sort.
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -366,7 +368,8 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // forced miss uses the separate fallback launch
     TK_TRY(launch_filter(p, tau, M, buf, counts, overlap_sms(tau_cluster, nsel), st));
     TK_TRY(mark(3));
-    TK_TRY(launch_fallback(p, k, M, buf, counts, fs, force, st));
+    // the miss check (and, on a miss, the selection from x) is part of the
+    // refinement kernel: no launch is spent on it when nothing missed
     TK_TRY(mark(4));
   } else {  // TOPK_PATH_EXACT
     TK_TRY(cudaMemsetAsync(base, 0, sizeof(DevHeader), st));
@@ -383,6 +386,12 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
   rj.xbuf = xbuf;
+  if (plan.path == TOPK_PATH_PROFK) {
+    rj.check_miss = true;
+    rj.force_miss = force != 0;
+    rj.r_seen = r_seen;
+    rj.misses = &hdr->misses;
+  }
   // expected survivors: E[R] = t (N+1)/(S+1) (Lemma 1, Eq. 2), with
   // headroom.  Only the cluster size depends on it; survivors beyond what the
   // cluster caches are streamed from L2, which a single CTA does slowly.

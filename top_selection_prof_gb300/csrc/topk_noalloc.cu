@@ -186,7 +186,6 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
     int tau_cluster = 0;
     NA_TRY(launch_select(p, tj, S, &tau_cluster, st));
     NA_TRY(launch_filter(p, tau, cap, buf, counts, overlap_sms(tau_cluster, nsel), st));
-    NA_TRY(launch_fallback(p, k, cap, buf, counts, fs, 0, st));
   } else {
     NA_TRY(cudaMemsetAsync(base, 0, o_tau, st));  // header, counts, r_seen
     NA_TRY(launch_fallback(p, k, cap, buf, counts, fs, 1, st));
@@ -201,6 +200,11 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
   rj.xbuf = reinterpret_cast<uint64_t*>(base + o_xbuf);
+  if (path == TOPK_PATH_PROFK) {  // the refinement checks for a miss itself
+    rj.check_miss = true;
+    rj.r_seen = reinterpret_cast<unsigned long long*>(base + o_rseen);
+    rj.misses = &hdr->misses;
+  }
   NA_TRY(launch_select(p, rj, cap, nullptr, st));
 #undef NA_TRY
   return TOPK_OK;
