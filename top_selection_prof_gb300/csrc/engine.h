@@ -86,6 +86,12 @@ cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* 
                             unsigned long long* counts, const FallbackScratch& fs, int force,
                             cudaStream_t st);
 
+// ---- direct path for many short rows (kernels_rows.cu) -----------------------
+// One block per selection, the row in registers: len <= 32768, k <= 1024.
+bool rows_supported(const Problem& p, int64_t k);
+cudaError_t launch_rows(const Problem& p, int64_t k, void* out_vals, int64_t* out_idx, int* status,
+                        cudaStream_t st);
+
 // ---- final selection (kernels_select.cu) -------------------------------------
 struct SelectJob {
   // source: either composite keys (keys != nullptr) or the raw input (p.x)
@@ -113,6 +119,7 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
 int64_t select_max_k();
 #ifdef TK_PHASE_TIMING
 int debug_phase_ns(unsigned long long* out);  // debug builds: per-phase timer stamps
+int debug_rows_ns(unsigned long long* out);   // debug builds: stamps of the short-row kernel
 #endif
 
 }  // namespace tk

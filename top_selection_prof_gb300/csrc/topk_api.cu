@@ -267,6 +267,27 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   }
 
   int cluster = 0;
+  if (plan.path == TOPK_PATH_DIRECT && rows_supported(p, k)) {
+    // short rows: one block per row, the row in registers; the status word
+    // is only kept when the caller asks for statistics
+    int* status = nullptr;
+    if (stats) {
+      void* ws = nullptr;
+      TK_TRY(workspace(st, ws_prefix(), &ws));
+      status = &static_cast<DevHeader*>(ws)->status;
+      TK_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
+    }
+    TK_TRY(launch_rows(p, k, out_vals, out_idx, status, st));
+    if (stats) {
+      stats->cluster = 1;
+      stats->R = p.len;
+      int dstat = 0;
+      TK_TRY(cudaMemcpyAsync(&dstat, status, sizeof(int), cudaMemcpyDeviceToHost, st));
+      TK_TRY(cudaStreamSynchronize(st));
+      if (dstat != kDevOk) return dstat == kDevTimeout ? TOPK_ETIMEOUT : TOPK_ECUDA;
+    }
+    return TOPK_OK;
+  }
   if (plan.path == TOPK_PATH_DIRECT) {
     // the status word and the sort's exchange buffer
     void* ws = nullptr;
@@ -502,6 +523,7 @@ int topk_version(void) { return 100; }
 
 #ifdef TK_PHASE_TIMING
 int topk_debug_phase_ns(unsigned long long* out) { return tk::debug_phase_ns(out); }
+int topk_debug_rows_ns(unsigned long long* out) { return tk::debug_rows_ns(out); }
 #endif
 
 int topk_index_bits(int64_t len) { return len < 1 ? 1 : index_bits(len); }

@@ -133,6 +133,11 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
   const size_t o_samples = off; off = up256(off + sizeof(uint64_t) * nsel * S);
   const size_t o_buf = off; off = up256(off + sizeof(uint64_t) * nsel * cap);
   const size_t o_xbuf = off; off = up256(off + sizeof(uint64_t) * 2 * nsel * k);
+  if (path == TOPK_PATH_DIRECT && rows_supported(p, k)) {
+    // short rows: one block per row, the row in registers, no scratch at all
+    const cudaError_t er = launch_rows(p, k, out_vals, out_idx, nullptr, st);
+    return er == cudaSuccess ? TOPK_OK : to_status(er);
+  }
   if (path == TOPK_PATH_DIRECT) {
     // the direct path needs only the header and the sort's exchange buffer
     if (up256(sizeof(DevHeader)) + sizeof(uint64_t) * 2 * nsel * k > kNoAllocScratchBytes)
