@@ -90,18 +90,17 @@ __device__ __forceinline__ unsigned scan_incl(unsigned v, unsigned* tmp) {
   return v + tmp[warp];  // (callers pass another barrier before tmp is written again)
 }
 
-// Number of keys in src[j0, j1) greater than v (eight loads in flight).
+// Number of keys in src[j0, j1) greater than v: rounds of eight independent,
+// predicated loads (a slot past j1 reads as key 0, which is never greater).
 __device__ __forceinline__ unsigned count_greater(const uint64_t* src, unsigned j0, unsigned j1, uint64_t v) {
   unsigned r = 0;
-  unsigned j = j0;
-  for (; j + 8 <= j1; j += 8) {
+  for (unsigned j = j0; j < j1; j += 8) {
     uint64_t t[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) t[q] = src[j + q];
+    for (int q = 0; q < 8; ++q) t[q] = j + q < j1 ? src[j + q] : 0ull;
 #pragma unroll
     for (int q = 0; q < 8; ++q) r += t[q] > v ? 1u : 0u;
   }
-  for (; j < j1; ++j) r += src[j] > v ? 1u : 0u;
   return r;
 }
 

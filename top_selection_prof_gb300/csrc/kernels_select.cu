@@ -270,20 +270,19 @@ __device__ __forceinline__ void write_out(const SelParams& a, int64_t row, int64
   }
 }
 
-// Number of keys in src[j0, j1) greater than v.  Eight independent loads are
-// in flight per step: the loop is bound by shared-memory latency, not by the
-// compares.
+// Number of keys in src[j0, j1) greater than v.  Rounds of eight
+// independent, predicated loads (a slot past j1 reads as key 0, which is
+// never greater): the loop is bound by shared-memory latency, not by the
+// compares, so no round may wait on the previous one.
 __device__ __forceinline__ unsigned count_above(const uint64_t* src, unsigned j0, unsigned j1, uint64_t v) {
   unsigned r = 0;
-  unsigned j = j0;
-  for (; j + 8 <= j1; j += 8) {
+  for (unsigned j = j0; j < j1; j += 8) {
     uint64_t t[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) t[q] = src[j + q];
+    for (int q = 0; q < 8; ++q) t[q] = j + q < j1 ? src[j + q] : 0ull;
 #pragma unroll
     for (int q = 0; q < 8; ++q) r += t[q] > v ? 1u : 0u;
   }
-  for (; j < j1; ++j) r += src[j] > v ? 1u : 0u;
   return r;
 }
 
@@ -355,6 +354,10 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
     const int64_t place = base_place + g0 + r;
     if (place >= w0 && place < w1) write_out(a, row, kout, place, v);
   }
+#ifdef TK_PHASE_TIMING
+  __syncthreads();
+  TK_STAMP(26);
+#endif
   return true;
 }
 
@@ -471,7 +474,7 @@ struct Layout {
   // scratch of the local LSD sort: per-warp counters, totals, bases, partials
   static constexpr int kLsdWords = kWarps * 256 + 2 * 256 + kQuarters * 256;
   static constexpr int kWorkWords = (3 * NB > kLsdWords - 2 * NB) ? 3 * NB : kLsdWords - 2 * NB;
-  static constexpr unsigned kGather = NB / 2 < 512 ? NB / 2 : 512;  // keys gathered into CTA 0
+  static constexpr unsigned kGather = NB / 2 < 1024 ? NB / 2 : 1024;  // keys gathered into CTA 0
   static constexpr size_t kBufA = 0;
   static constexpr size_t kBufB = kBufA + sizeof(uint64_t) * P;
   static constexpr size_t kH2 = kBufB + sizeof(uint64_t) * CB;     // 2 x NB counters (cluster-visible)
@@ -842,10 +845,71 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     const unsigned n = s_gcount < kGatherMax ? s_gcount : kGatherMax;
     if (tid == 0) xch[3] = 0ull;
     if (tid == 0 && s_gcount > kGatherMax) atomicCAS(a.status, kDevOk, kDevBadState);
+    // Local radix passes (8-bit digits, below the keys' highest varying bit)
+    // narrow the bucket to at most 32 keys, which are then ranked by
+    // counting: counting all of up to kGather keys against each other would
+    // cost n^2 / 32 shared-memory wavefronts.  The counters of the last
+    // cluster pass (h2's other half) are free here.
+    if (n <= 128u) {  // small: count directly (n^2 / 32 wavefronts is cheap)
+      __syncthreads();
+      for (unsigned i = tid; i < n; i += BLOCK)
+        if (count_above(g, 0u, n, g[i]) == rank - 1) xch[3] = g[i];
+    } else {
+    unsigned* lh = h2 + (pass & 1) * NB;  // 256 counters
+    uint64_t* small = reinterpret_cast<uint64_t*>(s_tmp);  // <= 32 keys (the scans are done by then)
+    {
+      unsigned long long o = 0, d = ~0ull;
+      for (unsigned i = tid; i < n; i += BLOCK) { o |= g[i]; d &= g[i]; }
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) {
+        o |= __shfl_xor_sync(kFull, o, m);
+        d &= __shfl_xor_sync(kFull, d, m);
+      }
+      if (tid == 0) { s_info[0] = 0ull; s_info[1] = ~0ull; }
+      __syncthreads();
+      if (lane == 0) { atomicOr(&s_info[0], o); atomicAnd(&s_info[1], d); }
+      __syncthreads();
+    }
+    const unsigned long long gv = s_info[0] ^ s_info[1];
     __syncthreads();
-    for (unsigned i = tid; i < n; i += BLOCK) {
-      const uint64_t mine = g[i];
-      if (count_above(g, 0u, n, mine) == rank - 1) xch[3] = mine;
+    int lsh = gv ? 63 - __clzll(static_cast<long long>(gv)) : 0;
+    lsh = lsh >= 7 ? lsh - 7 : 0;
+    uint64_t lpre = 0, lmsk = 0;
+    unsigned long long lrank = rank, lcnt = n;
+#pragma unroll 1
+    while (lcnt > 32) {
+      for (int i = tid; i < 256; i += BLOCK) lh[i] = 0u;
+      __syncthreads();
+      for (unsigned i = tid; i < n; i += BLOCK)
+        if ((g[i] & lmsk) == lpre) atomicAdd(&lh[255u - static_cast<unsigned>((g[i] >> lsh) & 255u)], 1u);
+      __syncthreads();
+      const unsigned long long c = tid < 256 ? lh[tid] : 0ull;
+      const unsigned long long incl = block_scan_incl(c, s_tmp);
+      if (tid < 256 && incl - c < lrank && lrank <= incl) {
+        s_info[0] = static_cast<unsigned long long>(tid);
+        s_info[1] = incl - c;
+        s_info[2] = c;
+      }
+      __syncthreads();
+      lpre |= static_cast<uint64_t>(255u - static_cast<unsigned>(s_info[0])) << lsh;
+      lmsk |= 255ull << lsh;
+      lrank -= s_info[1];
+      lcnt = s_info[2];
+      __syncthreads();
+      if (lsh == 0) break;
+      lsh = lsh >= 8 ? lsh - 8 : 0;
+    }
+    if (tid == 0) s_cnt = 0u;
+    __syncthreads();
+    for (unsigned i = tid; i < n; i += BLOCK)
+      if ((g[i] & lmsk) == lpre) {
+        const unsigned slot = atomicAdd(&s_cnt, 1u);
+        if (slot < 32u) small[slot] = g[i];
+      }
+    __syncthreads();
+    const unsigned ns = s_cnt < 32u ? s_cnt : 32u;
+    if (static_cast<unsigned>(tid) < ns && count_above(small, 0u, ns, small[tid]) == lrank - 1)
+      xch[3] = small[tid];
     }
     __syncthreads();
     const uint64_t tau = xch[3];
