@@ -20,6 +20,11 @@ struct Problem {
 };
 
 // ---- parameters (params.cpp) -------------------------------------------------
+// Whether the refinement kernel should handle a miss itself (no launch when
+// nothing misses, but its cluster alone streams x on a miss) rather than the
+// grid-wide fallback kernel: true when eps times the expected cost of that
+// slow miss is below the cost of the launch it saves.
+bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double eps);
 // Programmatic dependent launch for one pipeline edge (see params.cpp).
 constexpr unsigned kPdlTau = 1, kPdlFilter = 2, kPdlFallback = 4, kPdlRefine = 8;
 bool pdl_edge(unsigned bit);

@@ -19,6 +19,7 @@
 // Numerics: Phi^{-1} solves 0.5*erfc(x/sqrt 2) = q by safeguarded Newton steps
 // on log Q(x); binomial tails sum pmf terms from the tail inwards using
 // lgamma/log1p for the first term and the term ratio for the rest.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -159,6 +160,20 @@ bool choose_params(int64_t n, int64_t k, double eps, const ParamRule& pr, int64_
   *t_out = t;
   *M_out = M;
   return true;
+}
+
+bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double eps) {
+  constexpr double kLaunchUs = 4.0;       // a fallback launch that exits at once
+  constexpr double kSmBytesPerUs = 1e5;   // ~100 GB/s streamed per SM
+  const double row_bytes = static_cast<double>(p.len) * (p.dtype == 0 ? 4.0 : 2.0);  // f32 : bf16
+  int64_t g = (k + 11775) / 11776;        // the refinement cluster's size, at least
+  const double er = static_cast<double>(t) * (static_cast<double>(p.len) + 1.0) / (static_cast<double>(S) + 1.0);
+  const int64_t g_cache = static_cast<int64_t>(1.5 * er / 23552.0) + 1;
+  if (g_cache > g) g = g_cache;
+  if (g > 16) g = 16;
+  const double miss_us = 3.0 * row_bytes / (static_cast<double>(g) * kSmBytesPerUs);
+  const double p_any = std::min(1.0, eps * static_cast<double>(p.nsel));
+  return p_any * miss_us < kLaunchUs;
 }
 
 bool pdl_edge(unsigned bit) {

@@ -11,6 +11,7 @@
 // The miss decision is made on the device by the refinement kernel itself.
 // The exact path (no Prof-K) runs the grid-wide fallback_kernel and then the
 // same sort.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -76,6 +77,7 @@ size_t ws_prefix() { return ws_hist_offset() + 2 * kHistHalfBytes; }
 
 size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
+
 int index_bits(int64_t len) {
   int b = 1;
   while (b < 63 && (int64_t(1) << b) < len) ++b;
@@ -86,6 +88,7 @@ struct Plan {
   int path;
   int64_t S, t, M;
 };
+
 
 ParamRule rule_of(const topk_options_t* o) {
   ParamRule pr;
@@ -355,6 +358,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     if (!o || !o->events[i]) return cudaSuccess;
     return cudaEventRecord(static_cast<cudaEvent_t>(o->events[i]), st);
   };
+  bool fallback_launched = false;
   if (plan.path == TOPK_PATH_PROFK) {
     TK_TRY(mark(0));
     unsigned* hist_add = nullptr;
@@ -385,12 +389,18 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     if (std::getenv("TK_DEBUG_TWICE")) TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
 #endif
     TK_TRY(mark(2));
-    // the filter grid also checks for misses and falls back in place; a
-    // forced miss uses the separate fallback launch
     TK_TRY(launch_filter(p, tau, M, buf, counts, overlap_sms(tau_cluster, nsel), st));
     TK_TRY(mark(3));
-    // the miss check (and, on a miss, the selection from x) is part of the
-    // refinement kernel: no launch is spent on it when nothing missed
+    // Where to handle a miss: inside the refinement kernel (no launch when
+    // nothing missed, but on a miss its cluster alone streams x), or in the
+    // grid-wide fallback kernel (one launch per call, a fast miss).  The
+    // refinement takes it when the expected cost of its slow miss, eps times
+    // about three passes over a row at ~100 GB/s per SM of the cluster, is
+    // below the launch it saves.
+    if (!miss_in_refine(p, k, plan.t, plan.S, eps)) {
+      TK_TRY(launch_fallback(p, k, M, buf, counts, fs, force, st));
+      fallback_launched = true;
+    }
     TK_TRY(mark(4));
   } else {  // TOPK_PATH_EXACT
     TK_TRY(cudaMemsetAsync(base, 0, sizeof(DevHeader), st));
@@ -407,7 +417,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
   rj.xbuf = xbuf;
-  if (plan.path == TOPK_PATH_PROFK) {
+  if (plan.path == TOPK_PATH_PROFK && !fallback_launched) {
     rj.check_miss = true;
     rj.force_miss = force != 0;
     rj.r_seen = r_seen;

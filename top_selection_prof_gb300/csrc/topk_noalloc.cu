@@ -177,6 +177,7 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
   FallbackScratch fs{reinterpret_cast<unsigned*>(base + o_ghist), reinterpret_cast<unsigned*>(base + o_tiles),
                      hdr->barrier, &hdr->status, reinterpret_cast<unsigned long long*>(base + o_rseen),
                      &hdr->misses, reinterpret_cast<uint64_t*>(base + o_taux)};
+  bool refine_checks = false;
   if (path == TOPK_PATH_PROFK) {
     static uint64_t calls = 0;  // Philox call counter of this entry point
     const uint64_t counter = __atomic_fetch_add(&calls, 1, __ATOMIC_RELAXED);
@@ -191,6 +192,8 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
     int tau_cluster = 0;
     NA_TRY(launch_select(p, tj, S, &tau_cluster, st));
     NA_TRY(launch_filter(p, tau, cap, buf, counts, overlap_sms(tau_cluster, nsel), st));
+    refine_checks = miss_in_refine(p, k, t, S, eps);
+    if (!refine_checks) NA_TRY(launch_fallback(p, k, cap, buf, counts, fs, 0, st));
   } else {
     NA_TRY(cudaMemsetAsync(base, 0, o_tau, st));  // header, counts, r_seen
     NA_TRY(launch_fallback(p, k, cap, buf, counts, fs, 1, st));
@@ -205,7 +208,7 @@ extern "C" int topk_select_noalloc(const void* x, int dtype, int64_t rows, int64
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
   rj.xbuf = reinterpret_cast<uint64_t*>(base + o_xbuf);
-  if (path == TOPK_PATH_PROFK) {  // the refinement checks for a miss itself
+  if (refine_checks) {  // the refinement checks for a miss itself
     rj.check_miss = true;
     rj.r_seen = reinterpret_cast<unsigned long long*>(base + o_rseen);
     rj.misses = &hdr->misses;
