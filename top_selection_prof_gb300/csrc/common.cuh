@@ -158,6 +158,47 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
+#ifdef TK_PHASE_TIMING
+// Debug builds only: first-block start and last-block end of each kernel of
+// a call (0 sample, 1 threshold, 2 filter, 3 refinement, 4 bin sort,
+// 5 fallback), in globaltimer nanoseconds.
+// (one copy per translation unit; each unit exports an accessor)
+static __device__ unsigned long long g_timeline[8][2];
+#define TK_TIMELINE_ACCESSOR(name)                                                      \
+  int name(unsigned long long* out, int reset) {                                        \
+    if (reset) {                                                                        \
+      unsigned long long init[8][2];                                                    \
+      for (int i = 0; i < 8; ++i) { init[i][0] = ~0ull; init[i][1] = 0ull; }            \
+      return cudaMemcpyToSymbol(g_timeline, init, sizeof(init)) == cudaSuccess ? 0 : -3; \
+    }                                                                                   \
+    return cudaMemcpyFromSymbol(out, g_timeline, sizeof(g_timeline)) == cudaSuccess ? 0 : -3; \
+  }
+__device__ __forceinline__ void tl_begin(int id) {
+  if (threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    atomicMin(&g_timeline[id][0], t);
+  }
+}
+__device__ __forceinline__ void tl_end(int id) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    atomicMax(&g_timeline[id][1], t);
+  }
+}
+#define TK_TL_BEGIN(id) tk::tl_begin(id)
+#define TK_TL_END(id) tk::tl_end(id)
+#else
+#define TK_TL_BEGIN(id) \
+  do {                  \
+  } while (0)
+#define TK_TL_END(id) \
+  do {                \
+  } while (0)
+#endif
+
 // Device status codes written to the workspace status word.
 constexpr int kDevOk = 0;
 constexpr int kDevTimeout = 1;

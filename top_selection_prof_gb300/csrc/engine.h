@@ -117,7 +117,11 @@ struct SelectJob {
   bool force_miss = false;
   unsigned long long* r_seen = nullptr;   // per selection: R as the filter left it
   unsigned long long* misses = nullptr;   // incremented once per missed selection
+  // large k: per selection select_binfo_words(k) words; then the winners are
+  // sorted by a second grid of small blocks instead of the cluster alone
+  unsigned* binfo = nullptr;
 };
+int64_t select_binfo_words(int64_t k);  // 0 when k is too small for the bin sort
 // Returns the cluster size used via *cluster (may be null).
 cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source_bound, int* cluster,
                           cudaStream_t st);
@@ -125,6 +129,11 @@ int64_t select_max_k();
 #ifdef TK_PHASE_TIMING
 int debug_phase_ns(unsigned long long* out);  // debug builds: per-phase timer stamps
 int debug_rows_ns(unsigned long long* out);   // debug builds: stamps of the short-row kernel
+// debug builds: kernel start / end times, one table per translation unit
+int debug_timeline_select(unsigned long long* out, int reset);
+int debug_binsort_ns(unsigned long long* out);
+int debug_timeline_filter(unsigned long long* out, int reset);
+int debug_timeline_sample(unsigned long long* out, int reset);
 #endif
 
 }  // namespace tk

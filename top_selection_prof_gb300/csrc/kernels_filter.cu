@@ -589,15 +589,18 @@ template <int DT, bool LARGEST, int VEC>
 __global__ void __launch_bounds__(kFilterBlock) fallback_kernel(FallbackParams a) {
   __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
   __shared__ unsigned stage_n[kFilterBlock / 32];
+  TK_TL_BEGIN(5);
   grid_dependency_wait();    // the survivor counts come from the filter
   grid_launch_dependents();  // the final selection may start launching
   fallback_body<DT, LARGEST, VEC>(a, stage, stage_n);
+  TK_TL_END(5);
 }
 
 template <int DT, bool LARGEST, int VEC>
 __global__ void __launch_bounds__(kFilterBlock) filter_kernel(FilterParams fp) {
   __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
   __shared__ unsigned stage_n[kFilterBlock / 32];
+  TK_TL_BEGIN(2);
   grid_dependency_wait();  // tau and the zeroed counters come from the previous grid
   if ((threadIdx.x & 31) == 0) stage_n[threadIdx.x >> 5] = 0u;
   __syncwarp();
@@ -605,6 +608,7 @@ __global__ void __launch_bounds__(kFilterBlock) filter_kernel(FilterParams fp) {
   const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
   const Stage st{stage[threadIdx.x >> 5], &stage_n[threadIdx.x >> 5]};
   filter_tiles<DT, LARGEST, VEC>(fp, blockIdx.x, ntiles, gridDim.x, st);
+  TK_TL_END(2);
 }
 
 // One full wave: SMs x resident blocks per SM, less the SMs held by the
@@ -709,5 +713,9 @@ cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* 
   if (p.vec_ok) return largest ? launch_fallback_t<kBF16, true, 8>(a, st) : launch_fallback_t<kBF16, false, 8>(a, st);
   return largest ? launch_fallback_t<kBF16, true, 1>(a, st) : launch_fallback_t<kBF16, false, 1>(a, st);
 }
+
+#ifdef TK_PHASE_TIMING
+TK_TIMELINE_ACCESSOR(debug_timeline_filter)
+#endif
 
 }  // namespace tk

@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(256) sample_kernel(const void* __restrict__ x,
   using T = typename Dt<DT>::storage;
   constexpr unsigned DM = kSampleHistBins - 1;
   __shared__ unsigned sh[kSampleHistBins];
+  TK_TL_BEGIN(0);
   grid_launch_dependents();  // the threshold select may start launching
   const uint32_t row = blockIdx.y;
   const int64_t pair = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(256) sample_kernel(const void* __restrict__ x,
     for (int i = threadIdx.x; i < kSampleHistBins; i += blockDim.x)
       if (sh[i]) atomicAdd(h + i, sh[i]);
   }
+  TK_TL_END(0);
 }
 
 cudaError_t launch_sample(const Problem& p, int64_t S, uint64_t seed, uint64_t counter,
@@ -87,5 +89,9 @@ cudaError_t launch_sample(const Problem& p, int64_t S, uint64_t seed, uint64_t c
                                                  counts_to_zero, hdr, hist_add, hist_zero);
   return cudaGetLastError();
 }
+
+#ifdef TK_PHASE_TIMING
+TK_TIMELINE_ACCESSOR(debug_timeline_sample)
+#endif
 
 }  // namespace tk

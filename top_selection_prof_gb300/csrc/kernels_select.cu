@@ -91,7 +91,16 @@ struct SelParams {
   int force;
   unsigned long long* r_seen;         // per selection: R as the filter left it
   unsigned long long* misses;         // selections that missed
+  // large k: stop after partitioning the winners and publish the first-digit
+  // bins (kBinInfoWords words per selection) for the grid-wide bin sort
+  unsigned* binfo;
+  int handoff;
 };
+
+// Published per selection for the bin sort: NB bin starts, then the
+// first-digit prefix, mask and shift.
+constexpr int kBinInfoBins = 2048;
+constexpr int kBinInfoWords = kBinInfoBins + 8;
 
 // Source of the refinement kernel (template source 3), chosen at run time:
 // 0 = the candidate buffer, or after a miss 1 / 2 = x as f32 / bf16.
@@ -286,6 +295,10 @@ __device__ __forceinline__ unsigned count_above(const uint64_t* src, unsigned j0
   return r;
 }
 
+// Beyond this many compares per key on average, ranking inside groups by
+// counting gives way to the LSD radix sort.
+constexpr unsigned long long kMaxComparesPerKey = 24;
+
 // Places keys by counting ("Rank by Counting": a key's place is the number
 // of keys that outrank it; the keys are distinct, so places form a
 // permutation).  The n keys of src are first grouped, largest group first, by
@@ -295,7 +308,8 @@ __device__ __forceinline__ unsigned count_above(const uint64_t* src, unsigned j0
 // once (a broadcast) and run the same number of steps.  Only groups starting
 // in [split0, split1) are ranked here (how CTAs share the work); keys whose
 // place base_place + rank lies in [w0, w1) are written out.  Returns false
-// without writing when the largest group exceeds max_group.
+// without writing when the largest group exceeds max_group, or when the
+// groups are so uneven that counting would cost more than a radix sort.
 template <int BLOCK, int NB>
 __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long vary, unsigned split0,
                                 unsigned split1, uint64_t* grp, unsigned* gcount, unsigned* gstart,
@@ -303,9 +317,11 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
                                 const SelParams& a, int64_t row, int64_t kout, int64_t base_place, int64_t w0,
                                 int64_t w1) {
   static_assert(NB % BLOCK == 0, "whole groups per thread");
-  constexpr int kBits = NB == 2048 ? 11 : 8;
+  static_assert(NB == 256 || NB == 2048 || NB == 4096, "8, 11 or 12 leading bits");
+  constexpr int kBits = NB == 4096 ? 12 : (NB == 2048 ? 11 : 8);
   constexpr int kPer = NB / BLOCK;
   __shared__ unsigned s_gmax;
+  __shared__ unsigned long long s_cost;
   const int tid = threadIdx.x;
   const int hb = vary ? 63 - __clzll(static_cast<long long>(vary)) : 0;
   const int dsh = hb >= kBits - 1 ? hb - (kBits - 1) : 0;
@@ -317,12 +333,13 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
   __syncthreads();
   TK_STAMP(22);
   unsigned c[kPer];
-  unsigned long long sum = 0;
+  unsigned long long sum = 0, sq = 0;
   unsigned mx = 0;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
     c[q] = gcount[tid * kPer + q];
     sum += c[q];
+    sq += static_cast<unsigned long long>(c[q]) * c[q];
     mx = c[q] > mx ? c[q] : mx;
   }
   const unsigned long long incl = block_scan_incl(sum, s_tmp);
@@ -332,11 +349,16 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
     gstart[tid * kPer + q] = run;
     run += c[q];
   }
+  // the counting costs sum(group size^2) compares: with a few large groups
+  // (keys differing only in a few low value bits and the position) that
+  // exceeds a radix sort's cost, and the caller sorts instead
+  const unsigned long long compares = block_scan_incl(sq, s_tmp);
+  if (tid == BLOCK - 1) s_cost = compares;
   atomicMax(&s_gmax, mx);
   __syncthreads();
   TK_STAMP(23);
   if (blockIdx.x == 0 && threadIdx.x == 0) TK_DBG(0, s_gmax);
-  if (s_gmax > max_group) return false;
+  if (s_gmax > max_group || s_cost > kMaxComparesPerKey * static_cast<unsigned long long>(n)) return false;
   for (int i = tid; i < n; i += BLOCK) {
     const uint64_t key = src[i];
     const unsigned g = mask - static_cast<unsigned>((key >> dsh) & mask);
@@ -384,9 +406,9 @@ __device__ void block_or_and(const uint64_t* src, int n, unsigned long long* out
 
 // Stable LSD radix sort of src[0..n) into descending key order, one 8-bit
 // digit per pass, skipping digits on which all keys agree (bits of `vary`
-// clear).  Each warp ranks a contiguous segment stably (__match_any_sync
-// peers), per-warp counts are scanned per digit, and keys are scattered to
-// the other buffer.  `scratch` holds kWarps*256 + 2*256 + kQuarters*256
+// clear).  Each warp ranks a contiguous segment stably (lanes with equal
+// digits found with one ballot per digit bit), per-warp counts are scanned
+// per digit, and keys are scattered to the other buffer.  `scratch` holds kWarps*256 + 2*256 + kQuarters*256
 // counters.  Returns the buffer holding the result.
 template <int BLOCK, int P>
 __device__ __noinline__ uint64_t* lsd_sort(uint64_t* src, uint64_t* dst, int n, unsigned long long vary, unsigned* scratch) {
@@ -418,8 +440,16 @@ __device__ __noinline__ uint64_t* lsd_sort(uint64_t* src, uint64_t* dst, int n, 
       const int i = seg0 + j * 32 + lane;
       const bool v = i < seg1;
       key[j] = v ? src[i] : 0ull;
-      dig[j] = v ? 255u - static_cast<unsigned>((key[j] >> shift) & 255u) : 256u + lane;
-      const unsigned peers = __match_any_sync(kFull, dig[j]);
+      dig[j] = v ? 255u - static_cast<unsigned>((key[j] >> shift) & 255u) : 256u;
+      // lanes with the same digit: one ballot per digit bit (cheaper here
+      // than __match_any_sync); the lanes without a key share digit 256
+      unsigned peers = kFull;
+#pragma unroll
+      for (int bit = 0; bit < 9; ++bit) {
+        const bool set = (dig[j] >> bit) & 1u;
+        const unsigned bal = __ballot_sync(kFull, set);
+        peers &= set ? bal : ~bal;
+      }
       const unsigned before = __popc(peers & lt);
       const unsigned b = v ? wh[dig[j]] : 0u;
       __syncwarp();
@@ -1014,6 +1044,23 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     }
     gsync();  // all winners are in the exchange buffer
     TK_STAMP(11);
+    if constexpr (NB == kBinInfoBins) {
+      if (a.handoff) {
+        // the bin sort grid takes over from here: publish the bins
+        if (crank == 0) {
+          unsigned* bo = a.binfo + row * kBinInfoWords;
+          for (int i = tid; i < NB; i += BLOCK) bo[i] = bst[i];
+          if (tid == 0) {
+            bo[NB] = static_cast<unsigned>(prefix1);
+            bo[NB + 1] = static_cast<unsigned>(prefix1 >> 32);
+            bo[NB + 2] = static_cast<unsigned>(pmask1);
+            bo[NB + 3] = static_cast<unsigned>(pmask1 >> 32);
+            bo[NB + 4] = static_cast<unsigned>(shift1);
+          }
+        }
+        return;
+      }
+    }
 
     // ------------------------------------------------------------------ local sort
     // CTA c owns the places [my0, my1).  It takes the first-pass bins that
@@ -1151,9 +1198,16 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
 
 template <int BLOCK, int P, int CB, int NB, int SRC>
 __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelParams a) {
+#ifdef TK_PHASE_TIMING
+  if (blockIdx.x == 0 && threadIdx.x == 0) g_phase_ns[a.want_topk][27] = globaltimer_ns();
+#endif
+  TK_TL_BEGIN(a.want_topk ? 3 : 1);
   // programmatic dependent launch: everything below may read what earlier
   // grids wrote, so wait for them; the next grid may begin launching now
   grid_dependency_wait();
+#ifdef TK_PHASE_TIMING
+  if (blockIdx.x == 0 && threadIdx.x == 0) g_phase_ns[a.want_topk][28] = globaltimer_ns();
+#endif
   grid_launch_dependents();
   if constexpr (SRC == 3) {
     // The miss check of the refinement (section 4): with fewer than r
@@ -1175,12 +1229,201 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
     __syncthreads();
   }
   select_body<BLOCK, P, CB, NB, SRC>(a);
+  TK_TL_END(a.want_topk ? 3 : 1);
+}
+
+// ---------------------------------------------------------------------------
+// Bin sort (large k).  The refinement cluster has partitioned the k winners
+// of each selection by their first digit: bin b's winners sit at places
+// [bst[b], min(bst[b + 1], k)) of the exchange buffer, bins in descending key
+// order.  Each block of this grid owns kBinSortPlaces output places: it cuts
+// the bins at either end of its places by further 8-bit digits down to the
+// sub-bin holding the boundary place, collects the keys in between (a
+// contiguous key range) and ranks them by counting inside groups of equal
+// leading bits.  Many small blocks share the sort that one cluster would
+// otherwise do alone.
+constexpr int kBinSortBlock = 256;
+constexpr int kBinSortPlaces = 512;
+constexpr int kBinSortCap = 2048;  // keys one block sorts
+constexpr int kBinSortGroups = 4096;  // 12 leading varying bits: small groups even for few values
+constexpr int kBinSortScratch = 3 * kBinSortGroups;  // (also covers the LSD sort's counters)
+static_assert(kBinSortScratch >= (kBinSortBlock / 32) * 256 + 2 * 256 + (kBinSortBlock / 256) * 256, "lsd");
+constexpr size_t kBinSortSmem = sizeof(unsigned) * kBinInfoBins + 2 * sizeof(uint64_t) * kBinSortCap +
+                                sizeof(unsigned) * kBinSortScratch;
+
+struct BinSortParams {
+  SelParams a;  // the refinement's parameters: r = k, xbuf, binfo, outputs
+  int q;        // blocks per selection
+};
+
+__device__ __forceinline__ void bin_sort_body(const BinSortParams& bp);
+
+#ifdef TK_PHASE_TIMING
+__device__ unsigned long long g_bs_ns[1024][2];  // debug: per-block start and end of the bin sort
+__device__ unsigned g_bs_info[1024][4];          // debug: set size, cut iterations, max group, lsd
+#define TK_BS(i, v) \
+  do { if (threadIdx.x == 0 && blockIdx.x < 1024) g_bs_info[blockIdx.x][(i)] = (v); } while (0)
+#else
+#define TK_BS(i, v) \
+  do {              \
+  } while (0)
+#endif
+
+__global__ void __launch_bounds__(kBinSortBlock) bin_sort_kernel(BinSortParams bp) {
+  TK_TL_BEGIN(4);
+#ifdef TK_PHASE_TIMING
+  grid_dependency_wait();
+  if (threadIdx.x == 0 && blockIdx.x < 1024) g_bs_ns[blockIdx.x][0] = globaltimer_ns();
+#endif
+  bin_sort_body(bp);
+  TK_TL_END(4);
+#ifdef TK_PHASE_TIMING
+  if (threadIdx.x == 0 && blockIdx.x < 1024) g_bs_ns[blockIdx.x][1] = globaltimer_ns();
+#endif
+}
+
+__device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
+  constexpr int BLOCK = kBinSortBlock;
+  constexpr int NB = kBinInfoBins;
+  constexpr unsigned DM = 255u;  // 8-bit sub-digits
+  const SelParams& a = bp.a;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned* bst = reinterpret_cast<unsigned*>(smem);
+  uint64_t* bufA = reinterpret_cast<uint64_t*>(smem + sizeof(unsigned) * NB);
+  uint64_t* bufB = bufA + kBinSortCap;
+  unsigned* scr = reinterpret_cast<unsigned*>(bufB + kBinSortCap);
+  __shared__ unsigned long long s_tmp[32];
+  __shared__ unsigned long long s_info[5];
+  __shared__ unsigned s_cnt;
+  grid_dependency_wait();  // the partition comes from the previous grid
+  const int tid = threadIdx.x;
+  if (tid == 0) s_info[0] = static_cast<unsigned long long>(*reinterpret_cast<volatile int*>(a.status));
+  __syncthreads();
+  if (s_info[0] != static_cast<unsigned long long>(kDevOk)) return;  // the refinement failed
+  const int64_t row = blockIdx.x / bp.q;
+  const int64_t k = a.r;
+  const int64_t my0 = static_cast<int64_t>(blockIdx.x % bp.q) * kBinSortPlaces;
+  if (my0 >= k) return;
+  const int64_t my1 = my0 + kBinSortPlaces < k ? my0 + kBinSortPlaces : k;
+  const unsigned* bi = a.binfo + row * kBinInfoWords;
+  for (int i = tid; i < NB; i += BLOCK) bst[i] = __ldcg(bi + i);
+  const uint64_t prefix1 = static_cast<uint64_t>(__ldcg(bi + NB)) | (static_cast<uint64_t>(__ldcg(bi + NB + 1)) << 32);
+  const uint64_t pmask1 = static_cast<uint64_t>(__ldcg(bi + NB + 2)) | (static_cast<uint64_t>(__ldcg(bi + NB + 3)) << 32);
+  const int shift1 = static_cast<int>(__ldcg(bi + NB + 4));
+  const uint64_t* xb = a.xbuf + row * k;
+  if (tid == 0) { s_info[0] = 0; s_info[1] = 0; }
+  __syncthreads();
+  auto bin_end = [&](unsigned b) -> int64_t {
+    const int64_t e = (b + 1 < static_cast<unsigned>(NB)) ? static_cast<int64_t>(bst[b + 1]) : k;
+    return e < k ? e : k;
+  };
+  // first-digit bins holding places my0 and my1 - 1
+  for (int b = tid; b < NB; b += BLOCK) {
+    const int64_t bs = bst[b], be = bin_end(static_cast<unsigned>(b));
+    if (bs <= my0 && my0 < be) s_info[0] = static_cast<unsigned long long>(b);
+    if (bs <= my1 - 1 && my1 - 1 < be) s_info[1] = static_cast<unsigned long long>(b);
+  }
+  __syncthreads();
+  const unsigned bfirst = static_cast<unsigned>(s_info[0]), blast = static_cast<unsigned>(s_info[1]);
+  __syncthreads();
+  const int64_t r0 = bst[bfirst] < static_cast<unsigned>(k) ? bst[bfirst] : k, r1 = bin_end(blast);
+  uint64_t hi_key = ~0ull, lo_key = 0ull;
+  int64_t place0 = r0, place1 = r1;
+  unsigned cut_iters = 0;
+  if (r1 - r0 > kBinSortCap) {
+    const int64_t lim = (kBinSortCap - (my1 - my0)) / 2;
+    unsigned* lh = scr;  // 256 counters
+    // cut bin b down to the 8-bit sub-bin (and so on) holding place p
+    auto cut = [&](unsigned b, int64_t p, uint64_t& pre, uint64_t& msk, int64_t& s0, int64_t& s1) -> bool {
+      pre = prefix1 | (static_cast<uint64_t>(2047u - b) << shift1);
+      msk = pmask1 | (2047ull << shift1);
+      const int64_t bs = bst[b], be = bin_end(b);
+      s0 = bs;
+      s1 = be;
+      int sh = shift1;
+      while (s1 - s0 > lim && sh > 0) {
+        const int sh2 = sh >= 8 ? sh - 8 : 0;
+        lh[tid] = 0u;  // (BLOCK == 256 counters)
+        if (tid == 0) s_info[2] = ~0ull;
+        __syncthreads();
+        for (int64_t i = bs + tid; i < be; i += BLOCK) {
+          const uint64_t key = __ldcg(xb + i);
+          if ((key & msk) == pre) atomicAdd(&lh[DM - static_cast<unsigned>((key >> sh2) & DM)], 1u);
+        }
+        __syncthreads();
+        const unsigned long long c = lh[tid];
+        const unsigned long long incl = block_scan_incl(c, s_tmp);
+        const unsigned long long run = static_cast<unsigned long long>(s0) + incl - c;
+        if (run <= static_cast<unsigned long long>(p) && static_cast<unsigned long long>(p) < run + c) {
+          s_info[2] = static_cast<unsigned long long>(tid);
+          s_info[3] = run;
+          s_info[4] = c;
+        }
+        __syncthreads();
+        if (s_info[2] == ~0ull) return false;
+        pre |= static_cast<uint64_t>(DM - static_cast<unsigned>(s_info[2])) << sh2;
+        msk |= static_cast<uint64_t>(DM) << sh2;
+        s0 = static_cast<int64_t>(s_info[3]);
+        s1 = s0 + static_cast<int64_t>(s_info[4]);
+        sh = sh2;
+        ++cut_iters;
+        __syncthreads();
+      }
+      return true;
+    };
+    uint64_t pre, msk;
+    int64_t s0, s1;
+    bool ok = cut(bfirst, my0, pre, msk, s0, s1);
+    hi_key = pre | ~msk;
+    place0 = s0;
+    ok = ok && cut(blast, my1 - 1, pre, msk, s0, s1);
+    lo_key = pre;
+    place1 = s1;
+    TK_BS(1, cut_iters | (static_cast<unsigned>(bst[bfirst] < k ? bin_end(bfirst) - bst[bfirst] : 0) << 8));
+    if (!ok || place1 - place0 > kBinSortCap || place1 < place0) {
+      if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
+      return;
+    }
+  }
+  const int n_c = static_cast<int>(place1 - place0);
+  if (r1 - r0 <= kBinSortCap) {
+    for (int i = tid; i < n_c; i += BLOCK) bufA[i] = __ldcg(xb + r0 + i);
+  } else {
+    if (tid == 0) s_cnt = 0u;
+    __syncthreads();
+    for (int64_t iw = r0 + (tid & ~31); iw < r1; iw += BLOCK) {
+      const int64_t i = iw + (tid & 31);
+      const uint64_t key = i < r1 ? __ldcg(xb + i) : 0ull;
+      const bool want = i < r1 && key <= hi_key && key >= lo_key;
+      const unsigned slot = warp_append_slot(&s_cnt, want);
+      if (want && slot < static_cast<unsigned>(kBinSortCap)) bufA[slot] = key;
+    }
+    __syncthreads();
+    if (s_cnt != static_cast<unsigned>(n_c)) {
+      if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
+      return;
+    }
+  }
+  __syncthreads();
+  unsigned long long lo_or, lo_and;
+  block_or_and<BLOCK>(bufA, n_c, &lo_or, &lo_and);
+  TK_BS(0, static_cast<unsigned>(n_c));
+  if (place_by_groups<BLOCK, kBinSortGroups>(bufA, n_c, lo_or ^ lo_and, 0u, ~0u, bufB, scr, scr + kBinSortGroups,
+                                             scr + 2 * kBinSortGroups, s_tmp, 512u, a, row, k, place0, my0, my1))
+    return;
+  TK_BS(3, 1u);
+  const uint64_t* sorted = lsd_sort<BLOCK, kBinSortCap>(bufA, bufB, n_c, lo_or ^ lo_and, scr);
+  for (int i = tid; i < n_c; i += BLOCK) {
+    const int64_t place = place0 + i;
+    if (place >= my0 && place < my1) write_out(a, row, k, place, sorted[i]);
+  }
 }
 
 // Kernel variants: (block, sort positions per CTA, cache/second buffer).
 constexpr int kSmallBlock = 256, kSmallP = 1024, kSmallCB = 2048, kSmallNB = 256;
 constexpr int kBigBlock = 1024, kBigP = 11776, kBigCB = 11776, kBigNB = 2048;
-constexpr int64_t kTauSlice = 8192;  // samples streamed per CTA when tau starts from the histogram
+constexpr int64_t kTauSlice = 8192;
+constexpr int64_t kBinSortMinK = 16384;  // k from which the winners are sorted by the bin-sort grid  // samples streamed per CTA when tau starts from the histogram
 
 template <int BLOCK, int P, int CB, int NB, int SRC>
 cudaError_t configure(int* max_g) {
@@ -1272,8 +1515,14 @@ int sm_count() {
 }  // namespace
 
 int64_t select_max_k() { return static_cast<int64_t>(kMaxCluster) * kBigP; }
+int64_t select_binfo_words(int64_t k) { return k >= kBinSortMinK ? kBinInfoWords : 0; }
 
 #ifdef TK_PHASE_TIMING
+TK_TIMELINE_ACCESSOR(debug_timeline_select)
+int debug_binsort_ns(unsigned long long* out) {
+  if (cudaMemcpyFromSymbol(out, g_bs_ns, sizeof(g_bs_ns)) != cudaSuccess) return -3;
+  return cudaMemcpyFromSymbol(out + 2048, g_bs_info, sizeof(g_bs_info)) == cudaSuccess ? 0 : -3;
+}
 int debug_phase_ns(unsigned long long* out) {
   if (cudaMemcpyFromSymbol(out, g_phase_ns, sizeof(g_phase_ns)) != cudaSuccess) return -3;
   return cudaMemcpyFromSymbol(out + 64, g_cta_ns, sizeof(g_cta_ns)) == cudaSuccess ? 0 : -3;  // 2*16*8
@@ -1331,11 +1580,35 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
     const int64_t g_cache = (source_hint + kBigCache - 1) / kBigCache;
     G = many ? pow2_at_least(g_min) : pow2_at_least(g_min > g_cache ? g_min : g_cache);
   }
+  // large k: the cluster stops after partitioning the winners, and a grid of
+  // small blocks sorts them
+  const bool handoff = job.want_topk && job.binfo && !small && job.r >= kBinSortMinK;
+  a.binfo = handoff ? job.binfo : nullptr;
+  a.handoff = handoff ? 1 : 0;
   int used = G;
-  const cudaError_t e = small ? launch_src<kSmallBlock, kSmallP, kSmallCB, kSmallNB>(a, src, p.nsel, G, &used, st)
-                              : launch_src<kBigBlock, kBigP, kBigCB, kBigNB>(a, src, p.nsel, G, &used, st);
+  cudaError_t e = small ? launch_src<kSmallBlock, kSmallP, kSmallCB, kSmallNB>(a, src, p.nsel, G, &used, st)
+                        : launch_src<kBigBlock, kBigP, kBigCB, kBigNB>(a, src, p.nsel, G, &used, st);
   if (cluster) *cluster = used;
-  return e;
+  if (e != cudaSuccess || !handoff) return e;
+  static bool configured = false;
+  if (!configured) {
+    e = cudaFuncSetAttribute(bin_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kBinSortSmem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  BinSortParams bp{a, static_cast<int>((job.r + kBinSortPlaces - 1) / kBinSortPlaces)};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.nsel * bp.q), 1, 1);
+  cfg.blockDim = dim3(kBinSortBlock, 1, 1);
+  cfg.dynamicSmemBytes = kBinSortSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_edge(kPdlRefine) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, bin_sort_kernel, bp);
 }
 
 }  // namespace tk

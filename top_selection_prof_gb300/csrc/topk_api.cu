@@ -333,6 +333,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   const size_t o_samples = off; off = align_up(off + sizeof(uint64_t) * nsel * S);
   const size_t o_buf = off; off = align_up(off + sizeof(uint64_t) * nsel * M);
   const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * nsel * k);
+  const size_t o_binfo = off; off = align_up(off + sizeof(unsigned) * nsel * select_binfo_words(k));
   void* ws = nullptr;
   Workspace* wentry = nullptr;
   TK_TRY(workspace(st, off, &ws, &wentry));
@@ -417,6 +418,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
   rj.xbuf = xbuf;
+  rj.binfo = select_binfo_words(k) ? reinterpret_cast<unsigned*>(base + o_binfo) : nullptr;
   if (plan.path == TOPK_PATH_PROFK && !fallback_launched) {
     rj.check_miss = true;
     rj.force_miss = force != 0;
@@ -534,6 +536,24 @@ int topk_version(void) { return 100; }
 #ifdef TK_PHASE_TIMING
 int topk_debug_phase_ns(unsigned long long* out) { return tk::debug_phase_ns(out); }
 int topk_debug_rows_ns(unsigned long long* out) { return tk::debug_rows_ns(out); }
+int topk_debug_binsort_ns(unsigned long long* out) { return tk::debug_binsort_ns(out); }
+int topk_debug_timeline(unsigned long long* out, int reset) {
+  unsigned long long a[16], b[16], c[16];
+  if (tk::debug_timeline_select(a, reset) || tk::debug_timeline_filter(b, reset) ||
+      tk::debug_timeline_sample(c, reset))
+    return -3;
+  if (reset) return 0;
+  for (int i = 0; i < 8; ++i) {
+    unsigned long long s0 = a[2 * i], e0 = a[2 * i + 1];
+    s0 = b[2 * i] < s0 ? b[2 * i] : s0;
+    s0 = c[2 * i] < s0 ? c[2 * i] : s0;
+    e0 = b[2 * i + 1] > e0 ? b[2 * i + 1] : e0;
+    e0 = c[2 * i + 1] > e0 ? c[2 * i + 1] : e0;
+    out[2 * i] = s0;
+    out[2 * i + 1] = e0;
+  }
+  return 0;
+}
 #endif
 
 int topk_index_bits(int64_t len) { return len < 1 ? 1 : index_bits(len); }
