@@ -48,6 +48,9 @@ CASES = [
     ("specials", 5, 4099, 50, 1e-3, False, "direct"),
     ("constant", 1, 1 << 21, 500, 1e-3, False, "profk"),
     ("relu_normal_bf16", 7, 33_333, 20, 1e-3, False, None),
+    ("normal", 1, 1 << 22, 9000, 1e-3, False, "profk"),            # k just above the bin-sort bound
+    ("ties1000", 1, 1 << 24, 12000, 1e-3, False, "profk"),         # bin sort with a 2-CTA cluster
+    ("uniform", 1, (1 << 22) + 8, 9000, 0.0, False, "exact"),      # exact path, sort after the fallback
 ]
 
 

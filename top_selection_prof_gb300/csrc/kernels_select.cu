@@ -1423,7 +1423,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
 constexpr int kSmallBlock = 256, kSmallP = 1024, kSmallCB = 2048, kSmallNB = 256;
 constexpr int kBigBlock = 1024, kBigP = 11776, kBigCB = 11776, kBigNB = 2048;
 constexpr int64_t kTauSlice = 8192;
-constexpr int64_t kBinSortMinK = 16384;  // k from which the winners are sorted by the bin-sort grid  // samples streamed per CTA when tau starts from the histogram
+constexpr int64_t kBinSortMinK = 8192;  // k from which the winners are sorted by the bin-sort grid  // samples streamed per CTA when tau starts from the histogram
 
 template <int BLOCK, int P, int CB, int NB, int SRC>
 cudaError_t configure(int* max_g) {
@@ -1582,7 +1582,14 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   }
   // large k: the cluster stops after partitioning the winners, and a grid of
   // small blocks sorts them
-  const bool handoff = job.want_topk && job.binfo && !small && job.r >= kBinSortMinK;
+  if (!small) {  // the cluster size the device can schedule (as launch_variant clamps it)
+    int max_g = 1;
+    const cudaError_t ce = configure<kBigBlock, kBigP, kBigCB, kBigNB, 0>(&max_g);
+    if (ce != cudaSuccess) return ce;
+    if (G > max_g) G = max_g;
+  }
+  // (a one-CTA cluster sorts its winners in place and never partitions them)
+  const bool handoff = job.want_topk && job.binfo && !small && job.r >= kBinSortMinK && G > 1;
   a.binfo = handoff ? job.binfo : nullptr;
   a.handoff = handoff ? 1 : 0;
   int used = G;
