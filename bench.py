@@ -48,6 +48,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-miss-rate", action="store_true", help="skip the measured miss rate against eps")
     ap.add_argument("--scale-down", type=int, default=0,
                     help="divide the workload by 2^s (row length, or rows for global mode); for profiling")
     ap.add_argument("--seed", type=int, default=0)
@@ -209,6 +210,35 @@ def time_oracle(cfg, x, steps, warmup):
 # sample, threshold select, filter, refinement (which checks for a miss
 # itself); direct: one kernel; exact: the grid-wide fallback and the sort
 KERNELS_PER_STEP = {"profk": 4, "direct": 1, "exact": 2}
+
+
+def tk_plan(cfg):
+    """The exact tail bound P[R < k] + P[R > M] of the workload's own plan."""
+    import top_selection_prof_gb300 as tk
+    n = cfg["n"] * (cfg["rows"] if cfg.get("mode") == "global" else 1)
+    pl = tk.plan(n, cfg["k"], cfg["eps"])
+    return {"S": int(pl["S"]), "t": int(pl["t"]), "M": int(pl["M"]),
+            "p_recall_fail": float(pl["p_recall_fail"]), "p_overflow": float(pl["p_overflow"])}
+
+
+def measure_miss_rate(runs=300):
+    """Measured fallback frequency against the exact tail bound of the (S, t, M)
+    in use: a 2^20 uniform row, k = 100, eps = 0.2, S = 2048 draws, so that
+    misses are frequent enough to count (the same case as the stage tests)."""
+    import numpy as np
+    import torch
+    import top_selection_prof_gb300 as tk
+    from top_selection_prof_gb300 import workloads
+    n, k, eps, S = 1 << 20, 100, 0.2, 2048
+    xd = torch.from_numpy(workloads.make("uniform", 1, n, 5)).cuda()
+    misses = 0
+    for c in range(runs):
+        _, _, st = tk.select_ex(xd, k, eps=eps, counter=c, s_min=S, s_max=S)
+        misses += int(st["misses"])
+    pl = tk.plan(n, k, eps, s_min=S, s_max=S)
+    bound = float(pl["p_recall_fail"] + pl["p_overflow"])
+    return {"n": n, "k": k, "eps": eps, "S": int(pl["S"]), "t": int(pl["t"]), "M": int(pl["M"]), "calls": runs,
+            "misses": misses, "measured": round(misses / runs, 4), "exact_tail_bound": round(bound, 4)}
 
 
 def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, with_e2e=True):
@@ -445,6 +475,10 @@ def main():
             "roofline": res["roofline"], "stages": res["stages"], "cpu_baseline": cpu, "e2e": res["e2e"],
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "secondary": secondary,
         }
+        if cfg.get("eps", 0) > 0 and not args.no_miss_rate:
+            # the workload's own bound, and a measured rate where misses are countable
+            pl = tk_plan(cfg)
+            line["miss_rate"] = {"workload_bound": pl, "measured_case": measure_miss_rate()}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
