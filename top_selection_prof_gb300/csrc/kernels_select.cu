@@ -520,6 +520,78 @@ struct Layout {
   static_assert(NB % BLOCK == 0, "whole bins per thread");
 };
 
+// The key of 1-based descending rank `rank` among g[0..n) (distinct keys, in
+// shared or global memory); the thread that finds it writes it to *out (the
+// caller synchronises before reading).  Few keys are ranked by counting
+// directly; more are first narrowed by 8-bit radix passes below their
+// highest varying bit to at most 32, since counting all n keys against each
+// other costs n^2 / 32 shared-memory wavefronts.  lh holds 256 counters;
+// s_tmp 32 words; s_info 3.  Every thread of the block calls it.
+template <int BLOCK>
+__device__ void bucket_kth(const uint64_t* g, unsigned n, unsigned long long rank, unsigned* lh,
+                           unsigned long long* s_tmp, unsigned long long* s_info, unsigned* s_cnt, uint64_t* out) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (n <= 128u) {
+    __syncthreads();
+    for (unsigned i = tid; i < n; i += BLOCK)
+      if (count_above(g, 0u, n, g[i]) == rank - 1) *out = g[i];
+    return;
+  }
+  uint64_t* small = reinterpret_cast<uint64_t*>(s_tmp);  // <= 32 keys (the scans are done by then)
+  {
+    unsigned long long o = 0, d = ~0ull;
+    for (unsigned i = tid; i < n; i += BLOCK) { o |= g[i]; d &= g[i]; }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+      o |= __shfl_xor_sync(kFull, o, m);
+      d &= __shfl_xor_sync(kFull, d, m);
+    }
+    if (tid == 0) { s_info[0] = 0ull; s_info[1] = ~0ull; }
+    __syncthreads();
+    if (lane == 0) { atomicOr(&s_info[0], o); atomicAnd(&s_info[1], d); }
+    __syncthreads();
+  }
+  const unsigned long long gv = s_info[0] ^ s_info[1];
+  __syncthreads();
+  int lsh = gv ? 63 - __clzll(static_cast<long long>(gv)) : 0;
+  lsh = lsh >= 7 ? lsh - 7 : 0;
+  uint64_t lpre = 0, lmsk = 0;
+  unsigned long long lrank = rank, lcnt = n;
+#pragma unroll 1
+  while (lcnt > 32) {
+    for (int i = tid; i < 256; i += BLOCK) lh[i] = 0u;
+    __syncthreads();
+    for (unsigned i = tid; i < n; i += BLOCK)
+      if ((g[i] & lmsk) == lpre) atomicAdd(&lh[255u - static_cast<unsigned>((g[i] >> lsh) & 255u)], 1u);
+    __syncthreads();
+    const unsigned long long c = tid < 256 ? lh[tid] : 0ull;
+    const unsigned long long incl = block_scan_incl(c, s_tmp);
+    if (tid < 256 && incl - c < lrank && lrank <= incl) {
+      s_info[0] = static_cast<unsigned long long>(tid);
+      s_info[1] = incl - c;
+      s_info[2] = c;
+    }
+    __syncthreads();
+    lpre |= static_cast<uint64_t>(255u - static_cast<unsigned>(s_info[0])) << lsh;
+    lmsk |= 255ull << lsh;
+    lrank -= s_info[1];
+    lcnt = s_info[2];
+    __syncthreads();
+    if (lsh == 0) break;
+    lsh = lsh >= 8 ? lsh - 8 : 0;
+  }
+  if (tid == 0) *s_cnt = 0u;
+  __syncthreads();
+  for (unsigned i = tid; i < n; i += BLOCK)
+    if ((g[i] & lmsk) == lpre) {
+      const unsigned slot = atomicAdd(s_cnt, 1u);
+      if (slot < 32u) small[slot] = g[i];
+    }
+  __syncthreads();
+  const unsigned ns = *s_cnt < 32u ? *s_cnt : 32u;
+  if (static_cast<unsigned>(tid) < ns && count_above(small, 0u, ns, small[tid]) == lrank - 1) *out = small[tid];
+}
+
 template <int BLOCK, int P, int CB, int NB, int SRC>
 __device__ __forceinline__ void select_body(const SelParams& a) {
   using L = Layout<BLOCK, P, CB, NB>;
@@ -880,67 +952,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     // counting: counting all of up to kGather keys against each other would
     // cost n^2 / 32 shared-memory wavefronts.  The counters of the last
     // cluster pass (h2's other half) are free here.
-    if (n <= 128u) {  // small: count directly (n^2 / 32 wavefronts is cheap)
-      __syncthreads();
-      for (unsigned i = tid; i < n; i += BLOCK)
-        if (count_above(g, 0u, n, g[i]) == rank - 1) xch[3] = g[i];
-    } else {
-    unsigned* lh = h2 + (pass & 1) * NB;  // 256 counters
-    uint64_t* small = reinterpret_cast<uint64_t*>(s_tmp);  // <= 32 keys (the scans are done by then)
-    {
-      unsigned long long o = 0, d = ~0ull;
-      for (unsigned i = tid; i < n; i += BLOCK) { o |= g[i]; d &= g[i]; }
-#pragma unroll
-      for (int m = 16; m > 0; m >>= 1) {
-        o |= __shfl_xor_sync(kFull, o, m);
-        d &= __shfl_xor_sync(kFull, d, m);
-      }
-      if (tid == 0) { s_info[0] = 0ull; s_info[1] = ~0ull; }
-      __syncthreads();
-      if (lane == 0) { atomicOr(&s_info[0], o); atomicAnd(&s_info[1], d); }
-      __syncthreads();
-    }
-    const unsigned long long gv = s_info[0] ^ s_info[1];
-    __syncthreads();
-    int lsh = gv ? 63 - __clzll(static_cast<long long>(gv)) : 0;
-    lsh = lsh >= 7 ? lsh - 7 : 0;
-    uint64_t lpre = 0, lmsk = 0;
-    unsigned long long lrank = rank, lcnt = n;
-#pragma unroll 1
-    while (lcnt > 32) {
-      for (int i = tid; i < 256; i += BLOCK) lh[i] = 0u;
-      __syncthreads();
-      for (unsigned i = tid; i < n; i += BLOCK)
-        if ((g[i] & lmsk) == lpre) atomicAdd(&lh[255u - static_cast<unsigned>((g[i] >> lsh) & 255u)], 1u);
-      __syncthreads();
-      const unsigned long long c = tid < 256 ? lh[tid] : 0ull;
-      const unsigned long long incl = block_scan_incl(c, s_tmp);
-      if (tid < 256 && incl - c < lrank && lrank <= incl) {
-        s_info[0] = static_cast<unsigned long long>(tid);
-        s_info[1] = incl - c;
-        s_info[2] = c;
-      }
-      __syncthreads();
-      lpre |= static_cast<uint64_t>(255u - static_cast<unsigned>(s_info[0])) << lsh;
-      lmsk |= 255ull << lsh;
-      lrank -= s_info[1];
-      lcnt = s_info[2];
-      __syncthreads();
-      if (lsh == 0) break;
-      lsh = lsh >= 8 ? lsh - 8 : 0;
-    }
-    if (tid == 0) s_cnt = 0u;
-    __syncthreads();
-    for (unsigned i = tid; i < n; i += BLOCK)
-      if ((g[i] & lmsk) == lpre) {
-        const unsigned slot = atomicAdd(&s_cnt, 1u);
-        if (slot < 32u) small[slot] = g[i];
-      }
-    __syncthreads();
-    const unsigned ns = s_cnt < 32u ? s_cnt : 32u;
-    if (static_cast<unsigned>(tid) < ns && count_above(small, 0u, ns, small[tid]) == lrank - 1)
-      xch[3] = small[tid];
-    }
+    bucket_kth<BLOCK>(g, n, rank, h2 + (pass & 1) * NB, s_tmp, s_info, &s_cnt, reinterpret_cast<uint64_t*>(&xch[3]));
     __syncthreads();
     const uint64_t tau = xch[3];
     if (!a.want_topk) {
