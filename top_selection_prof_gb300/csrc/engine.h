@@ -109,7 +109,8 @@ struct SelectJob {
   void* out_vals;                      // want_topk
   int64_t* out_idx;
   int* status;                         // device status word (kDevBadState on inconsistency)
-  uint64_t* xbuf = nullptr;            // want_topk across CTAs: 2*r keys per selection (L2 exchange)
+  uint64_t* xbuf = nullptr;            // want_topk across CTAs: xbuf_stride keys per selection (L2 exchange)
+  int64_t xbuf_stride = 0;             // keys per selection in xbuf; at least r (0: r)
   const unsigned* sample_hist = nullptr;  // !want_topk: counts of the keys' leading bits (launch_sample)
   // refinement of the Prof-K buffer: check for a miss (counts[row] < r or >
   // key_stride, or force_miss) and then select from the whole row of x
@@ -122,6 +123,9 @@ struct SelectJob {
   unsigned* binfo = nullptr;
 };
 int64_t select_binfo_words(int64_t k);  // 0 when k is too small for the bin sort
+// Keys per selection the exchange buffer should hold for rank k (2k with the
+// bin sort: room to place the boundary's whole first-pass bin).
+int64_t select_xbuf_stride(int64_t k);
 // Returns the cluster size used via *cluster (may be null).
 cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source_bound, int* cluster,
                           cudaStream_t st);

@@ -83,7 +83,8 @@ struct SelParams {
   void* out_vals;
   int64_t* out_idx;
   int* status;
-  uint64_t* xbuf;                     // r keys per selection: the L2 exchange of the sort
+  uint64_t* xbuf;                     // xstride keys per selection: the L2 exchange of the sort
+  int64_t xstride;                    // >= r
   const unsigned* shist;              // tau only: first-digit counts of the samples (nullable)
   // refinement of a candidate buffer: when R < r or R > key_stride (a miss;
   // or force), select from x instead (source 1 = f32, 2 = bf16; 0 = no check)
@@ -98,7 +99,9 @@ struct SelParams {
 };
 
 // Published per selection for the bin sort: NB bin starts, then the
-// first-digit prefix, mask and shift.
+// first-digit prefix, mask and shift, and the end of the keys placed in the
+// exchange buffer (r when only winners were placed, else the end of the
+// boundary bin).
 constexpr int kBinInfoBins = 2048;
 constexpr int kBinInfoWords = kBinInfoBins + 8;
 
@@ -301,9 +304,13 @@ constexpr unsigned long long kMaxComparesPerKey = 24;
 
 // Places keys by counting ("Rank by Counting": a key's place is the number
 // of keys that outrank it; the keys are distinct, so places form a
-// permutation).  The n keys of src are first grouped, largest group first, by
-// the NB-bucket digit of their most significant varying bits, so a key only
-// compares against its own group.  The keys are then ranked in grouped order,
+// permutation).  The n keys of src are first grouped, largest group first,
+// by their offset above the smallest key kmin, cut to its leading log2(NB)
+// bits (NB equal slices of the range [kmin, kmax]), so a key only compares
+// against its own group.  Slicing the range rather than taking the leading
+// varying bits keeps groups small where keys straddle a carry (two adjacent
+// values such as ...0111 and ...1000 vary in many bits but span a short
+// range).  The keys are then ranked in grouped order,
 // so the lanes of a warp mostly share a group: they read each group member
 // once (a broadcast) and run the same number of steps.  Only groups starting
 // in [split0, split1) are ranked here (how CTAs share the work); keys whose
@@ -311,7 +318,7 @@ constexpr unsigned long long kMaxComparesPerKey = 24;
 // without writing when the largest group exceeds max_group, or when the
 // groups are so uneven that counting would cost more than a radix sort.
 template <int BLOCK, int NB>
-__device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long vary, unsigned split0,
+__device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint64_t kmax, unsigned split0,
                                 unsigned split1, uint64_t* grp, unsigned* gcount, unsigned* gstart,
                                 unsigned* gcur, unsigned long long* s_tmp, unsigned max_group,
                                 const SelParams& a, int64_t row, int64_t kout, int64_t base_place, int64_t w0,
@@ -323,13 +330,15 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
   __shared__ unsigned s_gmax;
   __shared__ unsigned long long s_cost;
   const int tid = threadIdx.x;
-  const int hb = vary ? 63 - __clzll(static_cast<long long>(vary)) : 0;
-  const int dsh = hb >= kBits - 1 ? hb - (kBits - 1) : 0;
+  const uint64_t span = kmax - kmin;
+  const int hb = span ? 63 - __clzll(static_cast<long long>(span)) : 0;
+  const int dsh = hb >= kBits - 1 ? hb - (kBits - 1) : 0;  // (span >> dsh) < NB
   const unsigned mask = NB - 1;
+  auto group = [&](uint64_t key) { return mask - static_cast<unsigned>((key - kmin) >> dsh); };
   for (int i = tid; i < NB; i += BLOCK) { gcount[i] = 0u; gcur[i] = 0u; }
   if (tid == 0) s_gmax = 0u;
   __syncthreads();
-  for (int i = tid; i < n; i += BLOCK) atomicAdd(&gcount[mask - static_cast<unsigned>((src[i] >> dsh) & mask)], 1u);
+  for (int i = tid; i < n; i += BLOCK) atomicAdd(&gcount[group(src[i])], 1u);
   __syncthreads();
   TK_STAMP(22);
   unsigned c[kPer];
@@ -361,14 +370,14 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
   if (s_gmax > max_group || s_cost > kMaxComparesPerKey * static_cast<unsigned long long>(n)) return false;
   for (int i = tid; i < n; i += BLOCK) {
     const uint64_t key = src[i];
-    const unsigned g = mask - static_cast<unsigned>((key >> dsh) & mask);
+    const unsigned g = group(key);
     grp[gstart[g] + atomicAdd(&gcur[g], 1u)] = key;
   }
   __syncthreads();
   TK_STAMP(25);
   for (int i = tid; i < n; i += BLOCK) {
     const uint64_t v = grp[i];
-    const unsigned g = mask - static_cast<unsigned>((v >> dsh) & mask);
+    const unsigned g = group(v);
     const unsigned g0 = gstart[g];
     if (g0 < split0 || g0 >= split1) continue;
     const unsigned g1 = g0 + gcount[g];
@@ -383,25 +392,46 @@ __device__ bool place_by_groups(const uint64_t* src, int n, unsigned long long v
   return true;
 }
 
-// OR and AND of src[0..n) over the block.
+// OR, AND, smallest and largest of src[0..n) over the block (n >= 1).
+struct KeySpan {
+  unsigned long long all_or, all_and;
+  uint64_t kmin, kmax;
+};
 template <int BLOCK>
-__device__ void block_or_and(const uint64_t* src, int n, unsigned long long* out_or, unsigned long long* out_and) {
-  __shared__ unsigned long long s_or[32], s_and[32];
-  unsigned long long o = 0, d = ~0ull;
-  for (int i = threadIdx.x; i < n; i += BLOCK) { o |= src[i]; d &= src[i]; }
+__device__ KeySpan block_span(const uint64_t* src, int n) {
+  __shared__ unsigned long long s_a[32], s_b[32];
+  unsigned long long o = 0, d = ~0ull, lo = ~0ull, hi = 0ull;
+  for (int i = threadIdx.x; i < n; i += BLOCK) {
+    const unsigned long long v = src[i];
+    o |= v;
+    d &= v;
+    lo = v < lo ? v : lo;
+    hi = v > hi ? v : hi;
+  }
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) {
     o |= __shfl_xor_sync(kFull, o, m);
     d &= __shfl_xor_sync(kFull, d, m);
+    const unsigned long long l2 = __shfl_xor_sync(kFull, lo, m), h2 = __shfl_xor_sync(kFull, hi, m);
+    lo = l2 < lo ? l2 : lo;
+    hi = h2 > hi ? h2 : hi;
   }
-  if ((threadIdx.x & 31) == 0) { s_or[threadIdx.x >> 5] = o; s_and[threadIdx.x >> 5] = d; }
+  // (two rounds through the same two arrays: the largest select variant has
+  // no shared memory to spare)
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) { s_a[w] = o; s_b[w] = d; }
   __syncthreads();
-  o = 0;
-  d = ~0ull;
-  for (int w = 0; w < BLOCK / 32; ++w) { o |= s_or[w]; d &= s_and[w]; }
-  *out_or = o;
-  *out_and = d;
+  KeySpan r{0ull, ~0ull, ~0ull, 0ull};
+  for (int j = 0; j < BLOCK / 32; ++j) { r.all_or |= s_a[j]; r.all_and &= s_b[j]; }
   __syncthreads();
+  if ((threadIdx.x & 31) == 0) { s_a[w] = lo; s_b[w] = hi; }
+  __syncthreads();
+  for (int j = 0; j < BLOCK / 32; ++j) {
+    r.kmin = s_a[j] < r.kmin ? s_a[j] : r.kmin;
+    r.kmax = s_b[j] > r.kmax ? s_b[j] : r.kmax;
+  }
+  __syncthreads();
+  return r;
 }
 
 // Stable LSD radix sort of src[0..n) into descending key order, one 8-bit
@@ -750,6 +780,14 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   unsigned* cur = work + 2 * NB;  // fill cursors
   int pass = 0;
   bool failed = false;
+  // Large k with the bin sort to follow: when the whole first-pass bin of the
+  // boundary fits the exchange buffer after the bins above it, every key of
+  // those bins is placed and the bin sort takes the first r places of their
+  // sorted order.  The exact r-th key is then never needed here: no further
+  // passes and no gather.
+  bool whole_bin = false;
+  const bool whole_bin_ok = NB == kBinInfoBins && a.want_topk && a.handoff && G > 1;
+  unsigned long long b1_end = 0;  // end of the first-pass bin of the boundary
   // keys a CTA would cache for the remaining passes: in tau mode the bucket
   // only, otherwise the bucket and everything above it
   unsigned long long cache_need = bucket_mine;
@@ -900,11 +938,15 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     rank -= s_info[1];
     bucket_tot = s_info[2];
     above_all += s_info[3];
-    if (pass == 0) b1 = bin; else above_b1 += s_info[3];
+    if (pass == 0) { b1 = bin; b1_end = s_info[1] + s_info[2]; } else above_b1 += s_info[3];
     bucket_mine = s_info[4];
     cache_need = a.want_topk ? above_all + bucket_mine : bucket_mine;
     TK_STAMP(3 + (pass < 6 ? pass : 6));
     __syncthreads();  // s_info is rewritten by the next pass
+    if (whole_bin_ok && pass == 0 && b1_end <= static_cast<unsigned long long>(a.xstride)) {
+      whole_bin = true;  // (the same totals in every CTA: the same choice)
+      break;
+    }
     if (bucket_tot <= kGatherMax || shift == 0) break;
     shift = shift >= DB ? shift - DB : 0;
   }
@@ -920,7 +962,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   // counting ("Rank by Counting").  Each key carries the CTA it came from,
   // so CTA 0 also counts every CTA's winners inside the first-pass bin.
   await_cluster();  // (when no pass ran) CTA 0 must be running before it is written
-  {
+  if (!whole_bin) {
     uint64_t* gb0 = cluster.map_shared_rank(reinterpret_cast<uint64_t*>(h2 + ((pass + 1) & 1) * NB), 0);
     unsigned* gc0 = cluster.map_shared_rank(&s_gcount, 0);
     unsigned char* go0 = cluster.map_shared_rank(gorg, 0);
@@ -940,9 +982,9 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     if (tid == 0) cluster.map_shared_rank(xch, 0)[8 + crank] = above_b1;
   }
   TK_CTA(5, globaltimer_ns());
-  gsync();  // the bucket is in CTA 0
+  if (!whole_bin) gsync();  // the bucket is in CTA 0
   TK_CTA(6, globaltimer_ns());
-  if (crank == 0) {
+  if (crank == 0 && !whole_bin) {
     const uint64_t* g = reinterpret_cast<const uint64_t*>(h2 + ((pass + 1) & 1) * NB);
     const unsigned n = s_gcount < kGatherMax ? s_gcount : kGatherMax;
     if (tid == 0) xch[3] = 0ull;
@@ -974,8 +1016,9 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   }
   TK_STAMP(10);
   if (!a.want_topk) return;  // nothing reads another CTA's shared memory any more
-  gsync();  // tau and the offsets are delivered
-  const uint64_t tau = xch[3];
+  if (!whole_bin) gsync();  // tau and the offsets are delivered
+  // whole-bin mode: every key of the bins down to the boundary's is placed
+  const uint64_t tau = whole_bin ? (prefix1 | (static_cast<uint64_t>(DM - b1) << shift1)) : xch[3];
   const int64_t k = a.r;
 
   int n_c = 0;
@@ -1036,14 +1079,16 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     // exchange buffer (bins in descending order: the bins' places).  Inside
     // the first-pass bin of the boundary, this CTA's winners start after those
     // of the CTAs before it.
-    uint64_t* xb = a.xbuf + row * k;
-    if (tid == 0) off[b1] = bst[b1] + static_cast<unsigned>(xch[4]);
+    // (whole-bin mode: the boundary bin too is split by CTA as the others)
+    uint64_t* xb = a.xbuf + row * a.xstride;
+    const unsigned long long xend = whole_bin ? b1_end : static_cast<unsigned long long>(k);
+    if (tid == 0 && !whole_bin) off[b1] = bst[b1] + static_cast<unsigned>(xch[4]);
     __syncthreads();
     {
       auto put = [&](uint64_t key) {
         const unsigned b = DM - static_cast<unsigned>((key >> shift1) & DM);
         const unsigned pos = off[b] + atomicAdd(&cur[b], 1u);
-        if (pos < static_cast<unsigned long long>(k)) xb[pos] = key;
+        if (pos < xend) xb[pos] = key;
       };
       if (cached) {
         for (unsigned i = tid; i < cache_n; i += BLOCK)
@@ -1068,6 +1113,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
             bo[NB + 2] = static_cast<unsigned>(pmask1);
             bo[NB + 3] = static_cast<unsigned>(pmask1 >> 32);
             bo[NB + 4] = static_cast<unsigned>(shift1);
+            bo[NB + 5] = static_cast<unsigned>(xend);
           }
         }
         return;
@@ -1190,16 +1236,15 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   __syncthreads();
   TK_STAMP(12);
   {
-    unsigned long long lo_or, lo_and;
-    block_or_and<BLOCK>(bufA, n_c, &lo_or, &lo_and);
-    if (place_by_groups<BLOCK, NB>(bufA, n_c, lo_or ^ lo_and, 0u, ~0u, bufB, work, work + NB, work + 2 * NB,
+    const KeySpan sp = block_span<BLOCK>(bufA, n_c);
+    if (place_by_groups<BLOCK, NB>(bufA, n_c, sp.kmin, sp.kmax, 0u, ~0u, bufB, work, work + NB, work + 2 * NB,
                                    s_tmp, 512u, a, row, k, place0, my0, my1)) {
       TK_STAMP(13);
       return;
     }
     // a group too large to rank by counting: stable LSD radix sort, one
     // 8-bit digit per pass, of the digits on which the local keys differ
-    const uint64_t* sorted = lsd_sort<BLOCK, P>(bufA, bufB, n_c, lo_or ^ lo_and, h2);
+    const uint64_t* sorted = lsd_sort<BLOCK, P>(bufA, bufB, n_c, sp.all_or ^ sp.all_and, h2);
     for (int i = tid; i < n_c; i += BLOCK) {
       const int64_t place = place0 + i;
       if (place >= my0 && place < my1) write_out(a, row, k, place, sorted[i]);
@@ -1322,12 +1367,13 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   const uint64_t prefix1 = static_cast<uint64_t>(__ldcg(bi + NB)) | (static_cast<uint64_t>(__ldcg(bi + NB + 1)) << 32);
   const uint64_t pmask1 = static_cast<uint64_t>(__ldcg(bi + NB + 2)) | (static_cast<uint64_t>(__ldcg(bi + NB + 3)) << 32);
   const int shift1 = static_cast<int>(__ldcg(bi + NB + 4));
-  const uint64_t* xb = a.xbuf + row * k;
+  const int64_t xend = static_cast<int64_t>(__ldcg(bi + NB + 5));  // keys placed: >= k
+  const uint64_t* xb = a.xbuf + row * a.xstride;
   if (tid == 0) { s_info[0] = 0; s_info[1] = 0; }
   __syncthreads();
   auto bin_end = [&](unsigned b) -> int64_t {
-    const int64_t e = (b + 1 < static_cast<unsigned>(NB)) ? static_cast<int64_t>(bst[b + 1]) : k;
-    return e < k ? e : k;
+    const int64_t e = (b + 1 < static_cast<unsigned>(NB)) ? static_cast<int64_t>(bst[b + 1]) : xend;
+    return e < xend ? e : xend;
   };
   // first-digit bins holding places my0 and my1 - 1
   for (int b = tid; b < NB; b += BLOCK) {
@@ -1417,14 +1463,13 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
     }
   }
   __syncthreads();
-  unsigned long long lo_or, lo_and;
-  block_or_and<BLOCK>(bufA, n_c, &lo_or, &lo_and);
+  const KeySpan sp = block_span<BLOCK>(bufA, n_c);
   TK_BS(0, static_cast<unsigned>(n_c));
-  if (place_by_groups<BLOCK, kBinSortGroups>(bufA, n_c, lo_or ^ lo_and, 0u, ~0u, bufB, scr, scr + kBinSortGroups,
+  if (place_by_groups<BLOCK, kBinSortGroups>(bufA, n_c, sp.kmin, sp.kmax, 0u, ~0u, bufB, scr, scr + kBinSortGroups,
                                              scr + 2 * kBinSortGroups, s_tmp, 512u, a, row, k, place0, my0, my1))
     return;
   TK_BS(3, 1u);
-  const uint64_t* sorted = lsd_sort<BLOCK, kBinSortCap>(bufA, bufB, n_c, lo_or ^ lo_and, scr);
+  const uint64_t* sorted = lsd_sort<BLOCK, kBinSortCap>(bufA, bufB, n_c, sp.all_or ^ sp.all_and, scr);
   for (int i = tid; i < n_c; i += BLOCK) {
     const int64_t place = place0 + i;
     if (place >= my0 && place < my1) write_out(a, row, k, place, sorted[i]);
@@ -1528,6 +1573,7 @@ int sm_count() {
 
 int64_t select_max_k() { return static_cast<int64_t>(kMaxCluster) * kBigP; }
 int64_t select_binfo_words(int64_t k) { return k >= kBinSortMinK ? kBinInfoWords : 0; }
+int64_t select_xbuf_stride(int64_t k) { return k >= kBinSortMinK ? 2 * k : k; }
 
 #ifdef TK_PHASE_TIMING
 TK_TIMELINE_ACCESSOR(debug_timeline_select)
@@ -1562,6 +1608,7 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   a.out_idx = job.out_idx;
   a.status = job.status;
   a.xbuf = job.xbuf;
+  a.xstride = job.xbuf_stride > job.r ? job.xbuf_stride : job.r;
   a.shist = job.want_topk ? nullptr : job.sample_hist;
   if (job.want_topk && job.keys && job.check_miss) {
     a.miss_src = p.dtype == kF32 ? 1 : 2;

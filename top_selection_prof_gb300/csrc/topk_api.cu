@@ -332,7 +332,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   const size_t o_tiles = off; off = align_up(off + sizeof(unsigned) * ntile);
   const size_t o_samples = off; off = align_up(off + sizeof(uint64_t) * nsel * S);
   const size_t o_buf = off; off = align_up(off + sizeof(uint64_t) * nsel * M);
-  const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * nsel * k);
+  const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * nsel * select_xbuf_stride(k));
   const size_t o_binfo = off; off = align_up(off + sizeof(unsigned) * nsel * select_binfo_words(k));
   void* ws = nullptr;
   Workspace* wentry = nullptr;
@@ -418,6 +418,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
   rj.xbuf = xbuf;
+  rj.xbuf_stride = select_xbuf_stride(k);
   rj.binfo = select_binfo_words(k) ? reinterpret_cast<unsigned*>(base + o_binfo) : nullptr;
   if (plan.path == TOPK_PATH_PROFK && !fallback_launched) {
     rj.check_miss = true;
