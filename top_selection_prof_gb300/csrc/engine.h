@@ -52,17 +52,45 @@ struct DevHeader {
 // ---- sample (kernels_sample.cu) ----------------------------------------------
 // Also resets counts[0..nsel) and the header (arrivals, status, misses) when
 // those pointers are non-null, so the filter and fallback start clean.
-// hist_add / hist_zero (nullable, kSampleHistBins counters per selection):
-// the sampled keys are counted by their leading kSampleHistBits bits into
-// hist_add (bin = kSampleHistBins - 1 - digit, largest keys first), and
+// hist_add / hist_zero (nullable, each kSampleHistHalfWords counters): the
+// sampled keys are counted by their leading kSampleHistBits bits into level 0
+// of hist_add (row-major, kSampleHistBins per selection; bin =
+// kSampleHistBins - 1 - digit, largest keys first), and the whole of
 // hist_zero is cleared for the next call.  Both must be zero-initialised
 // once; they then alternate between calls.
 constexpr int kSampleHistBits = 11;
 constexpr int kSampleHistBins = 1 << kSampleHistBits;
 constexpr int64_t kSampleHistMaxRows = 16;  // selections with a sample histogram
+constexpr int kSampleHistLevels = 6;        // 11-bit digits of a key of up to 64 bits
+// One histogram half: kSampleHistLevels levels of kSampleHistMaxRows rows.
+constexpr int64_t kSampleHistHalfWords = int64_t(kSampleHistLevels) * kSampleHistMaxRows * kSampleHistBins;
 cudaError_t launch_sample(const Problem& p, int64_t S, uint64_t seed, uint64_t counter,
                           uint64_t* keys, unsigned long long* counts_to_zero, DevHeader* hdr,
                           unsigned* hist_add, unsigned* hist_zero, cudaStream_t st);
+
+// Sampling and the threshold in one cooperative grid (kernels_sample.cu): the
+// t-th largest sampled key of each selection is found by a radix select over
+// the grid (11-bit digits counted into hist level by level, a grid barrier
+// per digit) until its bin holds at most kTauGather keys; those are gathered
+// and the last block of the selection ranks them.  hist / hist_zero are
+// histogram halves as above (hist counted into, hist_zero cleared); ctl holds
+// kTauCtlWords words and gather kTauGather keys per selection.  ctl must be
+// zero on entry; the kernel leaves its grid barrier and counters as it found
+// them except after a timeout, so the refinement clears ctl every call.
+constexpr int kTauGather = 1024;
+constexpr int kTauCtlWords = 2 + 2 * static_cast<int>(kSampleHistMaxRows);
+struct SampleTauScratch {
+  unsigned* hist;
+  unsigned* hist_zero;
+  unsigned* ctl;
+  uint64_t* gather;
+};
+// Whether the fused grid fits on the device at once (else launch_sample and
+// a threshold select are used).
+bool sample_tau_supported(const Problem& p, int64_t S);
+cudaError_t launch_sample_tau(const Problem& p, int64_t S, int64_t t, uint64_t seed, uint64_t counter,
+                              unsigned long long* counts_to_zero, DevHeader* hdr, const SampleTauScratch& sc,
+                              uint64_t* tau_out, cudaStream_t st);
 
 // ---- filter and fallback (kernels_filter.cu) ---------------------------------
 // SMs a threshold select of nsel clusters of G blocks holds while the filter
@@ -121,6 +149,8 @@ struct SelectJob {
   // large k: per selection select_binfo_words(k) words; then the winners are
   // sorted by a second grid of small blocks instead of the cluster alone
   unsigned* binfo = nullptr;
+  unsigned* clear_words = nullptr;  // want_topk: n_clear words zeroed after the earlier grids finish
+  int n_clear = 0;
 };
 int64_t select_binfo_words(int64_t k);  // 0 when k is too small for the bin sort
 // Keys per selection the exchange buffer should hold for rank k (2k with the
@@ -138,6 +168,7 @@ int debug_timeline_select(unsigned long long* out, int reset);
 int debug_binsort_ns(unsigned long long* out);
 int debug_timeline_filter(unsigned long long* out, int reset);
 int debug_timeline_sample(unsigned long long* out, int reset);
+int debug_sample_tau_ns(unsigned long long* out);  // debug builds: stamps of the fused threshold grid
 #endif
 
 }  // namespace tk

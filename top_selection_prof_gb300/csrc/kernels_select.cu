@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "engine.h"
+#include "rank.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -38,12 +39,11 @@ namespace tk {
 
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxCluster = 16;
 
 #ifdef TK_PHASE_TIMING
 // Debug builds only: globaltimer stamps of the first cluster's CTA 0.
-__device__ unsigned long long g_phase_ns[2][32];
+__device__ unsigned long long g_phase_ns[2][48];
 __device__ unsigned long long g_cta_ns[2][16][8];  // per CTA of the first cluster: debug stamps
 #define TK_STAMP(i)                                                                         \
   do {                                                                                      \
@@ -54,7 +54,13 @@ __device__ unsigned long long g_cta_ns[2][16][8];  // per CTA of the first clust
     if (blockIdx.x < 16 && threadIdx.x == 0) g_cta_ns[a.want_topk][blockIdx.x][(slot)] = (v); \
   } while (0)
 #define TK_DBG(slot, v) (g_cta_ns[1][15][(slot)] = (v))
+__device__ unsigned long long g_bs_ns[1024][8];  // debug: per-block phase stamps of the bin sort
+#define TK_BSP(i) \
+  do { if (threadIdx.x == 0 && blockIdx.x < 1024) g_bs_ns[blockIdx.x][(i)] = globaltimer_ns(); } while (0)
 #else
+#define TK_BSP(i) \
+  do {            \
+  } while (0)
 #define TK_DBG(slot, v) \
   do {                  \
   } while (0)
@@ -96,6 +102,8 @@ struct SelParams {
   // bins (kBinInfoWords words per selection) for the grid-wide bin sort
   unsigned* binfo;
   int handoff;
+  unsigned* clear_words;              // nullable: zeroed once every earlier grid has finished
+  int n_clear;
 };
 
 // Published per selection for the bin sort: NB bin starts, then the
@@ -208,18 +216,6 @@ __device__ __forceinline__ void for_cache(const uint64_t* cache, unsigned n, F&&
   }
 }
 
-// Appends key to dst[*counter ...] for lanes with want set: one shared atomic
-// per warp.  Returns the slot of this lane's key (meaningless when !want).
-// Called by all 32 lanes of the warp.
-__device__ __forceinline__ unsigned warp_append_slot(unsigned* counter, bool want) {
-  const unsigned m = __ballot_sync(kFull, want);
-  if (m == 0) return 0u;
-  const int leader = __ffs(m) - 1;
-  unsigned base = 0;
-  if (static_cast<int>(threadIdx.x & 31) == leader) base = atomicAdd(counter, __popc(m));
-  base = __shfl_sync(kFull, base, leader);
-  return base + __popc(m & lanemask_lt());
-}
 
 // 16-byte global -> shared copies that bypass registers (cp.async, L2 only).
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
@@ -230,34 +226,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// Block-wide inclusive scan of one 64-bit value per thread.  `tmp` holds 32
-// entries.  Ends with a barrier, so `tmp` may be reused at once.
-__device__ __forceinline__ unsigned long long block_scan_incl(unsigned long long v,
-                                                              unsigned long long* tmp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(kFull, v, o);
-    if (lane >= o) v += y;
-  }
-  if (lane == 31) tmp[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    const unsigned long long s = lane < nwarps ? tmp[lane] : 0ull;
-    unsigned long long si = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(kFull, si, o);
-      if (lane >= o) si += y;
-    }
-    if (lane < nwarps) tmp[lane] = si - s;
-  }
-  __syncthreads();
-  v += tmp[warp];
-  __syncthreads();
-  return v;
-}
 
 template <int BLOCK>
 constexpr int min_blocks() { return BLOCK >= 1024 ? 1 : 4; }
@@ -282,21 +250,6 @@ __device__ __forceinline__ void write_out(const SelParams& a, int64_t row, int64
   }
 }
 
-// Number of keys in src[j0, j1) greater than v.  Rounds of eight
-// independent, predicated loads (a slot past j1 reads as key 0, which is
-// never greater): the loop is bound by shared-memory latency, not by the
-// compares, so no round may wait on the previous one.
-__device__ __forceinline__ unsigned count_above(const uint64_t* src, unsigned j0, unsigned j1, uint64_t v) {
-  unsigned r = 0;
-  for (unsigned j = j0; j < j1; j += 8) {
-    uint64_t t[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) t[q] = j + q < j1 ? src[j + q] : 0ull;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) r += t[q] > v ? 1u : 0u;
-  }
-  return r;
-}
 
 // Beyond this many compares per key on average, ranking inside groups by
 // counting gives way to the LSD radix sort.
@@ -341,6 +294,7 @@ __device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint6
   for (int i = tid; i < n; i += BLOCK) atomicAdd(&gcount[group(src[i])], 1u);
   __syncthreads();
   TK_STAMP(22);
+  if constexpr (NB == 4096) TK_BSP(4);
   unsigned c[kPer];
   unsigned long long sum = 0, sq = 0;
   unsigned mx = 0;
@@ -366,6 +320,7 @@ __device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint6
   atomicMax(&s_gmax, mx);
   __syncthreads();
   TK_STAMP(23);
+  if constexpr (NB == 4096) TK_BSP(5);
   if (blockIdx.x == 0 && threadIdx.x == 0) TK_DBG(0, s_gmax);
   if (s_gmax > max_group || s_cost > kMaxComparesPerKey * static_cast<unsigned long long>(n)) return false;
   for (int i = tid; i < n; i += BLOCK) {
@@ -375,6 +330,7 @@ __device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint6
   }
   __syncthreads();
   TK_STAMP(25);
+  if constexpr (NB == 4096) TK_BSP(6);
   for (int i = tid; i < n; i += BLOCK) {
     const uint64_t v = grp[i];
     const unsigned g = group(v);
@@ -550,77 +506,6 @@ struct Layout {
   static_assert(NB % BLOCK == 0, "whole bins per thread");
 };
 
-// The key of 1-based descending rank `rank` among g[0..n) (distinct keys, in
-// shared or global memory); the thread that finds it writes it to *out (the
-// caller synchronises before reading).  Few keys are ranked by counting
-// directly; more are first narrowed by 8-bit radix passes below their
-// highest varying bit to at most 32, since counting all n keys against each
-// other costs n^2 / 32 shared-memory wavefronts.  lh holds 256 counters;
-// s_tmp 32 words; s_info 3.  Every thread of the block calls it.
-template <int BLOCK>
-__device__ void bucket_kth(const uint64_t* g, unsigned n, unsigned long long rank, unsigned* lh,
-                           unsigned long long* s_tmp, unsigned long long* s_info, unsigned* s_cnt, uint64_t* out) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (n <= 128u) {
-    __syncthreads();
-    for (unsigned i = tid; i < n; i += BLOCK)
-      if (count_above(g, 0u, n, g[i]) == rank - 1) *out = g[i];
-    return;
-  }
-  uint64_t* small = reinterpret_cast<uint64_t*>(s_tmp);  // <= 32 keys (the scans are done by then)
-  {
-    unsigned long long o = 0, d = ~0ull;
-    for (unsigned i = tid; i < n; i += BLOCK) { o |= g[i]; d &= g[i]; }
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) {
-      o |= __shfl_xor_sync(kFull, o, m);
-      d &= __shfl_xor_sync(kFull, d, m);
-    }
-    if (tid == 0) { s_info[0] = 0ull; s_info[1] = ~0ull; }
-    __syncthreads();
-    if (lane == 0) { atomicOr(&s_info[0], o); atomicAnd(&s_info[1], d); }
-    __syncthreads();
-  }
-  const unsigned long long gv = s_info[0] ^ s_info[1];
-  __syncthreads();
-  int lsh = gv ? 63 - __clzll(static_cast<long long>(gv)) : 0;
-  lsh = lsh >= 7 ? lsh - 7 : 0;
-  uint64_t lpre = 0, lmsk = 0;
-  unsigned long long lrank = rank, lcnt = n;
-#pragma unroll 1
-  while (lcnt > 32) {
-    for (int i = tid; i < 256; i += BLOCK) lh[i] = 0u;
-    __syncthreads();
-    for (unsigned i = tid; i < n; i += BLOCK)
-      if ((g[i] & lmsk) == lpre) atomicAdd(&lh[255u - static_cast<unsigned>((g[i] >> lsh) & 255u)], 1u);
-    __syncthreads();
-    const unsigned long long c = tid < 256 ? lh[tid] : 0ull;
-    const unsigned long long incl = block_scan_incl(c, s_tmp);
-    if (tid < 256 && incl - c < lrank && lrank <= incl) {
-      s_info[0] = static_cast<unsigned long long>(tid);
-      s_info[1] = incl - c;
-      s_info[2] = c;
-    }
-    __syncthreads();
-    lpre |= static_cast<uint64_t>(255u - static_cast<unsigned>(s_info[0])) << lsh;
-    lmsk |= 255ull << lsh;
-    lrank -= s_info[1];
-    lcnt = s_info[2];
-    __syncthreads();
-    if (lsh == 0) break;
-    lsh = lsh >= 8 ? lsh - 8 : 0;
-  }
-  if (tid == 0) *s_cnt = 0u;
-  __syncthreads();
-  for (unsigned i = tid; i < n; i += BLOCK)
-    if ((g[i] & lmsk) == lpre) {
-      const unsigned slot = atomicAdd(s_cnt, 1u);
-      if (slot < 32u) small[slot] = g[i];
-    }
-  __syncthreads();
-  const unsigned ns = *s_cnt < 32u ? *s_cnt : 32u;
-  if (static_cast<unsigned>(tid) < ns && count_above(small, 0u, ns, small[tid]) == lrank - 1) *out = small[tid];
-}
 
 template <int BLOCK, int P, int CB, int NB, int SRC>
 __device__ __forceinline__ void select_body(const SelParams& a) {
@@ -637,9 +522,10 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   unsigned char* gorg = smem + L::kGorg;
   unsigned long long* xch = reinterpret_cast<unsigned long long*>(smem + L::kXch);
   __shared__ unsigned long long s_tmp[32];
-  __shared__ unsigned long long s_info[5];
+  __shared__ unsigned long long s_info[6];
   __shared__ unsigned s_cnt;
   __shared__ unsigned s_gcount;
+  __shared__ unsigned s_gbase;
   __shared__ unsigned s_wcnt[kMaxCluster];
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -649,8 +535,10 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // Shared memory of another CTA may be used only once that CTA runs: arrive
-  // now, wait before the first remote access.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  // now, wait before the first remote access.  The gather counter is cleared
+  // first and released by the arrival, so no remote atomic precedes it.
+  if (threadIdx.x == 0) s_gcount = 0u;
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   bool cluster_started = false;
   auto await_cluster = [&]() {
     if (!cluster_started) {
@@ -672,7 +560,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   // slices start at even positions so key slices can be copied in 16-byte units
   const int64_t sb = (valid * crank / G) & ~int64_t(1);
   const int64_t se = (crank + 1 == G) ? valid : ((valid * (crank + 1) / G) & ~int64_t(1));
-  if (tid == 0) { s_gcount = 0u; s_cnt = 0u; }
+  if (tid == 0) s_cnt = 0u;
   if (tid < kMaxCluster) s_wcnt[tid] = 0u;
   TK_STAMP(0);
   TK_CTA(4, globaltimer_ns());
@@ -685,7 +573,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   // tau from the sample histogram: the first digit is already counted, and
   // only the boundary bucket's keys are read (streamed; cached if small)
   const bool from_hist = NB == 2048 && !a.want_topk && a.shist != nullptr;
-  const bool fits = !from_hist && (valid + G - 1) / G + 2 <= cache_cap;
+  const bool fits = (valid + G - 1) / G + 2 <= cache_cap;
   bool cached = false;
   unsigned cache_n = 0;
   __syncthreads();
@@ -719,7 +607,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   // this exchange and start at the top of the key.
   const int kb = a.key_bits + a.ib;
   unsigned long long all_or = (kb >= 64) ? ~0ull : ((1ull << kb) - 1ull), all_and = 0ull;
-  if (fits) {
+  if (fits && !from_hist) {
     // warp-reduce, then one shared atomic per warp; the CTA's result is
     // published in xch[0..1] and read by every CTA of the cluster
     if (tid == 0) { xch[0] = 0ull; xch[1] = ~0ull; }
@@ -774,6 +662,8 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   unsigned long long above_b1 = 0;   // this CTA's keys of the first-pass bin above the bucket
   unsigned long long above_all = 0;  // this CTA's keys above the bucket
   unsigned long long bucket_tot = 0, bucket_mine = static_cast<unsigned long long>(se - sb);
+  unsigned long long bucket_before = 0;  // keys of the CTAs before this one in the bucket
+  bool counted = false;                  // (a cluster pass counted the bucket per CTA)
   unsigned b1 = 0;
   unsigned* bst = work;           // first place of each first-pass bin
   unsigned* off = work + NB;      // this CTA's first place inside each first-pass bin
@@ -926,6 +816,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
         s_info[2] = tt[q];
         s_info[3] = mrun;   // this CTA's keys in the bins above
         s_info[4] = mm[q];
+        s_info[5] = bf[q];  // keys of the CTAs before this one in the bucket
       }
       trun += tt[q];
       mrun += mm[q];
@@ -940,6 +831,8 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     above_all += s_info[3];
     if (pass == 0) { b1 = bin; b1_end = s_info[1] + s_info[2]; } else above_b1 += s_info[3];
     bucket_mine = s_info[4];
+    bucket_before = s_info[5];
+    counted = true;
     cache_need = a.want_topk ? above_all + bucket_mine : bucket_mine;
     TK_STAMP(3 + (pass < 6 ? pass : 6));
     __syncthreads();  // s_info is rewritten by the next pass
@@ -963,32 +856,59 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   // so CTA 0 also counts every CTA's winners inside the first-pass bin.
   await_cluster();  // (when no pass ran) CTA 0 must be running before it is written
   if (!whole_bin) {
+    // Each CTA writes its bucket keys to its own range of CTA 0's buffer: the
+    // range starts after the keys of the CTAs before it, known from the last
+    // pass's counts or, when no pass ran, reserved with one remote atomic per
+    // CTA (one per warp on a single counter serialised on CTA 0).
     uint64_t* gb0 = cluster.map_shared_rank(reinterpret_cast<uint64_t*>(h2 + ((pass + 1) & 1) * NB), 0);
     unsigned* gc0 = cluster.map_shared_rank(&s_gcount, 0);
     unsigned char* go0 = cluster.map_shared_rank(gorg, 0);
-    auto give = [&](uint64_t k, bool in) {  // all 32 lanes; one remote atomic per warp
+    auto each = [&](auto&& f) {
+      if (cached) {
+        for_cache<BLOCK>(cache, cache_n, f);
+      } else {
+        for_slice<SRC, BLOCK>(a, row, sb, se, f);
+      }
+    };
+    if (tid == 0) s_cnt = 0u;
+    __syncthreads();
+    TK_STAMP(32);
+    if (!counted) {
+      each([&](uint64_t k, bool in) {
+        const unsigned m = __ballot_sync(kFull, in && (k & pmask) == prefix);
+        if (lane == 0 && m) atomicAdd(&s_cnt, static_cast<unsigned>(__popc(m)));
+      });
+      __syncthreads();
+      TK_STAMP(33);
+      if (tid == 0) {
+        s_gbase = atomicAdd(gc0, s_cnt);
+        s_cnt = 0u;
+      }
+      __syncthreads();
+      TK_STAMP(34);
+    }
+    const unsigned gbase = counted ? static_cast<unsigned>(bucket_before) : s_gbase;
+    each([&](uint64_t k, bool in) {
       const bool want = in && (k & pmask) == prefix;
-      const unsigned slot = warp_append_slot(gc0, want);
+      const unsigned slot = gbase + warp_append_slot(&s_cnt, want);
       if (want && slot < kGatherMax) {
         gb0[slot] = k;
         go0[slot] = static_cast<unsigned char>(crank);
       }
-    };
-    if (cached) {
-      for_cache<BLOCK>(cache, cache_n, give);
-    } else {
-      for_slice<SRC, BLOCK>(a, row, sb, se, give);
-    }
+    });
     if (tid == 0) cluster.map_shared_rank(xch, 0)[8 + crank] = above_b1;
+    TK_STAMP(35);
   }
   TK_CTA(5, globaltimer_ns());
   if (!whole_bin) gsync();  // the bucket is in CTA 0
   TK_CTA(6, globaltimer_ns());
+  TK_STAMP(36);
   if (crank == 0 && !whole_bin) {
     const uint64_t* g = reinterpret_cast<const uint64_t*>(h2 + ((pass + 1) & 1) * NB);
-    const unsigned n = s_gcount < kGatherMax ? s_gcount : kGatherMax;
+    const unsigned long long gn = counted ? bucket_tot : static_cast<unsigned long long>(s_gcount);
+    const unsigned n = gn < kGatherMax ? static_cast<unsigned>(gn) : kGatherMax;
     if (tid == 0) xch[3] = 0ull;
-    if (tid == 0 && s_gcount > kGatherMax) atomicCAS(a.status, kDevOk, kDevBadState);
+    if (tid == 0 && gn > kGatherMax) atomicCAS(a.status, kDevOk, kDevBadState);
     // Local radix passes (8-bit digits, below the keys' highest varying bit)
     // narrow the bucket to at most 32 keys, which are then ranked by
     // counting: counting all of up to kGather keys against each other would
@@ -1266,6 +1186,8 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
   if (blockIdx.x == 0 && threadIdx.x == 0) g_phase_ns[a.want_topk][28] = globaltimer_ns();
 #endif
   grid_launch_dependents();
+  if (a.clear_words && blockIdx.x == 0)  // control words of an earlier grid, ready for the next call
+    for (int i = threadIdx.x; i < a.n_clear; i += BLOCK) a.clear_words[i] = 0u;
   if constexpr (SRC == 3) {
     // The miss check of the refinement (section 4): with fewer than r
     // survivors, or more than the buffer holds, the candidates cannot give
@@ -1316,7 +1238,6 @@ struct BinSortParams {
 __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp);
 
 #ifdef TK_PHASE_TIMING
-__device__ unsigned long long g_bs_ns[1024][2];  // debug: per-block start and end of the bin sort
 __device__ unsigned g_bs_info[1024][4];          // debug: set size, cut iterations, max group, lsd
 #define TK_BS(i, v) \
   do { if (threadIdx.x == 0 && blockIdx.x < 1024) g_bs_info[blockIdx.x][(i)] = (v); } while (0)
@@ -1330,12 +1251,12 @@ __global__ void __launch_bounds__(kBinSortBlock) bin_sort_kernel(BinSortParams b
   TK_TL_BEGIN(4);
 #ifdef TK_PHASE_TIMING
   grid_dependency_wait();
-  if (threadIdx.x == 0 && blockIdx.x < 1024) g_bs_ns[blockIdx.x][0] = globaltimer_ns();
+  TK_BSP(0);
 #endif
   bin_sort_body(bp);
   TK_TL_END(4);
 #ifdef TK_PHASE_TIMING
-  if (threadIdx.x == 0 && blockIdx.x < 1024) g_bs_ns[blockIdx.x][1] = globaltimer_ns();
+  TK_BSP(7);
 #endif
 }
 
@@ -1382,6 +1303,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
     if (bs <= my1 - 1 && my1 - 1 < be) s_info[1] = static_cast<unsigned long long>(b);
   }
   __syncthreads();
+  TK_BSP(1);
   const unsigned bfirst = static_cast<unsigned>(s_info[0]), blast = static_cast<unsigned>(s_info[1]);
   __syncthreads();
   const int64_t r0 = bst[bfirst] < static_cast<unsigned>(k) ? bst[bfirst] : k, r1 = bin_end(blast);
@@ -1463,7 +1385,9 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
     }
   }
   __syncthreads();
+  TK_BSP(2);
   const KeySpan sp = block_span<BLOCK>(bufA, n_c);
+  TK_BSP(3);
   TK_BS(0, static_cast<unsigned>(n_c));
   if (place_by_groups<BLOCK, kBinSortGroups>(bufA, n_c, sp.kmin, sp.kmax, 0u, ~0u, bufB, scr, scr + kBinSortGroups,
                                              scr + 2 * kBinSortGroups, s_tmp, 512u, a, row, k, place0, my0, my1))
@@ -1579,11 +1503,11 @@ int64_t select_xbuf_stride(int64_t k) { return k >= kBinSortMinK ? 2 * k : k; }
 TK_TIMELINE_ACCESSOR(debug_timeline_select)
 int debug_binsort_ns(unsigned long long* out) {
   if (cudaMemcpyFromSymbol(out, g_bs_ns, sizeof(g_bs_ns)) != cudaSuccess) return -3;
-  return cudaMemcpyFromSymbol(out + 2048, g_bs_info, sizeof(g_bs_info)) == cudaSuccess ? 0 : -3;
+  return cudaMemcpyFromSymbol(out + 8192, g_bs_info, sizeof(g_bs_info)) == cudaSuccess ? 0 : -3;
 }
 int debug_phase_ns(unsigned long long* out) {
   if (cudaMemcpyFromSymbol(out, g_phase_ns, sizeof(g_phase_ns)) != cudaSuccess) return -3;
-  return cudaMemcpyFromSymbol(out + 64, g_cta_ns, sizeof(g_cta_ns)) == cudaSuccess ? 0 : -3;  // 2*16*8
+  return cudaMemcpyFromSymbol(out + 96, g_cta_ns, sizeof(g_cta_ns)) == cudaSuccess ? 0 : -3;  // 2*16*8
 }
 #endif
 
@@ -1608,6 +1532,8 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   a.out_idx = job.out_idx;
   a.status = job.status;
   a.xbuf = job.xbuf;
+  a.clear_words = job.clear_words;
+  a.n_clear = job.n_clear;
   a.xstride = job.xbuf_stride > job.r ? job.xbuf_stride : job.r;
   a.shist = job.want_topk ? nullptr : job.sample_hist;
   if (job.want_topk && job.keys && job.check_miss) {

@@ -66,14 +66,20 @@ cudaError_t workspace(cudaStream_t st, size_t bytes, void** out, Workspace** ent
 }
 
 // Every workspace starts with the same prefix, whatever the call's layout:
-// the device header, then two halves of the sample histograms.  The halves
+// the device header, two halves of the sample histograms, the fused
+// threshold grid's control words and its gather buffer.  The halves
 // alternate between Prof-K calls: a call's sample kernel counts into one and
 // clears the other for the next call, so they stay zero between calls
-// without a memset (the block is zeroed once when it is allocated).
+// without a memset (the block is zeroed once when it is allocated); the
+// control words are cleared by each call's refinement.
 size_t align_up(size_t v);
-constexpr size_t kHistHalfBytes = sizeof(unsigned) * kSampleHistBins * kSampleHistMaxRows;
+constexpr size_t kHistHalfBytes = sizeof(unsigned) * kSampleHistHalfWords;
 size_t ws_hist_offset() { return align_up(sizeof(DevHeader)); }
-size_t ws_prefix() { return ws_hist_offset() + 2 * kHistHalfBytes; }
+size_t ws_tau_ctl_offset() { return ws_hist_offset() + 2 * kHistHalfBytes; }
+size_t ws_tau_gather_offset() { return align_up(ws_tau_ctl_offset() + sizeof(unsigned) * kTauCtlWords); }
+size_t ws_prefix() {
+  return align_up(ws_tau_gather_offset() + sizeof(uint64_t) * kTauGather * kSampleHistMaxRows);
+}
 
 size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -370,27 +376,40 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
       hist_add = reinterpret_cast<unsigned*>(halves + parity * kHistHalfBytes);
       hist_zero = reinterpret_cast<unsigned*>(halves + (parity ^ 1u) * kHistHalfBytes);
     }
-    TK_TRY(launch_sample(p, S, seed, counter, samples, counts, hdr, hist_add, hist_zero, st));
+    // one or a few selections: sampling and the threshold in one grid
+    // (no threshold launch; then the sample and threshold stages share one
+    // event interval)
+    const bool fused = hist_add && sample_tau_supported(p, S);
+    int tau_cluster = 0;
+    if (fused) {
+      const SampleTauScratch sc{hist_add, hist_zero, reinterpret_cast<unsigned*>(base + ws_tau_ctl_offset()),
+                                reinterpret_cast<uint64_t*>(base + ws_tau_gather_offset())};
+      TK_TRY(launch_sample_tau(p, S, plan.t, seed, counter, counts, hdr, sc, tau, st));
+      tau_cluster = -1;  // the filter does not overlap it
+    } else {
+      TK_TRY(launch_sample(p, S, seed, counter, samples, counts, hdr, hist_add, hist_zero, st));
+    }
     if (hist_add) {
       std::lock_guard<std::mutex> lock(g_ws_mu);
       ++wentry->sample_calls;
     }
     TK_TRY(mark(1));
-    SelectJob tj{};
-    tj.keys = samples;
-    tj.key_stride = S;
-    tj.r = plan.t;
-    tj.want_topk = false;
-    tj.tau_out = tau;
-    tj.sample_hist = hist_add;
-    tj.status = &hdr->status;
-    int tau_cluster = 0;
-    TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
+    if (!fused) {
+      SelectJob tj{};
+      tj.keys = samples;
+      tj.key_stride = S;
+      tj.r = plan.t;
+      tj.want_topk = false;
+      tj.tau_out = tau;
+      tj.sample_hist = hist_add;
+      tj.status = &hdr->status;
+      TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
 #ifdef TK_PHASE_TIMING
-    if (std::getenv("TK_DEBUG_TWICE")) TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
+      if (std::getenv("TK_DEBUG_TWICE")) TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
 #endif
+    }
     TK_TRY(mark(2));
-    TK_TRY(launch_filter(p, tau, M, buf, counts, overlap_sms(tau_cluster, nsel), st));
+    TK_TRY(launch_filter(p, tau, M, buf, counts, tau_cluster < 0 ? -1 : overlap_sms(tau_cluster, nsel), st));
     TK_TRY(mark(3));
     // Where to handle a miss: inside the refinement kernel (no launch when
     // nothing missed, but on a miss its cluster alone streams x), or in the
@@ -419,6 +438,8 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.status = &hdr->status;
   rj.xbuf = xbuf;
   rj.xbuf_stride = select_xbuf_stride(k);
+  rj.clear_words = reinterpret_cast<unsigned*>(base + ws_tau_ctl_offset());  // the fused threshold grid's
+  rj.n_clear = kTauCtlWords;
   rj.binfo = select_binfo_words(k) ? reinterpret_cast<unsigned*>(base + o_binfo) : nullptr;
   if (plan.path == TOPK_PATH_PROFK && !fallback_launched) {
     rj.check_miss = true;
@@ -538,6 +559,7 @@ int topk_version(void) { return 100; }
 int topk_debug_phase_ns(unsigned long long* out) { return tk::debug_phase_ns(out); }
 int topk_debug_rows_ns(unsigned long long* out) { return tk::debug_rows_ns(out); }
 int topk_debug_binsort_ns(unsigned long long* out) { return tk::debug_binsort_ns(out); }
+int topk_debug_sample_tau_ns(unsigned long long* out) { return tk::debug_sample_tau_ns(out); }
 int topk_debug_timeline(unsigned long long* out, int reset) {
   unsigned long long a[16], b[16], c[16];
   if (tk::debug_timeline_select(a, reset) || tk::debug_timeline_filter(b, reset) ||
