@@ -179,11 +179,12 @@ bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double ep
 bool pdl_edge(unsigned bit) {
   // Programmatic dependent launch per pipeline edge (bits: 1 threshold
   // select, 2 filter, 4 fallback, 8 refinement).  On by default for the
-  // edges where it shortens the pipeline (1, 8); TOPK_PDL_MASK overrides
-  // (0 turns it off).
+  // edges where it shortens the pipeline (1, 2, 8; the filter edge only
+  // where the preceding grid leaves the filter's SMs free, see
+  // overlap_sms); TOPK_PDL_MASK overrides (0 turns it off).
   static const unsigned mask = [] {
     const char* m = std::getenv("TOPK_PDL_MASK");
-    return m ? static_cast<unsigned>(std::strtoul(m, nullptr, 0)) : (kPdlTau | kPdlRefine);
+    return m ? static_cast<unsigned>(std::strtoul(m, nullptr, 0)) : (kPdlTau | kPdlFilter | kPdlRefine);
   }();
   return (mask & bit) != 0;
 }

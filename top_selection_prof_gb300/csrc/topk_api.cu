@@ -385,7 +385,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
       const SampleTauScratch sc{hist_add, hist_zero, reinterpret_cast<unsigned*>(base + ws_tau_ctl_offset()),
                                 reinterpret_cast<uint64_t*>(base + ws_tau_gather_offset())};
       TK_TRY(launch_sample_tau(p, S, plan.t, seed, counter, counts, hdr, sc, tau, st));
-      tau_cluster = -1;  // the filter does not overlap it
+      tau_cluster = 0;  // holds no SMs once its blocks finish
     } else {
       TK_TRY(launch_sample(p, S, seed, counter, samples, counts, hdr, hist_add, hist_zero, st));
     }
@@ -409,7 +409,10 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
 #endif
     }
     TK_TRY(mark(2));
-    TK_TRY(launch_filter(p, tau, M, buf, counts, tau_cluster < 0 ? -1 : overlap_sms(tau_cluster, nsel), st));
+    // The filter may launch while the fused grid finishes (its blocks leave
+    // early, one block ranks at the end), not while a 16-CTA threshold
+    // cluster runs: that gained nothing.
+    TK_TRY(launch_filter(p, tau, M, buf, counts, fused ? 0 : -1, st));
     TK_TRY(mark(3));
     // Where to handle a miss: inside the refinement kernel (no launch when
     // nothing missed, but on a miss its cluster alone streams x), or in the
