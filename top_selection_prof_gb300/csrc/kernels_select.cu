@@ -210,9 +210,40 @@ __device__ __forceinline__ void for_slice(const SelParams& a, int64_t row, int64
 template <int BLOCK, typename F>
 __device__ __forceinline__ void for_cache(const uint64_t* cache, unsigned n, F&& f) {
   const unsigned lane = threadIdx.x & 31;
+#pragma unroll 4
   for (unsigned iw = threadIdx.x & ~31u; iw < n; iw += BLOCK) {
     const unsigned i = iw + lane;
     f(i < n ? cache[i] : 0ull, i < n);
+  }
+}
+
+// Appends the cached keys that satisfy pred: write(key, slot) with slots
+// from *counter (shared memory) onwards, in no particular order.  Four keys
+// per thread and round, so each warp issues one atomic and one broadcast per
+// 128 keys instead of per 32 (the rounds are a chain of dependent steps).
+template <int BLOCK, typename P, typename W>
+__device__ __forceinline__ void cache_append(const uint64_t* cache, unsigned n, unsigned* counter, P&& pred,
+                                             W&& write) {
+  const unsigned lane = threadIdx.x & 31, lt = lanemask_lt();
+  for (unsigned c0 = 0; c0 < n; c0 += 4 * BLOCK) {
+    uint64_t k[4];
+    unsigned m[4], tot = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const unsigned i = c0 + j * BLOCK + threadIdx.x;
+      k[j] = i < n ? cache[i] : 0ull;
+      m[j] = __ballot_sync(kFull, i < n && pred(k[j]));
+      tot += __popc(m[j]);
+    }
+    if (tot == 0) continue;  // (the same for every lane)
+    unsigned b = 0;
+    if (lane == 0) b = atomicAdd(counter, tot);
+    b = __shfl_sync(kFull, b, 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if ((m[j] >> lane) & 1u) write(k[j], b + __popc(m[j] & lt));
+      b += __popc(m[j]);
+    }
   }
 }
 
@@ -228,7 +259,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 
 template <int BLOCK>
-constexpr int min_blocks() { return BLOCK >= 1024 ? 1 : 4; }
+constexpr int min_blocks() { return BLOCK >= 512 ? 1 : 4; }
 
 // Writes out_vals / out_idx for one winner key at output place `place`.
 __device__ __forceinline__ void write_out(const SelParams& a, int64_t row, int64_t k, int64_t place,
@@ -317,7 +348,8 @@ __device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint6
   // exceeds a radix sort's cost, and the caller sorts instead
   const unsigned long long compares = block_scan_incl(sq, s_tmp);
   if (tid == BLOCK - 1) s_cost = compares;
-  atomicMax(&s_gmax, mx);
+  mx = __reduce_max_sync(kFull, mx);  // one shared atomic per warp
+  if ((threadIdx.x & 31) == 0) atomicMax(&s_gmax, mx);
   __syncthreads();
   TK_STAMP(23);
   if constexpr (NB == 4096) TK_BSP(5);
@@ -353,9 +385,30 @@ struct KeySpan {
   unsigned long long all_or, all_and;
   uint64_t kmin, kmax;
 };
+// Warp reductions of 64-bit values with the 32-bit redux instruction: OR and
+// AND per half; the minimum (maximum) as the extreme high half, then the
+// extreme low half among the lanes holding it.
+__device__ __forceinline__ unsigned long long warp_or64(unsigned long long v) {
+  return (static_cast<unsigned long long>(__reduce_or_sync(kFull, static_cast<unsigned>(v >> 32))) << 32) |
+         __reduce_or_sync(kFull, static_cast<unsigned>(v));
+}
+__device__ __forceinline__ unsigned long long warp_and64(unsigned long long v) {
+  return (static_cast<unsigned long long>(__reduce_and_sync(kFull, static_cast<unsigned>(v >> 32))) << 32) |
+         __reduce_and_sync(kFull, static_cast<unsigned>(v));
+}
+__device__ __forceinline__ unsigned long long warp_min64(unsigned long long v) {
+  const unsigned hi = __reduce_min_sync(kFull, static_cast<unsigned>(v >> 32));
+  const unsigned lo = __reduce_min_sync(kFull, static_cast<unsigned>(v >> 32) == hi ? static_cast<unsigned>(v) : ~0u);
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+__device__ __forceinline__ unsigned long long warp_max64(unsigned long long v) {
+  const unsigned hi = __reduce_max_sync(kFull, static_cast<unsigned>(v >> 32));
+  const unsigned lo = __reduce_max_sync(kFull, static_cast<unsigned>(v >> 32) == hi ? static_cast<unsigned>(v) : 0u);
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
 template <int BLOCK>
 __device__ KeySpan block_span(const uint64_t* src, int n) {
-  __shared__ unsigned long long s_a[32], s_b[32];
+  __shared__ unsigned long long s_span[4];
   unsigned long long o = 0, d = ~0ull, lo = ~0ull, hi = 0ull;
   for (int i = threadIdx.x; i < n; i += BLOCK) {
     const unsigned long long v = src[i];
@@ -364,28 +417,25 @@ __device__ KeySpan block_span(const uint64_t* src, int n) {
     lo = v < lo ? v : lo;
     hi = v > hi ? v : hi;
   }
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) {
-    o |= __shfl_xor_sync(kFull, o, m);
-    d &= __shfl_xor_sync(kFull, d, m);
-    const unsigned long long l2 = __shfl_xor_sync(kFull, lo, m), h2 = __shfl_xor_sync(kFull, hi, m);
-    lo = l2 < lo ? l2 : lo;
-    hi = h2 > hi ? h2 : hi;
+  if (threadIdx.x == 0) {
+    s_span[0] = 0ull;
+    s_span[1] = ~0ull;
+    s_span[2] = ~0ull;
+    s_span[3] = 0ull;
   }
-  // (two rounds through the same two arrays: the largest select variant has
-  // no shared memory to spare)
-  const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) { s_a[w] = o; s_b[w] = d; }
+  o = warp_or64(o);
+  d = warp_and64(d);
+  lo = warp_min64(lo);
+  hi = warp_max64(hi);
   __syncthreads();
-  KeySpan r{0ull, ~0ull, ~0ull, 0ull};
-  for (int j = 0; j < BLOCK / 32; ++j) { r.all_or |= s_a[j]; r.all_and &= s_b[j]; }
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) { s_a[w] = lo; s_b[w] = hi; }
-  __syncthreads();
-  for (int j = 0; j < BLOCK / 32; ++j) {
-    r.kmin = s_a[j] < r.kmin ? s_a[j] : r.kmin;
-    r.kmax = s_b[j] > r.kmax ? s_b[j] : r.kmax;
+  if ((threadIdx.x & 31) == 0) {  // one shared atomic per warp and quantity
+    atomicOr(&s_span[0], o);
+    atomicAnd(&s_span[1], d);
+    atomicMin(&s_span[2], lo);
+    atomicMax(&s_span[3], hi);
   }
+  __syncthreads();
+  const KeySpan r{s_span[0], s_span[1], s_span[2], s_span[3]};
   __syncthreads();
   return r;
 }
@@ -677,6 +727,9 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   // passes and no gather.
   bool whole_bin = false;
   const bool whole_bin_ok = NB == kBinInfoBins && a.want_topk && a.handoff && G > 1;
+  // Few winners (at most NB: h2's 2 x NB words hold them) and several CTAs:
+  // the winners are collected in CTA 0, which sorts them all (see below).
+  const bool collect = a.want_topk && G > 1 && !a.handoff && a.r <= static_cast<int64_t>(NB);
   unsigned long long b1_end = 0;  // end of the first-pass bin of the boundary
   // keys a CTA would cache for the remaining passes: in tau mode the bucket
   // only, otherwise the bucket and everything above it
@@ -773,6 +826,12 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
             const uint2 v = *reinterpret_cast<const uint2*>(r);
             rv[j][0] = v.x;
             rv[j][1] = v.y;
+          } else if constexpr (kPer == 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(r);
+            rv[j][0] = v.x;
+            rv[j][1] = v.y;
+            rv[j][2] = v.z;
+            rv[j][3] = v.w;
           } else {
 #pragma unroll
             for (int q = 0; q < kPer; ++q) rv[j][q] = r[q];
@@ -888,15 +947,27 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
       TK_STAMP(34);
     }
     const unsigned gbase = counted ? static_cast<unsigned>(bucket_before) : s_gbase;
-    each([&](uint64_t k, bool in) {
-      const bool want = in && (k & pmask) == prefix;
-      const unsigned slot = gbase + warp_append_slot(&s_cnt, want);
-      if (want && slot < kGatherMax) {
-        gb0[slot] = k;
-        go0[slot] = static_cast<unsigned char>(crank);
-      }
-    });
-    if (tid == 0) cluster.map_shared_rank(xch, 0)[8 + crank] = above_b1;
+    if (cached) {
+      cache_append<BLOCK>(cache, cache_n, &s_cnt, [&](uint64_t k) { return (k & pmask) == prefix; },
+                          [&](uint64_t k, unsigned slot) {
+                            if (gbase + slot < kGatherMax) {
+                              gb0[gbase + slot] = k;
+                              go0[gbase + slot] = static_cast<unsigned char>(crank);
+                            }
+                          });
+    } else {
+      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t k, bool in) {
+        const bool want = in && (k & pmask) == prefix;
+        const unsigned slot = gbase + warp_append_slot(&s_cnt, want);
+        if (want && slot < kGatherMax) {
+          gb0[slot] = k;
+          go0[slot] = static_cast<unsigned char>(crank);
+        }
+      });
+    }
+    // (collecting: this CTA's winners above the bucket, so that CTA 0 hands
+    // every CTA the first place of its winners)
+    if (tid == 0) cluster.map_shared_rank(xch, 0)[8 + crank] = collect ? above_all : above_b1;
     TK_STAMP(35);
   }
   TK_CTA(5, globaltimer_ns());
@@ -928,7 +999,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
         for (unsigned c = 0; c < G; ++c) {
           unsigned long long* rx = cluster.map_shared_rank(xch, c);
           rx[3] = tau;
-          rx[4] = run;  // winners of the first-pass bin held by the CTAs before c
+          rx[4] = run;  // winners of the first-pass bin (collecting: all winners) of the CTAs before c
           run += xch[8 + c] + s_wcnt[c];
         }
       }
@@ -992,6 +1063,32 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
       if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
       return;
     }
+    n_c = static_cast<int>(k);
+  } else if (collect) {
+    // ------------------------------------------------------------------ collect
+    // Every CTA sends its winners to CTA 0, from the first place CTA 0 handed
+    // it (xch[4]); CTA 0 sorts all of them.  No exchange through global
+    // memory, and no CTA ranks keys that belong to another CTA's places.
+    uint64_t* col0 = cluster.map_shared_rank(reinterpret_cast<uint64_t*>(h2), 0);
+    const unsigned cbase = static_cast<unsigned>(xch[4]);
+    if (tid == 0) s_cnt = 0u;
+    __syncthreads();
+    if (cached) {
+      cache_append<BLOCK>(cache, cache_n, &s_cnt, [&](uint64_t key) { return key >= tau; },
+                          [&](uint64_t key, unsigned slot) {
+                            if (cbase + slot < static_cast<unsigned>(k)) col0[cbase + slot] = key;
+                          });
+    } else {
+      for_slice<SRC, BLOCK>(a, row, sb, se, [&](uint64_t key, bool in) {
+        const bool w = in && key >= tau;
+        const unsigned slot = cbase + warp_append_slot(&s_cnt, w);
+        if (w && slot < static_cast<unsigned>(k)) col0[slot] = key;
+      });
+    }
+    gsync();  // every winner is in CTA 0
+    if (crank != 0) return;
+    const uint64_t* col = reinterpret_cast<const uint64_t*>(h2);
+    for (int i = tid; i < static_cast<int>(k); i += BLOCK) bufA[i] = col[i];
     n_c = static_cast<int>(k);
   } else {
     // ------------------------------------------------------------------ partition
@@ -1402,7 +1499,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
 
 // Kernel variants: (block, sort positions per CTA, cache/second buffer).
 constexpr int kSmallBlock = 256, kSmallP = 1024, kSmallCB = 2048, kSmallNB = 256;
-constexpr int kBigBlock = 1024, kBigP = 11776, kBigCB = 11776, kBigNB = 2048;
+constexpr int kBigBlock = 512, kBigP = 11776, kBigCB = 11776, kBigNB = 2048;
 constexpr int64_t kTauSlice = 8192;
 constexpr int64_t kBinSortMinK = 8192;  // k from which the winners are sorted by the bin-sort grid  // samples streamed per CTA when tau starts from the histogram
 
