@@ -207,9 +207,6 @@ def time_oracle(cfg, x, steps, warmup):
 # ---------------------------------------------------------------------------
 # our engine
 # ---------------------------------------------------------------------------
-# sample, threshold select, filter, refinement (which checks for a miss
-# itself); direct: one kernel; exact: the grid-wide fallback and the sort
-KERNELS_PER_STEP = {"profk": 4, "direct": 1, "exact": 2}
 
 
 def tk_plan(cfg):
@@ -391,7 +388,10 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
     return {
         "value": value, "ms_per_step": ms_step, "path": path, "stats": st, "stages": stages,
         "roofline": roofline, "e2e": e2e, "clocks": clock_info,
-        "gpu_launches": KERNELS_PER_STEP.get(path, 0) * steps,
+        # the library reports the kernels each call launched (sample and
+        # threshold, filter, fallback when it runs as its own grid, refinement,
+        # bin sort for large k; the direct path's one kernel)
+        "gpu_launches": int(st["launches"]) * steps,
         "hbm_gbs_whole_step": n_elems * bytes_per_elem / (ms_step * 1e-3) / 1e9,
     }
 

@@ -104,6 +104,7 @@ typedef struct {
   uint64_t seed;       /* Philox key and counter the sampler used */
   int64_t counter;
   int cluster;         /* CTAs per thread-block cluster in the final selection */
+  int launches;        /* kernels this call launched on the stream */
 } topk_stats_t;
 
 /* Parameters the engine would use for a selection of k out of n (host only). */

@@ -132,3 +132,14 @@ def test_repeated_calls_and_streams():
             v, i = tk.select(xd, 512)
         s.synchronize()
         assert_same(v, i, ov, oi, "rep %d" % rep)
+
+
+@pytest.mark.parametrize("kind,rows,n,k,eps,global_,expect", [
+    ("pareto15", 1, 1 << 22, 1024, 1e-6, False, 3),            # sample + threshold, filter, refinement
+    ("relu_normal_bf16", 256, 65536, 100000, 1e-3, True, 4),   # ... + bin sort (cluster of 16)
+    ("normal", 64, 32768, 64, 1e-3, False, 1),                 # direct: one kernel
+])
+def test_launch_count(kind, rows, n, k, eps, global_, expect):
+    x = workloads.make(kind, rows, n, seed=11)
+    st = _check(x, k, eps=eps, global_=global_)
+    assert st["launches"] == expect, st

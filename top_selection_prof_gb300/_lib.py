@@ -30,7 +30,8 @@ class TopkStats(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("index_bits", ctypes.c_int), ("S", ctypes.c_int64),
                 ("t", ctypes.c_int64), ("M", ctypes.c_int64), ("R", ctypes.c_int64),
                 ("misses", ctypes.c_int64), ("tau", ctypes.c_uint64), ("tau_index", ctypes.c_int64),
-                ("seed", ctypes.c_uint64), ("counter", ctypes.c_int64), ("cluster", ctypes.c_int)]
+                ("seed", ctypes.c_uint64), ("counter", ctypes.c_int64), ("cluster", ctypes.c_int),
+                ("launches", ctypes.c_int)]
 
 
 class TopkPlan(ctypes.Structure):

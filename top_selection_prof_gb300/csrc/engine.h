@@ -151,6 +151,7 @@ struct SelectJob {
   unsigned* binfo = nullptr;
   unsigned* clear_words = nullptr;  // want_topk: n_clear words zeroed after the earlier grids finish
   int n_clear = 0;
+  int* launch_count = nullptr;      // nullable: incremented once per kernel launched
 };
 int64_t select_binfo_words(int64_t k);  // 0 when k is too small for the bin sort
 // Keys per selection the exchange buffer should hold for rank k (2k with the

@@ -865,9 +865,12 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     for (int q = 0; q < kPer; ++q) {
       const int b = tid * kPer + q;
       if (pass == 0 && a.want_topk && G > 1) {
+        // this CTA's keys of bin b go to places trun + bf[q] + j; cur[b]
+        // starts at their place among this CTA's own keys (mrun), so that
+        // off[b] + (mrun + j) is the place (unsigned arithmetic wraps)
         bst[b] = static_cast<unsigned>(trun);
-        off[b] = static_cast<unsigned>(trun) + bf[q];
-        cur[b] = 0u;
+        off[b] = static_cast<unsigned>(trun) + bf[q] - static_cast<unsigned>(mrun);
+        cur[b] = static_cast<unsigned>(mrun);
       }
       if (trun < rank && rank <= trun + tt[q]) {
         s_info[0] = static_cast<unsigned long long>(b);
@@ -1099,15 +1102,37 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     // (whole-bin mode: the boundary bin too is split by CTA as the others)
     uint64_t* xb = a.xbuf + row * a.xstride;
     const unsigned long long xend = whole_bin ? b1_end : static_cast<unsigned long long>(k);
-    if (tid == 0 && !whole_bin) off[b1] = bst[b1] + static_cast<unsigned>(xch[4]);
+    if (tid == 0 && !whole_bin) off[b1] = bst[b1] + static_cast<unsigned>(xch[4]) - cur[b1];
     __syncthreads();
     {
+      auto bin_of = [&](uint64_t key) { return DM - static_cast<unsigned>((key >> shift1) & DM); };
       auto put = [&](uint64_t key) {
-        const unsigned b = DM - static_cast<unsigned>((key >> shift1) & DM);
+        const unsigned b = bin_of(key);
         const unsigned pos = off[b] + atomicAdd(&cur[b], 1u);
         if (pos < xend) xb[pos] = key;
       };
-      if (cached) {
+      if (cached && cache_n <= static_cast<unsigned>(P)) {
+        // Staged: the winners are first sorted by bin inside this CTA (the
+        // second buffer is free while the cache fits the first), at their
+        // places among this CTA's keys, which are dense from 0; each then
+        // goes to off[bin] + its staged index, so consecutive threads write
+        // consecutive places of a bin (scattered 8-byte stores cost one
+        // memory transaction each).
+        uint64_t* stage = bufB;
+#pragma unroll 4
+        for (unsigned i = tid; i < cache_n; i += BLOCK) {
+          const uint64_t key = cache[i];
+          if (key >= tau) stage[atomicAdd(&cur[bin_of(key)], 1u)] = key;
+        }
+        __syncthreads();
+        const unsigned nst = cur[b1];
+#pragma unroll 4
+        for (unsigned i = tid; i < nst && i < static_cast<unsigned>(CB); i += BLOCK) {
+          const uint64_t key = stage[i];
+          const unsigned pos = off[bin_of(key)] + i;
+          if (pos < xend) xb[pos] = key;
+        }
+      } else if (cached) {
         for (unsigned i = tid; i < cache_n; i += BLOCK)
           if (cache[i] >= tau) put(cache[i]);
       } else {
@@ -1678,6 +1703,7 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   cudaError_t e = small ? launch_src<kSmallBlock, kSmallP, kSmallCB, kSmallNB>(a, src, p.nsel, G, &used, st)
                         : launch_src<kBigBlock, kBigP, kBigCB, kBigNB>(a, src, p.nsel, G, &used, st);
   if (cluster) *cluster = used;
+  if (e == cudaSuccess && job.launch_count) ++*job.launch_count;
   if (e != cudaSuccess || !handoff) return e;
   static bool configured = false;
   if (!configured) {
@@ -1697,7 +1723,9 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_edge(kPdlRefine) ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, bin_sort_kernel, bp);
+  e = cudaLaunchKernelEx(&cfg, bin_sort_kernel, bp);
+  if (e == cudaSuccess && job.launch_count) ++*job.launch_count;
+  return e;
 }
 
 }  // namespace tk

@@ -288,6 +288,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     }
     TK_TRY(launch_rows(p, k, out_vals, out_idx, status, st));
     if (stats) {
+      stats->launches = 1;
       stats->cluster = 1;
       stats->R = p.len;
       int dstat = 0;
@@ -311,8 +312,11 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     job.out_idx = out_idx;
     job.status = &hdr->status;
     job.xbuf = reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + ws_prefix());
+    int nl = 0;
+    job.launch_count = &nl;
     TK_TRY(launch_select(p, job, p.len, &cluster, st));
     if (stats) {
+      stats->launches = nl;
       stats->cluster = cluster;
       stats->R = p.len;
       int dstat = 0;
@@ -366,6 +370,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     return cudaEventRecord(static_cast<cudaEvent_t>(o->events[i]), st);
   };
   bool fallback_launched = false;
+  int nl = 0;  // kernels launched
   if (plan.path == TOPK_PATH_PROFK) {
     TK_TRY(mark(0));
     unsigned* hist_add = nullptr;
@@ -385,9 +390,11 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
       const SampleTauScratch sc{hist_add, hist_zero, reinterpret_cast<unsigned*>(base + ws_tau_ctl_offset()),
                                 reinterpret_cast<uint64_t*>(base + ws_tau_gather_offset())};
       TK_TRY(launch_sample_tau(p, S, plan.t, seed, counter, counts, hdr, sc, tau, st));
+      ++nl;
       tau_cluster = 0;  // holds no SMs once its blocks finish
     } else {
       TK_TRY(launch_sample(p, S, seed, counter, samples, counts, hdr, hist_add, hist_zero, st));
+      ++nl;
     }
     if (hist_add) {
       std::lock_guard<std::mutex> lock(g_ws_mu);
@@ -403,6 +410,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
       tj.tau_out = tau;
       tj.sample_hist = hist_add;
       tj.status = &hdr->status;
+      tj.launch_count = &nl;
       TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
 #ifdef TK_PHASE_TIMING
       if (std::getenv("TK_DEBUG_TWICE")) TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
@@ -413,6 +421,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // early, one block ranks at the end), not while a 16-CTA threshold
     // cluster runs: that gained nothing.
     TK_TRY(launch_filter(p, tau, M, buf, counts, fused ? 0 : -1, st));
+    ++nl;
     TK_TRY(mark(3));
     // Where to handle a miss: inside the refinement kernel (no launch when
     // nothing missed, but on a miss its cluster alone streams x), or in the
@@ -422,6 +431,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // below the launch it saves.
     if (!miss_in_refine(p, k, plan.t, plan.S, eps)) {
       TK_TRY(launch_fallback(p, k, M, buf, counts, fs, force, st));
+      ++nl;
       fallback_launched = true;
     }
     TK_TRY(mark(4));
@@ -429,6 +439,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     TK_TRY(cudaMemsetAsync(base, 0, sizeof(DevHeader), st));
     TK_TRY(cudaMemsetAsync(base + o_counts, 0, o_tau - o_counts, st));  // counts, r_seen
     TK_TRY(launch_fallback(p, k, M, buf, counts, fs, 1, st));
+    ++nl;
   }
   SelectJob rj{};
   rj.keys = buf;
@@ -443,6 +454,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.xbuf_stride = select_xbuf_stride(k);
   rj.clear_words = reinterpret_cast<unsigned*>(base + ws_tau_ctl_offset());  // the fused threshold grid's
   rj.n_clear = kTauCtlWords;
+  rj.launch_count = &nl;
   rj.binfo = select_binfo_words(k) ? reinterpret_cast<unsigned*>(base + o_binfo) : nullptr;
   if (plan.path == TOPK_PATH_PROFK && !fallback_launched) {
     rj.check_miss = true;
@@ -482,6 +494,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     stats->seed = seed;
     stats->counter = static_cast<int64_t>(counter);
     stats->cluster = cluster;
+    stats->launches = nl;
     if (h.status != kDevOk) return h.status == kDevTimeout ? TOPK_ETIMEOUT : TOPK_ECUDA;
   }
   return TOPK_OK;
