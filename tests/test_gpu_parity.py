@@ -51,6 +51,8 @@ CASES = [
     ("normal", 1, 1 << 22, 9000, 1e-3, False, "profk"),            # k just above the bin-sort bound
     ("ties1000", 1, 1 << 24, 12000, 1e-3, False, "profk"),         # bin sort with a 2-CTA cluster
     ("uniform", 1, (1 << 22) + 8, 9000, 0.0, False, "exact"),      # exact path, sort after the fallback
+    ("ties1000", 5, 1 << 22, 12000, 1e-3, False, "profk"),         # more rows than the grid refinement takes
+    ("normal", 4, 1 << 21, 8500, 1e-3, False, "profk"),            # grid refinement over four rows
 ]
 
 
@@ -136,10 +138,76 @@ def test_repeated_calls_and_streams():
 
 @pytest.mark.parametrize("kind,rows,n,k,eps,global_,expect", [
     ("pareto15", 1, 1 << 22, 1024, 1e-6, False, 3),            # sample + threshold, filter, refinement
-    ("relu_normal_bf16", 256, 65536, 100000, 1e-3, True, 4),   # ... + bin sort (cluster of 16)
+    ("relu_normal_bf16", 256, 65536, 100000, 1e-3, True, 4),   # ... grid refinement + bin sort
+    ("ties1000", 5, 1 << 22, 12000, 1e-3, False, 4),           # five rows: refinement cluster + bin sort
     ("normal", 64, 32768, 64, 1e-3, False, 1),                 # direct: one kernel
 ])
 def test_launch_count(kind, rows, n, k, eps, global_, expect):
     x = workloads.make(kind, rows, n, seed=11)
     st = _check(x, k, eps=eps, global_=global_)
     assert st["launches"] == expect, st
+
+
+# Large k on one cooperative grid: the miss check, the fallback and the
+# partition of the winners, then the bin sort.
+@pytest.mark.parametrize("largest", [True, False])
+def test_grid_refinement_forced_miss(largest):
+    x = workloads.make("relu_normal_bf16", 64, 65536, seed=12)
+    st = _check(x, 20000, largest=largest, eps=1e-3, global_=True, force_miss=1)
+    assert st["misses"] == 1 and st["path_name"] == "profk"
+
+
+def test_grid_refinement_overflow_is_repaired():
+    x = workloads.make("ties1000", 1, 1 << 22, seed=13)
+    st = _check(x, 10000, eps=1e-3, m_override=10050)   # the buffer overflows almost surely
+    assert st["misses"] == 1 and st["R"] > st["M"]
+
+
+def test_grid_refinement_exact_kth_key():
+    # One outlier and a constant row: the first digit below the top varying
+    # bit puts every candidate but the outlier in one bin, which holds more
+    # than the exchange buffer's 2k places; the k-th key is then found by
+    # further digits across the grid and only the winners are placed.
+    import numpy as np
+    x = np.full((1, 1 << 22), 1.0, dtype=np.float32)
+    x[0, 12345] = 3.0e38
+    k = 9000
+    _check(x, k, eps=1e-3)  # (few candidates: the whole boundary bin fits)
+    # S = 41286 for this size: t = 266 keeps about 27,000 candidates (> 2k)
+    st = _check(x, k, eps=1e-3, m_override=200000, t_override=266)
+    assert st["misses"] == 0 and st["R"] > 2 * k, st
+
+
+def test_grid_refinement_repeated_calls_alternate_control_words():
+    import torch
+    tk = _tk()
+    x = workloads.make("relu_normal_bf16", 32, 65536, seed=14)
+    xd = to_device(x)
+    ov, oi = plain.topk(x, 10000, global_=True)
+    for rep in range(5):
+        v, i = tk.select_global(xd, 10000)
+        torch.cuda.synchronize()
+        assert_same(v, i, ov, oi, "rep %d" % rep)
+
+
+@pytest.mark.parametrize("kind,rows,n,k,global_,cluster", [
+    ("relu_normal_bf16", 64, 65536, 20000, True, 1),   # one selection, large k: the grid refinement
+    ("ties1000", 5, 1 << 22, 12000, False, 2),          # five selections: a refinement cluster per row
+])
+def test_large_k_refinement_route(kind, rows, n, k, global_, cluster):
+    x = workloads.make(kind, rows, n, seed=15)
+    st = _check(x, k, eps=1e-3, global_=global_)
+    assert st["cluster"] == cluster and st["launches"] == 4, st
+
+
+def test_grid_refinement_more_rows_after_fewer():
+    # The refinement's control words alternate between two copies; a call
+    # with four selections after calls with one must find every row clean.
+    x4 = workloads.make("normal", 4, 1 << 21, seed=16)
+    x1 = workloads.make("relu_normal_bf16", 32, 65536, seed=17)
+    for rep in range(2):   # four rows, three single selections, four rows: the first copy again
+        _check(x4, 8500, largest=rep == 0)
+        _check(x1, 9000, global_=True)
+        _check(x1, 9000, global_=True, largest=False)
+        _check(x1, 9500, global_=True)
+        _check(x4, 8500, largest=rep == 1)

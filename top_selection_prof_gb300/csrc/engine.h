@@ -119,6 +119,34 @@ cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* 
                             unsigned long long* counts, const FallbackScratch& fs, int force,
                             cudaStream_t st);
 
+// Refinement of a few selections with large k on one cooperative grid
+// (kernels_filter.cu): the miss check and, on a miss, the fallback above,
+// then the exact partition of each selection's candidates by the first
+// 11-bit digit below their most significant varying bit into the exchange
+// buffer, published for the bin sort (launch_bin_sort) in the bin-info
+// format of the refinement cluster.
+constexpr int kRefineGridBins = 2048;          // first-digit bins (the bin sort's)
+constexpr int kRefineGridLevels = 6;           // 11-bit digits of a key of up to 64 bits
+constexpr int64_t kRefineGridMaxSel = 4;       // selections one grid refines
+// Control words per selection: OR and NOT-AND of the keys (2 x 64 bits), the
+// boundary bin's placed winners, then one counter per bin and digit level.
+constexpr int64_t kRefineGridCtlWords = 8 + int64_t(kRefineGridLevels) * kRefineGridBins;
+struct RefineGridScratch {
+  unsigned* ctl;          // this call's control words: kRefineGridCtlWords per selection, zero on entry
+  unsigned* ctl_next;     // the other copy (kRefineGridMaxSel selections), cleared here for the next call
+  uint64_t* xbuf;         // exchange buffer, xstride keys per selection
+  int64_t xstride;        // >= 2k
+  unsigned* binfo;        // select_binfo_words(k) words per selection
+  unsigned* clear_words;  // nullable: words of an earlier grid zeroed once that grid has finished
+  int n_clear;
+};
+// Largest buffer capacity (keys per selection) the grid refinement takes, or
+// 0 when it does not apply (too many selections).
+int64_t refine_grid_capacity(const Problem& p);
+cudaError_t launch_refine_grid(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,
+                               unsigned long long* counts, const FallbackScratch& fs, int force,
+                               const RefineGridScratch& rg, cudaStream_t st);
+
 // ---- direct path for many short rows (kernels_rows.cu) -----------------------
 // One block per selection, the row in registers: len <= 32768, k <= 1024.
 bool rows_supported(const Problem& p, int64_t k);
@@ -154,6 +182,9 @@ struct SelectJob {
   int* launch_count = nullptr;      // nullable: incremented once per kernel launched
 };
 int64_t select_binfo_words(int64_t k);  // 0 when k is too small for the bin sort
+// The bin sort alone (job: r = k, xbuf, xbuf_stride, binfo, status, outputs),
+// after the grid refinement has partitioned the winners.
+cudaError_t launch_bin_sort(const Problem& p, const SelectJob& job, cudaStream_t st);
 // Keys per selection the exchange buffer should hold for rank k (2k with the
 // bin sort: room to place the boundary's whole first-pass bin).
 int64_t select_xbuf_stride(int64_t k);
@@ -170,6 +201,7 @@ int debug_binsort_ns(unsigned long long* out);
 int debug_timeline_filter(unsigned long long* out, int reset);
 int debug_timeline_sample(unsigned long long* out, int reset);
 int debug_sample_tau_ns(unsigned long long* out);  // debug builds: stamps of the fused threshold grid
+int debug_refine_grid_ns(unsigned long long* out);  // debug builds: stamps of the grid refinement's block 0
 #endif
 
 }  // namespace tk

@@ -1358,6 +1358,8 @@ struct BinSortParams {
 };
 
 __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp);
+cudaError_t launch_bin_sort_a(const SelParams& a, int64_t nsel, int* launch_count, cudaStream_t st);
+static_assert(kBinInfoBins == kRefineGridBins, "the grid refinement publishes the bin sort's bins");
 
 #ifdef TK_PHASE_TIMING
 __device__ unsigned g_bs_info[1024][4];          // debug: set size, cut iterations, max group, lsd
@@ -1705,16 +1707,43 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   if (cluster) *cluster = used;
   if (e == cudaSuccess && job.launch_count) ++*job.launch_count;
   if (e != cudaSuccess || !handoff) return e;
+  return launch_bin_sort_a(a, p.nsel, job.launch_count, st);
+}
+
+cudaError_t launch_bin_sort(const Problem& p, const SelectJob& job, cudaStream_t st) {
+  if (!job.binfo || !job.xbuf || job.xbuf_stride < job.r || job.r < kBinSortMinK) return cudaErrorInvalidValue;
+  SelParams a{};
+  a.x = p.x;
+  a.len = p.len;
+  a.ib = p.ib;
+  a.flip = p.flip;
+  a.key_bits = p.dtype == kF32 ? 32 : 16;
+  a.r = job.r;
+  a.want_topk = 1;
+  a.out_vals = job.out_vals;
+  a.out_idx = job.out_idx;
+  a.status = job.status;
+  a.xbuf = job.xbuf;
+  a.xstride = job.xbuf_stride;
+  a.binfo = job.binfo;
+  a.handoff = 1;
+  return launch_bin_sort_a(a, p.nsel, job.launch_count, st);
+}
+
+namespace {
+
+cudaError_t launch_bin_sort_a(const SelParams& a, int64_t nsel, int* launch_count, cudaStream_t st) {
   static bool configured = false;
+  cudaError_t e;
   if (!configured) {
     e = cudaFuncSetAttribute(bin_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kBinSortSmem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  BinSortParams bp{a, static_cast<int>((job.r + kBinSortPlaces - 1) / kBinSortPlaces)};
+  BinSortParams bp{a, static_cast<int>((a.r + kBinSortPlaces - 1) / kBinSortPlaces)};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.nsel * bp.q), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(nsel * bp.q), 1, 1);
   cfg.blockDim = dim3(kBinSortBlock, 1, 1);
   cfg.dynamicSmemBytes = kBinSortSmem;
   cfg.stream = st;
@@ -1724,8 +1753,10 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   cfg.attrs = attr;
   cfg.numAttrs = pdl_edge(kPdlRefine) ? 1 : 0;
   e = cudaLaunchKernelEx(&cfg, bin_sort_kernel, bp);
-  if (e == cudaSuccess && job.launch_count) ++*job.launch_count;
+  if (e == cudaSuccess && launch_count) ++*launch_count;
   return e;
 }
+
+}  // namespace
 
 }  // namespace tk

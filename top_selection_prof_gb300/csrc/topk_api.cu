@@ -36,6 +36,7 @@ struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
   uint64_t sample_calls = 0;  // calls whose sample kernel launched: picks the histogram half
+  uint64_t refine_calls = 0;  // calls of the grid refinement: picks its control words' copy
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
@@ -67,19 +68,23 @@ cudaError_t workspace(cudaStream_t st, size_t bytes, void** out, Workspace** ent
 
 // Every workspace starts with the same prefix, whatever the call's layout:
 // the device header, two halves of the sample histograms, the fused
-// threshold grid's control words and its gather buffer.  The halves
-// alternate between Prof-K calls: a call's sample kernel counts into one and
-// clears the other for the next call, so they stay zero between calls
-// without a memset (the block is zeroed once when it is allocated); the
-// control words are cleared by each call's refinement.
+// threshold grid's control words and its gather buffer, and two copies of
+// the grid refinement's control words.  The halves alternate between Prof-K
+// calls: a call's sample kernel counts into one and clears the other for the
+// next call, so they stay zero between calls without a memset (the block is
+// zeroed once when it is allocated); the threshold grid's control words are
+// cleared by each call's refinement; the grid refinement's copies alternate
+// like the halves.
 size_t align_up(size_t v);
 constexpr size_t kHistHalfBytes = sizeof(unsigned) * kSampleHistHalfWords;
 size_t ws_hist_offset() { return align_up(sizeof(DevHeader)); }
 size_t ws_tau_ctl_offset() { return ws_hist_offset() + 2 * kHistHalfBytes; }
 size_t ws_tau_gather_offset() { return align_up(ws_tau_ctl_offset() + sizeof(unsigned) * kTauCtlWords); }
-size_t ws_prefix() {
+size_t ws_refine_ctl_offset() {
   return align_up(ws_tau_gather_offset() + sizeof(uint64_t) * kTauGather * kSampleHistMaxRows);
 }
+constexpr size_t kRefineCtlCopyBytes = sizeof(unsigned) * kRefineGridMaxSel * kRefineGridCtlWords;
+size_t ws_prefix() { return align_up(ws_refine_ctl_offset() + 2 * kRefineCtlCopyBytes); }
 
 size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -364,6 +369,11 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   const uint64_t counter = (o && o->counter >= 0) ? static_cast<uint64_t>(o->counter)
                                                   : g_counter.fetch_add(1);
   const int force = (o && o->force_miss) ? 1 : 0;
+  // Large k and a few selections: the miss check, the fallback and the
+  // partition of the winners run on one cooperative grid over every SM, and
+  // the bin sort follows (no refinement cluster).
+  const bool grid_refine = select_binfo_words(k) > 0 && nsel <= kRefineGridMaxSel &&
+                           M <= refine_grid_capacity(p);
 
   auto mark = [&](int i) -> cudaError_t {
     if (!o || !o->events[i]) return cudaSuccess;
@@ -429,7 +439,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // refinement takes it when the expected cost of its slow miss, eps times
     // about three passes over a row at ~100 GB/s per SM of the cluster, is
     // below the launch it saves.
-    if (!miss_in_refine(p, k, plan.t, plan.S, eps)) {
+    if (!grid_refine && !miss_in_refine(p, k, plan.t, plan.S, eps)) {
       TK_TRY(launch_fallback(p, k, M, buf, counts, fs, force, st));
       ++nl;
       fallback_launched = true;
@@ -438,8 +448,10 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   } else {  // TOPK_PATH_EXACT
     TK_TRY(cudaMemsetAsync(base, 0, sizeof(DevHeader), st));
     TK_TRY(cudaMemsetAsync(base + o_counts, 0, o_tau - o_counts, st));  // counts, r_seen
-    TK_TRY(launch_fallback(p, k, M, buf, counts, fs, 1, st));
-    ++nl;
+    if (!grid_refine) {
+      TK_TRY(launch_fallback(p, k, M, buf, counts, fs, 1, st));
+      ++nl;
+    }
   }
   SelectJob rj{};
   rj.keys = buf;
@@ -472,10 +484,32 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     if (1.5 * er < static_cast<double>(M)) hint = static_cast<int64_t>(1.5 * er);
     if (hint < k) hint = k;
   }
-  TK_TRY(launch_select(p, rj, hint, &cluster, st));
+  if (grid_refine) {
+    uint64_t parity;
+    {
+      std::lock_guard<std::mutex> lock(g_ws_mu);
+      parity = wentry->refine_calls++ & 1u;
+    }
+    char* copies = base + ws_refine_ctl_offset();
+    RefineGridScratch rg{};
+    rg.ctl = reinterpret_cast<unsigned*>(copies + parity * kRefineCtlCopyBytes);
+    rg.ctl_next = reinterpret_cast<unsigned*>(copies + (parity ^ 1u) * kRefineCtlCopyBytes);
+    rg.xbuf = xbuf;
+    rg.xstride = rj.xbuf_stride;
+    rg.binfo = rj.binfo;
+    rg.clear_words = rj.clear_words;
+    rg.n_clear = rj.n_clear;
+    const int fforce = plan.path == TOPK_PATH_PROFK ? force : 1;
+    TK_TRY(launch_refine_grid(p, k, M, buf, counts, fs, fforce, rg, st));
+    ++nl;
+    TK_TRY(launch_bin_sort(p, rj, st));
+    cluster = 1;
+  } else {
+    TK_TRY(launch_select(p, rj, hint, &cluster, st));
 #ifdef TK_PHASE_TIMING
-  if (std::getenv("TK_DEBUG_TWICE")) TK_TRY(launch_select(p, rj, hint, &cluster, st));
+    if (std::getenv("TK_DEBUG_TWICE")) TK_TRY(launch_select(p, rj, hint, &cluster, st));
 #endif
+  }
   if (plan.path == TOPK_PATH_PROFK) TK_TRY(mark(5));
 
   if (stats) {
@@ -576,6 +610,7 @@ int topk_debug_phase_ns(unsigned long long* out) { return tk::debug_phase_ns(out
 int topk_debug_rows_ns(unsigned long long* out) { return tk::debug_rows_ns(out); }
 int topk_debug_binsort_ns(unsigned long long* out) { return tk::debug_binsort_ns(out); }
 int topk_debug_sample_tau_ns(unsigned long long* out) { return tk::debug_sample_tau_ns(out); }
+int topk_debug_refine_grid_ns(unsigned long long* out) { return tk::debug_refine_grid_ns(out); }
 int topk_debug_timeline(unsigned long long* out, int reset) {
   unsigned long long a[16], b[16], c[16];
   if (tk::debug_timeline_select(a, reset) || tk::debug_timeline_filter(b, reset) ||
