@@ -19,6 +19,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -32,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "single_row_2p28_pareto15_k1024"
 SECONDARY_WORKLOAD = "batchtopk_4096x65536_relu_bf16_k131072"
+SECONDARY_MIN_STEPS = 1000
 NORTH_STAR_GBS = 8000.0
 CLOCK_SOAK_S = 1.5
 ORACLE_SAMPLE_ELEMS = 1 << 25
@@ -52,6 +54,8 @@ def parse_args():
     ap.add_argument("--scale-down", type=int, default=0,
                     help="divide the workload by 2^s (row length, or rows for global mode); for profiling")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="the paper's N x K sweep: Prof-K against torch.topk on the same GPU (one JSON line)")
     return ap.parse_args()
 
 
@@ -325,6 +329,22 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
         call(handles[s_] if path == "profk" else None)
     torch.cuda.synchronize()
 
+    # The miss path: calls whose every selection takes the fallback (a miss
+    # is injected on the host), timed alone.
+    forced_miss_ms = None
+    if path == "profk":
+        opt.force_miss = 1
+        call()
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(3):
+            call()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        forced_miss_ms = round(f0.elapsed_time(f1) / 3, 4)
+        opt.force_miss = 0
+
     if world > 1:
         t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -387,7 +407,7 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
 
     return {
         "value": value, "ms_per_step": ms_step, "path": path, "stats": st, "stages": stages,
-        "roofline": roofline, "e2e": e2e, "clocks": clock_info,
+        "roofline": roofline, "e2e": e2e, "clocks": clock_info, "forced_miss_ms_per_step": forced_miss_ms,
         # the library reports the kernels each call launched (sample and
         # threshold, filter, fallback when it runs as its own grid, refinement,
         # bin sort for large k; the direct path's one kernel)
@@ -396,10 +416,93 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
     }
 
 
+# ---------------------------------------------------------------------------
+# the paper's sweep (section 5, Figure 2): N x K x distribution, against
+# torch.topk timed on the same GPU (context; torch.topk is not on our path)
+# ---------------------------------------------------------------------------
+SWEEP_NS = [1 << p for p in (22, 24, 26, 28, 30)]
+SWEEP_KS = [32, 1024, 32768, 131072]
+SWEEP_DISTS = ["uniform", "normal", "pareto15"]
+L2_BYTES = 126 << 20
+
+
+def sweep_input(dist, n, gen, dev):
+    import torch
+    if dist == "uniform":
+        return torch.rand(n, generator=gen, device=dev)
+    if dist == "normal":
+        return torch.randn(n, generator=gen, device=dev)
+    # Pareto(1.5), x_m = 1, random sign: +-U^(-2/3), U in (0, 1]
+    u = 1.0 - torch.rand(n, generator=gen, device=dev)
+    sign = torch.where(torch.rand(n, generator=gen, device=dev) < 0.5, -1.0, 1.0)
+    return sign * u.pow(-2.0 / 3.0)
+
+
+def time_call(fn, reps, flush):
+    """Median device time of one call (CUDA events on the current stream), L2 flushed first when given."""
+    import torch
+    for _ in range(2):
+        fn()
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(times)
+
+
+def run_sweep(args):
+    import torch
+    import top_selection_prof_gb300 as tk
+    torch.cuda.set_device(0)
+    tk._lib.get()   # fails loudly if the engine is not built
+    dev = torch.device("cuda", 0)
+    flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed)
+    reps = max(3, min(args.steps, 20))
+    points = []
+    for n in SWEEP_NS:
+        for dist in SWEEP_DISTS:
+            x = sweep_input(dist, n, gen, dev)
+            fl = flush if n * 4 < 2 * L2_BYTES else None
+            for k in SWEEP_KS:
+                if k > n // 8:
+                    continue
+                ours_us = time_call(lambda: tk.select(x, k, eps=1e-3), reps, fl)
+                torch_us = time_call(lambda: torch.topk(x, k, sorted=True), reps, fl)
+                v, _ = tk.select(x, k, eps=1e-3)
+                tv, _ = torch.topk(x, k, sorted=True)
+                _, _, st = tk.select_ex(x, k, eps=1e-3)
+                points.append({"n": n, "k": k, "dist": dist, "path": st["path_name"],
+                               "ours_us": round(ours_us, 1), "torch_topk_us": round(torch_us, 1),
+                               "speedup": round(torch_us / ours_us, 2),
+                               "ours_gbs": round(n * 4 / (ours_us * 1e-6) / 1e9, 1),
+                               "values_equal_torch": bool(torch.equal(v, tv))})
+            del x
+    sp = [p["speedup"] for p in points]
+    geo = float(math.exp(sum(math.log(v) for v in sp) / len(sp)))
+    line = {"sweep": "Prof-K (topk_select, eps=1e-3, f32, one row) vs torch.topk(sorted=True), same GPU",
+            "gpu": torch.cuda.get_device_name(0), "torch": torch.__version__, "reps": reps,
+            "l2": "flushed before each call when the input is below 2x L2", "data": "synthetic (torch generator)",
+            "points": points,
+            "summary": {"speedup_min": min(sp), "speedup_max": max(sp), "speedup_geomean": round(geo, 2),
+                        "all_values_equal": all(p["values_equal_torch"] for p in points)}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
     cfg = workload(args.workload, args.scale_down)
+    if args.sweep:
+        return run_sweep(args) if rank == 0 else 0
 
     if args.impl == "reference":
         if rank != 0:
@@ -439,13 +542,18 @@ def main():
         c2 = workload(SECONDARY_WORKLOAD, args.scale_down)
         del x
         x2 = make_input(c2, args.seed + rank)
-        r2 = run_ours(c2, SECONDARY_WORKLOAD, x2, args.steps, args.warmup, world, rank, with_clocks=False,
-                      with_e2e=False)
+        # (at least 1000 steps: a miss, about one call in 1/eps = 1000, costs
+        # ~1.3 ms, so a short window that happens to hold one overstates the
+        # expected cost of eps x 1.3 ms per call many times over)
+        r2 = run_ours(c2, SECONDARY_WORKLOAD, x2, max(args.steps, SECONDARY_MIN_STEPS), args.warmup, world, rank,
+                      with_clocks=False, with_e2e=False)
         secondary = {"workload": SECONDARY_WORKLOAD, "value": round(r2["value"], 3), "unit": "G elem/s",
                      "ms_per_step": round(r2["ms_per_step"], 4), "path": r2["path"],
                      "hbm_gbs_whole_step": round(r2["hbm_gbs_whole_step"], 1),
                      "frac_of_8tbs_whole_step": round(r2["hbm_gbs_whole_step"] / NORTH_STAR_GBS, 4),
                      "roofline": r2["roofline"], "stages": r2["stages"], "R": r2["stats"]["R"],
+                     "forced_miss_ms_per_step": r2["forced_miss_ms_per_step"],
+                     "steps": max(args.steps, SECONDARY_MIN_STEPS),
                      "S_t_M": [r2["stats"]["S"], r2["stats"]["t"], r2["stats"]["M"]]}
         x = None
 
@@ -474,6 +582,7 @@ def main():
             "frac_of_8tbs_whole_step": round(res["hbm_gbs_whole_step"] / NORTH_STAR_GBS, 4),
             "roofline": res["roofline"], "stages": res["stages"], "cpu_baseline": cpu, "e2e": res["e2e"],
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "secondary": secondary,
+            "forced_miss_ms_per_step": res["forced_miss_ms_per_step"],
         }
         if cfg.get("eps", 0) > 0 and not args.no_miss_rate:
             # the workload's own bound, and a measured rate where misses are countable

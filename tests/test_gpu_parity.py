@@ -53,6 +53,7 @@ CASES = [
     ("uniform", 1, (1 << 22) + 8, 9000, 0.0, False, "exact"),      # exact path, sort after the fallback
     ("ties1000", 5, 1 << 22, 12000, 1e-3, False, "profk"),         # more rows than the grid refinement takes
     ("normal", 4, 1 << 21, 8500, 1e-3, False, "profk"),            # grid refinement over four rows
+    ("normal", 1, 1 << 22, 131072, 1e-3, False, "profk"),          # candidates crossing powers of two
 ]
 
 

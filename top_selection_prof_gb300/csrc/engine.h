@@ -121,15 +121,16 @@ cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* 
 
 // Refinement of a few selections with large k on one cooperative grid
 // (kernels_filter.cu): the miss check and, on a miss, the fallback above,
-// then the exact partition of each selection's candidates by the first
-// 11-bit digit below their most significant varying bit into the exchange
-// buffer, published for the bin sort (launch_bin_sort) in the bin-info
-// format of the refinement cluster.
+// then the exact partition of each selection's candidates into 2048 equal
+// slices of their key range (the first 11-bit digit of key - smallest key)
+// in the exchange buffer, published for the bin sort (launch_bin_sort) in the
+// bin-info format of the refinement cluster.
 constexpr int kRefineGridBins = 2048;          // first-digit bins (the bin sort's)
 constexpr int kRefineGridLevels = 6;           // 11-bit digits of a key of up to 64 bits
 constexpr int64_t kRefineGridMaxSel = 4;       // selections one grid refines
-// Control words per selection: OR and NOT-AND of the keys (2 x 64 bits), the
-// boundary bin's placed winners, then one counter per bin and digit level.
+// Control words per selection: NOT of the smallest and the largest key (2 x
+// 64 bits), the boundary bin's placed winners, then one counter per bin and
+// digit level.
 constexpr int64_t kRefineGridCtlWords = 8 + int64_t(kRefineGridLevels) * kRefineGridBins;
 struct RefineGridScratch {
   unsigned* ctl;          // this call's control words: kRefineGridCtlWords per selection, zero on entry

@@ -744,11 +744,12 @@ cudaError_t launch_fallback_t(const FallbackParams& a, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // Stage 4 for a few selections with many winners, on every SM at once: the
 // miss check and fallback above, then the candidates of each selection are
-// partitioned by their first 11-bit digit below the most significant bit on
-// which they differ ("count into buckets", Find the Cutoff Instead).  Each
-// block caches its slice of the buffer, the slices' OR / AND give the varying
-// bits, one histogram per block is added into a grid-wide one (the returned
-// old count is the block's offset inside each bin), and after a grid barrier
+// partitioned into 2048 equal slices of their key range ("count into
+// buckets", Find the Cutoff Instead): the first 11-bit digit of key - kmin.
+// Each block caches its slice of the buffer, the slices' minima and maxima
+// give the range, one histogram per block is added into a grid-wide one (the
+// returned old count is the block's offset inside each bin), and after a
+// grid barrier
 // every block scans the same totals and knows every bin's first place.  When
 // the bin holding rank k fits the exchange buffer after the bins above it,
 // every key of those bins is placed and the bin sort keeps the first k
@@ -819,47 +820,54 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   __shared__ unsigned s_ws[32];
   __shared__ unsigned s_info[4];
   __shared__ unsigned s_total;
-  __shared__ unsigned long long s_or, s_nand;
+  __shared__ unsigned long long s_nmin, s_max;
   __shared__ unsigned s_w;
   unsigned* ctl = rg.ctl + row * kRefineGridCtlWords;
-  unsigned long long* g_or = reinterpret_cast<unsigned long long*>(ctl);
-  unsigned long long* g_nand = g_or + 1;
+  unsigned long long* g_nmin = reinterpret_cast<unsigned long long*>(ctl);  // NOT of the smallest key
+  unsigned long long* g_max = g_nmin + 1;
   unsigned* g_win = ctl + 4;
   unsigned* g_lev = ctl + 8;
   const int tid = threadIdx.x;
 
-  // ---- the block's slice, cached; OR / AND over the grid
+  // ---- the block's slice, cached; the smallest and largest key over the grid
   const unsigned long long R = __ldcg(fp.counts + row);
   const int64_t n = R < static_cast<unsigned long long>(fp.cap) ? static_cast<int64_t>(R) : fp.cap;
   const int64_t sb = n * blockIdx.x / gridDim.x, se = n * (blockIdx.x + 1) / gridDim.x;
   const int cn = static_cast<int>(se - sb);  // <= kPartCache: the host checks n <= gridDim.x * kPartCache
   const uint64_t* src = fp.buf + row * fp.cap + sb;
-  unsigned long long o = 0ull, d = ~0ull;
+  unsigned long long mn = ~0ull, mx = 0ull;
   for (int i = tid; i < cn; i += kFilterBlock) {
     const uint64_t key = __ldcg(src + i);
     cache[i] = key;
-    o |= key;
-    d &= key;
+    mn = key < mn ? key : mn;
+    mx = key > mx ? key : mx;
   }
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) {
-    o |= __shfl_xor_sync(kFull, o, m);
-    d &= __shfl_xor_sync(kFull, d, m);
+    const unsigned long long a = __shfl_xor_sync(kFull, mn, m), b = __shfl_xor_sync(kFull, mx, m);
+    mn = a < mn ? a : mn;
+    mx = b > mx ? b : mx;
   }
-  if (tid == 0) { s_or = 0ull; s_nand = 0ull; }
+  if (tid == 0) { s_nmin = 0ull; s_max = 0ull; }
   __syncthreads();
-  if ((tid & 31) == 0) { atomicOr(&s_or, o); atomicOr(&s_nand, ~d); }
+  if ((tid & 31) == 0) { atomicMax(&s_nmin, ~mn); atomicMax(&s_max, mx); }
   __syncthreads();
-  if (tid == 0 && cn > 0) { atomicOr(g_or, s_or); atomicOr(g_nand, s_nand); }
+  if (tid == 0 && cn > 0) { atomicMax(g_nmin, s_nmin); atomicMax(g_max, s_max); }
   TK_RG(3);
   if (!grid_barrier(fs.barrier, fs.status)) return false;
   TK_RG(4);
-  const unsigned long long all_or = __ldcg(g_or), all_and = ~__ldcg(g_nand);
-  const unsigned long long vary = all_or ^ all_and;
-  const int hb = vary ? 63 - __clzll(static_cast<long long>(vary)) : 0;
+  // Digits are taken of key - kmin: 2048 equal slices of the keys' range.
+  // (Digits of the keys themselves below their top varying bit leave only a
+  // few non-empty bins when the candidates' values cross a power of two.)
+  // The cache holds key - kmin from here on; the order is the same.
+  const uint64_t kmin = ~__ldcg(g_nmin), kmax = __ldcg(g_max);
+  const uint64_t span = kmax - kmin;
+  const int hb = span ? 63 - __clzll(static_cast<long long>(span)) : 0;
   const uint64_t pmask1 = hb >= 63 ? 0ull : (~0ull << (hb + 1));
-  const uint64_t prefix1 = all_and & pmask1;
+  const uint64_t prefix1 = 0ull;
   const int shift1 = hb >= kPartDigit - 1 ? hb - (kPartDigit - 1) : 0;
+  for (int i = tid; i < cn; i += kFilterBlock) cache[i] -= kmin;
+  __syncthreads();
   auto bin_of = [&](uint64_t key) { return kPartDM - static_cast<unsigned>((key >> shift1) & kPartDM); };
 
   // ---- first digit: this block's histogram, its range inside each bin
@@ -915,7 +923,7 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
       rank -= s_info[1];
       __syncthreads();  // s_info is rewritten by the next level
     }
-    kappa = prefix;  // every bit fixed: the k-th largest key
+    kappa = prefix;  // every bit fixed: the k-th largest key (less kmin)
     // this block's winners inside the boundary bin, and where they start
     unsigned w = 0;
     for (int i = tid; i < cn; i += kFilterBlock) {
@@ -969,7 +977,7 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   for (unsigned i = tid; i < nst; i += kFilterBlock) {
     const uint64_t key = stg[i];
     const unsigned pos = mine[bin_of(key)] + i;
-    if (pos < xend) xb[pos] = key;
+    if (pos < xend) xb[pos] = key + kmin;
   }
   if (blockIdx.x == 0) {
     // the bin sort's view of the partition
@@ -982,6 +990,8 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
       bo[kRefineGridBins + 3] = static_cast<unsigned>(pmask1 >> 32);
       bo[kRefineGridBins + 4] = static_cast<unsigned>(shift1);
       bo[kRefineGridBins + 5] = xend;
+      bo[kRefineGridBins + 6] = static_cast<unsigned>(kmin);  // digits are of key - kmin
+      bo[kRefineGridBins + 7] = static_cast<unsigned>(kmin >> 32);
     }
   }
   __syncthreads();  // the shared arrays are reused by the next selection

@@ -107,9 +107,10 @@ struct SelParams {
 };
 
 // Published per selection for the bin sort: NB bin starts, then the
-// first-digit prefix, mask and shift, and the end of the keys placed in the
+// first-digit prefix, mask and shift, the end of the keys placed in the
 // exchange buffer (r when only winners were placed, else the end of the
-// boundary bin).
+// boundary bin), and a base the digits are taken relative to (digits,
+// prefixes and masks describe key - base; 0 from the refinement cluster).
 constexpr int kBinInfoBins = 2048;
 constexpr int kBinInfoWords = kBinInfoBins + 8;
 
@@ -1156,6 +1157,8 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
             bo[NB + 3] = static_cast<unsigned>(pmask1 >> 32);
             bo[NB + 4] = static_cast<unsigned>(shift1);
             bo[NB + 5] = static_cast<unsigned>(xend);
+            bo[NB + 6] = 0u;  // digits of the keys themselves (no base)
+            bo[NB + 7] = 0u;
           }
         }
         return;
@@ -1413,6 +1416,8 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   const uint64_t pmask1 = static_cast<uint64_t>(__ldcg(bi + NB + 2)) | (static_cast<uint64_t>(__ldcg(bi + NB + 3)) << 32);
   const int shift1 = static_cast<int>(__ldcg(bi + NB + 4));
   const int64_t xend = static_cast<int64_t>(__ldcg(bi + NB + 5));  // keys placed: >= k
+  // digits, prefixes and masks are of key - kbase
+  const uint64_t kbase = static_cast<uint64_t>(__ldcg(bi + NB + 6)) | (static_cast<uint64_t>(__ldcg(bi + NB + 7)) << 32);
   const uint64_t* xb = a.xbuf + row * a.xstride;
   if (tid == 0) { s_info[0] = 0; s_info[1] = 0; }
   __syncthreads();
@@ -1451,7 +1456,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
         if (tid == 0) s_info[2] = ~0ull;
         __syncthreads();
         for (int64_t i = bs + tid; i < be; i += BLOCK) {
-          const uint64_t key = __ldcg(xb + i);
+          const uint64_t key = __ldcg(xb + i) - kbase;
           if ((key & msk) == pre) atomicAdd(&lh[DM - static_cast<unsigned>((key >> sh2) & DM)], 1u);
         }
         __syncthreads();
@@ -1498,7 +1503,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
     for (int64_t iw = r0 + (tid & ~31); iw < r1; iw += BLOCK) {
       const int64_t i = iw + (tid & 31);
       const uint64_t key = i < r1 ? __ldcg(xb + i) : 0ull;
-      const bool want = i < r1 && key <= hi_key && key >= lo_key;
+      const bool want = i < r1 && key - kbase <= hi_key && key - kbase >= lo_key;
       const unsigned slot = warp_append_slot(&s_cnt, want);
       if (want && slot < static_cast<unsigned>(kBinSortCap)) bufA[slot] = key;
     }
