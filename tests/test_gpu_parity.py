@@ -212,3 +212,13 @@ def test_grid_refinement_more_rows_after_fewer():
         _check(x1, 9000, global_=True, largest=False)
         _check(x1, 9500, global_=True)
         _check(x4, 8500, largest=rep == 1)
+
+
+@pytest.mark.parametrize("largest", [True, False])
+def test_few_winners_from_many_candidates(largest):
+    # k <= 1024 is refined by one CTA; with about 40,000 candidates (S = 32768
+    # here, t = 312) they do not fit its shared memory and every pass re-reads
+    # them from L2.
+    x = workloads.make("normal", 1, 1 << 22, seed=18)
+    st = _check(x, 1000, largest=largest, eps=1e-3, t_override=312, m_override=200000)
+    assert st["misses"] == 0 and st["R"] > 30000, st
