@@ -72,12 +72,14 @@ cudaError_t launch_sample(const Problem& p, int64_t S, uint64_t seed, uint64_t c
 // t-th largest sampled key of each selection is found by a radix select over
 // the grid (11-bit digits counted into hist level by level, a grid barrier
 // per digit) until its bin holds at most kTauGather keys; those are gathered
-// and the last block of the selection ranks them.  hist / hist_zero are
+// and the last block of the selection ranks them.  When blocks x t <=
+// kTauGather, each block instead keeps its own t largest keys and the last
+// block ranks their union (no grid barrier).  hist / hist_zero are
 // histogram halves as above (hist counted into, hist_zero cleared); ctl holds
 // kTauCtlWords words and gather kTauGather keys per selection.  ctl must be
 // zero on entry; the kernel leaves its grid barrier and counters as it found
 // them except after a timeout, so the refinement clears ctl every call.
-constexpr int kTauGather = 1024;
+constexpr int kTauGather = 2048;
 constexpr int kTauCtlWords = 2 + 2 * static_cast<int>(kSampleHistMaxRows);
 struct SampleTauScratch {
   unsigned* hist;

@@ -116,7 +116,8 @@ struct SampleTauParams {
   SampleTauScratch sc;
   uint64_t* tau_out;
   int64_t t;
-  int q;  // blocks per selection
+  int q;      // blocks per selection
+  int local;  // q * t <= kTauGather: each block keeps its own top t (no grid barrier)
 };
 
 constexpr int kSampleBlock = 256;
@@ -199,12 +200,31 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
   }
   TK_ST(1);
 
+  // Few candidates in all (q * t <= kTauGather): the t largest sampled keys
+  // are among the union of every block's own t largest, so each block ranks
+  // its keys, keeps its top t, and the last block ranks the union -- no grid
+  // barrier and no grid-wide histogram.
+  uint64_t bound = 0ull;
+  if (p.local) {
+    const int64_t first = 2 * (static_cast<int64_t>(static_cast<int>(blockIdx.x) % p.q) * BLOCK);
+    const int64_t left = p.S - first;
+    const unsigned nloc = static_cast<unsigned>(left < 2 * BLOCK ? left : 2 * BLOCK);
+    if (one) gk[2 * tid] = k0;
+    if (two) gk[2 * tid + 1] = k1;  // (the valid keys are gk[0 .. nloc))
+    if (nloc > static_cast<unsigned>(p.t)) {
+      bucket_kth<BLOCK>(gk, nloc, static_cast<unsigned long long>(p.t), sh, s_tmp, s_info, &s_cnt, &s_tau);
+      __syncthreads();
+      bound = s_tau;  // this block's t-th largest: keep the keys at or above it
+    }
+    __syncthreads();  // gk and s_tau are reused below
+  }
+
   // radix select of the t-th largest key over the grid, one digit a level
   const int kb = Dt<DT>::kKeyBits + p.ib;
   uint64_t prefix = 0ull, pmask = (kb >= 64) ? 0ull : (~0ull << kb);
   int shift = kb - kSampleHistBits;
   unsigned long long rank = static_cast<unsigned long long>(p.t);
-  for (int level = 0;; ++level) {
+  for (int level = 0; !p.local; ++level) {
     for (int i = tid; i < kSampleHistBins; i += BLOCK) sh[i] = 0u;
     __syncthreads();
     if (one && (k0 & pmask) == prefix) atomicAdd(&sh[DM - static_cast<unsigned>((k0 >> shift) & DM)], 1u);
@@ -256,11 +276,13 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
     shift = shift >= kSampleHistBits ? shift - kSampleHistBits : 0;
   }
 
-  // gather the boundary bin; the last block of the selection ranks it
+  // gather the boundary bin (or each block's top t); the last block of the
+  // selection ranks what was gathered
   unsigned* gctl = p.sc.ctl + 2 + 2 * row;  // gathered count, ticket
   uint64_t* gat = p.sc.gather + static_cast<int64_t>(row) * kTauGather;
   {
-    const bool w0 = one && (k0 & pmask) == prefix, w1 = two && (k1 & pmask) == prefix;
+    const bool w0 = one && (p.local ? k0 >= bound : (k0 & pmask) == prefix);
+    const bool w1 = two && (p.local ? k1 >= bound : (k1 & pmask) == prefix);
     const unsigned s0 = warp_append_slot(gctl, w0);
     if (w0 && s0 < static_cast<unsigned>(kTauGather)) gat[s0] = k0;
     const unsigned s1 = warp_append_slot(gctl, w1);
@@ -336,15 +358,16 @@ cudaError_t launch_sample_tau(const Problem& p, int64_t S, int64_t t, uint64_t s
   sp.tau_out = tau_out;
   sp.t = t;
   sp.q = static_cast<int>(((S + 1) / 2 + kSampleBlock - 1) / kSampleBlock);
+  sp.local = static_cast<int64_t>(sp.q) * t <= kTauGather ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sp.q * p.nsel), 1, 1);
   cfg.blockDim = dim3(kSampleBlock, 1, 1);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].id = cudaLaunchAttributeCooperative;  // the grid barrier needs every block resident
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = sp.local ? 0 : 1;  // (no block waits on another in the local mode)
   if (p.dtype == kF32) return cudaLaunchKernelEx(&cfg, sample_tau_kernel<kF32>, sp);
   return cudaLaunchKernelEx(&cfg, sample_tau_kernel<kBF16>, sp);
 }
