@@ -60,6 +60,11 @@ def test_sample_keys_rank_like_the_oracle(largest):
     ("ties1000", 1 << 22, 10000, 1e-3, 0),
     ("ties1000_sorted", 1 << 22, 10000, 1e-3, 0),
     ("relu_normal_bf16", 65536, 8192, 1e-3, 256),
+    # 32768 draws from 65600 elements: many positions drawn twice, also at
+    # the boundary ranks (k = 20: each block keeps its own top t; k = 100:
+    # the grid-wide radix select)
+    ("uniform", 65600, 20, 1e-3, 0),
+    ("uniform", 65600, 100, 1e-3, 0),
 ])
 def test_threshold_and_survivor_count_match_oracle(kind, n, k, eps, global_rows):
     tk = _tk()

@@ -117,7 +117,7 @@ struct SampleTauParams {
   uint64_t* tau_out;
   int64_t t;
   int q;      // blocks per selection
-  int local;  // q * t <= kTauGather: each block keeps its own top t (no grid barrier)
+  int local;  // q * (t + 1) <= kTauGather: each block keeps its own top t (no grid barrier)
 };
 
 constexpr int kSampleBlock = 256;
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
   }
   TK_ST(1);
 
-  // Few candidates in all (q * t <= kTauGather): the t largest sampled keys
+  // Few candidates in all (q * (t + 1) <= kTauGather): the t largest sampled keys
   // are among the union of every block's own t largest, so each block ranks
   // its keys, keeps its top t, and the last block ranks the union -- no grid
   // barrier and no grid-wide histogram.
@@ -358,7 +358,8 @@ cudaError_t launch_sample_tau(const Problem& p, int64_t S, int64_t t, uint64_t s
   sp.tau_out = tau_out;
   sp.t = t;
   sp.q = static_cast<int>(((S + 1) / 2 + kSampleBlock - 1) / kSampleBlock);
-  sp.local = static_cast<int64_t>(sp.q) * t <= kTauGather ? 1 : 0;
+  // (one key of slack per block: equal keys at a block's bound are all kept)
+  sp.local = static_cast<int64_t>(sp.q) * (t + 1) <= kTauGather ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sp.q * p.nsel), 1, 1);
   cfg.blockDim = dim3(kSampleBlock, 1, 1);

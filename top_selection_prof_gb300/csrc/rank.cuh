@@ -70,9 +70,18 @@ __device__ __forceinline__ unsigned count_above(const uint64_t* src, unsigned j0
   return r;
 }
 
-// The key of 1-based descending rank `rank` among g[0..n) (distinct keys, in
-// shared or global memory); the thread that finds it writes it to *out (the
-// caller synchronises before reading).  Few keys are ranked by counting
+// Number of keys in src[0, i) equal to v: with it, equal keys (the same
+// position drawn twice by the sampler) take consecutive ranks in slot order.
+__device__ __forceinline__ unsigned count_equal_before(const uint64_t* src, unsigned i, uint64_t v) {
+  unsigned r = 0;
+  for (unsigned j = 0; j < i; ++j) r += src[j] == v ? 1u : 0u;
+  return r;
+}
+
+// The key of 1-based descending rank `rank` among g[0..n) (in shared or
+// global memory; equal keys count once each, ranked in slot order); the
+// thread that finds it writes it to *out (the caller synchronises before
+// reading).  Few keys are ranked by counting
 // directly; more are first narrowed by 8-bit radix passes below their
 // highest varying bit to at most 32, since counting all n keys against each
 // other costs n^2 / 32 shared-memory wavefronts.  lh holds 256 counters;
@@ -84,7 +93,7 @@ __device__ void bucket_kth(const uint64_t* g, unsigned n, unsigned long long ran
   if (n <= 128u) {
     __syncthreads();
     for (unsigned i = tid; i < n; i += BLOCK)
-      if (count_above(g, 0u, n, g[i]) == rank - 1) *out = g[i];
+      if (count_above(g, 0u, n, g[i]) + count_equal_before(g, i, g[i]) == rank - 1) *out = g[i];
     return;
   }
   uint64_t* small = reinterpret_cast<uint64_t*>(s_tmp);  // <= 32 keys (the scans are done by then)
@@ -139,7 +148,9 @@ __device__ void bucket_kth(const uint64_t* g, unsigned n, unsigned long long ran
     }
   __syncthreads();
   const unsigned ns = *s_cnt < 32u ? *s_cnt : 32u;
-  if (static_cast<unsigned>(tid) < ns && count_above(small, 0u, ns, small[tid]) == lrank - 1) *out = small[tid];
+  if (static_cast<unsigned>(tid) < ns &&
+      count_above(small, 0u, ns, small[tid]) + count_equal_before(small, tid, small[tid]) == lrank - 1)
+    *out = small[tid];
 }
 
 }  // namespace
