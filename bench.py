@@ -66,6 +66,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms, device, world):
+    """The slowest rank's time: every rank runs its own replica, so the job
+    takes as long as its slowest one (all-reduce MAX; no-op with one rank)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gelems(n_elems_per_rank, world, ms_step):
+    """Elements selected by all ranks per second (G elem/s), at the slowest rank's step time."""
+    return n_elems_per_rank * world / (ms_step * 1e-3) / 1e9
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -345,12 +362,9 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
         forced_miss_ms = round(f0.elapsed_time(f1) / 3, 4)
         opt.force_miss = 0
 
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev, world)
     ms_step = ms_total / steps
-    value = n_elems * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_gelems(n_elems, world, ms_step)
 
     stages = None
     filt_ms = None
@@ -395,12 +409,8 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
             idx_h.copy_(i2, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = e0.elapsed_time(e1) / e2e_steps
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": round(n_elems * world / (ms_e2e * 1e-3) / 1e9, 3), "unit": "G elem/s",
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev, world)
+        e2e = {"value": round(whole_job_gelems(n_elems, world, ms_e2e), 3), "unit": "G elem/s",
                "h2d_bytes_per_step": n_elems * bytes_per_elem,
                "d2h_bytes_per_step": (k if glob else rows * k) * (bytes_per_elem + 8),
                "ms_per_step": round(ms_e2e, 4), "steps": e2e_steps}
