@@ -172,7 +172,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 def filter_source_sha():
     h = hashlib.sha256()
-    for f in ("kernels_filter.cu", "common.cuh"):
+    for f in ("kernels_filter.cu", "filter_core.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "top_selection_prof_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -362,6 +362,23 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
         forced_miss_ms = round(f0.elapsed_time(f1) / 3, 4)
         opt.force_miss = 0
 
+    # BatchTopK needs only the set of winners: the same selection with the
+    # sort left out (the unsorted option), timed alone
+    unsorted_ms = None
+    if glob and path == "profk" and k >= 8192:
+        opt.unsorted = 1
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for _ in range(steps):
+            call()
+        u1.record(stream)
+        torch.cuda.synchronize()
+        unsorted_ms = round(u0.elapsed_time(u1) / steps, 4)
+        opt.unsorted = 0
+
     ms_total = max_over_ranks(ms_total, dev, world)
     ms_step = ms_total / steps
     value = whole_job_gelems(n_elems, world, ms_step)
@@ -418,6 +435,7 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
     return {
         "value": value, "ms_per_step": ms_step, "path": path, "stats": st, "stages": stages,
         "roofline": roofline, "e2e": e2e, "clocks": clock_info, "forced_miss_ms_per_step": forced_miss_ms,
+        "unsorted_ms_per_step": unsorted_ms,
         # the library reports the kernels each call launched (sample and
         # threshold, filter, fallback when it runs as its own grid, refinement,
         # bin sort for large k; the direct path's one kernel)
@@ -563,6 +581,7 @@ def main():
                      "frac_of_8tbs_whole_step": round(r2["hbm_gbs_whole_step"] / NORTH_STAR_GBS, 4),
                      "roofline": r2["roofline"], "stages": r2["stages"], "R": r2["stats"]["R"],
                      "forced_miss_ms_per_step": r2["forced_miss_ms_per_step"],
+                     "unsorted_ms_per_step": r2["unsorted_ms_per_step"],
                      "steps": max(args.steps, SECONDARY_MIN_STEPS),
                      "S_t_M": [r2["stats"]["S"], r2["stats"]["t"], r2["stats"]["M"]]}
         x = None

@@ -90,6 +90,13 @@ typedef struct {
    * after the fallback check, [5] after the final selection.  The caller owns
    * the events; they are only recorded, never created or destroyed here. */
   void* events[6];
+  /* Non-zero: the caller needs only the set of winners (BatchTopK keeps the
+   * K largest activations, in any order: Prof-K paper, section 5).  For
+   * selections refined on the grid (k >= 8192, at most 4 selections) the
+   * k winners are then written in no particular order and the final sort
+   * is skipped; every other path still sorts.  The set, the values and the
+   * positions are exact either way.  Default 0. */
+  int unsorted;
 } topk_options_t;
 
 /* Per-call report (row 0 for the per-row fields). */

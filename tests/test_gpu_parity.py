@@ -222,3 +222,40 @@ def test_few_winners_from_many_candidates(largest):
     x = workloads.make("normal", 1, 1 << 22, seed=18)
     st = _check(x, 1000, largest=largest, eps=1e-3, t_override=312, m_override=200000)
     assert st["misses"] == 0 and st["R"] > 30000, st
+
+
+def _check_set(x, k, largest=True, global_=False, **opts):
+    """Unsorted output: the oracle's winners as a set, each with its own input bits."""
+    import numpy as np
+    tk = _tk()
+    v, i, st = tk.select_ex(to_device(x), k, largest=largest, eps=1e-3, global_=global_, unsorted=1, **opts)
+    ov, oi = plain.topk(x, k, largest=largest, global_=global_)
+    rows = 1 if global_ else x.shape[0]
+    gi = i.cpu().numpy().reshape(rows, k)
+    assert np.array_equal(np.sort(gi, axis=1), np.sort(np.asarray(oi).reshape(rows, k), axis=1)), "winner sets"
+    flat = x.reshape(rows, -1)
+    bits = (v.view(__import__("torch").int16).cpu().numpy().view(np.uint16) if flat.dtype == np.uint16
+            else v.cpu().numpy().view(np.uint32)).reshape(rows, k)
+    want = np.take_along_axis(flat, gi, axis=1)
+    want = want.view(np.uint16) if flat.dtype == np.uint16 else want.view(np.uint32)
+    assert np.array_equal(bits, want), "values are the input's bits at the returned positions"
+    return st
+
+
+@pytest.mark.parametrize("largest", [True, False])
+def test_unsorted_output_is_the_exact_set(largest):
+    st = _check_set(workloads.make("relu_normal_bf16", 64, 65536, seed=19), 20000, largest=largest, global_=True)
+    assert st["launches"] == 3, st          # sample + threshold, filter, grid refinement: no sort
+    _check_set(workloads.make("ties1000", 1, 1 << 22, seed=20), 10000, largest=largest)
+    _check_set(workloads.make("normal", 4, 1 << 21, seed=21), 8500, largest=largest)
+
+
+def test_unsorted_output_after_a_miss():
+    st = _check_set(workloads.make("relu_normal_bf16", 64, 65536, seed=22), 20000, global_=True, force_miss=1)
+    assert st["misses"] == 1
+
+
+def test_unsorted_request_elsewhere_still_sorts():
+    # (k below the grid refinement's range: the option is a permission, the output stays sorted)
+    x = workloads.make("pareto15", 1, 1 << 22, seed=23)
+    _check(x, 1000, eps=1e-3, unsorted=1)

@@ -23,7 +23,7 @@ class TopkOptions(ctypes.Structure):
     _fields_ = [("s_min", ctypes.c_int64), ("s_max", ctypes.c_int64), ("cost_ratio", ctypes.c_double),
                 ("rule", ctypes.c_int), ("path", ctypes.c_int), ("seed", ctypes.c_uint64),
                 ("counter", ctypes.c_int64), ("force_miss", ctypes.c_int), ("m_override", ctypes.c_int64),
-                ("t_override", ctypes.c_int64), ("events", ctypes.c_void_p * 6)]
+                ("t_override", ctypes.c_int64), ("events", ctypes.c_void_p * 6), ("unsorted", ctypes.c_int)]
 
 
 class TopkStats(ctypes.Structure):

@@ -17,8 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libtopk_gb300.so")
 BUILD = os.path.join(ROOT, "_build")
-SOURCES = ["topk_api.cu", "kernels_sample.cu", "kernels_filter.cu", "kernels_select.cu", "kernels_rows.cu",
-           "params.cpp", "topk_noalloc.cu"]
+SOURCES = ["topk_api.cu", "kernels_sample.cu", "kernels_filter.cu", "kernels_fallback.cu", "kernels_select.cu",
+           "kernels_rows.cu", "params.cpp", "topk_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

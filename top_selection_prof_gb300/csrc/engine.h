@@ -94,7 +94,7 @@ cudaError_t launch_sample_tau(const Problem& p, int64_t S, int64_t t, uint64_t s
                               unsigned long long* counts_to_zero, DevHeader* hdr, const SampleTauScratch& sc,
                               uint64_t* tau_out, cudaStream_t st);
 
-// ---- filter and fallback (kernels_filter.cu) ---------------------------------
+// ---- filter (kernels_filter.cu) and fallback (kernels_fallback.cu) ----------
 // SMs a threshold select of nsel clusters of G blocks holds while the filter
 // launches, or -1 when it spans too many SMs to overlap.
 inline int overlap_sms(int G, int64_t nsel) {
@@ -122,7 +122,7 @@ cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* 
                             cudaStream_t st);
 
 // Refinement of a few selections with large k on one cooperative grid
-// (kernels_filter.cu): the miss check and, on a miss, the fallback above,
+// (kernels_fallback.cu): the miss check and, on a miss, the fallback above,
 // then the exact partition of each selection's candidates into 2048 equal
 // slices of their key range (the first 11-bit digit of key - smallest key)
 // in the exchange buffer, published for the bin sort (launch_bin_sort) in the
@@ -142,6 +142,12 @@ struct RefineGridScratch {
   unsigned* binfo;        // select_binfo_words(k) words per selection
   unsigned* clear_words;  // nullable: words of an earlier grid zeroed once that grid has finished
   int n_clear;
+  // unsorted != 0: find the exact k-th key and write the k winners straight
+  // to out_vals / out_idx (k per selection, in no particular order); no bin
+  // sort follows.  (Inside the kernel: 1 = f32 output, 2 = bf16.)
+  int unsorted = 0;
+  void* out_vals = nullptr;
+  int64_t* out_idx = nullptr;
 };
 // Largest buffer capacity (keys per selection) the grid refinement takes, or
 // 0 when it does not apply (too many selections).
@@ -202,6 +208,7 @@ int debug_rows_ns(unsigned long long* out);   // debug builds: stamps of the sho
 int debug_timeline_select(unsigned long long* out, int reset);
 int debug_binsort_ns(unsigned long long* out);
 int debug_timeline_filter(unsigned long long* out, int reset);
+int debug_timeline_fallback(unsigned long long* out, int reset);
 int debug_timeline_sample(unsigned long long* out, int reset);
 int debug_sample_tau_ns(unsigned long long* out);  // debug builds: stamps of the fused threshold grid
 int debug_refine_grid_ns(unsigned long long* out);  // debug builds: stamps of the grid refinement's block 0

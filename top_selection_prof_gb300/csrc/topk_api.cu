@@ -374,6 +374,9 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   // the bin sort follows (no refinement cluster).
   const bool grid_refine = select_binfo_words(k) > 0 && nsel <= kRefineGridMaxSel &&
                            M <= refine_grid_capacity(p);
+  // Winners in no particular order (allowed by the caller): the grid
+  // refinement writes them itself and no sort follows.
+  const bool unsorted_out = grid_refine && o && o->unsorted;
 
   auto mark = [&](int i) -> cudaError_t {
     if (!o || !o->events[i]) return cudaSuccess;
@@ -499,10 +502,13 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     rg.binfo = rj.binfo;
     rg.clear_words = rj.clear_words;
     rg.n_clear = rj.n_clear;
+    rg.unsorted = unsorted_out ? 1 : 0;
+    rg.out_vals = out_vals;
+    rg.out_idx = out_idx;
     const int fforce = plan.path == TOPK_PATH_PROFK ? force : 1;
     TK_TRY(launch_refine_grid(p, k, M, buf, counts, fs, fforce, rg, st));
     ++nl;
-    TK_TRY(launch_bin_sort(p, rj, st));
+    if (!unsorted_out) TK_TRY(launch_bin_sort(p, rj, st));
     cluster = 1;
   } else {
     TK_TRY(launch_select(p, rj, hint, &cluster, st));
@@ -612,17 +618,19 @@ int topk_debug_binsort_ns(unsigned long long* out) { return tk::debug_binsort_ns
 int topk_debug_sample_tau_ns(unsigned long long* out) { return tk::debug_sample_tau_ns(out); }
 int topk_debug_refine_grid_ns(unsigned long long* out) { return tk::debug_refine_grid_ns(out); }
 int topk_debug_timeline(unsigned long long* out, int reset) {
-  unsigned long long a[16], b[16], c[16];
+  unsigned long long a[16], b[16], c[16], d[16];
   if (tk::debug_timeline_select(a, reset) || tk::debug_timeline_filter(b, reset) ||
-      tk::debug_timeline_sample(c, reset))
+      tk::debug_timeline_sample(c, reset) || tk::debug_timeline_fallback(d, reset))
     return -3;
   if (reset) return 0;
   for (int i = 0; i < 8; ++i) {
     unsigned long long s0 = a[2 * i], e0 = a[2 * i + 1];
     s0 = b[2 * i] < s0 ? b[2 * i] : s0;
     s0 = c[2 * i] < s0 ? c[2 * i] : s0;
+    s0 = d[2 * i] < s0 ? d[2 * i] : s0;
     e0 = b[2 * i + 1] > e0 ? b[2 * i + 1] : e0;
     e0 = c[2 * i + 1] > e0 ? c[2 * i + 1] : e0;
+    e0 = d[2 * i + 1] > e0 ? d[2 * i + 1] : e0;
     out[2 * i] = s0;
     out[2 * i + 1] = e0;
   }
