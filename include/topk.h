@@ -167,7 +167,9 @@ int topk_plan(int64_t n, int64_t k, double eps, const topk_options_t* opt, topk_
 /* Static text for a status code. */
 const char* topk_status_str(int status);
 
-/* Library version: major*10000 + minor*100 + patch. */
+/* Library version: major*10000 + minor*100 + patch.  0.2.0 (200) added the
+ * `unsorted` field at the end of topk_options_t; fill the struct with
+ * topk_options_init from the same version's library. */
 int topk_version(void);
 
 /* ------------------------------------------------------------------------

@@ -609,7 +609,8 @@ const char* topk_status_str(int status) {
   }
 }
 
-int topk_version(void) { return 100; }
+// 0.2.0: topk_options_t gained `unsorted` (a caller built against 0.1 passes a shorter struct).
+int topk_version(void) { return 200; }
 
 #ifdef TK_PHASE_TIMING
 int topk_debug_phase_ns(unsigned long long* out) { return tk::debug_phase_ns(out); }
