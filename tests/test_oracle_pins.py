@@ -362,3 +362,104 @@ def test_sampled_threshold_rank_follows_the_binomial_law():
     r_grid = np.arange(0, n)
     mean = float(stats.binom.cdf(t - 1, s, r_grid / n).sum())
     assert abs(rs.mean() - mean) < 4 * rs.std() / math.sqrt(runs)
+
+
+# --------------------------------------------------------------------------
+# The survivor count R and the sampled order statistic (section 3, stages 2-3)
+# --------------------------------------------------------------------------
+
+def _ranks_with_reading(x, largest=True):
+    """Brute-force 0-based ranks under the special-value reading: NaN ranks
+    above every number (below, when smallest first), all NaNs are equal,
+    -0 == +0; an equal element outranks you only when its index is lower
+    (Rank by Counting, Goal).  Written independently of the C++ comparators."""
+    n = x.size
+    nan = np.isnan(x)
+    idx = np.arange(n)
+    ranks = np.empty(n, dtype=np.int64)
+    for i in range(n):
+        if largest:
+            better = (nan & ~nan[i]) | (~nan & ~nan[i] & (x > x[i]))
+        else:
+            better = (~nan & nan[i]) | (~nan & ~nan[i] & (x < x[i]))
+        equal = (nan & nan[i]) | (~nan & ~nan[i] & (x == x[i]))
+        ranks[i] = np.count_nonzero(better) + np.count_nonzero(equal & (idx < i))
+    return ranks
+
+
+def _tied_specials(seed, n):
+    rng = np.random.default_rng(seed)
+    x = rng.integers(0, 6, size=n).astype(np.float32)          # six values: massive ties
+    pick = rng.integers(0, 10, size=n)
+    x[pick == 0] = np.float32(np.nan)
+    x[pick == 1] = np.float32(-0.0)
+    x[pick == 2] = np.float32(0.0)
+    x[pick == 3] = np.float32(np.inf)
+    x[pick == 4] = np.float32(-np.inf)
+    return x
+
+
+@pytest.mark.parametrize("largest", [True, False])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_count_at_or_above_is_the_pivots_rank_plus_one(seed, largest):
+    """R for a threshold element = the elements ranking at or above it, the pivot
+    included: rank(pivot) + 1.  Ties at the pivot's value split by index, so an
+    excluded pivot or a reversed tie order fails here."""
+    x = _tied_specials(seed, 700)
+    ranks = _ranks_with_reading(x, largest)
+    assert np.array_equal(np.sort(ranks), np.arange(x.size))
+    for pivot in range(0, x.size, 7):
+        assert plain.count_at_or_above(x, pivot, largest=largest) == ranks[pivot] + 1, pivot
+    # bf16 carries the same reading (widened exactly)
+    h = workloads.f32_to_bf16_bits(x)
+    h[np.isnan(x)] = np.uint16(0x7FC0)
+    hr = _ranks_with_reading(workloads.bf16_bits_to_f32(h), largest)
+    for pivot in range(3, x.size, 11):
+        assert plain.count_at_or_above(h, pivot, largest=largest) == hr[pivot] + 1, pivot
+
+
+@pytest.mark.parametrize("largest", [True, False])
+def test_sample_order_stat_counts_repeated_draws(largest):
+    """The t-th best of the sampled positions, a position drawn twice taking two
+    places: an independent sort of the drawn (rank, draw) pairs."""
+    x = _tied_specials(2, 60)
+    ranks = _ranks_with_reading(x, largest)
+    rng = np.random.default_rng(3)
+    for trial in range(20):
+        draws = rng.integers(0, x.size, size=150)              # 150 draws of 60 positions
+        order = sorted(range(draws.size), key=lambda j: (ranks[draws[j]], j))
+        for t in (1, 2, 3, 37, 75, 149, 150):
+            want = int(draws[order[t - 1]])
+            assert plain.sample_order_stat(x, draws, t, largest=largest) == want, (trial, t)
+    # a position drawn t times in a row is also the t-th best when it is the best
+    best = int(np.argmin(ranks))
+    draws = np.array([best] * 4 + list(rng.integers(0, x.size, size=10)), dtype=np.int64)
+    for t in (1, 2, 3, 4):
+        assert plain.sample_order_stat(x, draws, t, largest=largest) == best
+
+
+# --------------------------------------------------------------------------
+# Algorithm 1, dense regime: t is the smallest rank meeting Eq. 5
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,k,eps", [(1 << 26, 10000, 1e-3), (1 << 28, 131072, 1e-3),
+                                     (1 << 24, 4096, 1e-2), (1 << 22, 100000, 1e-4),
+                                     (10 ** 8, 50000, 1e-6)])
+def test_alg1_t_is_the_smallest_rank_meeting_eq5(n, k, eps):
+    """With q = t/S and the substitution the text makes before Eq. 6
+    (q(1-q) ~ alpha(1-alpha)), Eq. 5 bounds P(R < k) by
+    Phi(-(q - alpha) / sqrt(alpha(1-alpha) f / S)) with eps_A = eps/2.
+    Algorithm 1's t (dense branch) must satisfy it and t - 1 must not.
+    The normal CDF here is scipy.stats.norm, not the quantile the oracle uses."""
+    from scipy import stats
+    s, t, _ = params.alg1(n, k, eps)
+    alpha, f = k / n, 1.0 - s / n
+    assert alpha * s >= -math.log(eps / 2.0)                  # the dense branch applies
+    sd = math.sqrt(alpha * (1.0 - alpha) * f / s)
+
+    def p_fail(tt):
+        return float(stats.norm.cdf(-((tt / s) - alpha) / sd))
+
+    assert t > 1
+    assert p_fail(t) <= eps / 2.0
+    assert p_fail(t - 1) > eps / 2.0
