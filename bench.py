@@ -11,7 +11,8 @@ flush is needed between steps.  Prints one JSON line (rank 0).
 
 With N > 1 GPUs (torchrun) every rank runs an independent replica of the same
 selection; there is no data-path collective.  `--impl reference` times the CPU
-oracle (plain nth_element + sort) on a bounded sample of the same workload.
+oracle (plain nth_element + sort, one host core) on the same workload, or on a
+prefix of it when the full one would not finish within a few minutes.
 """
 from __future__ import annotations
 
@@ -37,6 +38,8 @@ SECONDARY_MIN_STEPS = 1000
 NOMINAL_READ_GBS = 8000.0  # GB300 HBM3e nominal rate: the one-read roofline the fractions use
 CLOCK_SOAK_S = 1.5
 ORACLE_SAMPLE_ELEMS = 1 << 25
+REFERENCE_BUDGET_S = 240.0   # the reference arm's whole run: full workload when it fits, else a prefix
+CONFIG_MISS_CALLS = 10000
 
 
 def parse_args():
@@ -51,6 +54,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-miss-rate", action="store_true", help="skip the measured miss rate against eps")
+    ap.add_argument("--miss-calls", type=int, default=CONFIG_MISS_CALLS,
+                    help="seeded calls per workload and rule for the miss rate on the tied rows and BatchTopK")
     ap.add_argument("--scale-down", type=int, default=0,
                     help="divide the workload by 2^s (row length, or rows for global mode); for profiling")
     ap.add_argument("--seed", type=int, default=0)
@@ -196,7 +201,20 @@ def recorded_traffic(workload_name, n_elems):
 # ---------------------------------------------------------------------------
 # the CPU oracle, as it stands (baseline and reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample(cfg, x):
+def cpu_model():
+    """The host CPU's model name (lscpu), else what the platform module reports."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_prefix(cfg, x):
     """A bounded sample of the workload for the CPU oracle: a prefix of the selection."""
     if cfg["mode"] == "global":
         flat = x.reshape(-1)[:ORACLE_SAMPLE_ELEMS]
@@ -209,20 +227,35 @@ def oracle_sample(cfg, x):
     return x[:rows], False, "%d of %d rows of %d, k=%d per row" % (rows, cfg["rows"], cfg["n"], cfg["k"])
 
 
-def time_oracle(cfg, x, steps, warmup):
+def time_oracle(cfg, x, steps, warmup, budget_s=None, parallel=False):
+    """The CPU oracle timed on the host cores (single thread as it stands, or
+    the all-cores variant), on the full workload -- or on a prefix of it when
+    `steps` calls of the full one would exceed `budget_s` seconds."""
     from oracle import plain
-    sample, glob, desc = oracle_sample(cfg, x)
+    glob = cfg["mode"] == "global"
+    fn = plain.topk_parallel if parallel else plain.topk
+    threads = os.cpu_count() or 1
+    sample, desc = x, "the full workload (%s, k=%d%s)" % (
+        "x".join(str(d) for d in x.shape), cfg["k"], ", global" if glob else " per row")
+    t0 = time.perf_counter()
+    fn(sample, cfg["k"], global_=glob)
+    first = time.perf_counter() - t0
+    same = True
+    if budget_s is not None and first * (steps + warmup) > budget_s:
+        sample, glob, desc = oracle_prefix(cfg, x)
+        same = False
     k = min(cfg["k"], sample.size if glob else sample.shape[1])
-    for _ in range(warmup):
-        plain.topk(sample, k, global_=glob)
+    for _ in range(warmup if not same else max(0, warmup - 1)):
+        fn(sample, k, global_=glob)
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        plain.topk(sample, k, global_=glob)
+        fn(sample, k, global_=glob)
         times.append(time.perf_counter() - t0)
     per_step = statistics.mean(times)
-    return {"value": sample.size / per_step / 1e9, "unit": "G elem/s", "cores": 1, "kind": "oracle",
-            "sample": desc, "seconds_per_step": per_step}
+    return {"value": sample.size / per_step / 1e9, "unit": "G elem/s", "cores": threads if parallel else 1,
+            "kind": "oracle_parallel" if parallel else "oracle", "sample": desc, "same_config": same,
+            "cpu_model": cpu_model(), "host_cores": threads, "seconds_per_step": per_step}
 
 
 # ---------------------------------------------------------------------------
@@ -239,11 +272,18 @@ def tk_plan(cfg):
             "p_recall_fail": float(pl["p_recall_fail"]), "p_overflow": float(pl["p_overflow"])}
 
 
+def binomial_ci95(x, n):
+    """Clopper-Pearson 95 % interval for x successes in n trials."""
+    from scipy import stats
+    lo = 0.0 if x == 0 else float(stats.beta.ppf(0.025, x, n - x + 1))
+    hi = 1.0 if x == n else float(stats.beta.ppf(0.975, x + 1, n - x))
+    return [lo, hi]
+
+
 def measure_miss_rate(runs=300):
     """Measured fallback frequency against the exact tail bound of the (S, t, M)
     in use: a 2^20 uniform row, k = 100, eps = 0.2, S = 2048 draws, so that
     misses are frequent enough to count (the same case as the stage tests)."""
-    import numpy as np
     import torch
     import top_selection_prof_gb300 as tk
     from top_selection_prof_gb300 import workloads
@@ -256,7 +296,48 @@ def measure_miss_rate(runs=300):
     pl = tk.plan(n, k, eps, s_min=S, s_max=S)
     bound = float(pl["p_recall_fail"] + pl["p_overflow"])
     return {"n": n, "k": k, "eps": eps, "S": int(pl["S"]), "t": int(pl["t"]), "M": int(pl["M"]), "calls": runs,
-            "misses": misses, "measured": round(misses / runs, 4), "exact_tail_bound": round(bound, 4)}
+            "misses": misses, "measured": round(misses / runs, 4), "exact_tail_bound": round(bound, 4),
+            "ci95": [round(v, 4) for v in binomial_ci95(misses, runs)]}
+
+
+MISS_RATE_WORKLOADS = ["single_row_2p26_ties1000_k10000", "single_row_2p26_ties1000_sorted_k10000",
+                       "batchtopk_4096x65536_relu_bf16_k131072"]
+
+
+def measure_config_miss_rates(calls, seed=0):
+    """Theorem 3 on the workloads themselves: `calls` seeded calls (Philox
+    counter = call number) per workload and parameter rule, each reporting
+    whether its selection took the fallback; the count, a binomial 95 %
+    interval and the exact tail bound P[R < k] + P[R > M] of the plan."""
+    import numpy as np
+    import torch
+    import top_selection_prof_gb300 as tk
+    out = []
+    for name in MISS_RATE_WORKLOADS:
+        cfg = workload(name)
+        x = make_input(cfg, seed)
+        bf16 = x.dtype == np.uint16
+        xd = torch.from_numpy(x.view(np.int16) if bf16 else x).cuda()
+        if bf16:
+            xd = xd.view(torch.bfloat16)
+        del x
+        glob = cfg["mode"] == "global"
+        n_sel = cfg["n"] * (cfg["rows"] if glob else 1)
+        for rule_name, rule in (("exact", tk.TOPK_RULE_EXACT), ("alg1", tk.TOPK_RULE_ALG1)):
+            pl = tk.plan(n_sel, cfg["k"], cfg["eps"], rule=rule)
+            misses = 0
+            t0 = time.time()
+            for c in range(calls):
+                _, _, st = tk.select_ex(xd, cfg["k"], eps=cfg["eps"], global_=glob, counter=c, rule=rule)
+                misses += int(st["misses"])
+            bound = float(pl["p_recall_fail"] + pl["p_overflow"])
+            out.append({"workload": name, "rule": rule_name, "eps": cfg["eps"], "S": int(pl["S"]),
+                        "t": int(pl["t"]), "M": int(pl["M"]), "calls": calls, "misses": misses,
+                        "rate": misses / calls, "ci95": binomial_ci95(misses, calls),
+                        "exact_tail_bound": bound, "seconds": round(time.time() - t0, 1)})
+        del xd
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, with_e2e=True):
@@ -536,7 +617,7 @@ def main():
         if rank != 0:
             return 0
         x = make_input(cfg, args.seed)
-        r = time_oracle(cfg, x, args.steps, args.warmup)
+        r = time_oracle(cfg, x, args.steps, args.warmup, budget_s=REFERENCE_BUDGET_S)
         line = {"metric": "top-k G elem/s and achieved HBM GB/s vs ~8 TB/s peak, 1xGB300", "impl": "reference",
                 "value": round(r["value"], 4), "unit": "G elem/s", "n_gpus": 0, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(r["seconds_per_step"] * 1e3, 3),
@@ -545,7 +626,8 @@ def main():
                 "data": "synthetic (seeded numpy)",
                 "config": {"workload": args.workload, "rows": cfg["rows"], "n": cfg["n"], "k": cfg["k"],
                            "eps": cfg["eps"], "mode": cfg["mode"]},
-                "cpu_baseline": {k2: r[k2] for k2 in ("value", "unit", "cores", "kind", "sample")},
+                "cpu_baseline": {k2: r[k2] for k2 in ("value", "unit", "cores", "kind", "sample", "same_config",
+                                                      "cpu_model", "host_cores")},
                 "e2e": {"value": round(r["value"], 4), "unit": "G elem/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -586,11 +668,15 @@ def main():
                      "S_t_M": [r2["stats"]["S"], r2["stats"]["t"], r2["stats"]["M"]]}
         x = None
 
-    cpu = None
+    cpu = cpu_par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xb = make_input(cfg, args.seed) if x is None else x
-        cb = time_oracle(cfg, xb, steps=2, warmup=0)
-        cpu = {k2: cb[k2] for k2 in ("value", "unit", "cores", "kind", "sample")}
+        keys = ("value", "unit", "cores", "kind", "sample", "same_config", "cpu_model", "host_cores")
+        cb = time_oracle(cfg, xb, steps=2, warmup=0, budget_s=40.0)
+        cpu = {k2: cb[k2] for k2 in keys}
+        cp = time_oracle(cfg, xb, steps=3, warmup=1, budget_s=40.0, parallel=True)
+        cpu_par = {k2: cp[k2] for k2 in keys}
+        del xb
 
     if rank == 0:
         st = res["stats"]
@@ -609,7 +695,8 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "hbm_gbs_whole_step": round(res["hbm_gbs_whole_step"], 1),
             "frac_of_8tbs_whole_step": round(res["hbm_gbs_whole_step"] / NOMINAL_READ_GBS, 4),
-            "roofline": res["roofline"], "stages": res["stages"], "cpu_baseline": cpu, "e2e": res["e2e"],
+            "roofline": res["roofline"], "stages": res["stages"], "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_par, "e2e": res["e2e"],
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "secondary": secondary,
             "forced_miss_ms_per_step": res["forced_miss_ms_per_step"],
         }
@@ -617,6 +704,8 @@ def main():
             # the workload's own bound, and a measured rate where misses are countable
             pl = tk_plan(cfg)
             line["miss_rate"] = {"workload_bound": pl, "measured_case": measure_miss_rate()}
+            if world == 1 and args.miss_calls > 0:
+                line["miss_rate"]["configs"] = measure_config_miss_rates(args.miss_calls)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -47,7 +47,7 @@ typedef enum {
   TOPK_ENOMEM = -2,        /* workspace allocation failed */
   TOPK_ECUDA = -3,         /* a CUDA runtime call or kernel launch failed */
   TOPK_EUNSUPPORTED = -4,  /* valid request outside the engine's limits (see topk_select) */
-  TOPK_ETIMEOUT = -5       /* a bounded device-side wait gave up (reported with stats only) */
+  TOPK_ETIMEOUT = -5       /* a bounded device-side wait gave up (with stats, or from topk_last_status) */
 } topk_status_t;
 
 /* Parameter rule for (t, M).  Both use Algorithm 1's sample size S.
@@ -97,6 +97,16 @@ typedef struct {
    * is skipped; every other path still sorts.  The set, the values and the
    * positions are exact either way.  Default 0. */
   int unsorted;
+  /* > 0: limit in nanoseconds of each grid-wide wait of the exact fallback
+   * (default 0 = 2 s).  After it the kernel records a timeout, returns, and
+   * the call reports TOPK_ETIMEOUT (with stats, or from topk_last_status). */
+  int64_t wait_limit_ns;
+  /* Testing only (fault injection on the host's request, no GPU fault): when
+   * the fallback runs, one of its blocks leaves its first grid-wide wait
+   * without arriving, so every other block's bounded wait runs out.  The
+   * call's output is then undefined and its status is TOPK_ETIMEOUT; the next
+   * call on the stream starts clean.  Default 0. */
+  int inject_wait_timeout;
 } topk_options_t;
 
 /* Per-call report (row 0 for the per-row fields). */
@@ -164,12 +174,28 @@ int topk_select_ex(const void* x, int dtype, int64_t rows, int64_t n, int64_t k,
  * in opt (NULL = defaults).  EINVAL on bad arguments. */
 int topk_plan(int64_t n, int64_t k, double eps, const topk_options_t* opt, topk_plan_t* plan);
 
+/*
+ * Device-side status of the most recent selection issued on `stream` (of the
+ * current device) by topk_select, topk_select_global, topk_select_ex or
+ * topk_select_noalloc.  Synchronises `stream` first.  Returns TOPK_OK, or
+ * TOPK_ETIMEOUT when one of that call's bounded device waits gave up (its
+ * output is then undefined), or TOPK_ECUDA when its kernels found their state
+ * inconsistent; CUDA errors of the synchronisation itself map to TOPK_ECUDA.
+ * The status words are reset by each call, so this reports the last call
+ * only.  The short-row direct path (rows of at most 32768 elements, k <= 1024)
+ * keeps a status word only when topk_select_ex is given `stats`; otherwise
+ * this returns TOPK_OK for it.  Calls without any selection on `stream`
+ * return TOPK_OK.
+ */
+int topk_last_status(void* stream);
+
 /* Static text for a status code. */
 const char* topk_status_str(int status);
 
 /* Library version: major*10000 + minor*100 + patch.  0.2.0 (200) added the
- * `unsorted` field at the end of topk_options_t; fill the struct with
- * topk_options_init from the same version's library. */
+ * `unsorted` field at the end of topk_options_t; 0.3.0 (300) added
+ * `wait_limit_ns` and `inject_wait_timeout` after it, and topk_last_status.
+ * Fill the struct with topk_options_init from the same version's library. */
 int topk_version(void);
 
 /* ------------------------------------------------------------------------
@@ -223,6 +249,8 @@ int topk_prof_filter(const void* x, int dtype, int64_t rows, int64_t n, int glob
  * latency-critical loops that cannot take cudaMalloc's implicit device
  * synchronisation.  All scratch comes from one static device array of 8 MiB
  * inside the library, held by every GPU that loads the library until exit.
+ * The selection runs through the same kernels and the same choices of path
+ * as topk_select; only the scratch memory differs.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
@@ -230,9 +258,14 @@ int topk_prof_filter(const void* x, int dtype, int64_t rows, int64_t n, int glob
  *     contents; the library clears the words that must start at zero.  Calls
  *     that overlap on the GPU (e.g. unordered streams of one device) race on
  *     the array: order them on one stream.
- *   - A request whose scratch would exceed 8 MiB (roughly: sample plus buffer
- *     plus per-4096-element counters of all selections) returns
- *     TOPK_EUNSUPPORTED before anything is launched; use topk_select then.
+ *   - A request whose scratch would exceed 8 MiB returns TOPK_EUNSUPPORTED
+ *     before anything is launched; use topk_select then.  About 2.2 MiB is a
+ *     fixed part; the rest grows with the selections: roughly 8 bytes per
+ *     sample (S) and per buffer slot (M), 16 bytes per winner (k), and 1 byte
+ *     per 1024 input elements.  The 4096 x 65536 bf16 BatchTopK selection
+ *     (K = 131072) fits.
+ *   - A bounded device wait that gives up is reported by topk_last_status on
+ *     the same stream (this call itself does not synchronise).
  * Arguments, outputs, limits and the other error codes are those of
  * topk_select / topk_select_global.
  */

@@ -2,6 +2,7 @@
 
 Functions (each follows the passage cited in ``topk_oracle.cpp``):
   topk(x, k, largest, global_)        -- exact top-k, (value desc, index asc).
+  topk_parallel(x, k, ...)            -- the same answer from all host cores (CPU baseline).
   count_at_or_above(x_row, pivot)     -- R for a threshold element (section 3).
   sample_order_stat(x_row, idx, t)    -- tau = t-th best sampled element.
 
@@ -26,7 +27,7 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the C++ oracle into ``oracle/liboracle_topk.so`` (host code only)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        cmd = ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", _SRC, "-o", _LIB + ".tmp"]
+        cmd = ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", _SRC, "-o", _LIB + ".tmp"]
         subprocess.check_call(cmd)
         os.replace(_LIB + ".tmp", _LIB)
     return _LIB
@@ -40,6 +41,8 @@ def _load():
         vp, i64, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.oracle_topk.argtypes = [vp, c_int, i64, i64, i64, c_int, c_int, vp, vp]
         lib.oracle_topk.restype = c_int
+        lib.oracle_topk_parallel.argtypes = [vp, c_int, i64, i64, i64, c_int, c_int, c_int, vp, vp]
+        lib.oracle_topk_parallel.restype = c_int
         lib.oracle_count_at_or_above.argtypes = [vp, c_int, i64, i64, c_int]
         lib.oracle_count_at_or_above.restype = i64
         lib.oracle_sample_order_stat.argtypes = [vp, c_int, vp, i64, i64, c_int]
@@ -75,6 +78,26 @@ def topk(x: np.ndarray, k: int, largest: bool = True, global_: bool = False):
                              vals.ctypes.data, idx.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_topk rejected its arguments (k=%d, shape=%s)" % (k, x.shape))
+    if global_:
+        return vals[0], idx[0]
+    return vals, idx
+
+
+def topk_parallel(x: np.ndarray, k: int, largest: bool = True, global_: bool = False, threads: int = 0):
+    """``topk`` computed by ``threads`` host threads (0 = every core): chunked
+    nth_element and a merge.  A multi-threaded CPU baseline; checked against ``topk``."""
+    x = np.ascontiguousarray(x)
+    if x.ndim == 1:
+        x = x[None, :]
+    rows, n = x.shape
+    threads = threads or os.cpu_count() or 1
+    out_rows = 1 if global_ else rows
+    vals = np.empty((out_rows, k), dtype=x.dtype)
+    idx = np.empty((out_rows, k), dtype=np.int64)
+    rc = _load().oracle_topk_parallel(x.ctypes.data, _dtype_code(x), rows, n, k, int(bool(largest)),
+                                      int(bool(global_)), int(threads), vals.ctypes.data, idx.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_topk_parallel rejected its arguments (k=%d, shape=%s)" % (k, x.shape))
     if global_:
         return vals[0], idx[0]
     return vals, idx

@@ -31,6 +31,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <thread>
 #include <vector>
 
 namespace {
@@ -105,6 +106,65 @@ int oracle_topk(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, in
     select_sorted(items, k, largest);
     for (int64_t j = 0; j < k; ++j) {
       const Item& it = items[static_cast<size_t>(j)];
+      out_idx[r * k + j] = it.i;
+      if (dtype == 0) {
+        std::memcpy(static_cast<uint32_t*>(out_vals) + r * k + j, &it.bits, 4);
+      } else {
+        static_cast<uint16_t*>(out_vals)[r * k + j] = static_cast<uint16_t>(it.bits);
+      }
+    }
+  }
+  return 0;
+}
+
+// The same answer as oracle_topk from several host threads: each selection's
+// elements are cut into `threads` contiguous chunks, each chunk keeps its own
+// k best (nth_element) in parallel, and the union of those candidates -- which
+// holds the k best of the whole selection -- is selected and sorted as
+// above.  A CPU baseline over all host cores, not a reference answer: the
+// tests check it against oracle_topk.
+int oracle_topk_parallel(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,
+                         int global, int threads, void* out_vals, int64_t* out_idx) {
+  if (rows < 0 || n < 0 || k < 1 || (dtype != 0 && dtype != 1) || threads < 1) return -1;
+  if (rows == 0) return 0;
+  const int64_t len = global ? rows * n : n;
+  const int64_t nsel = global ? 1 : rows;
+  if (k > len) return -1;
+  auto cmp = largest ? before_largest : before_smallest;
+  for (int64_t r = 0; r < nsel; ++r) {
+    const int64_t nt = std::min<int64_t>(threads, std::max<int64_t>(1, len / std::max<int64_t>(k, 1)));
+    std::vector<std::vector<Item>> kept(static_cast<size_t>(nt));
+    std::vector<std::thread> pool;
+    for (int64_t c = 0; c < nt; ++c) {
+      pool.emplace_back([&, c]() {
+        const int64_t b = len * c / nt, e = len * (c + 1) / nt;
+        std::vector<Item>& v = kept[static_cast<size_t>(c)];
+        v.resize(static_cast<size_t>(e - b));
+        for (int64_t i = b; i < e; ++i) {
+          Item& it = v[static_cast<size_t>(i - b)];
+          it.i = i;
+          if (dtype == 0) {
+            const float* xf = static_cast<const float*>(x) + r * len;
+            it.v = xf[i];
+            std::memcpy(&it.bits, &xf[i], 4);
+          } else {
+            const uint16_t* xh = static_cast<const uint16_t*>(x) + r * len;
+            it.v = widen_bf16(xh[i]);
+            it.bits = xh[i];
+          }
+        }
+        if (static_cast<int64_t>(v.size()) > k) {
+          std::nth_element(v.begin(), v.begin() + (k - 1), v.end(), cmp);
+          v.resize(static_cast<size_t>(k));
+        }
+      });
+    }
+    for (auto& t : pool) t.join();
+    std::vector<Item> cand;
+    for (auto& v : kept) cand.insert(cand.end(), v.begin(), v.end());
+    select_sorted(cand, k, largest);
+    for (int64_t j = 0; j < k; ++j) {
+      const Item& it = cand[static_cast<size_t>(j)];
       out_idx[r * k + j] = it.i;
       if (dtype == 0) {
         std::memcpy(static_cast<uint32_t*>(out_vals) + r * k + j, &it.bits, 4);

@@ -463,3 +463,22 @@ def test_alg1_t_is_the_smallest_rank_meeting_eq5(n, k, eps):
     assert t > 1
     assert p_fail(t) <= eps / 2.0
     assert p_fail(t - 1) > eps / 2.0
+
+
+@pytest.mark.parametrize("threads", [1, 3, 8])
+@pytest.mark.parametrize("largest", [True, False])
+def test_parallel_cpu_baseline_equals_the_oracle(threads, largest):
+    """The multi-threaded CPU baseline returns exactly the oracle's answer (ties
+    straddling chunk borders, special values, per-row and global)."""
+    x = _tied_specials(4, 5000).reshape(5, 1000)
+    for k in (1, 7, 400, 1000):
+        v, i = plain.topk(x, k, largest=largest)
+        vp, ip = plain.topk_parallel(x, k, largest=largest, threads=threads)
+        assert np.array_equal(ip, i) and np.array_equal(vp.view(np.uint32), v.view(np.uint32))
+    v, i = plain.topk(x, 2500, largest=largest, global_=True)
+    vp, ip = plain.topk_parallel(x, 2500, largest=largest, global_=True, threads=threads)
+    assert np.array_equal(ip, i) and np.array_equal(vp.view(np.uint32), v.view(np.uint32))
+    h = workloads.make("relu_normal_bf16", 4, 3000, 6)
+    v, i = plain.topk(h, 900, largest=largest, global_=True)
+    vp, ip = plain.topk_parallel(h, 900, largest=largest, global_=True, threads=threads)
+    assert np.array_equal(ip, i) and np.array_equal(vp, v)

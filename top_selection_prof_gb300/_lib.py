@@ -16,14 +16,15 @@ PATH_NAMES = {TOPK_PATH_DIRECT: "direct", TOPK_PATH_PROFK: "profk", TOPK_PATH_EX
 # Every symbol include/topk.h declares.
 EXPORTS = ("topk_options_init", "topk_select", "topk_select_global", "topk_select_ex", "topk_plan",
            "topk_status_str", "topk_version", "topk_index_bits", "topk_prof_sample", "topk_prof_filter",
-           "topk_select_noalloc")
+           "topk_select_noalloc", "topk_last_status")
 
 
 class TopkOptions(ctypes.Structure):
     _fields_ = [("s_min", ctypes.c_int64), ("s_max", ctypes.c_int64), ("cost_ratio", ctypes.c_double),
                 ("rule", ctypes.c_int), ("path", ctypes.c_int), ("seed", ctypes.c_uint64),
                 ("counter", ctypes.c_int64), ("force_miss", ctypes.c_int), ("m_override", ctypes.c_int64),
-                ("t_override", ctypes.c_int64), ("events", ctypes.c_void_p * 6), ("unsorted", ctypes.c_int)]
+                ("t_override", ctypes.c_int64), ("events", ctypes.c_void_p * 6), ("unsorted", ctypes.c_int),
+                ("wait_limit_ns", ctypes.c_int64), ("inject_wait_timeout", ctypes.c_int)]
 
 
 class TopkStats(ctypes.Structure):
@@ -63,6 +64,8 @@ def get():
         lib.topk_select_ex.restype = c_int
         lib.topk_plan.argtypes = [i64, i64, c_double, ctypes.POINTER(TopkOptions), ctypes.POINTER(TopkPlan)]
         lib.topk_plan.restype = c_int
+        lib.topk_last_status.argtypes = [vp]
+        lib.topk_last_status.restype = c_int
         lib.topk_status_str.argtypes = [c_int]
         lib.topk_status_str.restype = ctypes.c_char_p
         lib.topk_version.argtypes = []

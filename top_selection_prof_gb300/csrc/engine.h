@@ -22,9 +22,13 @@ struct Problem {
 // ---- parameters (params.cpp) -------------------------------------------------
 // Whether the refinement kernel should handle a miss itself (no launch when
 // nothing misses, but its cluster alone streams x on a miss) rather than the
-// grid-wide fallback kernel: true when eps times the expected cost of that
-// slow miss is below the cost of the launch it saves.
-bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double eps);
+// grid-wide fallback kernel: true when the miss probability of the plan in
+// use (P[R < k] + P[R > M] for its S, t and M, per selection) times the
+// expected cost of that slow miss is below the cost of the launch it saves.
+bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double p_miss);
+// P[R < k] + P[R > M] for one selection of k out of n with (S, t, M) under the
+// with-replacement sampler (the exact tails of Lemma 1's counting argument).
+double plan_miss_probability(int64_t n, int64_t k, int64_t S, int64_t t, int64_t M);
 // Programmatic dependent launch for one pipeline edge (see params.cpp).
 constexpr unsigned kPdlTau = 1, kPdlFilter = 2, kPdlFallback = 4, kPdlRefine = 8;
 bool pdl_edge(unsigned bit);
@@ -110,6 +114,9 @@ struct FallbackScratch {
   unsigned long long* r_seen;  // per selection: R as the filter left it
   unsigned long long* misses;  // number of selections that fell back
   uint64_t* tau_exact;         // per selection: exact k-th key written on a miss
+  uint64_t wait_ns;            // limit of each grid-wide wait (kWaitLimitNs unless a caller sets it)
+  int stall_block;             // testing: this block leaves its first grid-wide wait without
+                               // arriving, so the others' bounded wait runs out (-1: none)
 };
 constexpr int64_t kFallbackTile = 4096;
 // reserved_sms: SMs the preceding grid (the threshold select) holds; the
@@ -201,6 +208,27 @@ int64_t select_xbuf_stride(int64_t k);
 cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source_bound, int* cluster,
                           cudaStream_t st);
 int64_t select_max_k();
+
+// ---- the C ABI's pipeline on caller-provided scratch (topk_api.cu) -----------
+// Counters that pick which copy of the alternating zero-kept regions a call
+// uses (see the workspace layout in topk_api.cu); one set per scratch block.
+struct ScratchCounters {
+  uint64_t sample_calls = 0;
+  uint64_t refine_calls = 0;
+};
+// A fixed device block used instead of the per-stream pool: zero-initialised
+// once, 256-byte aligned, owned by the caller for the life of the process.
+struct FixedScratch {
+  void* base;
+  size_t bytes;
+  ScratchCounters* counters;
+};
+// topk_select (global == false) / topk_select_global with every piece of
+// scratch taken from `fs`; TOPK_EUNSUPPORTED, before anything is launched,
+// when the call's layout needs more than fs.bytes.
+int select_with_fixed_scratch(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,
+                              double eps, void* out_vals, int64_t* out_idx, cudaStream_t st, bool global,
+                              const FixedScratch& fs);
 #ifdef TK_PHASE_TIMING
 int debug_phase_ns(unsigned long long* out);  // debug builds: per-phase timer stamps
 int debug_rows_ns(unsigned long long* out);   // debug builds: stamps of the short-row kernel

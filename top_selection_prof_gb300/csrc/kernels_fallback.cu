@@ -30,31 +30,37 @@ struct FallbackParams {
   FallbackScratch fs;
 };
 
-// Grid-wide barrier for a cooperative launch.  Gives up after kWaitLimitNs and
+// Grid-wide barrier for a cooperative launch.  Gives up after fs.wait_ns and
 // records kDevTimeout in the status word; returns false then (and when another
-// block already reported an error).
-__device__ bool grid_barrier(unsigned* bar, int* status) {
+// block already reported an error).  Test knob: block fs.stall_block leaves
+// without arriving (and returns false), so every other block's wait runs out.
+__device__ bool grid_barrier(const FallbackScratch& fs) {
   __shared__ int s_ok;
+  unsigned* bar = fs.barrier;
+  int* status = fs.status;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const unsigned gen = ld_acquire_u32(bar + 1);
-    __threadfence();
-    const unsigned arrived = atomicAdd(bar, 1u) + 1u;
-    if (arrived == gridDim.x) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      atomicAdd(bar + 1, 1u);
+    if (static_cast<int>(blockIdx.x) == fs.stall_block) {
+      ok = 0;
     } else {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_u32(bar + 1) == gen) {
-        if (*reinterpret_cast<volatile int*>(status) != kDevOk ||
-            globaltimer_ns() - t0 > kWaitLimitNs) {
-          atomicCAS(status, kDevOk, kDevTimeout);
-          ok = 0;
-          break;
+      const unsigned gen = ld_acquire_u32(bar + 1);
+      __threadfence();
+      const unsigned arrived = atomicAdd(bar, 1u) + 1u;
+      if (arrived == gridDim.x) {
+        atomicExch(bar, 0u);
+        __threadfence();
+        atomicAdd(bar + 1, 1u);
+      } else {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_u32(bar + 1) == gen) {
+          if (*reinterpret_cast<volatile int*>(status) != kDevOk || globaltimer_ns() - t0 > fs.wait_ns) {
+            atomicCAS(status, kDevOk, kDevTimeout);
+            ok = 0;
+            break;
+          }
+          __nanosleep(128);
         }
-        __nanosleep(128);
       }
     }
     __threadfence();
@@ -170,7 +176,7 @@ __device__ int fallback_body(const FallbackParams& a, uint64_t (*stage)[kWarpSta
     TK_FB(0);
     if (blockIdx.x == 0)
       for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) fs.ghist[i] = 0u;
-    if (!grid_barrier(fs.barrier, fs.status)) return -1;
+    if (!grid_barrier(fs)) return -1;
     TK_FB(1);
 
     // -- phase A: radix select of the k-th largest value key
@@ -191,7 +197,7 @@ __device__ int fallback_body(const FallbackParams& a, uint64_t (*stage)[kWarpSta
         if (s) atomicAdd(&fs.ghist[pass * 256 + d], s);
       }
       TK_FB(2 + 2 * pass);
-      if (!grid_barrier(fs.barrier, fs.status)) return -1;
+      if (!grid_barrier(fs)) return -1;
       TK_FB(3 + 2 * pass);
       // every block finds the digit holding the rank-th largest (same answer
       // everywhere); thread j looks at digit 255 - j (kFilterBlock == 256)
@@ -249,7 +255,7 @@ __device__ int fallback_body(const FallbackParams& a, uint64_t (*stage)[kWarpSta
       __syncthreads();
     }
     TK_FB(11);
-    if (!grid_barrier(fs.barrier, fs.status)) return -1;
+    if (!grid_barrier(fs)) return -1;
     TK_FB(12);
 
     if (blockIdx.x == 0) {
@@ -301,7 +307,7 @@ __device__ int fallback_body(const FallbackParams& a, uint64_t (*stage)[kWarpSta
       }
     }
     TK_FB(13);
-    if (!grid_barrier(fs.barrier, fs.status)) return -1;
+    if (!grid_barrier(fs)) return -1;
     if (*reinterpret_cast<volatile int*>(fs.status) != kDevOk) return -1;
     TK_FB(14);
 
@@ -496,7 +502,7 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   __syncthreads();
   if (tid == 0 && cn > 0) { atomicMax(g_nmin, s_nmin); atomicMax(g_max, s_max); }
   TK_RG(3);
-  if (!grid_barrier(fs.barrier, fs.status)) return false;
+  if (!grid_barrier(fs)) return false;
   TK_RG(4);
   // Digits are taken of key - kmin: 2048 equal slices of the keys' range.
   // (Digits of the keys themselves below their top varying bit leave only a
@@ -522,7 +528,7 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
     cur[i] = c ? atomicAdd(g_lev + i, c) : 0u;
   }
   TK_RG(5);
-  if (!grid_barrier(fs.barrier, fs.status)) return false;
+  if (!grid_barrier(fs)) return false;
   TK_RG(6);
   if (!find_rank_bin(g_lev, k, bst, s_ws, s_info)) {
     if (tid == 0) atomicCAS(fs.status, kDevOk, kDevBadState);
@@ -556,7 +562,7 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
       unsigned* gl = g_lev + level * kRefineGridBins;
       for (int i = tid; i < kRefineGridBins; i += kFilterBlock)
         if (lh[i]) atomicAdd(gl + i, lh[i]);
-      if (!grid_barrier(fs.barrier, fs.status)) return false;
+      if (!grid_barrier(fs)) return false;
       if (!find_rank_bin(gl, rank, nullptr, s_ws, s_info)) {
         if (tid == 0) atomicCAS(fs.status, kDevOk, kDevBadState);
         return false;
@@ -670,7 +676,7 @@ __global__ void __launch_bounds__(kFilterBlock, 2) refine_grid_kernel(RefineGrid
   TK_RG(2);
   if (missed < 0) return;
   // a rebuilt buffer is complete once every block has filtered its tiles
-  if (missed > 0 && !grid_barrier(a.fb.fs.barrier, a.fb.fs.status)) return;
+  if (missed > 0 && !grid_barrier(a.fb.fs)) return;
   uint64_t* cache = &stage[0][0];
   for (int64_t row = 0; row < a.fb.fp.nsel; ++row)
     if (!partition_row(a, row, cache, part_smem)) return;

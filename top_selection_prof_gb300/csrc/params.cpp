@@ -162,9 +162,17 @@ bool choose_params(int64_t n, int64_t k, double eps, const ParamRule& pr, int64_
   return true;
 }
 
-bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double eps) {
+double plan_miss_probability(int64_t n, int64_t k, int64_t S, int64_t t, int64_t M) {
+  const double nd = static_cast<double>(n);
+  const double pm = M >= n ? 1.0 : static_cast<double>(M) / nd;
+  return binom_upper_tail(S, (static_cast<double>(k) - 1.0) / nd, t) + binom_lower_tail(S, pm, t - 1);
+}
+
+bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double p_miss) {
   constexpr double kLaunchUs = 4.0;       // a fallback launch that exits at once
-  constexpr double kSmBytesPerUs = 1e5;   // ~100 GB/s streamed per SM
+  // ~12 GB/s per SM of the cluster over its passes (a miss of the 1 GiB f32
+  // row in a 2-CTA cluster measured ~135 ms)
+  constexpr double kSmBytesPerUs = 1.2e4;
   const double row_bytes = static_cast<double>(p.len) * (p.dtype == 0 ? 4.0 : 2.0);  // f32 : bf16
   int64_t g = (k + 11775) / 11776;        // the refinement cluster's size, at least
   const double er = static_cast<double>(t) * (static_cast<double>(p.len) + 1.0) / (static_cast<double>(S) + 1.0);
@@ -172,7 +180,8 @@ bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double ep
   if (g_cache > g) g = g_cache;
   if (g > 16) g = 16;
   const double miss_us = 3.0 * row_bytes / (static_cast<double>(g) * kSmBytesPerUs);
-  const double p_any = std::min(1.0, eps * static_cast<double>(p.nsel));
+  // probability that some selection of the call misses
+  const double p_any = std::min(1.0, p_miss * static_cast<double>(p.nsel));
   return p_any * miss_us < kLaunchUs;
 }
 

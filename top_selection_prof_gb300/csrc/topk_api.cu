@@ -8,9 +8,12 @@
 //   filter_kernel    one pass over x, keys >= tau -> buffer, R    (stage 3)
 //   select_kernel    exact top-k of the buffer, sorted -> outputs (stage 4);
 //                    on a miss (R < k or R > M) it selects from x instead
-// The miss decision is made on the device by the refinement kernel itself.
-// The exact path (no Prof-K) runs the grid-wide fallback_kernel and then the
-// same sort.
+// The miss decision is made on the device, by the refinement kernel itself
+// or by the grid-wide fallback_kernel launched after the filter (chosen per
+// call from the plan's miss probability).  The exact path (no Prof-K) runs
+// the grid-wide fallback_kernel and then the same sort.  Scratch memory comes
+// from a per-(device, stream) pool, or from a fixed block the caller owns
+// (select_with_fixed_scratch, used by topk_select_noalloc).
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -35,15 +38,14 @@ std::atomic<uint64_t> g_counter{0};
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
-  uint64_t sample_calls = 0;  // calls whose sample kernel launched: picks the histogram half
-  uint64_t refine_calls = 0;  // calls of the grid refinement: picks its control words' copy
+  ScratchCounters counters;  // pick the alternating zero-kept regions (see the layout below)
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
 // Returns a device block of at least `bytes` for this (device, stream); grows
 // with stream-ordered allocation (the old block is released in stream order).
-cudaError_t workspace(cudaStream_t st, size_t bytes, void** out, Workspace** entry = nullptr) {
+cudaError_t workspace(cudaStream_t st, size_t bytes, void** out, ScratchCounters** counters = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -62,8 +64,34 @@ cudaError_t workspace(cudaStream_t st, size_t bytes, void** out, Workspace** ent
     w.bytes = grow;
   }
   *out = w.ptr;
-  if (entry) *entry = &w;
+  if (counters) *counters = &w.counters;
   return cudaSuccess;
+}
+
+// Where a call's scratch comes from: the per-(device, stream) pool above, or
+// a fixed block the caller owns (no allocation; too small -> unsupported).
+struct ScratchSource {
+  const FixedScratch* fixed = nullptr;
+};
+constexpr cudaError_t kScratchTooSmall = cudaErrorInvalidValue;  // (mapped to TOPK_EUNSUPPORTED)
+
+cudaError_t acquire(const ScratchSource& src, cudaStream_t st, size_t bytes, void** out,
+                    ScratchCounters** counters = nullptr) {
+  if (!src.fixed) return workspace(st, bytes, out, counters);
+  if (bytes > src.fixed->bytes) return kScratchTooSmall;
+  *out = src.fixed->base;
+  if (counters) *counters = src.fixed->counters;
+  return cudaSuccess;
+}
+
+// The device status word of the last call on each (device, stream), or null
+// when that call kept none; read back by topk_last_status.
+std::map<std::pair<int, cudaStream_t>, int*> g_last_status;
+void record_status_word(cudaStream_t st, int* word) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  g_last_status[std::make_pair(dev, st)] = word;
 }
 
 // Every workspace starts with the same prefix, whatever the call's layout:
@@ -98,6 +126,7 @@ int index_bits(int64_t len) {
 struct Plan {
   int path;
   int64_t S, t, M;
+  double p_miss;  // P[R < k] + P[R > M] per selection for (S, t, M) (Prof-K path)
 };
 
 
@@ -133,12 +162,13 @@ struct PlanKey {
 struct PlanVal {
   bool ok;
   int64_t S, t, M;
+  double p_miss;
 };
 std::mutex g_plan_mu;
 std::map<PlanKey, PlanVal> g_plans;
 
 bool cached_params(int64_t len, int64_t k, double eps, const ParamRule& pr, int64_t* S, int64_t* t,
-                   int64_t* M) {
+                   int64_t* M, double* p_miss) {
   const PlanKey key{len, k, eps, pr.s_min, pr.s_max, pr.cost_ratio, pr.rule};
   {
     std::lock_guard<std::mutex> lock(g_plan_mu);
@@ -147,17 +177,20 @@ bool cached_params(int64_t len, int64_t k, double eps, const ParamRule& pr, int6
       *S = it->second.S;
       *t = it->second.t;
       *M = it->second.M;
+      *p_miss = it->second.p_miss;
       return it->second.ok;
     }
   }
   PlanVal v{};
   v.ok = choose_params(len, k, eps, pr, &v.S, &v.t, &v.M);
+  v.p_miss = v.ok && v.t >= 1 && v.t <= v.S ? plan_miss_probability(len, k, v.S, v.t, v.M) : 1.0;
   std::lock_guard<std::mutex> lock(g_plan_mu);
   if (g_plans.size() > 4096) g_plans.clear();
   g_plans[key] = v;
   *S = v.S;
   *t = v.t;
   *M = v.M;
+  *p_miss = v.p_miss;
   return v.ok;
 }
 
@@ -165,6 +198,7 @@ bool cached_params(int64_t len, int64_t k, double eps, const ParamRule& pr, int6
 int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
               const topk_options_t* o, Plan* plan) {
   plan->S = plan->t = plan->M = 0;
+  plan->p_miss = 0.0;
   const int forced = o ? o->path : TOPK_PATH_AUTO;
   bool profk_ok = false;
   if (eps > 0.0) {
@@ -172,12 +206,16 @@ int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
     if (pr.s_min < 1 || pr.s_max < pr.s_min || !(pr.cost_ratio > 0.0) || (pr.rule != 0 && pr.rule != 1))
       return TOPK_EINVAL;
     int64_t S = 0, t = 0, M = 0;
-    if (cached_params(len, k, eps, pr, &S, &t, &M)) {
+    double p_miss = 1.0;
+    if (cached_params(len, k, eps, pr, &S, &t, &M, &p_miss)) {
+      const bool overridden = o && (o->t_override > 0 || o->m_override > 0);
       if (o && o->t_override > 0) t = o->t_override;
       if (o && o->m_override > 0) M = o->m_override;
+      if (overridden) p_miss = t >= 1 && t <= S ? plan_miss_probability(len, k, S, t, M) : 1.0;
       plan->S = S;
       plan->t = t;
       plan->M = M;
+      plan->p_miss = p_miss;
       profk_ok = t >= 1 && t <= S && 2 * S < len && 2 * M <= len && M >= k && nsel <= 65535;
     }
   }
@@ -200,7 +238,10 @@ int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
     default:
       return TOPK_EINVAL;
   }
-  if (plan->path != TOPK_PATH_PROFK) plan->S = plan->t = plan->M = 0;
+  if (plan->path != TOPK_PATH_PROFK) {
+    plan->S = plan->t = plan->M = 0;
+    plan->p_miss = 0.0;
+  }
   return TOPK_OK;
 }
 
@@ -262,7 +303,7 @@ int status_of(cudaError_t e) {
 
 int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest, double eps,
         void* out_vals, int64_t* out_idx, cudaStream_t st, bool global, const topk_options_t* o,
-        topk_stats_t* stats) {
+        topk_stats_t* stats, const ScratchSource& src = ScratchSource{}) {
   int rc = check_common(x, dtype, rows, n, k, eps, out_vals, out_idx, global);
   if (rc != TOPK_OK) return rc;
   if (stats) std::memset(stats, 0, sizeof(*stats));
@@ -279,6 +320,8 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     stats->t = plan.t;
     stats->M = plan.M;
   }
+  // (a fixed block that is too small: nothing has been launched yet)
+  auto scratch_status = [](cudaError_t e) { return e == kScratchTooSmall ? TOPK_EUNSUPPORTED : status_of(e); };
 
   int cluster = 0;
   if (plan.path == TOPK_PATH_DIRECT && rows_supported(p, k)) {
@@ -287,11 +330,13 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     int* status = nullptr;
     if (stats) {
       void* ws = nullptr;
-      TK_TRY(workspace(st, ws_prefix(), &ws));
+      const cudaError_t e = acquire(src, st, ws_prefix(), &ws);
+      if (e != cudaSuccess) return scratch_status(e);
       status = &static_cast<DevHeader*>(ws)->status;
       TK_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
     }
     TK_TRY(launch_rows(p, k, out_vals, out_idx, status, st));
+    record_status_word(st, status);
     if (stats) {
       stats->launches = 1;
       stats->cluster = 1;
@@ -306,7 +351,8 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   if (plan.path == TOPK_PATH_DIRECT) {
     // the status word and the sort's exchange buffer
     void* ws = nullptr;
-    TK_TRY(workspace(st, ws_prefix() + sizeof(uint64_t) * p.nsel * k, &ws));
+    const cudaError_t e = acquire(src, st, ws_prefix() + sizeof(uint64_t) * p.nsel * k, &ws);
+    if (e != cudaSuccess) return scratch_status(e);
     DevHeader* hdr = static_cast<DevHeader*>(ws);
     TK_TRY(cudaMemsetAsync(&hdr->status, 0, sizeof(int), st));
     SelectJob job{};
@@ -320,6 +366,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     int nl = 0;
     job.launch_count = &nl;
     TK_TRY(launch_select(p, job, p.len, &cluster, st));
+    record_status_word(st, &hdr->status);
     if (stats) {
       stats->launches = nl;
       stats->cluster = cluster;
@@ -332,10 +379,15 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     return TOPK_OK;
   }
 
-  // workspace layout
+  // one or a few selections: sampling and the threshold in one grid (no
+  // threshold launch; the sample and threshold stages then share one event
+  // interval), which needs no sample array
   const int64_t nsel = p.nsel;
   const int64_t M = plan.path == TOPK_PATH_PROFK ? plan.M : k;
   const int64_t S = plan.S;
+  const bool fused = plan.path == TOPK_PATH_PROFK && nsel <= kSampleHistMaxRows && sample_tau_supported(p, S);
+
+  // workspace layout
   const int64_t ntile = (p.len + kFallbackTile - 1) / kFallbackTile;
   const size_t o_hdr = 0;
   size_t off = ws_prefix();
@@ -345,13 +397,16 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   const size_t o_taux = off; off = align_up(off + sizeof(uint64_t) * nsel);
   const size_t o_ghist = off; off = align_up(off + sizeof(unsigned) * 8 * 256);
   const size_t o_tiles = off; off = align_up(off + sizeof(unsigned) * ntile);
-  const size_t o_samples = off; off = align_up(off + sizeof(uint64_t) * nsel * S);
+  const size_t o_samples = off; off = align_up(off + (fused ? 0 : sizeof(uint64_t) * nsel * S));
   const size_t o_buf = off; off = align_up(off + sizeof(uint64_t) * nsel * M);
   const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * nsel * select_xbuf_stride(k));
   const size_t o_binfo = off; off = align_up(off + sizeof(unsigned) * nsel * select_binfo_words(k));
   void* ws = nullptr;
-  Workspace* wentry = nullptr;
-  TK_TRY(workspace(st, off, &ws, &wentry));
+  ScratchCounters* wcnt = nullptr;
+  {
+    const cudaError_t e = acquire(src, st, off, &ws, &wcnt);
+    if (e != cudaSuccess) return scratch_status(e);
+  }
   char* base = static_cast<char*>(ws);
   DevHeader* hdr = reinterpret_cast<DevHeader*>(base + o_hdr);
   auto* counts = reinterpret_cast<unsigned long long*>(base + o_counts);
@@ -364,7 +419,10 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   auto* buf = reinterpret_cast<uint64_t*>(base + o_buf);
   auto* xbuf = reinterpret_cast<uint64_t*>(base + o_xbuf);
 
-  FallbackScratch fs{ghist, tiles, hdr->barrier, &hdr->status, r_seen, &hdr->misses, tau_x};
+  FallbackScratch fs{ghist, tiles, hdr->barrier, &hdr->status, r_seen, &hdr->misses, tau_x,
+                     kWaitLimitNs, -1};
+  if (o && o->wait_limit_ns > 0) fs.wait_ns = static_cast<uint64_t>(o->wait_limit_ns);
+  if (o && o->inject_wait_timeout) fs.stall_block = 0;
   const uint64_t seed = (o && o->seed) ? o->seed : kDefaultSeed;
   const uint64_t counter = (o && o->counter >= 0) ? static_cast<uint64_t>(o->counter)
                                                   : g_counter.fetch_add(1);
@@ -390,28 +448,22 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     unsigned* hist_zero = nullptr;
     if (nsel <= kSampleHistMaxRows) {
       char* halves = base + ws_hist_offset();
-      const uint64_t parity = wentry->sample_calls & 1u;
+      uint64_t parity;
+      {
+        std::lock_guard<std::mutex> lock(g_ws_mu);
+        parity = wcnt->sample_calls++ & 1u;
+      }
       hist_add = reinterpret_cast<unsigned*>(halves + parity * kHistHalfBytes);
       hist_zero = reinterpret_cast<unsigned*>(halves + (parity ^ 1u) * kHistHalfBytes);
     }
-    // one or a few selections: sampling and the threshold in one grid
-    // (no threshold launch; then the sample and threshold stages share one
-    // event interval)
-    const bool fused = hist_add && sample_tau_supported(p, S);
-    int tau_cluster = 0;
     if (fused) {
       const SampleTauScratch sc{hist_add, hist_zero, reinterpret_cast<unsigned*>(base + ws_tau_ctl_offset()),
                                 reinterpret_cast<uint64_t*>(base + ws_tau_gather_offset())};
       TK_TRY(launch_sample_tau(p, S, plan.t, seed, counter, counts, hdr, sc, tau, st));
       ++nl;
-      tau_cluster = 0;  // holds no SMs once its blocks finish
     } else {
       TK_TRY(launch_sample(p, S, seed, counter, samples, counts, hdr, hist_add, hist_zero, st));
       ++nl;
-    }
-    if (hist_add) {
-      std::lock_guard<std::mutex> lock(g_ws_mu);
-      ++wentry->sample_calls;
     }
     TK_TRY(mark(1));
     if (!fused) {
@@ -424,6 +476,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
       tj.sample_hist = hist_add;
       tj.status = &hdr->status;
       tj.launch_count = &nl;
+      int tau_cluster = 0;
       TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
 #ifdef TK_PHASE_TIMING
       if (std::getenv("TK_DEBUG_TWICE")) TK_TRY(launch_select(p, tj, S, &tau_cluster, st));
@@ -439,10 +492,11 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // Where to handle a miss: inside the refinement kernel (no launch when
     // nothing missed, but on a miss its cluster alone streams x), or in the
     // grid-wide fallback kernel (one launch per call, a fast miss).  The
-    // refinement takes it when the expected cost of its slow miss, eps times
-    // about three passes over a row at ~100 GB/s per SM of the cluster, is
-    // below the launch it saves.
-    if (!grid_refine && !miss_in_refine(p, k, plan.t, plan.S, eps)) {
+    // refinement takes it when the expected cost of its slow miss -- the
+    // plan's own miss probability times about three passes over a row at
+    // ~100 GB/s per SM of the cluster -- is below the launch it saves.  A
+    // miss forced by the caller always takes the grid-wide fallback.
+    if (!grid_refine && (force || !miss_in_refine(p, k, plan.t, plan.S, plan.p_miss))) {
       TK_TRY(launch_fallback(p, k, M, buf, counts, fs, force, st));
       ++nl;
       fallback_launched = true;
@@ -491,7 +545,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     uint64_t parity;
     {
       std::lock_guard<std::mutex> lock(g_ws_mu);
-      parity = wentry->refine_calls++ & 1u;
+      parity = wcnt->refine_calls++ & 1u;
     }
     char* copies = base + ws_refine_ctl_offset();
     RefineGridScratch rg{};
@@ -517,6 +571,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
 #endif
   }
   if (plan.path == TOPK_PATH_PROFK) TK_TRY(mark(5));
+  record_status_word(st, &hdr->status);
 
   if (stats) {
     DevHeader h;
@@ -541,6 +596,15 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
 }
 
 }  // namespace
+
+int select_with_fixed_scratch(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest,
+                              double eps, void* out_vals, int64_t* out_idx, cudaStream_t st, bool global,
+                              const FixedScratch& fs) {
+  ScratchSource src;
+  src.fixed = &fs;
+  return run(x, dtype, rows, n, k, largest, eps, out_vals, out_idx, st, global, nullptr, nullptr, src);
+}
+
 }  // namespace tk
 
 using namespace tk;
@@ -557,6 +621,8 @@ void topk_options_init(topk_options_t* opt) {
   opt->path = TOPK_PATH_AUTO;
   opt->seed = kDefaultSeed;
   opt->counter = -1;
+  opt->wait_limit_ns = 0;
+  opt->inject_wait_timeout = 0;
 }
 
 int topk_select(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest, double eps,
@@ -597,6 +663,24 @@ int topk_plan(int64_t n, int64_t k, double eps, const topk_options_t* opt, topk_
   return TOPK_OK;
 }
 
+int topk_last_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  TK_TRY(cudaGetDevice(&dev));
+  int* word = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    auto it = g_last_status.find(std::make_pair(dev, st));
+    if (it != g_last_status.end()) word = it->second;
+  }
+  TK_TRY(cudaStreamSynchronize(st));
+  if (!word) return TOPK_OK;
+  int dstat = 0;
+  TK_TRY(cudaMemcpy(&dstat, word, sizeof(int), cudaMemcpyDeviceToHost));
+  if (dstat == kDevOk) return TOPK_OK;
+  return dstat == kDevTimeout ? TOPK_ETIMEOUT : TOPK_ECUDA;
+}
+
 const char* topk_status_str(int status) {
   switch (status) {
     case TOPK_OK: return "ok";
@@ -610,7 +694,8 @@ const char* topk_status_str(int status) {
 }
 
 // 0.2.0: topk_options_t gained `unsorted` (a caller built against 0.1 passes a shorter struct).
-int topk_version(void) { return 200; }
+// 0.3.0: topk_options_t gained `wait_limit_ns` and `inject_wait_timeout`; topk_last_status.
+int topk_version(void) { return 300; }
 
 #ifdef TK_PHASE_TIMING
 int topk_debug_phase_ns(unsigned long long* out) { return tk::debug_phase_ns(out); }
