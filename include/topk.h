@@ -107,6 +107,17 @@ typedef struct {
    * call's output is then undefined and its status is TOPK_ETIMEOUT; the next
    * call on the stream starts clean.  Default 0. */
   int inject_wait_timeout;
+  /* Relaxed recall (Prof-K paper, abstract: "relaxing the recall target (e.g.,
+   * recovering 95% of the true top-k values)").  0 (default) or >= 1: exact.
+   * In (0, 1): the threshold rank t is chosen for rank ceil(recall * k)
+   * instead of k, so that P[fewer than ceil(recall * k) of the true top-k
+   * survive] <= eps/2, and fewer than k survivors no longer take the
+   * fallback: when R < k, the first R places of the row hold the exact top-R
+   * (all of them true top-k elements), sorted as usual, and places R..k-1
+   * hold index -1 and the value -inf (+inf when largest == 0).  A buffer
+   * overflow (R > M) still takes the exact fallback.  Applies to the Prof-K
+   * path; the direct and exact paths return the exact top-k. */
+  double recall;
 } topk_options_t;
 
 /* Per-call report (row 0 for the per-row fields). */
@@ -122,13 +133,14 @@ typedef struct {
   int64_t counter;
   int cluster;         /* CTAs per thread-block cluster in the final selection */
   int launches;        /* kernels this call launched on the stream */
+  int64_t shortfalls;  /* rows that returned fewer than k winners (relaxed recall only) */
 } topk_stats_t;
 
 /* Parameters the engine would use for a selection of k out of n (host only). */
 typedef struct {
   int path;            /* topk_path_t the automatic choice resolves to */
   int64_t S, t, M;
-  double p_recall_fail;  /* P[R < k] for these (S, t) under the with-replacement sampler */
+  double p_recall_fail;  /* P[R < k] (relaxed recall: P[R < ceil(recall*k)]) under the with-replacement sampler */
   double p_overflow;     /* P[R > M] */
 } topk_plan_t;
 
@@ -194,7 +206,8 @@ const char* topk_status_str(int status);
 
 /* Library version: major*10000 + minor*100 + patch.  0.2.0 (200) added the
  * `unsorted` field at the end of topk_options_t; 0.3.0 (300) added
- * `wait_limit_ns` and `inject_wait_timeout` after it, and topk_last_status.
+ * `wait_limit_ns`, `inject_wait_timeout` and `recall` after it, `shortfalls`
+ * at the end of topk_stats_t, and topk_last_status.
  * Fill the struct with topk_options_init from the same version's library. */
 int topk_version(void);
 

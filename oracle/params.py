@@ -125,3 +125,23 @@ def negative_hypergeometric_moments(n: int, s: int, t: int):
     mean = (n + 1) / (s + 1) * t
     var = t * (s - t + 1) * (n + 1) * (n - s) / ((s + 1) ** 2 * (s + 2))
     return mean, var
+
+
+def recall_rank(k: int, recall: float) -> int:
+    """The rank the threshold targets under relaxed recall: ceil(recall * k) (k when exact)."""
+    if not 0.0 < recall < 1.0:
+        return k
+    return max(1, min(k, math.ceil(recall * k - 1e-9)))
+
+
+def exact_relaxed(n: int, k: int, eps: float, recall: float, s_min: int = S_MIN_DEFAULT,
+                  s_max: int = S_MAX_DEFAULT, cost_ratio: float = COST_RATIO_DEFAULT):
+    """Relaxed recall (Prof-K paper, abstract: recovering e.g. 95% of the true
+    top-k): the same S, t chosen so that fewer than ceil(recall*k) survivors
+    occur with probability <= eps/2, and M so that the buffer (which must hold
+    k) overflows with probability <= eps/2.  Returns (S, t, M)."""
+    s = sample_size(n, k, eps, s_min, s_max, cost_ratio)
+    t = exact_t(n, recall_rank(k, recall), s, eps)
+    if t == 0:
+        return s, 0, n
+    return s, t, exact_m(n, k, s, t, eps)

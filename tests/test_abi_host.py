@@ -130,3 +130,24 @@ def test_random_plan_grid_parity(lib):
         p = _plan(lib, n, k, eps)
         if p.path == 2:
             assert (p.S, p.t, p.M) == oparams.exact(n, k, eps), (n, k, eps)
+
+
+@pytest.mark.parametrize("n,k,eps,recall", [(1 << 28, 131072, 1e-3, 0.95), (1 << 26, 10000, 1e-3, 0.9),
+                                            (1 << 20, 1000, 0.2, 0.9), (1 << 28, 1024, 1e-6, 0.5),
+                                            (1 << 24, 100, 1e-3, 0.999)])
+def test_relaxed_recall_rule_parity_with_oracle(lib, n, k, eps, recall):
+    """Relaxed recall: t for rank ceil(recall*k), M for k (the buffer's size), same S."""
+    from top_selection_prof_gb300 import _lib
+    opt = _lib.TopkOptions()
+    lib.topk_options_init(ctypes.byref(opt))
+    opt.recall = recall
+    p = _lib.TopkPlan()
+    assert lib.topk_plan(n, k, eps, ctypes.byref(opt), ctypes.byref(p)) == 0
+    s, t, m = oparams.exact_relaxed(n, k, eps, recall)
+    kt = oparams.recall_rank(k, recall)
+    assert p.path == 2 and (p.S, p.t, p.M) == (s, t, m)
+    # the recall target's failure bound and minimality, and t never above the exact rule's
+    assert oparams.p_recall_fail(n, kt, s, t) <= eps / 2
+    assert t == 1 or oparams.p_recall_fail(n, kt, s, t - 1) > eps / 2
+    assert abs(p.p_recall_fail - oparams.p_recall_fail(n, kt, s, t)) <= 1e-9 * eps + 1e-12
+    assert t <= oparams.exact(n, k, eps)[1]

@@ -140,7 +140,9 @@ def test_repeated_calls_and_streams():
 @pytest.mark.parametrize("kind,rows,n,k,eps,global_,expect", [
     ("pareto15", 1, 1 << 22, 1024, 1e-6, False, 3),            # sample + threshold, filter, refinement
     ("relu_normal_bf16", 256, 65536, 100000, 1e-3, True, 4),   # ... grid refinement + bin sort
-    ("ties1000", 5, 1 << 22, 12000, 1e-3, False, 4),           # five rows: refinement cluster + bin sort
+    # five rows: fallback kernel (a miss in one of five clusters is expected to
+    # cost more than the launch), refinement cluster + bin sort
+    ("ties1000", 5, 1 << 22, 12000, 1e-3, False, 5),
     ("normal", 64, 32768, 64, 1e-3, False, 1),                 # direct: one kernel
 ])
 def test_launch_count(kind, rows, n, k, eps, global_, expect):
@@ -193,14 +195,14 @@ def test_grid_refinement_repeated_calls_alternate_control_words():
         assert_same(v, i, ov, oi, "rep %d" % rep)
 
 
-@pytest.mark.parametrize("kind,rows,n,k,global_,cluster", [
-    ("relu_normal_bf16", 64, 65536, 20000, True, 1),   # one selection, large k: the grid refinement
-    ("ties1000", 5, 1 << 22, 12000, False, 2),          # five selections: a refinement cluster per row
+@pytest.mark.parametrize("kind,rows,n,k,global_,cluster,launches", [
+    ("relu_normal_bf16", 64, 65536, 20000, True, 1, 4),   # one selection, large k: the grid refinement
+    ("ties1000", 5, 1 << 22, 12000, False, 2, 5),          # five selections: a refinement cluster per row
 ])
-def test_large_k_refinement_route(kind, rows, n, k, global_, cluster):
+def test_large_k_refinement_route(kind, rows, n, k, global_, cluster, launches):
     x = workloads.make(kind, rows, n, seed=15)
     st = _check(x, k, eps=1e-3, global_=global_)
-    assert st["cluster"] == cluster and st["launches"] == 4, st
+    assert st["cluster"] == cluster and st["launches"] == launches, st
 
 
 def test_grid_refinement_more_rows_after_fewer():

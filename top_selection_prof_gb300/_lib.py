@@ -24,7 +24,7 @@ class TopkOptions(ctypes.Structure):
                 ("rule", ctypes.c_int), ("path", ctypes.c_int), ("seed", ctypes.c_uint64),
                 ("counter", ctypes.c_int64), ("force_miss", ctypes.c_int), ("m_override", ctypes.c_int64),
                 ("t_override", ctypes.c_int64), ("events", ctypes.c_void_p * 6), ("unsorted", ctypes.c_int),
-                ("wait_limit_ns", ctypes.c_int64), ("inject_wait_timeout", ctypes.c_int)]
+                ("wait_limit_ns", ctypes.c_int64), ("inject_wait_timeout", ctypes.c_int), ("recall", ctypes.c_double)]
 
 
 class TopkStats(ctypes.Structure):
@@ -32,7 +32,7 @@ class TopkStats(ctypes.Structure):
                 ("t", ctypes.c_int64), ("M", ctypes.c_int64), ("R", ctypes.c_int64),
                 ("misses", ctypes.c_int64), ("tau", ctypes.c_uint64), ("tau_index", ctypes.c_int64),
                 ("seed", ctypes.c_uint64), ("counter", ctypes.c_int64), ("cluster", ctypes.c_int),
-                ("launches", ctypes.c_int)]
+                ("launches", ctypes.c_int), ("shortfalls", ctypes.c_int64)]
 
 
 class TopkPlan(ctypes.Structure):

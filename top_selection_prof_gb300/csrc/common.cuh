@@ -140,6 +140,10 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p, uint64_t policy) {
   return v;
 }
 
+// Four consecutive 32-bit counters in one 16-byte load through L2 (p 16-byte
+// aligned): a block reading a counter table then requests each line once.
+__device__ __forceinline__ uint4 ldcg_u4(const unsigned* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

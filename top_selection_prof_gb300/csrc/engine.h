@@ -1,9 +1,18 @@
 // Internal interface between the C ABI (topk_api.cu) and the kernel
-// translation units.  Host code only; no torch types anywhere.
+// translation units: host declarations, constants, and a few functions both
+// sides use.  No torch types anywhere.
 #pragma once
 
 #include <cstdint>
 #include <cuda_runtime.h>
+
+// Functions both the host and the kernels use (this header is also compiled
+// by the host compiler, which knows no CUDA qualifiers).
+#ifdef __CUDACC__
+#define TK_HOST_DEVICE __host__ __device__
+#else
+#define TK_HOST_DEVICE
+#endif
 
 namespace tk {
 
@@ -30,13 +39,16 @@ bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double p_
 // with-replacement sampler (the exact tails of Lemma 1's counting argument).
 double plan_miss_probability(int64_t n, int64_t k, int64_t S, int64_t t, int64_t M);
 // Programmatic dependent launch for one pipeline edge (see params.cpp).
-constexpr unsigned kPdlTau = 1, kPdlFilter = 2, kPdlFallback = 4, kPdlRefine = 8;
+constexpr unsigned kPdlTau = 1, kPdlFilter = 2, kPdlFallback = 4, kPdlRefine = 8, kPdlGridRefine = 16;
 bool pdl_edge(unsigned bit);
 struct ParamRule {
   int64_t s_min = 32768, s_max = 131072;
   double cost_ratio = 1.0;
   int rule = 0;  // 0 exact tails, 1 Algorithm 1 as printed
+  double recall = 0.0;  // in (0, 1): t is chosen for rank ceil(recall * k) (relaxed recall)
 };
+// The rank the threshold is chosen for: k, or ceil(recall * k) under relaxed recall.
+int64_t recall_rank(int64_t k, double recall);
 double inv_normal_upper(double q);  // x with P[Z > x] = q
 double binom_upper_tail(int64_t s, double p, int64_t t);  // P[Bin(s,p) >= t]
 double binom_lower_tail(int64_t s, double p, int64_t t);  // P[Bin(s,p) <= t]
@@ -49,7 +61,7 @@ bool choose_params(int64_t n, int64_t k, double eps, const ParamRule& pr, int64_
 struct DevHeader {
   unsigned barrier[2];         // grid barrier of the fallback: arrivals, generation
   int status;                  // kDevOk / kDevTimeout / kDevBadState
-  int pad;
+  unsigned shortfalls;         // selections that returned fewer than k winners (relaxed recall)
   unsigned long long misses;   // selections that took the fallback
 };
 
@@ -83,6 +95,9 @@ cudaError_t launch_sample(const Problem& p, int64_t S, uint64_t seed, uint64_t c
 // kTauCtlWords words and gather kTauGather keys per selection.  ctl must be
 // zero on entry; the kernel leaves its grid barrier and counters as it found
 // them except after a timeout, so the refinement clears ctl every call.
+// refine_ctl (nullable): the grid refinement's control words of this call
+// (kRefineGridCtlWords per selection, zero on entry); the largest sampled key
+// of each selection is recorded there (atomic max at kRefineGridKmaxWord).
 constexpr int kTauGather = 2048;
 constexpr int kTauCtlWords = 2 + 2 * static_cast<int>(kSampleHistMaxRows);
 struct SampleTauScratch {
@@ -90,6 +105,7 @@ struct SampleTauScratch {
   unsigned* hist_zero;
   unsigned* ctl;
   uint64_t* gather;
+  unsigned* refine_ctl = nullptr;
 };
 // Whether the fused grid fits on the device at once (else launch_sample and
 // a threshold select are used).
@@ -113,7 +129,14 @@ struct FallbackScratch {
   int* status;
   unsigned long long* r_seen;  // per selection: R as the filter left it
   unsigned long long* misses;  // number of selections that fell back
-  uint64_t* tau_exact;         // per selection: exact k-th key written on a miss
+  unsigned* shortfalls;        // number of selections returned short (relaxed recall)
+  uint64_t* tau_exact;         // per selection: exact k-th key written on a miss; under relaxed
+                               // recall also the bound below which keys are padding (0: none)
+  // Relaxed recall (nullable): the sampled tau per selection.  A selection
+  // with R < k survivors (and R within the buffer) then takes no fallback:
+  // slots R..k-1 of its buffer receive the sentinel keys tau - 1 - j, which
+  // rank below every survivor and are written out as padding.
+  const uint64_t* relax_tau;
   uint64_t wait_ns;            // limit of each grid-wide wait (kWaitLimitNs unless a caller sets it)
   int stall_block;             // testing: this block leaves its first grid-wide wait without
                                // arriving, so the others' bounded wait runs out (-1: none)
@@ -121,8 +144,15 @@ struct FallbackScratch {
 constexpr int64_t kFallbackTile = 4096;
 // reserved_sms: SMs the preceding grid (the threshold select) holds; the
 // launch may overlap that grid only when it is >= 0.
+// refine_ctl (nullable): the grid refinement's control words of this call,
+// holding each selection's largest sampled key (from the fused sampler); the
+// survivors are then also counted into the histogram at
+// kRefineGridFilterHist, 2048 bins of their offset above tau: bin = 2047 -
+// ((key - tau) >> shift), or 0 when that exceeds 2046, with shift =
+// survivor_shift(tau, largest sampled key) (filter_core.cuh).
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
-                          unsigned long long* counts, int reserved_sms, cudaStream_t st);
+                          unsigned long long* counts, int reserved_sms, cudaStream_t st,
+                          unsigned* refine_ctl = nullptr);
 // force: 0 = only rows that missed, 1 = every row (fault injection / exact path).
 cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,
                             unsigned long long* counts, const FallbackScratch& fs, int force,
@@ -138,9 +168,12 @@ constexpr int kRefineGridBins = 2048;          // first-digit bins (the bin sort
 constexpr int kRefineGridLevels = 6;           // 11-bit digits of a key of up to 64 bits
 constexpr int64_t kRefineGridMaxSel = 4;       // selections one grid refines
 // Control words per selection: NOT of the smallest and the largest key (2 x
-// 64 bits), the boundary bin's placed winners, then one counter per bin and
-// digit level.
-constexpr int64_t kRefineGridCtlWords = 8 + int64_t(kRefineGridLevels) * kRefineGridBins;
+// 64 bits), the boundary bin's placed winners, the largest sampled key (64
+// bits at kRefineGridKmaxWord), then one counter per bin and digit level,
+// then the filter's survivor histogram (kRefineGridFilterHist).
+constexpr int64_t kRefineGridKmaxWord = 6;
+constexpr int64_t kRefineGridFilterHist = 8 + int64_t(kRefineGridLevels) * kRefineGridBins;
+constexpr int64_t kRefineGridCtlWords = kRefineGridFilterHist + kRefineGridBins;
 struct RefineGridScratch {
   unsigned* ctl;          // this call's control words: kRefineGridCtlWords per selection, zero on entry
   unsigned* ctl_next;     // the other copy (kRefineGridMaxSel selections), cleared here for the next call
@@ -155,7 +188,19 @@ struct RefineGridScratch {
   int unsorted = 0;
   void* out_vals = nullptr;
   int64_t* out_idx = nullptr;
+  // Non-null when the filter counted its survivors into the histogram at
+  // kRefineGridFilterHist of ctl (and the sampler recorded the largest
+  // sampled key at kRefineGridKmaxWord): the sampled tau per selection.  The
+  // partition then takes the bin totals from that histogram (no min / max
+  // pass, no grid barrier) when no selection missed, the top bin is empty
+  // and the boundary bin fits the exchange buffer.
+  const uint64_t* tau = nullptr;
 };
+// The padding of relaxed recall for one output element: value bits of -inf
+// (+inf when the smallest are selected), as f32 or bf16 bits.
+inline uint32_t pad_bits(int dtype, bool largest) {
+  return dtype == 0 ? (largest ? 0xFF800000u : 0x7F800000u) : (largest ? 0xFF80u : 0x7F80u);
+}
 // Largest buffer capacity (keys per selection) the grid refinement takes, or
 // 0 when it does not apply (too many selections).
 int64_t refine_grid_capacity(const Problem& p);
@@ -196,8 +241,18 @@ struct SelectJob {
   unsigned* clear_words = nullptr;  // want_topk: n_clear words zeroed after the earlier grids finish
   int n_clear = 0;
   int* launch_count = nullptr;      // nullable: incremented once per kernel launched
+  // relaxed recall (nullable): per selection the bound below which keys are
+  // the fallback's padding sentinels (the fallback's tau_exact words), written
+  // as index -1 and -inf (+inf)
+  const uint64_t* relax_tau = nullptr;
 };
 int64_t select_binfo_words(int64_t k);  // 0 when k is too small for the bin sort
+// Output places one bin-sort block owns, and the words of bin information
+// per selection (bin starts, the digit, one descriptor per chunk: binfo.cuh).
+constexpr int64_t kBinSortChunk = 512;
+TK_HOST_DEVICE inline int64_t binfo_words(int64_t k) {
+  return kRefineGridBins + 8 + 6 * ((k + kBinSortChunk - 1) / kBinSortChunk);
+}
 // The bin sort alone (job: r = k, xbuf, xbuf_stride, binfo, status, outputs),
 // after the grid refinement has partitioned the winners.
 cudaError_t launch_bin_sort(const Problem& p, const SelectJob& job, cudaStream_t st);

@@ -50,7 +50,33 @@ struct FilterParams {
   uint64_t* buf;
   unsigned long long* counts;
   Divider tiles_per_row;  // set by the launcher for its tile size
+  // survivor histogram (HIST variants): the grid refinement's control words
+  // (kRefineGridCtlWords per selection) hold the largest sampled key and
+  // receive the counts
+  unsigned* refine_ctl = nullptr;
 };
+
+__device__ __forceinline__ unsigned long long sampled_kmax(const unsigned* refine_ctl, int64_t row) {
+  return __ldcg(reinterpret_cast<const unsigned long long*>(refine_ctl + row * kRefineGridCtlWords +
+                                                            kRefineGridKmaxWord));
+}
+
+// Bins of a survivor's offset above tau for the grid refinement: 2048 bins in
+// descending key order, bin = 2047 - ((key - tau) >> shift) while the offset
+// is below 2047 << shift, bin 0 above that.  The shift makes the span from
+// tau to the largest sampled key cover fewer than 1024 bins, so the keys
+// above the largest sampled one (about N / S of them) still have room.
+__host__ __device__ __forceinline__ int survivor_shift(uint64_t tau, uint64_t kmax) {
+  const uint64_t span = kmax > tau ? kmax - tau : 0ull;
+  int bits = 0;
+  while (bits < 64 && (span >> bits) != 0ull) ++bits;
+  return bits > 10 ? bits - 10 : 0;
+}
+__device__ __forceinline__ unsigned survivor_bin(uint64_t key, uint64_t tau, int shift) {
+  const uint64_t d = (key - tau) >> shift;  // key >= tau
+  return d >= static_cast<uint64_t>(kRefineGridBins - 1) ? 0u
+                                                          : static_cast<unsigned>(kRefineGridBins - 1) - static_cast<unsigned>(d);
+}
 
 // Element e of a packed group of raw words (VEC elements).
 template <int DT, int VEC>
@@ -160,6 +186,7 @@ struct RowTau {
   float value;    // its value (0 for the zero key)
   uint32_t v2;    // bf16: the value's bits in both halves of a word
   bool nan;       // tau's value is NaN: fall back to composite-key compares
+  int hshift;     // survivor histogram: survivor_shift(tau, largest sampled key)
 };
 
 template <int DT>
@@ -243,11 +270,12 @@ __device__ __forceinline__ uint32_t exact_mask(const uint4& v, int64_t pos, cons
 }
 
 // Appends the elements of `mask` to the warp's stage with one shared atomic;
-// what does not fit is appended to the buffer directly.
-template <int DT, int VEC>
+// what does not fit is appended to the buffer directly.  HIST: each survivor
+// is also counted into the block's histogram of its offset above tau.
+template <int DT, int VEC, bool HIST>
 __device__ __forceinline__ void lane_append(uint32_t mask, const uint4& v, int64_t pos, int ib, uint32_t flip,
                                             const Stage& st, int64_t row, int64_t cap, uint64_t* buf,
-                                            unsigned long long* counts) {
+                                            unsigned long long* counts, const RowTau& t, unsigned* sh_hist) {
   const unsigned n = __popc(mask);
   const unsigned slot = atomicAdd(st.n, n);
   const unsigned fit = slot >= static_cast<unsigned>(kWarpStage)
@@ -260,6 +288,7 @@ __device__ __forceinline__ void lane_append(uint32_t mask, const uint4& v, int64
     const int e = __ffs(mask) - 1;
     mask &= mask - 1;
     const uint64_t key = compose(Dt<DT>::key(elem<DT, VEC>(v, e)) ^ flip, static_cast<uint64_t>(pos + e), ib);
+    if (HIST) atomicAdd(&sh_hist[survivor_bin(key, t.key, t.hshift)], 1u);
     if (j < fit) {
       st.s[slot + j] = key;
     } else {
@@ -270,33 +299,67 @@ __device__ __forceinline__ void lane_append(uint32_t mask, const uint4& v, int64
   }
 }
 
-template <int DT, bool LARGEST, int VEC>
+// Adds the block's survivor histogram of one selection to the global one and
+// clears it.  Called by the whole block at the same point.
+__device__ __forceinline__ void hist_flush(unsigned* sh_hist, const FilterParams& fp, int64_t row) {
+  __syncthreads();
+  unsigned* g = fp.refine_ctl + row * kRefineGridCtlWords + kRefineGridFilterHist;
+  for (int i = threadIdx.x; i < kRefineGridBins; i += blockDim.x) {
+    const unsigned c = sh_hist[i];
+    if (c) {
+      atomicAdd(g + i, c);
+      sh_hist[i] = 0u;
+    }
+  }
+  __syncthreads();
+}
+
+template <int DT, bool LARGEST, int VEC, bool HIST>
 __device__ __forceinline__ void test_group(const uint4& v, int64_t pos, const RowTau& t, const FilterParams& fp,
-                                           const Stage& st, int64_t row) {
+                                           const Stage& st, int64_t row, unsigned* sh_hist) {
   if (group_candidate<DT, LARGEST, VEC>(v, t.value) || t.nan) {
     const uint32_t mask = exact_mask<DT, LARGEST, VEC>(v, pos, t, fp.ib, fp.flip);
-    if (mask) lane_append<DT, VEC>(mask, v, pos, fp.ib, fp.flip, st, row, fp.cap, fp.buf, fp.counts);
+    if (mask)
+      lane_append<DT, VEC, HIST>(mask, v, pos, fp.ib, fp.flip, st, row, fp.cap, fp.buf, fp.counts, t, sh_hist);
   }
 }
 
 // Filter the tiles [tile_begin, tile_end) (stride tile_step) of the flattened
 // tile space (selection-major).  Used by the filter kernel and the fallback.
-template <int DT, bool LARGEST, int VEC>
+// HIST: survivors are also counted into sh_hist (block shared memory,
+// kRefineGridBins counters, zero on entry), flushed to fp.hist per selection.
+// Every thread of the block must call this with the same tiles (the block
+// synchronises where the selection changes).
+template <int DT, bool LARGEST, int VEC, bool HIST = false>
 __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t tile_end,
-                             int64_t tile_step, const Stage& st) {
+                             int64_t tile_step, const Stage& st, unsigned* sh_hist = nullptr) {
   using T = typename Dt<DT>::storage;
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   const int64_t tiles_per_row = (fp.len + kTile - 1) / kTile;
   const uint64_t pol = l2_evict_first_policy();
+  // tau (and the largest sampled key) of the current selection: one thread
+  // loads them and the block reads shared memory -- a load by every thread of
+  // every block would queue thousands of requests on the same L2 line
+  __shared__ uint64_t s_row_words[2];
   int64_t cur_row = -1;
   RowTau t{};
   for (int64_t tile = tile_begin; tile < tile_end; tile += tile_step) {
     const int64_t row = static_cast<int64_t>(divide(static_cast<uint64_t>(tile), fp.tiles_per_row));
     const int64_t base = (tile - row * tiles_per_row) * kTile;
     if (row != cur_row) {
-      if (cur_row >= 0) stage_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
+      if (cur_row >= 0) {
+        stage_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
+        if (HIST) hist_flush(sh_hist, fp, cur_row);
+      }
       cur_row = row;
-      t = row_tau<DT>(__ldcg(fp.tau + row), fp.ib, fp.flip);
+      if (threadIdx.x == 0) {
+        s_row_words[0] = __ldcg(fp.tau + row);
+        if (HIST) s_row_words[1] = sampled_kmax(fp.refine_ctl, row);
+      }
+      __syncthreads();
+      t = row_tau<DT>(s_row_words[0], fp.ib, fp.flip);
+      t.hshift = HIST ? survivor_shift(t.key, s_row_words[1]) : 0;
+      __syncthreads();  // (the words are rewritten at the next selection)
     }
     const T* xr = static_cast<const T*>(fp.x) + row * fp.len;
     uint4 v[kFilterUnroll];
@@ -306,14 +369,15 @@ __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t
         v[u] = load_group<DT, VEC>(xr + base + (u * kFilterBlock + threadIdx.x) * VEC, pol);
 #pragma unroll
       for (int u = 0; u < kFilterUnroll; ++u)
-        test_group<DT, LARGEST, VEC>(v[u], base + (u * kFilterBlock + threadIdx.x) * VEC, t, fp, st, row);
+        test_group<DT, LARGEST, VEC, HIST>(v[u], base + (u * kFilterBlock + threadIdx.x) * VEC, t, fp, st, row,
+                                           sh_hist);
     } else {  // the last, partial tile of a selection
 #pragma unroll
       for (int u = 0; u < kFilterUnroll; ++u) {
         const int64_t pos = base + (u * kFilterBlock + threadIdx.x) * VEC;
         if (pos < fp.len) {
           v[u] = load_group<DT, VEC>(xr + pos, pol);
-          test_group<DT, LARGEST, VEC>(v[u], pos, t, fp, st, row);
+          test_group<DT, LARGEST, VEC, HIST>(v[u], pos, t, fp, st, row, sh_hist);
         }
       }
     }
@@ -322,7 +386,10 @@ __device__ void filter_tiles(const FilterParams& fp, int64_t tile_begin, int64_t
     if (__shfl_sync(kFull, *st.n, 0) >= static_cast<unsigned>(kWarpStage / 2))
       stage_flush(st, row, fp.cap, fp.buf, fp.counts);
   }
-  if (cur_row >= 0) stage_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
+  if (cur_row >= 0) {
+    stage_flush(st, cur_row, fp.cap, fp.buf, fp.counts);
+    if (HIST) hist_flush(sh_hist, fp, cur_row);
+  }
 }
 
 }  // namespace

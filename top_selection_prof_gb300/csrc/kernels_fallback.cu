@@ -13,6 +13,7 @@
 // partitions the candidates of a few selections with many winners (below).
 #include <cooperative_groups.h>
 
+#include "binfo.cuh"
 #include "filter_core.cuh"
 
 namespace tk {
@@ -149,6 +150,7 @@ __device__ int fallback_body(const FallbackParams& a, uint64_t (*stage)[kWarpSta
   __shared__ unsigned long long s_bucket_info[2];
   __shared__ int s_tile_found;
   __shared__ unsigned long long s_found_pos;
+  __shared__ unsigned long long s_row_words[2];
 
   // the re-filter compares against the exact threshold found here
   FilterParams fp = a.fp;
@@ -161,12 +163,37 @@ __device__ int fallback_body(const FallbackParams& a, uint64_t (*stage)[kWarpSta
 
   int missed = 0;
   for (int64_t row = 0; row < fp.nsel; ++row) {
-    const unsigned long long R = __ldcg(fp.counts + row);
-    const bool miss = a.force || R < static_cast<unsigned long long>(a.k) ||
-                      R > static_cast<unsigned long long>(fp.cap);
+    // (one thread loads the words the whole grid reads; the block shares them)
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      s_row_words[0] = __ldcg(fp.counts + row);
+      s_row_words[1] = fs.relax_tau ? __ldcg(fs.relax_tau + row) : 0ull;
+    }
+    __syncthreads();
+    const unsigned long long R = s_row_words[0];
+    const unsigned long long kk = static_cast<unsigned long long>(a.k);
+    // Relaxed recall: fewer than k survivors are the exact top-R and are
+    // returned as they are.  Slots R..k-1 of the buffer get the sentinel keys
+    // tau - 1 - j (below every survivor, distinct), written out as padding.
+    // (Needs tau >= k for the sentinels; otherwise the row takes the exact
+    // fallback like any other miss.)
+    const uint64_t rtau = s_row_words[1];
+    const bool shortfall = fs.relax_tau && !a.force && R < kk && rtau >= kk;
+    const bool miss = a.force || (R < kk && !shortfall) || R > static_cast<unsigned long long>(fp.cap);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
       fs.r_seen[row] = R;
       if (miss) atomicAdd(fs.misses, 1ull);
+      if (shortfall) atomicAdd(fs.shortfalls, 1u);
+      // the bound below which keys are padding (a missed row: its exact
+      // k-th key, written below, which no key of the rebuilt buffer is under)
+      if (fs.relax_tau && !miss) fs.tau_exact[row] = shortfall ? rtau : 0ull;
+    }
+    if (shortfall) {
+      uint64_t* dst = fp.buf + row * fp.cap;
+      for (int64_t j = static_cast<int64_t>(R) + gtid; j < a.k; j += nthreads)
+        dst[j] = rtau - 1ull - static_cast<uint64_t>(j - static_cast<int64_t>(R));
+      missed = 1;  // the buffer changed
+      continue;
     }
     if (!miss) continue;
     missed = 1;
@@ -412,12 +439,15 @@ struct RefineGridParams {
 __device__ bool find_rank_bin(const unsigned* g, unsigned long long rank, unsigned* starts, unsigned* warp_sums,
                               unsigned* info) {
   __shared__ unsigned s_total;
+  static_assert(kPartPer == 8, "two 16-byte loads per thread");
   unsigned c[kPartPer], sum = 0;
-#pragma unroll
-  for (int q = 0; q < kPartPer; ++q) {
-    c[q] = __ldcg(g + threadIdx.x * kPartPer + q);
-    sum += c[q];
+  {
+    const uint4 lo = ldcg_u4(g + threadIdx.x * kPartPer), hi = ldcg_u4(g + threadIdx.x * kPartPer + 4);
+    c[0] = lo.x; c[1] = lo.y; c[2] = lo.z; c[3] = lo.w;
+    c[4] = hi.x; c[5] = hi.y; c[6] = hi.z; c[7] = hi.w;
   }
+#pragma unroll
+  for (int q = 0; q < kPartPer; ++q) sum += c[q];
   if (threadIdx.x == 0) info[0] = ~0u;
   unsigned run = block_exclusive_scan(sum, warp_sums, &s_total);
 #pragma unroll
@@ -438,8 +468,14 @@ __device__ bool find_rank_bin(const unsigned* g, unsigned long long rank, unsign
 // One winner to its output slot: the position, and the input's own bits (the
 // key gives them back except for zeros and NaNs, whose bits are read from x).
 __device__ __forceinline__ void write_winner(const FilterParams& fp, const RefineGridScratch& rg, int64_t row,
-                                             int64_t k, int64_t slot, uint64_t key) {
+                                             int64_t k, int64_t slot, uint64_t key, uint64_t pad_below) {
   const int64_t oi = row * k + slot;
+  if (key < pad_below) {  // a padding sentinel of relaxed recall
+    rg.out_idx[oi] = -1;
+    if (rg.unsorted == 1) static_cast<uint32_t*>(rg.out_vals)[oi] = fp.flip ? 0x7F800000u : 0xFF800000u;
+    else static_cast<uint16_t*>(rg.out_vals)[oi] = static_cast<uint16_t>(fp.flip ? 0x7F80u : 0xFF80u);
+    return;
+  }
   const uint64_t pos = position_of(key, fp.ib);
   rg.out_idx[oi] = static_cast<int64_t>(pos);
   const uint32_t vk = vkey_of(key, fp.ib) ^ fp.flip;
@@ -456,7 +492,8 @@ __device__ __forceinline__ void write_winner(const FilterParams& fp, const Refin
   }
 }
 
-__device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* cache, unsigned char* dsm) {
+__device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* cache, unsigned char* dsm,
+                              bool hist_ok) {
   const FilterParams& fp = a.fb.fp;
   const FallbackScratch& fs = a.fb.fs;
   const RefineGridScratch& rg = a.rg;
@@ -477,45 +514,116 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   unsigned* g_lev = ctl + 8;
   const int tid = threadIdx.x;
 
-  // ---- the block's slice, cached; the smallest and largest key over the grid
-  const unsigned long long R = __ldcg(fp.counts + row);
-  const int64_t n = R < static_cast<unsigned long long>(fp.cap) ? static_cast<int64_t>(R) : fp.cap;
+  // ---- the filter's histogram of the survivors' offsets above tau, when it
+  // was kept and the buffer holds exactly the survivors it counted (no miss):
+  // it gives every bin's total at once.  Usable when its top bin is empty
+  // (every offset below 2047 << shift, so the bins are a plain digit of key -
+  // tau) and the boundary bin fits the exchange buffer after the bins above.
+  // the words every block reads, loaded by one thread each and shared: R,
+  // the relaxed-recall tau, tau and the largest sampled key
+  __shared__ unsigned long long s_words[4];
+  if (tid == 0) {
+    s_words[0] = __ldcg(fp.counts + row);
+    s_words[1] = fs.relax_tau ? __ldcg(fs.relax_tau + row) : 0ull;
+    s_words[2] = hist_ok ? __ldcg(rg.tau + row) : 0ull;
+    s_words[3] = hist_ok ? sampled_kmax(rg.ctl, row) : 0ull;
+  }
+  bool fast = false;
+  unsigned bb = 0, bb_start = 0, bb_tot = 0;
+  if (hist_ok) {
+    const unsigned* fh = ctl + kRefineGridFilterHist;
+    if (find_rank_bin(fh, k, bst, s_ws, s_info)) {  // (synchronises the block)
+      bb = s_info[0];
+      bb_start = s_info[1];
+      bb_tot = s_info[2];
+      fast = bst[1] == 0u && static_cast<int64_t>(bb_start) + bb_tot <= rg.xstride;  // top bin empty
+    }
+  }
+  __syncthreads();  // s_info is rewritten below; s_words are visible
+
+  // ---- the block's slice, cached; the base and the digit of the partition
+  const unsigned long long R = s_words[0];
+  int64_t n = R < static_cast<unsigned long long>(fp.cap) ? static_cast<int64_t>(R) : fp.cap;
+  // relaxed recall: a row returned short holds sentinel keys up to slot k
+  // (the fallback's decision, recomputed here from the same words)
+  uint64_t pad_below = 0ull;
+  if (fs.relax_tau && !a.fb.force && R < k) {
+    const uint64_t rtau = s_words[1];
+    if (rtau >= k) {
+      n = static_cast<int64_t>(k);
+      pad_below = rtau;
+    }
+  }
   const int64_t sb = n * blockIdx.x / gridDim.x, se = n * (blockIdx.x + 1) / gridDim.x;
   const int cn = static_cast<int>(se - sb);  // <= kPartCache: the host checks n <= gridDim.x * kPartCache
   const uint64_t* src = fp.buf + row * fp.cap + sb;
-  unsigned long long mn = ~0ull, mx = 0ull;
-  for (int i = tid; i < cn; i += kFilterBlock) {
-    const uint64_t key = __ldcg(src + i);
-    cache[i] = key;
-    mn = key < mn ? key : mn;
-    mx = key > mx ? key : mx;
-  }
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) {
-    const unsigned long long a = __shfl_xor_sync(kFull, mn, m), b = __shfl_xor_sync(kFull, mx, m);
-    mn = a < mn ? a : mn;
-    mx = b > mx ? b : mx;
-  }
-  if (tid == 0) { s_nmin = 0ull; s_max = 0ull; }
-  __syncthreads();
-  if ((tid & 31) == 0) { atomicMax(&s_nmin, ~mn); atomicMax(&s_max, mx); }
-  __syncthreads();
-  if (tid == 0 && cn > 0) { atomicMax(g_nmin, s_nmin); atomicMax(g_max, s_max); }
-  TK_RG(3);
-  if (!grid_barrier(fs)) return false;
-  TK_RG(4);
-  // Digits are taken of key - kmin: 2048 equal slices of the keys' range.
-  // (Digits of the keys themselves below their top varying bit leave only a
-  // few non-empty bins when the candidates' values cross a power of two.)
-  // The cache holds key - kmin from here on; the order is the same.
-  const uint64_t kmin = ~__ldcg(g_nmin), kmax = __ldcg(g_max);
-  const uint64_t span = kmax - kmin;
-  const int hb = span ? 63 - __clzll(static_cast<long long>(span)) : 0;
-  const uint64_t pmask1 = hb >= 63 ? 0ull : (~0ull << (hb + 1));
+  uint64_t kmin, pmask1;
+  int shift1;
   const uint64_t prefix1 = 0ull;
-  const int shift1 = hb >= kPartDigit - 1 ? hb - (kPartDigit - 1) : 0;
-  for (int i = tid; i < cn; i += kFilterBlock) cache[i] -= kmin;
-  __syncthreads();
+  if (fast) {
+    // digits of key - tau with the filter's shift; the cache holds key - tau
+    kmin = s_words[2];
+    shift1 = survivor_shift(kmin, s_words[3]);
+    pmask1 = shift1 + kPartDigit >= 64 ? 0ull : (~0ull << (shift1 + kPartDigit));
+    // (a slice holds at most kPartCache keys: every load of the thread in flight at once)
+    constexpr int kSliceLoads = kPartCache / kFilterBlock;
+    uint64_t kv[kSliceLoads];
+#pragma unroll
+    for (int q = 0; q < kSliceLoads; ++q) {
+      const int i = tid + q * kFilterBlock;
+      kv[q] = i < cn ? __ldcg(src + i) : 0ull;
+    }
+#pragma unroll
+    for (int q = 0; q < kSliceLoads; ++q) {
+      const int i = tid + q * kFilterBlock;
+      if (i < cn) cache[i] = kv[q] - kmin;
+    }
+    __syncthreads();
+    TK_RG(3);
+  } else {
+    unsigned long long mn = ~0ull, mx = 0ull;
+    constexpr int kSliceLoads = kPartCache / kFilterBlock;
+    uint64_t kv[kSliceLoads];
+#pragma unroll
+    for (int q = 0; q < kSliceLoads; ++q) {
+      const int i = tid + q * kFilterBlock;
+      kv[q] = i < cn ? __ldcg(src + i) : 0ull;
+    }
+#pragma unroll
+    for (int q = 0; q < kSliceLoads; ++q) {
+      const int i = tid + q * kFilterBlock;
+      if (i < cn) {
+        cache[i] = kv[q];
+        mn = kv[q] < mn ? kv[q] : mn;
+        mx = kv[q] > mx ? kv[q] : mx;
+      }
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+      const unsigned long long a = __shfl_xor_sync(kFull, mn, m), b = __shfl_xor_sync(kFull, mx, m);
+      mn = a < mn ? a : mn;
+      mx = b > mx ? b : mx;
+    }
+    if (tid == 0) { s_nmin = 0ull; s_max = 0ull; }
+    __syncthreads();
+    if ((tid & 31) == 0) { atomicMax(&s_nmin, ~mn); atomicMax(&s_max, mx); }
+    __syncthreads();
+    if (tid == 0 && cn > 0) { atomicMax(g_nmin, s_nmin); atomicMax(g_max, s_max); }
+    TK_RG(3);
+    if (!grid_barrier(fs)) return false;
+    TK_RG(4);
+    // Digits are taken of key - kmin: 2048 equal slices of the keys' range.
+    // (Digits of the keys themselves below their top varying bit leave only a
+    // few non-empty bins when the candidates' values cross a power of two.)
+    // The cache holds key - kmin from here on; the order is the same.
+    kmin = ~__ldcg(g_nmin);
+    const uint64_t span = __ldcg(g_max) - kmin;
+    const int hb = span ? 63 - __clzll(static_cast<long long>(span)) : 0;
+    pmask1 = hb >= 63 ? 0ull : (~0ull << (hb + 1));
+    shift1 = hb >= kPartDigit - 1 ? hb - (kPartDigit - 1) : 0;
+    for (int i = tid; i < cn; i += kFilterBlock) cache[i] -= kmin;
+    __syncthreads();
+  }
   auto bin_of = [&](uint64_t key) { return kPartDM - static_cast<unsigned>((key >> shift1) & kPartDM); };
 
   // ---- first digit: this block's histogram, its range inside each bin
@@ -523,21 +631,35 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   __syncthreads();
   for (int i = tid; i < cn; i += kFilterBlock) atomicAdd(&mine[bin_of(cache[i])], 1u);
   __syncthreads();
-  for (int i = tid; i < kRefineGridBins; i += kFilterBlock) {
-    const unsigned c = mine[i];
-    cur[i] = c ? atomicAdd(g_lev + i, c) : 0u;
+  {
+    // every atomic of the thread in flight at once (each returns this
+    // block's offset inside one bin)
+    unsigned c[kPartPer], r[kPartPer];
+#pragma unroll
+    for (int q = 0; q < kPartPer; ++q) c[q] = mine[tid + q * kFilterBlock];
+#pragma unroll
+    for (int q = 0; q < kPartPer; ++q) r[q] = c[q] ? atomicAdd(g_lev + tid + q * kFilterBlock, c[q]) : 0u;
+#pragma unroll
+    for (int q = 0; q < kPartPer; ++q) cur[tid + q * kFilterBlock] = r[q];
   }
   TK_RG(5);
-  if (!grid_barrier(fs)) return false;
-  TK_RG(6);
-  if (!find_rank_bin(g_lev, k, bst, s_ws, s_info)) {
-    if (tid == 0) atomicCAS(fs.status, kDevOk, kDevBadState);
-    return false;
+  if (!fast) {
+    // the totals of every block's histogram
+    if (!grid_barrier(fs)) return false;
+    TK_RG(6);
+    if (!find_rank_bin(g_lev, k, bst, s_ws, s_info)) {
+      if (tid == 0) atomicCAS(fs.status, kDevOk, kDevBadState);
+      return false;
+    }
+    bb = s_info[0];
+    bb_start = s_info[1];
+    bb_tot = s_info[2];
+  } else {
+    __syncthreads();  // cur is complete
   }
   TK_RG(7);
-  const unsigned bb = s_info[0], bb_start = s_info[1], bb_tot = s_info[2];
   // (unsorted output: the exact k-th key is always found, and only winners placed)
-  const bool whole = !rg.unsorted && static_cast<int64_t>(bb_start) + bb_tot <= rg.xstride;
+  const bool whole = fast || (!rg.unsorted && static_cast<int64_t>(bb_start) + bb_tot <= rg.xstride);
   uint64_t kappa = 0ull;
   if (!whole) {
     // ---- the exact k-th key: further digits inside the boundary bin
@@ -628,15 +750,16 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
     const unsigned pos = mine[bin_of(key)] + i;
     if (pos >= xend) continue;
     if (rg.unsorted) {
-      write_winner(fp, rg, row, static_cast<int64_t>(k), pos, key + kmin);
+      write_winner(fp, rg, row, static_cast<int64_t>(k), pos, key + kmin, pad_below);
     } else {
       xb[pos] = key + kmin;
     }
   }
   if (blockIdx.x == 0 && !rg.unsorted) {
     // the bin sort's view of the partition
-    unsigned* bo = rg.binfo + row * (kRefineGridBins + 8);
+    unsigned* bo = rg.binfo + row * binfo_words(static_cast<int64_t>(k));
     for (int i = tid; i < kRefineGridBins; i += kFilterBlock) bo[i] = bst[i];
+    publish_chunks(bst, xend, static_cast<int64_t>(k), bo + kRefineGridBins + 8, tid, kFilterBlock);
     if (tid == 0) {
       bo[kRefineGridBins] = static_cast<unsigned>(prefix1);
       bo[kRefineGridBins + 1] = static_cast<unsigned>(prefix1 >> 32);
@@ -678,8 +801,9 @@ __global__ void __launch_bounds__(kFilterBlock, 2) refine_grid_kernel(RefineGrid
   // a rebuilt buffer is complete once every block has filtered its tiles
   if (missed > 0 && !grid_barrier(a.fb.fs)) return;
   uint64_t* cache = &stage[0][0];
+  const bool hist_ok = rg.tau != nullptr && !rg.unsorted && missed == 0;
   for (int64_t row = 0; row < a.fb.fp.nsel; ++row)
-    if (!partition_row(a, row, cache, part_smem)) return;
+    if (!partition_row(a, row, cache, part_smem, hist_ok)) return;
   TK_TL_END(3);
 }
 
@@ -720,7 +844,7 @@ cudaError_t launch_refine_grid_t(const RefineGridParams& a, cudaStream_t st) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_edge(kPdlFallback) ? 2 : 1;
+  cfg.numAttrs = pdl_edge(kPdlGridRefine) ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, refine_grid_kernel<DT, LARGEST, VEC>, args);
 }
 

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(256) sample_kernel(const void* __restrict__ x,
       hdr->barrier[0] = 0u;  // arrival count of the fallback's grid barrier
       hdr->status = kDevOk;
       hdr->misses = 0ull;
+      hdr->shortfalls = 0u;
     }
   }
   if (hist_add) {
@@ -115,6 +116,7 @@ struct SampleTauParams {
   DevHeader* hdr;
   SampleTauScratch sc;
   uint64_t* tau_out;
+  unsigned* refine_ctl;  // nullable: the grid refinement's control words; the largest sampled key goes there
   int64_t t;
   int q;      // blocks per selection
   int local;  // q * (t + 1) <= kTauGather: each block keeps its own top t (no grid barrier)
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
   __shared__ unsigned s_cnt;
   __shared__ int s_last;
   __shared__ uint64_t s_tau;
+  __shared__ unsigned long long s_kmax;
   TK_TL_BEGIN(0);
   TK_ST(0);
   grid_launch_dependents();
@@ -179,11 +182,15 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
       p.hdr->barrier[0] = 0u;  // arrival count of the fallback's grid barrier
       p.hdr->status = kDevOk;
       p.hdr->misses = 0ull;
+      p.hdr->shortfalls = 0u;
     }
   }
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * BLOCK + tid; i < kSampleHistHalfWords;
        i += static_cast<int64_t>(gridDim.x) * BLOCK)
     p.sc.hist_zero[i] = 0u;  // the next call's histograms
+
+  if (tid == 0) s_kmax = 0ull;
+  if (p.refine_ctl) __syncthreads();
 
   // two sampled keys per thread, kept in registers
   const bool one = 2 * pair < p.S, two = 2 * pair + 1 < p.S;
@@ -197,6 +204,20 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
     const uint32_t v1 = two ? static_cast<uint32_t>(__ldg(xr + p1)) : 0u;
     k0 = compose(Dt<DT>::key(v0) ^ p.flip, p0, p.ib);
     if (two) k1 = compose(Dt<DT>::key(v1) ^ p.flip, p1, p.ib);
+  }
+  if (p.refine_ctl) {
+    // the largest sampled key: a warp maximum, a block maximum, one atomic per block
+    unsigned long long m = k0 > k1 ? k0 : k1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(kFull, m, o);
+      m = y > m ? y : m;
+    }
+    if ((tid & 31) == 0 && m) atomicMax(&s_kmax, m);
+    __syncthreads();
+    if (tid == 0 && s_kmax)
+      atomicMax(reinterpret_cast<unsigned long long*>(p.refine_ctl + row * kRefineGridCtlWords + kRefineGridKmaxWord),
+                s_kmax);
   }
   TK_ST(1);
 
@@ -238,13 +259,17 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
     TK_ST(3 + 3 * (level < 3 ? level : 2));
     // every block reads the same totals and finds the same boundary bin
     constexpr int kPer = kSampleHistBins / BLOCK;
+    static_assert(kPer == 8, "two 16-byte loads per thread");
     unsigned c[kPer];
     unsigned long long sum = 0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      c[j] = __ldcg(h + tid * kPer + j);
-      sum += c[j];
+    {
+      // 16-byte loads: each line of the totals is requested once per block
+      const uint4 lo = ldcg_u4(h + tid * kPer), hi = ldcg_u4(h + tid * kPer + 4);
+      c[0] = lo.x; c[1] = lo.y; c[2] = lo.z; c[3] = lo.w;
+      c[4] = hi.x; c[5] = hi.y; c[6] = hi.z; c[7] = hi.w;
     }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) sum += c[j];
     if (tid == 0) s_info[0] = ~0ull;
     const unsigned long long incl = block_scan_incl(sum, s_tmp);
     unsigned long long run = incl - sum;
@@ -356,6 +381,7 @@ cudaError_t launch_sample_tau(const Problem& p, int64_t S, int64_t t, uint64_t s
   sp.hdr = hdr;
   sp.sc = sc;
   sp.tau_out = tau_out;
+  sp.refine_ctl = sc.refine_ctl;
   sp.t = t;
   sp.q = static_cast<int>(((S + 1) / 2 + kSampleBlock - 1) / kSampleBlock);
   // (one key of slack per block: equal keys at a block's bound are all kept)

@@ -29,6 +29,7 @@
 // (value descending, index ascending), so that is the output order.
 #include <cooperative_groups.h>
 
+#include "binfo.cuh"
 #include "common.cuh"
 #include "engine.h"
 #include "rank.cuh"
@@ -104,6 +105,10 @@ struct SelParams {
   int handoff;
   unsigned* clear_words;              // nullable: zeroed once every earlier grid has finished
   int n_clear;
+  // relaxed recall (nullable): per selection the bound below which keys are
+  // padding sentinels (index -1, value -inf / +inf); a selection returned
+  // short holds them in its buffer up to slot r
+  const uint64_t* relax_tau;
 };
 
 // Published per selection for the bin sort: NB bin starts, then the
@@ -266,6 +271,12 @@ constexpr int min_blocks() { return BLOCK >= 512 ? 1 : 4; }
 __device__ __forceinline__ void write_out(const SelParams& a, int64_t row, int64_t k, int64_t place,
                                           uint64_t key) {
   const int64_t oi = row * k + place;
+  if (a.relax_tau && key < __ldg(a.relax_tau + row)) {  // padding of relaxed recall
+    a.out_idx[oi] = -1;
+    if (a.key_bits == 32) static_cast<uint32_t*>(a.out_vals)[oi] = a.flip ? 0x7F800000u : 0xFF800000u;
+    else static_cast<uint16_t*>(a.out_vals)[oi] = static_cast<uint16_t>(a.flip ? 0x7F80u : 0xFF80u);
+    return;
+  }
   const uint64_t pos = position_of(key, a.ib);
   a.out_idx[oi] = static_cast<int64_t>(pos);
   const uint32_t vk = vkey_of(key, a.ib) ^ a.flip;
@@ -607,6 +618,8 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   if (from_buf && a.counts) {
     const unsigned long long c = __ldcg(a.counts + row);
     if (c < static_cast<unsigned long long>(valid)) valid = static_cast<int64_t>(c);
+    // (relaxed recall: a row returned short holds padding sentinels up to slot r)
+    if (a.relax_tau && valid < a.r && a.r <= a.key_stride) valid = a.r;
   }
   // slices start at even positions so key slices can be copied in 16-byte units
   const int64_t sb = (valid * crank / G) & ~int64_t(1);
@@ -1148,8 +1161,9 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
       if (a.handoff) {
         // the bin sort grid takes over from here: publish the bins
         if (crank == 0) {
-          unsigned* bo = a.binfo + row * kBinInfoWords;
+          unsigned* bo = a.binfo + row * binfo_words(k);
           for (int i = tid; i < NB; i += BLOCK) bo[i] = bst[i];
+          publish_chunks(bst, static_cast<unsigned>(xend), k, bo + NB + 8, tid, BLOCK);
           if (tid == 0) {
             bo[NB] = static_cast<unsigned>(prefix1);
             bo[NB + 1] = static_cast<unsigned>(prefix1 >> 32);
@@ -1347,13 +1361,12 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
 // leading bits.  Many small blocks share the sort that one cluster would
 // otherwise do alone.
 constexpr int kBinSortBlock = 256;
-constexpr int kBinSortPlaces = 512;
+constexpr int kBinSortPlaces = static_cast<int>(kBinSortChunk);
 constexpr int kBinSortCap = 2048;  // keys one block sorts
 constexpr int kBinSortGroups = 4096;  // 12 leading varying bits: small groups even for few values
 constexpr int kBinSortScratch = 3 * kBinSortGroups;  // (also covers the LSD sort's counters)
 static_assert(kBinSortScratch >= (kBinSortBlock / 32) * 256 + 2 * 256 + (kBinSortBlock / 256) * 256, "lsd");
-constexpr size_t kBinSortSmem = sizeof(unsigned) * kBinInfoBins + 2 * sizeof(uint64_t) * kBinSortCap +
-                                sizeof(unsigned) * kBinSortScratch;
+constexpr size_t kBinSortSmem = 2 * sizeof(uint64_t) * kBinSortCap + sizeof(unsigned) * kBinSortScratch;
 
 struct BinSortParams {
   SelParams a;  // the refinement's parameters: r = k, xbuf, binfo, outputs
@@ -1393,8 +1406,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   constexpr unsigned DM = 255u;  // 8-bit sub-digits
   const SelParams& a = bp.a;
   extern __shared__ __align__(16) unsigned char smem[];
-  unsigned* bst = reinterpret_cast<unsigned*>(smem);
-  uint64_t* bufA = reinterpret_cast<uint64_t*>(smem + sizeof(unsigned) * NB);
+  uint64_t* bufA = reinterpret_cast<uint64_t*>(smem);
   uint64_t* bufB = bufA + kBinSortCap;
   unsigned* scr = reinterpret_cast<unsigned*>(bufB + kBinSortCap);
   __shared__ unsigned long long s_tmp[32];
@@ -1402,40 +1414,37 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   __shared__ unsigned s_cnt;
   grid_dependency_wait();  // the partition comes from the previous grid
   const int tid = threadIdx.x;
-  if (tid == 0) s_info[0] = static_cast<unsigned long long>(*reinterpret_cast<volatile int*>(a.status));
-  __syncthreads();
-  if (s_info[0] != static_cast<unsigned long long>(kDevOk)) return;  // the refinement failed
   const int64_t row = blockIdx.x / bp.q;
   const int64_t k = a.r;
   const int64_t my0 = static_cast<int64_t>(blockIdx.x % bp.q) * kBinSortPlaces;
   if (my0 >= k) return;
   const int64_t my1 = my0 + kBinSortPlaces < k ? my0 + kBinSortPlaces : k;
-  const unsigned* bi = a.binfo + row * kBinInfoWords;
-  for (int i = tid; i < NB; i += BLOCK) bst[i] = __ldcg(bi + i);
-  const uint64_t prefix1 = static_cast<uint64_t>(__ldcg(bi + NB)) | (static_cast<uint64_t>(__ldcg(bi + NB + 1)) << 32);
-  const uint64_t pmask1 = static_cast<uint64_t>(__ldcg(bi + NB + 2)) | (static_cast<uint64_t>(__ldcg(bi + NB + 3)) << 32);
-  const int shift1 = static_cast<int>(__ldcg(bi + NB + 4));
-  const int64_t xend = static_cast<int64_t>(__ldcg(bi + NB + 5));  // keys placed: >= k
+  const unsigned* bi = a.binfo + row * binfo_words(k);
+  // one round of loads, one word per thread, shared through shared memory:
+  // the status word, the digit description and this block's chunk
+  // descriptor (its first and last bins with their bounds)
+  __shared__ unsigned s_words[1 + 8 + kChunkWords];
+  if (tid == 0) s_words[0] = static_cast<unsigned>(__ldcg(a.status));
+  else if (tid <= 8) s_words[tid] = __ldcg(bi + NB + (tid - 1));
+  else if (tid <= 8 + kChunkWords) s_words[tid] = __ldcg(bi + NB + 8 + (blockIdx.x % bp.q) * kChunkWords + (tid - 9));
+  __syncthreads();
+  if (s_words[0] != static_cast<unsigned>(kDevOk)) return;  // the refinement failed
+  unsigned hw[8], cd[kChunkWords];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) hw[q] = s_words[1 + q];
+#pragma unroll
+  for (int q = 0; q < kChunkWords; ++q) cd[q] = s_words[9 + q];
+  const uint64_t prefix1 = static_cast<uint64_t>(hw[0]) | (static_cast<uint64_t>(hw[1]) << 32);
+  const uint64_t pmask1 = static_cast<uint64_t>(hw[2]) | (static_cast<uint64_t>(hw[3]) << 32);
+  const int shift1 = static_cast<int>(hw[4]);
   // digits, prefixes and masks are of key - kbase
-  const uint64_t kbase = static_cast<uint64_t>(__ldcg(bi + NB + 6)) | (static_cast<uint64_t>(__ldcg(bi + NB + 7)) << 32);
+  const uint64_t kbase = static_cast<uint64_t>(hw[6]) | (static_cast<uint64_t>(hw[7]) << 32);
   const uint64_t* xb = a.xbuf + row * a.xstride;
-  if (tid == 0) { s_info[0] = 0; s_info[1] = 0; }
-  __syncthreads();
-  auto bin_end = [&](unsigned b) -> int64_t {
-    const int64_t e = (b + 1 < static_cast<unsigned>(NB)) ? static_cast<int64_t>(bst[b + 1]) : xend;
-    return e < xend ? e : xend;
-  };
-  // first-digit bins holding places my0 and my1 - 1
-  for (int b = tid; b < NB; b += BLOCK) {
-    const int64_t bs = bst[b], be = bin_end(static_cast<unsigned>(b));
-    if (bs <= my0 && my0 < be) s_info[0] = static_cast<unsigned long long>(b);
-    if (bs <= my1 - 1 && my1 - 1 < be) s_info[1] = static_cast<unsigned long long>(b);
-  }
-  __syncthreads();
+  // the first-digit bins holding places my0 and my1 - 1, and their bounds
+  const unsigned bfirst = cd[0], blast = cd[1];
+  const int64_t first_s = cd[2], first_e = cd[3], last_s = cd[4], last_e = cd[5];
   TK_BSP(1);
-  const unsigned bfirst = static_cast<unsigned>(s_info[0]), blast = static_cast<unsigned>(s_info[1]);
-  __syncthreads();
-  const int64_t r0 = bst[bfirst] < static_cast<unsigned>(k) ? bst[bfirst] : k, r1 = bin_end(blast);
+  const int64_t r0 = first_s < k ? first_s : k, r1 = last_e;
   uint64_t hi_key = ~0ull, lo_key = 0ull;
   int64_t place0 = r0, place1 = r1;
   unsigned cut_iters = 0;
@@ -1443,10 +1452,10 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
     const int64_t lim = (kBinSortCap - (my1 - my0)) / 2;
     unsigned* lh = scr;  // 256 counters
     // cut bin b down to the 8-bit sub-bin (and so on) holding place p
-    auto cut = [&](unsigned b, int64_t p, uint64_t& pre, uint64_t& msk, int64_t& s0, int64_t& s1) -> bool {
+    auto cut = [&](unsigned b, int64_t bs, int64_t be, int64_t p, uint64_t& pre, uint64_t& msk, int64_t& s0,
+                   int64_t& s1) -> bool {
       pre = prefix1 | (static_cast<uint64_t>(2047u - b) << shift1);
       msk = pmask1 | (2047ull << shift1);
-      const int64_t bs = bst[b], be = bin_end(b);
       s0 = bs;
       s1 = be;
       int sh = shift1;
@@ -1482,13 +1491,13 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
     };
     uint64_t pre, msk;
     int64_t s0, s1;
-    bool ok = cut(bfirst, my0, pre, msk, s0, s1);
+    bool ok = cut(bfirst, first_s, first_e, my0, pre, msk, s0, s1);
     hi_key = pre | ~msk;
     place0 = s0;
-    ok = ok && cut(blast, my1 - 1, pre, msk, s0, s1);
+    ok = ok && cut(blast, last_s, last_e, my1 - 1, pre, msk, s0, s1);
     lo_key = pre;
     place1 = s1;
-    TK_BS(1, cut_iters | (static_cast<unsigned>(bst[bfirst] < k ? bin_end(bfirst) - bst[bfirst] : 0) << 8));
+    TK_BS(1, cut_iters | (static_cast<unsigned>(first_s < k ? first_e - first_s : 0) << 8));
     if (!ok || place1 - place0 > kBinSortCap || place1 < place0) {
       if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
       return;
@@ -1496,7 +1505,19 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   }
   const int n_c = static_cast<int>(place1 - place0);
   if (r1 - r0 <= kBinSortCap) {
-    for (int i = tid; i < n_c; i += BLOCK) bufA[i] = __ldcg(xb + r0 + i);
+    // every load of the thread in flight at once (n_c <= kBinSortCap)
+    constexpr int kLoads = kBinSortCap / BLOCK;
+    uint64_t kv[kLoads];
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+      const int i = tid + q * BLOCK;
+      kv[q] = i < n_c ? __ldcg(xb + r0 + i) : 0ull;
+    }
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+      const int i = tid + q * BLOCK;
+      if (i < n_c) bufA[i] = kv[q];
+    }
   } else {
     if (tid == 0) s_cnt = 0u;
     __syncthreads();
@@ -1625,7 +1646,7 @@ int sm_count() {
 }  // namespace
 
 int64_t select_max_k() { return static_cast<int64_t>(kMaxCluster) * kBigP; }
-int64_t select_binfo_words(int64_t k) { return k >= kBinSortMinK ? kBinInfoWords : 0; }
+int64_t select_binfo_words(int64_t k) { return k >= kBinSortMinK ? binfo_words(k) : 0; }
 int64_t select_xbuf_stride(int64_t k) { return k >= kBinSortMinK ? 2 * k : k; }
 
 #ifdef TK_PHASE_TIMING
@@ -1663,6 +1684,7 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   a.xbuf = job.xbuf;
   a.clear_words = job.clear_words;
   a.n_clear = job.n_clear;
+  a.relax_tau = job.relax_tau;
   a.xstride = job.xbuf_stride > job.r ? job.xbuf_stride : job.r;
   a.shist = job.want_topk ? nullptr : job.sample_hist;
   if (job.want_topk && job.keys && job.check_miss) {
@@ -1732,6 +1754,7 @@ cudaError_t launch_bin_sort(const Problem& p, const SelectJob& job, cudaStream_t
   a.xstride = job.xbuf_stride;
   a.binfo = job.binfo;
   a.handoff = 1;
+  a.relax_tau = job.relax_tau;
   return launch_bin_sort_a(a, p.nsel, job.launch_count, st);
 }
 

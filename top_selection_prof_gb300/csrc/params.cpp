@@ -116,14 +116,23 @@ int64_t alg1_sample_size(int64_t n, int64_t k, double eps, const ParamRule& pr) 
   return static_cast<int64_t>(s);
 }
 
+int64_t recall_rank(int64_t k, double recall) {
+  if (!(recall > 0.0 && recall < 1.0)) return k;
+  const int64_t kt = static_cast<int64_t>(std::ceil(recall * static_cast<double>(k) - 1e-9));
+  return kt < 1 ? 1 : (kt > k ? k : kt);
+}
+
 bool choose_params(int64_t n, int64_t k, double eps, const ParamRule& pr, int64_t* S_out,
                    int64_t* t_out, int64_t* M_out) {
   const int64_t S = alg1_sample_size(n, k, eps, pr);
   const double nd = static_cast<double>(n), kd = static_cast<double>(k);
+  // relaxed recall: the threshold rank targets rank ceil(recall * k) instead
+  // of k; the buffer still has to hold k
+  const double kt = static_cast<double>(recall_rank(k, pr.recall));
   int64_t t = 0, M = 0;
   if (pr.rule == 1) {
     const double z = 2.0 * inv_normal_upper(eps / 2.0);
-    const double alpha = kd / nd;
+    const double alpha = kt / nd;
     const double Sd = static_cast<double>(S);
     const double f = 1.0 - Sd / nd;
     double tt = std::ceil(Sd * alpha + (z / 2.0) * std::sqrt(Sd * alpha * (1.0 - alpha) * f));
@@ -132,7 +141,7 @@ bool choose_params(int64_t n, int64_t k, double eps, const ParamRule& pr, int64_
     if (alpha * Sd < -std::log(eps / 2.0)) t = 1;
   } else {
     const double half = eps / 2.0;
-    const double p = (kd - 1.0) / nd;
+    const double p = (kt - 1.0) / nd;
     // smallest t in [1, S] with P[Bin(S, p) >= t] <= eps/2
     if (binom_upper_tail(S, p, S) > half) return false;
     int64_t lo = 0, hi = S;  // invariant: tail(hi) <= half, tail(lo) > half or lo == 0
@@ -187,10 +196,12 @@ bool miss_in_refine(const Problem& p, int64_t k, int64_t t, int64_t S, double p_
 
 bool pdl_edge(unsigned bit) {
   // Programmatic dependent launch per pipeline edge (bits: 1 threshold
-  // select, 2 filter, 4 fallback, 8 refinement).  On by default for the
-  // edges where it shortens the pipeline (1, 2, 8; the filter edge only
-  // where the preceding grid leaves the filter's SMs free, see
-  // overlap_sms); TOPK_PDL_MASK overrides (0 turns it off).
+  // select, 2 filter, 4 fallback, 8 refinement and bin sort, 16 grid
+  // refinement).  On by default for the edges where it shortens the
+  // pipeline (1, 2, 8; the filter edge only where the preceding grid leaves
+  // the filter's SMs free, see overlap_sms).  The grid refinement's edge
+  // gains nothing: a cooperative grid measured to start ~3 us after the
+  // filter ends either way.  TOPK_PDL_MASK overrides (0 turns it off).
   static const unsigned mask = [] {
     const char* m = std::getenv("TOPK_PDL_MASK");
     return m ? static_cast<unsigned>(std::strtoul(m, nullptr, 0)) : (kPdlTau | kPdlFilter | kPdlRefine);

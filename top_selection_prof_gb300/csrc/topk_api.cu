@@ -130,6 +130,8 @@ struct Plan {
 };
 
 
+bool relaxed_recall(const topk_options_t* o) { return o && o->recall > 0.0 && o->recall < 1.0; }
+
 ParamRule rule_of(const topk_options_t* o) {
   ParamRule pr;
   if (o) {
@@ -137,6 +139,7 @@ ParamRule rule_of(const topk_options_t* o) {
     pr.s_max = o->s_max;
     pr.cost_ratio = o->cost_ratio;
     pr.rule = o->rule;
+    pr.recall = relaxed_recall(o) ? o->recall : 0.0;
   }
   return pr;
 }
@@ -149,6 +152,7 @@ struct PlanKey {
   int64_t s_min, s_max;
   double ratio;
   int rule;
+  double recall;
   bool operator<(const PlanKey& o) const {
     if (len != o.len) return len < o.len;
     if (k != o.k) return k < o.k;
@@ -156,6 +160,7 @@ struct PlanKey {
     if (s_min != o.s_min) return s_min < o.s_min;
     if (s_max != o.s_max) return s_max < o.s_max;
     if (ratio != o.ratio) return ratio < o.ratio;
+    if (recall != o.recall) return recall < o.recall;
     return rule < o.rule;
   }
 };
@@ -167,9 +172,19 @@ struct PlanVal {
 std::mutex g_plan_mu;
 std::map<PlanKey, PlanVal> g_plans;
 
+// Probability that a selection takes the fallback: P[R < k] + P[R > M], or
+// only P[R > M] under relaxed recall (fewer survivors are returned as they are).
+double fallback_probability(int64_t len, int64_t k, int64_t S, int64_t t, int64_t M, double recall) {
+  if (recall > 0.0 && recall < 1.0) {
+    const double pm = M >= len ? 1.0 : static_cast<double>(M) / static_cast<double>(len);
+    return binom_lower_tail(S, pm, t - 1);
+  }
+  return plan_miss_probability(len, k, S, t, M);
+}
+
 bool cached_params(int64_t len, int64_t k, double eps, const ParamRule& pr, int64_t* S, int64_t* t,
                    int64_t* M, double* p_miss) {
-  const PlanKey key{len, k, eps, pr.s_min, pr.s_max, pr.cost_ratio, pr.rule};
+  const PlanKey key{len, k, eps, pr.s_min, pr.s_max, pr.cost_ratio, pr.rule, pr.recall};
   {
     std::lock_guard<std::mutex> lock(g_plan_mu);
     auto it = g_plans.find(key);
@@ -183,7 +198,7 @@ bool cached_params(int64_t len, int64_t k, double eps, const ParamRule& pr, int6
   }
   PlanVal v{};
   v.ok = choose_params(len, k, eps, pr, &v.S, &v.t, &v.M);
-  v.p_miss = v.ok && v.t >= 1 && v.t <= v.S ? plan_miss_probability(len, k, v.S, v.t, v.M) : 1.0;
+  v.p_miss = v.ok && v.t >= 1 && v.t <= v.S ? fallback_probability(len, k, v.S, v.t, v.M, pr.recall) : 1.0;
   std::lock_guard<std::mutex> lock(g_plan_mu);
   if (g_plans.size() > 4096) g_plans.clear();
   g_plans[key] = v;
@@ -211,7 +226,7 @@ int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
       const bool overridden = o && (o->t_override > 0 || o->m_override > 0);
       if (o && o->t_override > 0) t = o->t_override;
       if (o && o->m_override > 0) M = o->m_override;
-      if (overridden) p_miss = t >= 1 && t <= S ? plan_miss_probability(len, k, S, t, M) : 1.0;
+      if (overridden) p_miss = t >= 1 && t <= S ? fallback_probability(len, k, S, t, M, pr.recall) : 1.0;
       plan->S = S;
       plan->t = t;
       plan->M = M;
@@ -419,8 +434,10 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   auto* buf = reinterpret_cast<uint64_t*>(base + o_buf);
   auto* xbuf = reinterpret_cast<uint64_t*>(base + o_xbuf);
 
-  FallbackScratch fs{ghist, tiles, hdr->barrier, &hdr->status, r_seen, &hdr->misses, tau_x,
-                     kWaitLimitNs, -1};
+  // relaxed recall: fewer than k survivors are returned as they are, padded
+  const bool relaxed = plan.path == TOPK_PATH_PROFK && relaxed_recall(o);
+  FallbackScratch fs{ghist, tiles, hdr->barrier, &hdr->status, r_seen, &hdr->misses, &hdr->shortfalls, tau_x,
+                     relaxed ? tau : nullptr, kWaitLimitNs, -1};
   if (o && o->wait_limit_ns > 0) fs.wait_ns = static_cast<uint64_t>(o->wait_limit_ns);
   if (o && o->inject_wait_timeout) fs.stall_block = 0;
   const uint64_t seed = (o && o->seed) ? o->seed : kDefaultSeed;
@@ -440,6 +457,24 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     if (!o || !o->events[i]) return cudaSuccess;
     return cudaEventRecord(static_cast<cudaEvent_t>(o->events[i]), st);
   };
+  // The grid refinement's control words: two copies that alternate between
+  // its calls (the kernel clears the other one for the next call).  The copy
+  // is chosen here because the fused sampler and the filter write into it
+  // (the largest sampled key, the survivors' histogram by offset above tau)
+  // for the refinement to start from.
+  unsigned* refine_ctl = nullptr;
+  unsigned* refine_ctl_next = nullptr;
+  if (grid_refine) {
+    uint64_t parity;
+    {
+      std::lock_guard<std::mutex> lock(g_ws_mu);
+      parity = wcnt->refine_calls++ & 1u;
+    }
+    char* copies = base + ws_refine_ctl_offset();
+    refine_ctl = reinterpret_cast<unsigned*>(copies + parity * kRefineCtlCopyBytes);
+    refine_ctl_next = reinterpret_cast<unsigned*>(copies + (parity ^ 1u) * kRefineCtlCopyBytes);
+  }
+  const bool survivor_hist = grid_refine && fused && !unsorted_out;
   bool fallback_launched = false;
   int nl = 0;  // kernels launched
   if (plan.path == TOPK_PATH_PROFK) {
@@ -457,8 +492,10 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
       hist_zero = reinterpret_cast<unsigned*>(halves + (parity ^ 1u) * kHistHalfBytes);
     }
     if (fused) {
-      const SampleTauScratch sc{hist_add, hist_zero, reinterpret_cast<unsigned*>(base + ws_tau_ctl_offset()),
-                                reinterpret_cast<uint64_t*>(base + ws_tau_gather_offset())};
+      SampleTauScratch sc{hist_add, hist_zero, reinterpret_cast<unsigned*>(base + ws_tau_ctl_offset()),
+                          reinterpret_cast<uint64_t*>(base + ws_tau_gather_offset())};
+      sc.refine_ctl = survivor_hist ? refine_ctl : nullptr;
+
       TK_TRY(launch_sample_tau(p, S, plan.t, seed, counter, counts, hdr, sc, tau, st));
       ++nl;
     } else {
@@ -486,7 +523,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // The filter may launch while the fused grid finishes (its blocks leave
     // early, one block ranks at the end), not while a 16-CTA threshold
     // cluster runs: that gained nothing.
-    TK_TRY(launch_filter(p, tau, M, buf, counts, fused ? 0 : -1, st));
+    TK_TRY(launch_filter(p, tau, M, buf, counts, fused ? 0 : -1, st, survivor_hist ? refine_ctl : nullptr));
     ++nl;
     TK_TRY(mark(3));
     // Where to handle a miss: inside the refinement kernel (no launch when
@@ -496,7 +533,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // plan's own miss probability times about three passes over a row at
     // ~100 GB/s per SM of the cluster -- is below the launch it saves.  A
     // miss forced by the caller always takes the grid-wide fallback.
-    if (!grid_refine && (force || !miss_in_refine(p, k, plan.t, plan.S, plan.p_miss))) {
+    if (!grid_refine && (force || relaxed || !miss_in_refine(p, k, plan.t, plan.S, plan.p_miss))) {
       TK_TRY(launch_fallback(p, k, M, buf, counts, fs, force, st));
       ++nl;
       fallback_launched = true;
@@ -525,6 +562,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.n_clear = kTauCtlWords;
   rj.launch_count = &nl;
   rj.binfo = select_binfo_words(k) ? reinterpret_cast<unsigned*>(base + o_binfo) : nullptr;
+  rj.relax_tau = relaxed ? tau_x : nullptr;  // the fallback's per-row padding bound
   if (plan.path == TOPK_PATH_PROFK && !fallback_launched) {
     rj.check_miss = true;
     rj.force_miss = force != 0;
@@ -542,15 +580,10 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     if (hint < k) hint = k;
   }
   if (grid_refine) {
-    uint64_t parity;
-    {
-      std::lock_guard<std::mutex> lock(g_ws_mu);
-      parity = wcnt->refine_calls++ & 1u;
-    }
-    char* copies = base + ws_refine_ctl_offset();
     RefineGridScratch rg{};
-    rg.ctl = reinterpret_cast<unsigned*>(copies + parity * kRefineCtlCopyBytes);
-    rg.ctl_next = reinterpret_cast<unsigned*>(copies + (parity ^ 1u) * kRefineCtlCopyBytes);
+    rg.ctl = refine_ctl;
+    rg.ctl_next = refine_ctl_next;
+    rg.tau = survivor_hist ? tau : nullptr;
     rg.xbuf = xbuf;
     rg.xstride = rj.xbuf_stride;
     rg.binfo = rj.binfo;
@@ -590,6 +623,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     stats->counter = static_cast<int64_t>(counter);
     stats->cluster = cluster;
     stats->launches = nl;
+    stats->shortfalls = static_cast<int64_t>(h.shortfalls);
     if (h.status != kDevOk) return h.status == kDevTimeout ? TOPK_ETIMEOUT : TOPK_ECUDA;
   }
   return TOPK_OK;
@@ -623,6 +657,7 @@ void topk_options_init(topk_options_t* opt) {
   opt->counter = -1;
   opt->wait_limit_ns = 0;
   opt->inject_wait_timeout = 0;
+  opt->recall = 0.0;
 }
 
 int topk_select(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int largest, double eps,
@@ -657,7 +692,8 @@ int topk_plan(int64_t n, int64_t k, double eps, const topk_options_t* opt, topk_
   plan->p_overflow = 0.0;
   if (pl.path == TOPK_PATH_PROFK) {
     const double nd = static_cast<double>(n);
-    plan->p_recall_fail = binom_upper_tail(pl.S, (static_cast<double>(k) - 1.0) / nd, pl.t);
+    const int64_t kt = recall_rank(k, relaxed_recall(opt) ? opt->recall : 0.0);
+    plan->p_recall_fail = binom_upper_tail(pl.S, (static_cast<double>(kt) - 1.0) / nd, pl.t);
     plan->p_overflow = binom_lower_tail(pl.S, static_cast<double>(pl.M) / nd, pl.t - 1);
   }
   return TOPK_OK;
