@@ -565,7 +565,11 @@ def time_call(fn, reps, flush):
     return statistics.median(times)
 
 
+SWEEP_ORACLE_MAX_N = 1 << 24
+
+
 def run_sweep(args):
+    import numpy
     import torch
     import top_selection_prof_gb300 as tk
     torch.cuda.set_device(0)
@@ -585,14 +589,25 @@ def run_sweep(args):
                     continue
                 ours_us = time_call(lambda: tk.select(x, k, eps=1e-3), reps, fl)
                 torch_us = time_call(lambda: torch.topk(x, k, sorted=True), reps, fl)
-                v, _ = tk.select(x, k, eps=1e-3)
+                v, i = tk.select(x, k, eps=1e-3)
                 tv, _ = torch.topk(x, k, sorted=True)
                 _, _, st = tk.select_ex(x, k, eps=1e-3)
-                points.append({"n": n, "k": k, "dist": dist, "path": st["path_name"],
-                               "ours_us": round(ours_us, 1), "torch_topk_us": round(torch_us, 1),
-                               "speedup": round(torch_us / ours_us, 2),
-                               "ours_gbs": round(n * 4 / (ours_us * 1e-6) / 1e9, 1),
-                               "values_equal_torch": bool(torch.equal(v, tv))})
+                point = {"n": n, "k": k, "dist": dist, "path": st["path_name"],
+                         "ours_us": round(ours_us, 1), "torch_topk_us": round(torch_us, 1),
+                         "speedup": round(torch_us / ours_us, 2),
+                         "ours_gbs": round(n * 4 / (ours_us * 1e-6) / 1e9, 1),
+                         "values_equal_torch": bool(torch.equal(v, tv)),
+                         # (torch.topk does not fix the order of equal values: indices are
+                         # checked by what they point at, and against the oracle where it is cheap)
+                         "indices_hold_values": bool(torch.equal(x[i], v))}
+                if n <= SWEEP_ORACLE_MAX_N:
+                    from oracle import plain
+                    xh = x.cpu().numpy()
+                    ov, oi = plain.topk(xh[None, :], k)
+                    point["oracle_exact"] = bool(numpy.array_equal(i.cpu().numpy(), oi[0]) and
+                                                 numpy.array_equal(v.cpu().numpy().view(numpy.uint32),
+                                                                   ov[0].view(numpy.uint32)))
+                points.append(point)
             del x
     sp = [p["speedup"] for p in points]
     geo = float(math.exp(sum(math.log(v) for v in sp) / len(sp)))
@@ -601,7 +616,10 @@ def run_sweep(args):
             "l2": "flushed before each call when the input is below 2x L2", "data": "synthetic (torch generator)",
             "points": points,
             "summary": {"speedup_min": min(sp), "speedup_max": max(sp), "speedup_geomean": round(geo, 2),
-                        "all_values_equal": all(p["values_equal_torch"] for p in points)}}
+                        "all_values_equal": all(p["values_equal_torch"] for p in points),
+                        "all_indices_hold_values": all(p["indices_hold_values"] for p in points),
+                        "oracle_points": sum("oracle_exact" in p for p in points),
+                        "all_oracle_exact": all(p.get("oracle_exact", True) for p in points)}}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -76,7 +76,9 @@ typedef enum {
 typedef struct {
   int64_t s_min;       /* Algorithm 1 S_min (default 32768) */
   int64_t s_max;       /* Algorithm 1 S_max (default 131072) */
-  double cost_ratio;   /* tau_B / tau_A of Eq. 13 (default 1) */
+  double cost_ratio;   /* tau_B / tau_A of Eq. 13 (default 1); 0 = as measured on this device by
+                          topk_autotune (1 before that), which also applies the measured
+                          Prof-K / direct crossover to the automatic path choice */
   int rule;            /* topk_rule_t (default TOPK_RULE_EXACT) */
   int path;            /* topk_path_t; TOPK_PATH_AUTO lets the engine choose */
   uint64_t seed;       /* Philox key for the sampler (default fixed) */
@@ -201,13 +203,45 @@ int topk_plan(int64_t n, int64_t k, double eps, const topk_options_t* opt, topk_
  */
 int topk_last_status(void* stream);
 
+/* Measured cost model of this device (Prof-K paper, section 4, "Optimal
+ * Sample Size": the ratio tau_B / tau_A "may be estimated by lightweight
+ * microbenchmarking"; Figure 3 for the crossover with a direct method). */
+typedef struct {
+  double tau_a_ns;      /* sampling and threshold: device time per additional sampled element */
+  double tau_b_ns;      /* refinement: device time per additional buffered element, per log2 k */
+  double cost_ratio;    /* tau_b_ns / tau_a_ns, the ratio of Eq. 13 and 14 */
+  int64_t crossover_n;  /* smallest measured row length from which Prof-K beat the direct path
+                           at every larger measured length (0: it never did) */
+  int64_t crossover_k;  /* the k the crossover was measured at */
+} topk_tuning_t;
+
+/*
+ * Measures the cost model on the current device with synthetic uniform f32
+ * rows through the selection pipeline itself (CUDA events at its stage
+ * boundaries, medians of repeated calls): tau_A from the sampling and
+ * threshold stage at S = 32768 and S = 131072; tau_B from the refinement at
+ * two survivor counts (k = 1024); the crossover from full selections of k out
+ * of n = 2^16 ... 2^24 by the direct path and by Prof-K (eps = 1e-3).  Allocates
+ * about 256 MiB of device memory for the duration and synchronises `stream`;
+ * takes on the order of a second.  The result is kept for the device and used
+ * by calls whose options set cost_ratio = 0.  k: the k of the crossover (0 =
+ * 1024).  Errors: TOPK_EINVAL for a null `out` or k outside [0, 65536],
+ * TOPK_ENOMEM / TOPK_ECUDA.
+ */
+int topk_autotune(int64_t k, void* stream, topk_tuning_t* out);
+
+/* The measured cost model of the current device (TOPK_EINVAL when topk_autotune
+ * has not run on it). */
+int topk_tuning(topk_tuning_t* out);
+
 /* Static text for a status code. */
 const char* topk_status_str(int status);
 
 /* Library version: major*10000 + minor*100 + patch.  0.2.0 (200) added the
  * `unsorted` field at the end of topk_options_t; 0.3.0 (300) added
  * `wait_limit_ns`, `inject_wait_timeout` and `recall` after it, `shortfalls`
- * at the end of topk_stats_t, and topk_last_status.
+ * at the end of topk_stats_t, topk_last_status, topk_autotune and topk_tuning
+ * (cost_ratio = 0 meaning "measured").
  * Fill the struct with topk_options_init from the same version's library. */
 int topk_version(void);
 

@@ -151,3 +151,12 @@ def test_relaxed_recall_rule_parity_with_oracle(lib, n, k, eps, recall):
     assert t == 1 or oparams.p_recall_fail(n, kt, s, t - 1) > eps / 2
     assert abs(p.p_recall_fail - oparams.p_recall_fail(n, kt, s, t)) <= 1e-9 * eps + 1e-12
     assert t <= oparams.exact(n, k, eps)[1]
+
+
+def test_tuning_entry_points_without_gpu(lib):
+    from top_selection_prof_gb300 import _lib
+    t = _lib.TopkTuning()
+    assert lib.topk_autotune(1024, None, None) == -1          # null out
+    assert lib.topk_autotune(-1, None, ctypes.byref(t)) == -1 # k outside [0, 65536]
+    assert lib.topk_autotune(70000, None, ctypes.byref(t)) == -1
+    assert lib.topk_tuning(None) == -1

@@ -16,7 +16,7 @@ PATH_NAMES = {TOPK_PATH_DIRECT: "direct", TOPK_PATH_PROFK: "profk", TOPK_PATH_EX
 # Every symbol include/topk.h declares.
 EXPORTS = ("topk_options_init", "topk_select", "topk_select_global", "topk_select_ex", "topk_plan",
            "topk_status_str", "topk_version", "topk_index_bits", "topk_prof_sample", "topk_prof_filter",
-           "topk_select_noalloc", "topk_last_status")
+           "topk_select_noalloc", "topk_last_status", "topk_autotune", "topk_tuning")
 
 
 class TopkOptions(ctypes.Structure):
@@ -33,6 +33,11 @@ class TopkStats(ctypes.Structure):
                 ("misses", ctypes.c_int64), ("tau", ctypes.c_uint64), ("tau_index", ctypes.c_int64),
                 ("seed", ctypes.c_uint64), ("counter", ctypes.c_int64), ("cluster", ctypes.c_int),
                 ("launches", ctypes.c_int), ("shortfalls", ctypes.c_int64)]
+
+
+class TopkTuning(ctypes.Structure):
+    _fields_ = [("tau_a_ns", ctypes.c_double), ("tau_b_ns", ctypes.c_double), ("cost_ratio", ctypes.c_double),
+                ("crossover_n", ctypes.c_int64), ("crossover_k", ctypes.c_int64)]
 
 
 class TopkPlan(ctypes.Structure):
@@ -64,6 +69,10 @@ def get():
         lib.topk_select_ex.restype = c_int
         lib.topk_plan.argtypes = [i64, i64, c_double, ctypes.POINTER(TopkOptions), ctypes.POINTER(TopkPlan)]
         lib.topk_plan.restype = c_int
+        lib.topk_autotune.argtypes = [i64, vp, ctypes.POINTER(TopkTuning)]
+        lib.topk_autotune.restype = c_int
+        lib.topk_tuning.argtypes = [ctypes.POINTER(TopkTuning)]
+        lib.topk_tuning.restype = c_int
         lib.topk_last_status.argtypes = [vp]
         lib.topk_last_status.restype = c_int
         lib.topk_status_str.argtypes = [c_int]

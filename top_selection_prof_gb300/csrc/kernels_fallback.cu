@@ -514,13 +514,26 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   unsigned* g_lev = ctl + 8;
   const int tid = threadIdx.x;
 
+  // ---- this block's slice of the buffer: bounds fixed by the capacity (the
+  // host checks cap <= gridDim.x * kPartCache), so its loads are in flight
+  // before R is known; keys at or beyond the valid count are dropped below
+  const int64_t sb = fp.cap * blockIdx.x / gridDim.x, se = fp.cap * (blockIdx.x + 1) / gridDim.x;
+  const uint64_t* src = fp.buf + row * fp.cap + sb;
+  constexpr int kSliceLoads = kPartCache / kFilterBlock;
+  uint64_t kv[kSliceLoads];
+#pragma unroll
+  for (int q = 0; q < kSliceLoads; ++q) {
+    const int64_t i = tid + q * kFilterBlock;
+    kv[q] = i < se - sb ? __ldcg(src + i) : 0ull;
+  }
+
   // ---- the filter's histogram of the survivors' offsets above tau, when it
   // was kept and the buffer holds exactly the survivors it counted (no miss):
   // it gives every bin's total at once.  Usable when its top bin is empty
   // (every offset below 2047 << shift, so the bins are a plain digit of key -
   // tau) and the boundary bin fits the exchange buffer after the bins above.
-  // the words every block reads, loaded by one thread each and shared: R,
-  // the relaxed-recall tau, tau and the largest sampled key
+  // The words every block reads are loaded by one thread each and shared: R,
+  // the relaxed-recall tau, tau and the largest sampled key.
   __shared__ unsigned long long s_words[4];
   if (tid == 0) {
     s_words[0] = __ldcg(fp.counts + row);
@@ -554,9 +567,8 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
       pad_below = rtau;
     }
   }
-  const int64_t sb = n * blockIdx.x / gridDim.x, se = n * (blockIdx.x + 1) / gridDim.x;
-  const int cn = static_cast<int>(se - sb);  // <= kPartCache: the host checks n <= gridDim.x * kPartCache
-  const uint64_t* src = fp.buf + row * fp.cap + sb;
+  // the valid keys of this slice: [sb, min(se, n))
+  const int cn = static_cast<int>(n <= sb ? 0 : (n < se ? n - sb : se - sb));
   uint64_t kmin, pmask1;
   int shift1;
   const uint64_t prefix1 = 0ull;
@@ -565,14 +577,6 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
     kmin = s_words[2];
     shift1 = survivor_shift(kmin, s_words[3]);
     pmask1 = shift1 + kPartDigit >= 64 ? 0ull : (~0ull << (shift1 + kPartDigit));
-    // (a slice holds at most kPartCache keys: every load of the thread in flight at once)
-    constexpr int kSliceLoads = kPartCache / kFilterBlock;
-    uint64_t kv[kSliceLoads];
-#pragma unroll
-    for (int q = 0; q < kSliceLoads; ++q) {
-      const int i = tid + q * kFilterBlock;
-      kv[q] = i < cn ? __ldcg(src + i) : 0ull;
-    }
 #pragma unroll
     for (int q = 0; q < kSliceLoads; ++q) {
       const int i = tid + q * kFilterBlock;
@@ -582,13 +586,6 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
     TK_RG(3);
   } else {
     unsigned long long mn = ~0ull, mx = 0ull;
-    constexpr int kSliceLoads = kPartCache / kFilterBlock;
-    uint64_t kv[kSliceLoads];
-#pragma unroll
-    for (int q = 0; q < kSliceLoads; ++q) {
-      const int i = tid + q * kFilterBlock;
-      kv[q] = i < cn ? __ldcg(src + i) : 0ull;
-    }
 #pragma unroll
     for (int q = 0; q < kSliceLoads; ++q) {
       const int i = tid + q * kFilterBlock;

@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(kFilterBlock) filter_kernel(FilterParams fp) {
   __shared__ uint64_t stage[kFilterBlock / 32][kWarpStage];
   __shared__ unsigned stage_n[kFilterBlock / 32];
   __shared__ unsigned sh_hist[HIST ? kRefineGridBins : 1];
+  __shared__ uint4 queue_v[kFilterBlock / 32][kGroupQueue];
+  __shared__ int64_t queue_pos[kFilterBlock / 32][kGroupQueue];
   TK_TL_BEGIN(2);
   if (HIST) {
     for (int i = threadIdx.x; i < kRefineGridBins; i += kFilterBlock) sh_hist[i] = 0u;
@@ -35,7 +37,8 @@ __global__ void __launch_bounds__(kFilterBlock) filter_kernel(FilterParams fp) {
   constexpr int64_t kTile = static_cast<int64_t>(kFilterBlock) * kFilterUnroll * VEC;
   const int64_t ntiles = fp.nsel * ((fp.len + kTile - 1) / kTile);
   const Stage st{stage[threadIdx.x >> 5], &stage_n[threadIdx.x >> 5]};
-  filter_tiles<DT, LARGEST, VEC, HIST>(fp, blockIdx.x, ntiles, gridDim.x, st, sh_hist);
+  const GroupQueue q{queue_v[threadIdx.x >> 5], queue_pos[threadIdx.x >> 5]};
+  filter_tiles<DT, LARGEST, VEC, HIST>(fp, blockIdx.x, ntiles, gridDim.x, st, sh_hist, &q);
   TK_TL_END(2);
 }
 

@@ -320,8 +320,8 @@ __device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint6
                                 const SelParams& a, int64_t row, int64_t kout, int64_t base_place, int64_t w0,
                                 int64_t w1) {
   static_assert(NB % BLOCK == 0, "whole groups per thread");
-  static_assert(NB == 256 || NB == 2048 || NB == 4096, "8, 11 or 12 leading bits");
-  constexpr int kBits = NB == 4096 ? 12 : (NB == 2048 ? 11 : 8);
+  static_assert(NB == 256 || NB == 1024 || NB == 2048 || NB == 4096, "8, 10, 11 or 12 leading bits");
+  constexpr int kBits = NB == 4096 ? 12 : (NB == 2048 ? 11 : (NB == 1024 ? 10 : 8));
   constexpr int kPer = NB / BLOCK;
   __shared__ unsigned s_gmax;
   __shared__ unsigned long long s_cost;
@@ -337,7 +337,7 @@ __device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint6
   for (int i = tid; i < n; i += BLOCK) atomicAdd(&gcount[group(src[i])], 1u);
   __syncthreads();
   TK_STAMP(22);
-  if constexpr (NB == 4096) TK_BSP(4);
+  if constexpr (NB == 1024) TK_BSP(4);  // (the bin sort's group count)
   unsigned c[kPer];
   unsigned long long sum = 0, sq = 0;
   unsigned mx = 0;
@@ -364,7 +364,7 @@ __device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint6
   if ((threadIdx.x & 31) == 0) atomicMax(&s_gmax, mx);
   __syncthreads();
   TK_STAMP(23);
-  if constexpr (NB == 4096) TK_BSP(5);
+  if constexpr (NB == 1024) TK_BSP(5);  // (the bin sort's group count)
   if (blockIdx.x == 0 && threadIdx.x == 0) TK_DBG(0, s_gmax);
   if (s_gmax > max_group || s_cost > kMaxComparesPerKey * static_cast<unsigned long long>(n)) return false;
   for (int i = tid; i < n; i += BLOCK) {
@@ -374,7 +374,7 @@ __device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint6
   }
   __syncthreads();
   TK_STAMP(25);
-  if constexpr (NB == 4096) TK_BSP(6);
+  if constexpr (NB == 1024) TK_BSP(6);  // (the bin sort's group count)
   for (int i = tid; i < n; i += BLOCK) {
     const uint64_t v = grp[i];
     const unsigned g = group(v);
@@ -1363,7 +1363,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
 constexpr int kBinSortBlock = 256;
 constexpr int kBinSortPlaces = static_cast<int>(kBinSortChunk);
 constexpr int kBinSortCap = 2048;  // keys one block sorts
-constexpr int kBinSortGroups = 4096;  // 12 leading varying bits: small groups even for few values
+constexpr int kBinSortGroups = 1024;  // slices of the block's key range: ~2 keys each for 2048 keys
 constexpr int kBinSortScratch = 3 * kBinSortGroups;  // (also covers the LSD sort's counters)
 static_assert(kBinSortScratch >= (kBinSortBlock / 32) * 256 + 2 * 256 + (kBinSortBlock / 256) * 256, "lsd");
 constexpr size_t kBinSortSmem = 2 * sizeof(uint64_t) * kBinSortCap + sizeof(unsigned) * kBinSortScratch;

@@ -23,6 +23,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "../../include/topk.h"
 #include "common.cuh"
@@ -132,12 +133,31 @@ struct Plan {
 
 bool relaxed_recall(const topk_options_t* o) { return o && o->recall > 0.0 && o->recall < 1.0; }
 
+// The cost model measured by topk_autotune, per device.
+std::mutex g_tune_mu;
+std::map<int, topk_tuning_t> g_tuning;
+bool tuned_model(topk_tuning_t* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(g_tune_mu);
+  auto it = g_tuning.find(dev);
+  if (it == g_tuning.end()) return false;
+  *out = it->second;
+  return true;
+}
+// cost_ratio == 0 asks for the measured model
+bool wants_tuned(const topk_options_t* o) { return o && o->cost_ratio == 0.0; }
+
 ParamRule rule_of(const topk_options_t* o) {
   ParamRule pr;
   if (o) {
     pr.s_min = o->s_min;
     pr.s_max = o->s_max;
     pr.cost_ratio = o->cost_ratio;
+    if (wants_tuned(o)) {
+      topk_tuning_t tm;
+      pr.cost_ratio = tuned_model(&tm) && tm.cost_ratio > 0.0 ? tm.cost_ratio : 1.0;
+    }
     pr.rule = o->rule;
     pr.recall = relaxed_recall(o) ? o->recall : 0.0;
   }
@@ -218,7 +238,8 @@ int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
   bool profk_ok = false;
   if (eps > 0.0) {
     const ParamRule pr = rule_of(o);
-    if (pr.s_min < 1 || pr.s_max < pr.s_min || !(pr.cost_ratio > 0.0) || (pr.rule != 0 && pr.rule != 1))
+    if (pr.s_min < 1 || pr.s_max < pr.s_min || !(pr.cost_ratio > 0.0) || (pr.rule != 0 && pr.rule != 1) ||
+        (o && o->cost_ratio < 0.0))
       return TOPK_EINVAL;
     int64_t S = 0, t = 0, M = 0;
     double p_miss = 1.0;
@@ -233,6 +254,11 @@ int make_plan(int64_t len, int64_t k, double eps, int64_t nsel, bool many_rows,
       plan->p_miss = p_miss;
       profk_ok = t >= 1 && t <= S && 2 * S < len && 2 * M <= len && M >= k && nsel <= 65535;
     }
+  }
+  // the measured crossover (cost_ratio = 0): the direct path below it
+  if (profk_ok && forced == TOPK_PATH_AUTO && wants_tuned(o) && (len <= kDirectMaxLen || many_rows)) {
+    topk_tuning_t tm;
+    if (tuned_model(&tm) && (tm.crossover_n == 0 || len < tm.crossover_n)) profk_ok = false;
   }
   switch (forced) {
     case TOPK_PATH_AUTO:
@@ -639,6 +665,176 @@ int select_with_fixed_scratch(const void* x, int dtype, int64_t rows, int64_t n,
   return run(x, dtype, rows, n, k, largest, eps, out_vals, out_idx, st, global, nullptr, nullptr, src);
 }
 
+namespace {
+
+// Synthetic uniform values in [0, 1) from a counter hash (the tuning input).
+__global__ void tune_fill_kernel(float* x, int64_t n) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    uint64_t h = static_cast<uint64_t>(i) * 0x9E3779B97F4A7C15ull;
+    h ^= h >> 31;
+    h *= 0xBF58476D1CE4E5B9ull;
+    h ^= h >> 29;
+    x[i] = static_cast<float>(h >> 40) * (1.0f / 16777216.0f);
+  }
+}
+
+struct StageTimer {
+  cudaEvent_t ev[6] = {};
+  bool ok = true;
+  StageTimer() {
+    for (auto& e : ev) ok = ok && cudaEventCreate(&e) == cudaSuccess;
+  }
+  ~StageTimer() {
+    for (auto& e : ev)
+      if (e) cudaEventDestroy(e);
+  }
+};
+
+double median(std::vector<double> v) {
+  std::sort(v.begin(), v.end());
+  return v.empty() ? 0.0 : v[v.size() / 2];
+}
+
+// Median device time (us) between stage events e0 and e1 over `reps` calls of
+// one selection of k out of n with the given options (events filled in).
+int time_stage(const float* x, int64_t n, int64_t k, double eps, topk_options_t opt, int e0, int e1, int reps,
+               float* vals, int64_t* idx, cudaStream_t st, StageTimer& tm, double* us, int64_t* r_out) {
+  for (int i = 0; i < 6; ++i) opt.events[i] = tm.ev[i];
+  std::vector<double> t;
+  for (int rep = -2; rep < reps; ++rep) {
+    topk_stats_t stats;
+    const int rc = run(x, TOPK_F32, 1, n, k, 1, eps, vals, idx, st, false, &opt, &stats);
+    if (rc != TOPK_OK) return rc;
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, tm.ev[e0], tm.ev[e1]) != cudaSuccess) return TOPK_ECUDA;
+    if (rep >= 0) t.push_back(1e3 * ms);
+    if (r_out) *r_out = stats.R;
+  }
+  *us = median(t);
+  return TOPK_OK;
+}
+
+// Median time (us) of whole selections through one forced path.
+int time_call(const float* x, int64_t n, int64_t k, int path, int reps, float* vals, int64_t* idx, cudaStream_t st,
+              StageTimer& tm, double* us) {
+  topk_options_t opt;
+  topk_options_init(&opt);
+  opt.path = path;
+  std::vector<double> t;
+  for (int rep = -2; rep < reps; ++rep) {
+    if (cudaEventRecord(tm.ev[0], st) != cudaSuccess) return TOPK_ECUDA;
+    const int rc = run(x, TOPK_F32, 1, n, k, 1, 1e-3, vals, idx, st, false, &opt, nullptr);
+    if (rc != TOPK_OK) return rc;
+    if (cudaEventRecord(tm.ev[1], st) != cudaSuccess || cudaEventSynchronize(tm.ev[1]) != cudaSuccess)
+      return TOPK_ECUDA;
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, tm.ev[0], tm.ev[1]) != cudaSuccess) return TOPK_ECUDA;
+    if (rep >= 0) t.push_back(1e3 * ms);
+  }
+  *us = median(t);
+  return TOPK_OK;
+}
+
+int autotune(int64_t k_cross, cudaStream_t st, topk_tuning_t* out) {
+  constexpr int64_t kN = int64_t(1) << 26;  // 256 MiB of f32: larger than L2
+  constexpr int64_t kMaxK = 65536;
+  constexpr int kReps = 15;
+  float* x = nullptr;
+  float* vals = nullptr;
+  int64_t* idx = nullptr;
+  StageTimer tm;
+  if (!tm.ok) return TOPK_ECUDA;
+  cudaError_t e = cudaMalloc(&x, sizeof(float) * kN);
+  if (e == cudaSuccess) e = cudaMalloc(&vals, sizeof(float) * kMaxK);
+  if (e == cudaSuccess) e = cudaMalloc(&idx, sizeof(int64_t) * kMaxK);
+  int rc = status_of(e);
+  if (rc == TOPK_OK) {
+    tune_fill_kernel<<<1216, 256, 0, st>>>(x, kN);
+    rc = status_of(cudaGetLastError());
+  }
+  topk_tuning_t r{};
+  r.crossover_k = k_cross;
+  // tau_A: the sampling and threshold stage (events 0 -> 2) at two sample sizes
+  double ta1 = 0, ta2 = 0;
+  const int64_t s1 = 32768, s2 = 131072;
+  topk_options_t o;
+  topk_options_init(&o);
+  if (rc == TOPK_OK) {
+    o.s_min = o.s_max = s1;
+    rc = time_stage(x, kN, 1024, 1e-3, o, 0, 2, kReps, vals, idx, st, tm, &ta1, nullptr);
+  }
+  if (rc == TOPK_OK) {
+    o.s_min = o.s_max = s2;
+    rc = time_stage(x, kN, 1024, 1e-3, o, 0, 2, kReps, vals, idx, st, tm, &ta2, nullptr);
+  }
+  // tau_B: the refinement (events 4 -> 5) at two survivor counts (S fixed,
+  // t raised; the buffer sized for the larger count), per log2 k
+  double tb1 = 0, tb2 = 0;
+  int64_t r1 = 0, r2 = 0;
+  if (rc == TOPK_OK) {
+    topk_options_init(&o);
+    o.s_min = o.s_max = s1;
+    o.t_override = 8;
+    o.m_override = 1 << 17;
+    rc = time_stage(x, kN, 1024, 1e-3, o, 4, 5, kReps, vals, idx, st, tm, &tb1, &r1);
+  }
+  if (rc == TOPK_OK) {
+    o.t_override = 32;
+    rc = time_stage(x, kN, 1024, 1e-3, o, 4, 5, kReps, vals, idx, st, tm, &tb2, &r2);
+  }
+  if (rc == TOPK_OK) {
+    r.tau_a_ns = std::max(1e-6, 1e3 * (ta2 - ta1) / static_cast<double>(s2 - s1));
+    r.tau_b_ns = std::max(1e-6, r2 > r1 ? 1e3 * (tb2 - tb1) / static_cast<double>(r2 - r1) / std::log2(1024.0) : 0.0);
+    r.cost_ratio = r.tau_b_ns / r.tau_a_ns;
+    // the crossover: forced Prof-K against the direct path, n = 2^16 .. 2^24
+    int64_t cross = 0;
+    bool beaten_since = false;
+    for (int lg = 16; lg <= 24 && rc == TOPK_OK; ++lg) {
+      const int64_t n = int64_t(1) << lg;
+      if (k_cross * 8 > n) continue;
+      Plan pl;
+      topk_options_t po;
+      topk_options_init(&po);
+      po.path = TOPK_PATH_PROFK;
+      if (make_plan(n, k_cross, 1e-3, 1, false, &po, &pl) != TOPK_OK) {  // Prof-K not applicable here
+        beaten_since = false;
+        continue;
+      }
+      double td = 0, tp = 0;
+      rc = time_call(x, n, k_cross, TOPK_PATH_DIRECT, kReps, vals, idx, st, tm, &td);
+      if (rc == TOPK_OK) rc = time_call(x, n, k_cross, TOPK_PATH_PROFK, kReps, vals, idx, st, tm, &tp);
+      if (rc != TOPK_OK) break;
+      if (tp < td) {
+        if (!beaten_since) cross = n;
+        beaten_since = true;
+      } else {
+        beaten_since = false;
+        cross = 0;
+      }
+    }
+    r.crossover_n = cross;
+  }
+  if (x) cudaFree(x);
+  if (vals) cudaFree(vals);
+  if (idx) cudaFree(idx);
+  if (rc != TOPK_OK) return rc;
+  int dev = 0;
+  TK_TRY(cudaGetDevice(&dev));
+  {
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    g_tuning[dev] = r;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    g_plans.clear();  // plans that asked for the measured ratio are recomputed
+  }
+  *out = r;
+  return TOPK_OK;
+}
+
+}  // namespace
+
 }  // namespace tk
 
 using namespace tk;
@@ -697,6 +893,16 @@ int topk_plan(int64_t n, int64_t k, double eps, const topk_options_t* opt, topk_
     plan->p_overflow = binom_lower_tail(pl.S, static_cast<double>(pl.M) / nd, pl.t - 1);
   }
   return TOPK_OK;
+}
+
+int topk_autotune(int64_t k, void* stream, topk_tuning_t* out) {
+  if (!out || k < 0 || k > 65536) return TOPK_EINVAL;
+  return autotune(k ? k : 1024, static_cast<cudaStream_t>(stream), out);
+}
+
+int topk_tuning(topk_tuning_t* out) {
+  if (!out) return TOPK_EINVAL;
+  return tuned_model(out) ? TOPK_OK : TOPK_EINVAL;
 }
 
 int topk_last_status(void* stream) {
