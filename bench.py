@@ -38,6 +38,7 @@ SECONDARY_MIN_STEPS = 1000
 NOMINAL_READ_GBS = 8000.0  # GB300 HBM3e nominal rate: the one-read roofline the fractions use
 CLOCK_SOAK_S = 1.5
 ORACLE_SAMPLE_ELEMS = 1 << 25
+RELAXED_RECALL = 0.95
 REFERENCE_BUDGET_S = 240.0   # the reference arm's whole run: full workload when it fits, else a prefix
 CONFIG_MISS_CALLS = 10000
 
@@ -54,6 +55,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-miss-rate", action="store_true", help="skip the measured miss rate against eps")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the side measurements (forced miss, unsorted, relaxed recall, autotune); for profiling")
     ap.add_argument("--miss-calls", type=int, default=CONFIG_MISS_CALLS,
                     help="seeded calls per workload and rule for the miss rate on the tied rows and BatchTopK")
     ap.add_argument("--scale-down", type=int, default=0,
@@ -340,7 +343,7 @@ def measure_config_miss_rates(calls, seed=0):
     return out
 
 
-def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, with_e2e=True):
+def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, with_e2e=True, extras=True):
     import numpy as np
     import torch
     import torch.distributed as dist
@@ -430,7 +433,7 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
     # The miss path: calls whose every selection takes the fallback (a miss
     # is injected on the host), timed alone.
     forced_miss_ms = None
-    if path == "profk":
+    if path == "profk" and extras:
         opt.force_miss = 1
         call()
         torch.cuda.synchronize()
@@ -446,7 +449,7 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
     # BatchTopK needs only the set of winners: the same selection with the
     # sort left out (the unsorted option), timed alone
     unsorted_ms = None
-    if glob and path == "profk" and k >= 8192:
+    if glob and path == "profk" and k >= 8192 and extras:
         opt.unsorted = 1
         for _ in range(3):
             call()
@@ -459,6 +462,45 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
         torch.cuda.synchronize()
         unsorted_ms = round(u0.elapsed_time(u1) / steps, 4)
         opt.unsorted = 0
+
+    def time_steps(nsteps):
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(nsteps):
+            call()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / nsteps
+
+    # Relaxed recall (the paper's accuracy-speed trade-off): the same
+    # selection with a recall target of 0.95, and the recall it returned
+    relaxed = None
+    if path == "profk" and world == 1 and extras:
+        opt.recall = RELAXED_RECALL
+        r_ms = time_steps(steps)
+        _, i_r, st_r = tk.select_ex(xd, k, eps=eps, global_=glob, recall=RELAXED_RECALL)
+        real = int((i_r >= 0).sum().item())
+        relaxed = {"recall_target": RELAXED_RECALL, "ms_per_step": round(r_ms, 4), "S_t_M": [st_r["S"], st_r["t"], st_r["M"]],
+                   "R": st_r["R"], "returned_fraction_of_k": round(real / i_r.numel(), 6)}
+        opt.recall = 0.0
+
+    # The cost model measured on this device (topk_autotune) and the same
+    # selection with the sample size it gives (cost_ratio = 0)
+    autotuned = None
+    if path == "profk" and world == 1 and extras:
+        tn = _lib.TopkTuning()
+        rc = lib.topk_autotune(0, sp, ctypes.byref(tn))
+        if rc == 0:
+            opt.cost_ratio = 0.0
+            a_ms = time_steps(steps)
+            _, _, st_a = tk.select_ex(xd, k, eps=eps, global_=glob, cost_ratio=0.0)
+            autotuned = {"tau_a_ns": tn.tau_a_ns, "tau_b_ns": tn.tau_b_ns, "cost_ratio": tn.cost_ratio,
+                         "crossover_n_at_k1024": tn.crossover_n, "ms_per_step": round(a_ms, 4),
+                         "S_t_M": [st_a["S"], st_a["t"], st_a["M"]], "path": st_a["path_name"]}
+            opt.cost_ratio = 1.0
 
     ms_total = max_over_ranks(ms_total, dev, world)
     ms_step = ms_total / steps
@@ -516,7 +558,7 @@ def run_ours(cfg, name, x_host, steps, warmup, world, rank, with_clocks=True, wi
     return {
         "value": value, "ms_per_step": ms_step, "path": path, "stats": st, "stages": stages,
         "roofline": roofline, "e2e": e2e, "clocks": clock_info, "forced_miss_ms_per_step": forced_miss_ms,
-        "unsorted_ms_per_step": unsorted_ms,
+        "unsorted_ms_per_step": unsorted_ms, "relaxed_recall": relaxed, "autotuned": autotuned,
         # the library reports the kernels each call launched (sample and
         # threshold, filter, fallback when it runs as its own grid, refinement,
         # bin sort for large k; the direct path's one kernel)
@@ -663,7 +705,7 @@ def main():
 
     x = make_input(cfg, args.seed + rank)
     res = run_ours(cfg, args.workload, x, args.steps, args.warmup, world, rank,
-                   with_clocks=not args.no_clocks, with_e2e=not args.no_e2e)
+                   with_clocks=not args.no_clocks, with_e2e=not args.no_e2e, extras=not args.no_extras)
 
     secondary = None
     if not args.no_secondary and args.workload != SECONDARY_WORKLOAD:
@@ -674,7 +716,7 @@ def main():
         # ~1.3 ms, so a short window that happens to hold one overstates the
         # expected cost of eps x 1.3 ms per call many times over)
         r2 = run_ours(c2, SECONDARY_WORKLOAD, x2, max(args.steps, SECONDARY_MIN_STEPS), args.warmup, world, rank,
-                      with_clocks=False, with_e2e=False)
+                      with_clocks=False, with_e2e=False, extras=not args.no_extras)
         secondary = {"workload": SECONDARY_WORKLOAD, "value": round(r2["value"], 3), "unit": "G elem/s",
                      "ms_per_step": round(r2["ms_per_step"], 4), "path": r2["path"],
                      "hbm_gbs_whole_step": round(r2["hbm_gbs_whole_step"], 1),
@@ -682,6 +724,7 @@ def main():
                      "roofline": r2["roofline"], "stages": r2["stages"], "R": r2["stats"]["R"],
                      "forced_miss_ms_per_step": r2["forced_miss_ms_per_step"],
                      "unsorted_ms_per_step": r2["unsorted_ms_per_step"],
+                     "relaxed_recall": r2["relaxed_recall"], "autotuned": r2["autotuned"],
                      "steps": max(args.steps, SECONDARY_MIN_STEPS),
                      "S_t_M": [r2["stats"]["S"], r2["stats"]["t"], r2["stats"]["M"]]}
         x = None
@@ -717,6 +760,7 @@ def main():
             "cpu_baseline_all_cores": cpu_par, "e2e": res["e2e"],
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "secondary": secondary,
             "forced_miss_ms_per_step": res["forced_miss_ms_per_step"],
+            "relaxed_recall": res["relaxed_recall"], "autotuned": res["autotuned"],
         }
         if cfg.get("eps", 0) > 0 and not args.no_miss_rate:
             # the workload's own bound, and a measured rate where misses are countable

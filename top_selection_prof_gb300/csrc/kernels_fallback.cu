@@ -752,11 +752,20 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
       xb[pos] = key + kmin;
     }
   }
-  if (blockIdx.x == 0 && !rg.unsorted) {
-    // the bin sort's view of the partition
+  if (!rg.unsorted) {
+    // the bin sort's view of the partition, written by every block (each
+    // holds the same bin starts): a slice of the starts and some chunks'
+    // descriptors each, the digit description by block 0
     unsigned* bo = rg.binfo + row * binfo_words(static_cast<int64_t>(k));
-    for (int i = tid; i < kRefineGridBins; i += kFilterBlock) bo[i] = bst[i];
-    publish_chunks(bst, xend, static_cast<int64_t>(k), bo + kRefineGridBins + 8, tid, kFilterBlock);
+    const int per = (kRefineGridBins + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+    if (tid < per && static_cast<int>(blockIdx.x) * per + tid < kRefineGridBins)
+      bo[blockIdx.x * per + tid] = bst[blockIdx.x * per + tid];
+    publish_chunks(bst, xend, static_cast<int64_t>(k), bo + kRefineGridBins + 8,
+                   static_cast<int>(blockIdx.x) + tid * static_cast<int>(gridDim.x),
+                   static_cast<int>(gridDim.x) * kFilterBlock);
+  }
+  if (blockIdx.x == 0 && !rg.unsorted) {
+    unsigned* bo = rg.binfo + row * binfo_words(static_cast<int64_t>(k));
     if (tid == 0) {
       bo[kRefineGridBins] = static_cast<unsigned>(prefix1);
       bo[kRefineGridBins + 1] = static_cast<unsigned>(prefix1 >> 32);
