@@ -226,7 +226,23 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
   // its keys, keeps its top t, and the last block ranks the union -- no grid
   // barrier and no grid-wide histogram.
   uint64_t bound = 0ull;
-  if (p.local) {
+  // small t: each block's t largest by warp rounds (no radix passes), appended
+  // at once; the last block takes the t-th of their union the same way
+  __shared__ uint64_t s_lists[(BLOCK / 32) * 32];
+  __shared__ unsigned s_lcount[BLOCK / 32];
+  __shared__ uint64_t s_top[kSmallTopT];
+  __shared__ unsigned s_topn;
+  const bool small_t = p.local && p.t <= kSmallTopT;
+  if (small_t) {
+    uint64_t v[2] = {k0, k1};
+    const int nt = block_top_small<BLOCK, 2>(v, (one ? 1 : 0) + (two ? 1 : 0), static_cast<int>(p.t), s_lists,
+                                             s_lcount, s_top, &s_topn);
+    unsigned* gctl0 = p.sc.ctl + 2 + 2 * row;
+    uint64_t* gat0 = p.sc.gather + static_cast<int64_t>(row) * kTauGather;
+    if (tid == 0) s_cnt = nt ? atomicAdd(gctl0, static_cast<unsigned>(nt)) : 0u;
+    __syncthreads();
+    if (tid < nt && s_cnt + tid < static_cast<unsigned>(kTauGather)) gat0[s_cnt + tid] = s_top[tid];
+  } else if (p.local) {
     const int64_t first = 2 * (static_cast<int64_t>(static_cast<int>(blockIdx.x) % p.q) * BLOCK);
     const int64_t left = p.S - first;
     const unsigned nloc = static_cast<unsigned>(left < 2 * BLOCK ? left : 2 * BLOCK);
@@ -305,7 +321,7 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
   // selection ranks what was gathered
   unsigned* gctl = p.sc.ctl + 2 + 2 * row;  // gathered count, ticket
   uint64_t* gat = p.sc.gather + static_cast<int64_t>(row) * kTauGather;
-  {
+  if (!small_t) {
     const bool w0 = one && (p.local ? k0 >= bound : (k0 & pmask) == prefix);
     const bool w1 = two && (p.local ? k1 >= bound : (k1 & pmask) == prefix);
     const unsigned s0 = warp_append_slot(gctl, w0);
@@ -323,17 +339,44 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
   __threadfence();
   const unsigned gn = *reinterpret_cast<volatile unsigned*>(gctl);
   const unsigned n = gn < static_cast<unsigned>(kTauGather) ? gn : static_cast<unsigned>(kTauGather);
-  for (unsigned i = tid; i < n; i += BLOCK) gk[i] = __ldcg(gat + i);
-  if (tid == 0) {
-    s_tau = 0ull;
-    if (gn > static_cast<unsigned>(kTauGather)) atomicCAS(status, kDevOk, kDevBadState);
-    gctl[0] = 0u;  // ready for the next call
-    gctl[1] = 0u;
+  if (small_t) {
+    // the union (at most kTauGather keys: eight a thread), its t-th largest
+    constexpr int kPerThread = kTauGather / BLOCK;
+    uint64_t v[kPerThread];
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      const unsigned i = tid + j * BLOCK;
+      v[j] = i < n ? __ldcg(gat + i) : 0ull;
+      c += i < n ? 1 : 0;
+    }
+    if (tid == 0) {
+      s_tau = 0ull;
+      if (gn > static_cast<unsigned>(kTauGather)) atomicCAS(status, kDevOk, kDevBadState);
+      gctl[0] = 0u;  // ready for the next call
+      gctl[1] = 0u;
+    }
+    TK_STL(1);
+    // (each thread's keys are a strided slice: the exchange network sorts them)
+    const int nt = block_top_small<BLOCK, kPerThread>(v, c, static_cast<int>(p.t), s_lists, s_lcount, s_top, &s_topn);
+    if (tid == 0) {
+      if (nt == static_cast<int>(p.t)) s_tau = s_top[nt - 1];
+      else atomicCAS(status, kDevOk, kDevBadState);
+    }
+    __syncthreads();
+  } else {
+    for (unsigned i = tid; i < n; i += BLOCK) gk[i] = __ldcg(gat + i);
+    if (tid == 0) {
+      s_tau = 0ull;
+      if (gn > static_cast<unsigned>(kTauGather)) atomicCAS(status, kDevOk, kDevBadState);
+      gctl[0] = 0u;  // ready for the next call
+      gctl[1] = 0u;
+    }
+    __syncthreads();
+    TK_STL(1);
+    bucket_kth<BLOCK>(gk, n, rank, sh, s_tmp, s_info, &s_cnt, &s_tau);
+    __syncthreads();
   }
-  __syncthreads();
-  TK_STL(1);
-  bucket_kth<BLOCK>(gk, n, rank, sh, s_tmp, s_info, &s_cnt, &s_tau);
-  __syncthreads();
   TK_STL(2);
   if (tid == 0) p.tau_out[row] = s_tau;
 #ifdef TK_PHASE_TIMING

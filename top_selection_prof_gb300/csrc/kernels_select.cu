@@ -120,8 +120,10 @@ constexpr int kBinInfoBins = 2048;
 constexpr int kBinInfoWords = kBinInfoBins + 8;
 
 // Source of the refinement kernel (template source 3), chosen at run time:
-// 0 = the candidate buffer, or after a miss 1 / 2 = x as f32 / bf16.
+// 0 = the candidate buffer, or after a miss 1 / 2 = x as f32 / bf16; and the
+// count R its prologue read (the body uses it instead of reading it again).
 __shared__ int s_source;
+__shared__ unsigned long long s_prologue_r;
 
 // Eight consecutive source elements i0 .. i0+7 (i0 a multiple of 8) as
 // composite keys.  Only elements in [lo, hi) are meaningful; vector loads may
@@ -320,8 +322,8 @@ __device__ bool place_by_groups(const uint64_t* src, int n, uint64_t kmin, uint6
                                 const SelParams& a, int64_t row, int64_t kout, int64_t base_place, int64_t w0,
                                 int64_t w1) {
   static_assert(NB % BLOCK == 0, "whole groups per thread");
-  static_assert(NB == 256 || NB == 1024 || NB == 2048 || NB == 4096, "8, 10, 11 or 12 leading bits");
-  constexpr int kBits = NB == 4096 ? 12 : (NB == 2048 ? 11 : (NB == 1024 ? 10 : 8));
+  static_assert(NB == 256 || NB == 512 || NB == 1024 || NB == 2048 || NB == 4096, "8 to 12 leading bits");
+  constexpr int kBits = NB == 4096 ? 12 : (NB == 2048 ? 11 : (NB == 1024 ? 10 : (NB == 512 ? 9 : 8)));
   constexpr int kPer = NB / BLOCK;
   __shared__ unsigned s_gmax;
   __shared__ unsigned long long s_cost;
@@ -616,7 +618,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   const bool from_buf = SRC == 0 || (SRC == 3 && s_source == 0);
   int64_t valid = from_buf ? a.key_stride : a.len;
   if (from_buf && a.counts) {
-    const unsigned long long c = __ldcg(a.counts + row);
+    const unsigned long long c = SRC == 3 ? s_prologue_r : __ldcg(a.counts + row);
     if (c < static_cast<unsigned long long>(valid)) valid = static_cast<int64_t>(c);
     // (relaxed recall: a row returned short holds padding sentinels up to slot r)
     if (a.relax_tau && valid < a.r && a.r <= a.key_stride) valid = a.r;
@@ -1296,8 +1298,16 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   TK_STAMP(12);
   {
     const KeySpan sp = block_span<BLOCK>(bufA, n_c);
-    if (place_by_groups<BLOCK, NB>(bufA, n_c, sp.kmin, sp.kmax, 0u, ~0u, bufB, work, work + NB, work + 2 * NB,
-                                   s_tmp, 512u, a, row, k, place0, my0, my1)) {
+    // (up to 1024 keys: 512 groups, a quarter of the counters to clear and
+    // scan, still ~2 keys a group)
+    constexpr int kFewGroups = NB > 512 && BLOCK <= 512 ? 512 : NB;
+    const bool placed =
+        n_c <= 1024 ? place_by_groups<BLOCK, kFewGroups>(bufA, n_c, sp.kmin, sp.kmax, 0u, ~0u, bufB, work,
+                                                         work + kFewGroups, work + 2 * kFewGroups, s_tmp, 512u, a,
+                                                         row, k, place0, my0, my1)
+                    : place_by_groups<BLOCK, NB>(bufA, n_c, sp.kmin, sp.kmax, 0u, ~0u, bufB, work, work + NB,
+                                                 work + 2 * NB, s_tmp, 512u, a, row, k, place0, my0, my1);
+    if (placed) {
       TK_STAMP(13);
       return;
     }
@@ -1339,6 +1349,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
       const bool miss = a.force || R < static_cast<unsigned long long>(a.r) ||
                         R > static_cast<unsigned long long>(a.key_stride);
       s_source = miss ? a.miss_src : 0;
+      s_prologue_r = R;
       if (cluster.block_rank() == 0) {
         a.r_seen[row] = R;
         if (miss) atomicAdd(a.misses, 1ull);

@@ -164,5 +164,95 @@ __device__ void bucket_kth(const uint64_t* g, unsigned n, unsigned long long ran
     *out = small[tid];
 }
 
+// ---------------------------------------------------------------------------
+// The t largest of a block's keys for small t (t <= kSmallTopT), with
+// multiplicity (equal keys -- a position drawn twice -- count once each):
+// every lane sorts its few keys, each warp pops its t largest by t rounds of
+// a warp maximum (the lowest lane holding it advances), and warp 0 does the
+// same over the warps' lists.  A handful of instructions per round instead
+// of radix passes with a block barrier each.
+constexpr int kSmallTopT = 32;
+
+// Sorts v[0..MAXK) descending (a compile-time exchange network).
+template <int MAXK>
+__device__ __forceinline__ void sort_desc(uint64_t (&v)[MAXK]) {
+#pragma unroll
+  for (int i = 0; i < MAXK; ++i)
+#pragma unroll
+    for (int j = 0; j + 1 < MAXK - i; ++j)
+      if (v[j] < v[j + 1]) {
+        const uint64_t w = v[j];
+        v[j] = v[j + 1];
+        v[j + 1] = w;
+      }
+}
+
+// The lanes hold v[0..c) sorted descending.  Pops the warp's t largest
+// (t <= 32); lane r returns the r-th (0-based) in *out and the function
+// returns how many were popped (fewer when the warp holds fewer keys).
+template <int MAXK>
+__device__ __forceinline__ int warp_pop_top(uint64_t (&v)[MAXK], int c, int t, uint64_t* out) {
+  const int lane = threadIdx.x & 31;
+  int popped = 0;
+  for (int r = 0; r < t; ++r) {
+    const bool has = c > 0;
+    const uint64_t head = v[0];
+    const unsigned hi = __reduce_max_sync(kFull, has ? static_cast<unsigned>(head >> 32) : 0u);
+    const unsigned lo =
+        __reduce_max_sync(kFull, (has && static_cast<unsigned>(head >> 32) == hi) ? static_cast<unsigned>(head) : 0u);
+    const uint64_t m = (static_cast<uint64_t>(hi) << 32) | lo;
+    const unsigned wins = __ballot_sync(kFull, has && head == m);
+    if (wins == 0u) break;  // (warp-uniform)
+    if (lane == r) *out = m;
+    if (lane == __ffs(wins) - 1) {
+#pragma unroll
+      for (int j = 0; j + 1 < MAXK; ++j) v[j] = v[j + 1];
+      --c;
+    }
+    ++popped;
+  }
+  return popped;
+}
+
+// The block's t largest keys (t <= kSmallTopT), from v[0..c) per thread (any
+// order; slots >= c ignored), into top[0..n) in descending order; returns n =
+// min(t, keys held).  lists: (BLOCK / 32) * 32 keys of shared memory;
+// counts: BLOCK / 32 words; top: kSmallTopT keys; s_n: one word.  Every
+// thread of the block calls it; top and the result are valid on return.
+template <int BLOCK, int MAXK>
+__device__ int block_top_small(uint64_t (&v)[MAXK], int c, int t, uint64_t* lists, unsigned* counts,
+                               uint64_t* top, unsigned* s_n) {
+  static_assert(BLOCK / 32 <= 8, "warp 0 merges at most eight warps' lists (8 keys a lane)");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int j = 0; j < MAXK; ++j)
+    if (j >= c) v[j] = 0ull;
+  sort_desc(v);
+  uint64_t mine = 0ull;
+  const int np = warp_pop_top(v, c, t, &mine);
+  if (lane < np) lists[warp * 32 + lane] = mine;
+  if (lane == 0) counts[warp] = static_cast<unsigned>(np);
+  __syncthreads();
+  if (warp == 0) {
+    // lane l takes eight consecutive entries of one warp's (sorted) list
+    constexpr int kW = BLOCK / 32;
+    uint64_t u[8];
+    int cu = 0;
+    const int w = lane / 4, r0 = (lane % 4) * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool ok = w < kW && r0 + j < static_cast<int>(counts[w < kW ? w : 0]);
+      u[j] = ok ? lists[w * 32 + r0 + j] : 0ull;
+      cu += ok ? 1 : 0;
+    }
+    uint64_t best = 0ull;
+    const int n = warp_pop_top(u, cu, t, &best);
+    if (lane < n) top[lane] = best;
+    if (lane == 0) *s_n = static_cast<unsigned>(n);
+  }
+  __syncthreads();
+  return static_cast<int>(*s_n);
+}
+
 }  // namespace
 }  // namespace tk
