@@ -152,7 +152,7 @@ constexpr int64_t kFallbackTile = 4096;
 // survivor_shift(tau, largest sampled key) (filter_core.cuh).
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
                           unsigned long long* counts, int reserved_sms, cudaStream_t st,
-                          unsigned* refine_ctl = nullptr);
+                          unsigned* refine_ctl = nullptr, int* status = nullptr);
 // force: 0 = only rows that missed, 1 = every row (fault injection / exact path).
 cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,
                             unsigned long long* counts, const FallbackScratch& fs, int force,

@@ -54,6 +54,7 @@ struct FilterParams {
   // (kRefineGridCtlWords per selection) hold the largest sampled key and
   // receive the counts
   unsigned* refine_ctl = nullptr;
+  int* status = nullptr;  // nullable: the call's device status word (a wait that gave up)
 };
 
 __device__ __forceinline__ unsigned long long sampled_kmax(const unsigned* refine_ctl, int64_t row) {
@@ -376,6 +377,32 @@ __device__ __forceinline__ void queue_group(bool cand, const uint4& v, int64_t p
   }
 }
 
+// The common path of one full tile of a single selection: this thread's
+// kFilterUnroll groups (group u at position base + u * kFilterBlock * VEC)
+// are tested against tau's value, candidate groups queued, and the warp's
+// stage moved out once it is half full.  Called by the whole warp.
+template <int DT, bool LARGEST, int VEC, bool HIST>
+__device__ __forceinline__ void single_tile_groups(const uint4 (&v)[kFilterUnroll], int64_t base, const RowTau& t,
+                                                   const FilterParams& fp, const Stage& st, unsigned* sh_hist,
+                                                   const GroupQueue& q, unsigned& qn) {
+  bool cand[kFilterUnroll];
+  bool any = false;
+#pragma unroll
+  for (int u = 0; u < kFilterUnroll; ++u) {
+    cand[u] = group_candidate<DT, LARGEST, VEC>(v[u], t.value) || t.nan;
+    any |= cand[u];
+  }
+  if (__any_sync(kFull, any)) {
+#pragma unroll
+    for (int u = 0; u < kFilterUnroll; ++u)
+      queue_group<DT, LARGEST, VEC, HIST>(cand[u], v[u], base + u * kFilterBlock * VEC, q, qn, t, fp, st, 0,
+                                          sh_hist);
+    // a warp-uniform point: move the stage out once it is half full
+    if (__shfl_sync(kFull, *st.n, 0) >= static_cast<unsigned>(kWarpStage / 2))
+      stage_flush(st, 0, fp.cap, fp.buf, fp.counts);
+  }
+}
+
 // Tile loop of a single selection (the whole input is one row): no row
 // arithmetic per tile, one pointer step, candidate groups queued.  Covers the
 // full tiles [tile_begin, tile_end) with stride tile_step; `t` is the row's
@@ -394,23 +421,7 @@ __device__ __forceinline__ void filter_full_tiles_single(const FilterParams& fp,
     uint4 v[kFilterUnroll];
 #pragma unroll
     for (int u = 0; u < kFilterUnroll; ++u) v[u] = load_group<DT, VEC>(p + u * kFilterBlock * VEC, pol);
-    const int64_t base = tile * kTile + threadIdx.x * VEC;
-    bool cand[kFilterUnroll];
-    bool any = false;
-#pragma unroll
-    for (int u = 0; u < kFilterUnroll; ++u) {
-      cand[u] = group_candidate<DT, LARGEST, VEC>(v[u], t.value) || t.nan;
-      any |= cand[u];
-    }
-    if (__any_sync(kFull, any)) {
-#pragma unroll
-      for (int u = 0; u < kFilterUnroll; ++u)
-        queue_group<DT, LARGEST, VEC, HIST>(cand[u], v[u], base + u * kFilterBlock * VEC, q, qn, t, fp, st, 0,
-                                            sh_hist);
-      // a warp-uniform point: move the stage out once it is half full
-      if (__shfl_sync(kFull, *st.n, 0) >= static_cast<unsigned>(kWarpStage / 2))
-        stage_flush(st, 0, fp.cap, fp.buf, fp.counts);
-    }
+    single_tile_groups<DT, LARGEST, VEC, HIST>(v, tile * kTile + threadIdx.x * VEC, t, fp, st, sh_hist, q, qn);
     p += pstep;
   }
   if (qn) drain_groups<DT, LARGEST, VEC, HIST>(q, 0u, qn, t, fp, st, 0, sh_hist);

@@ -159,38 +159,6 @@ __device__ __forceinline__ void write_winner(const RowsParams& a, int64_t row, i
   else static_cast<uint16_t*>(a.out_vals)[oi] = static_cast<uint16_t>(raw);
 }
 
-// ---- bulk copies (TMA engine) completing on a shared-memory mbarrier
-__device__ __forceinline__ unsigned smem_addr(const void* p) {
-  return static_cast<unsigned>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
-  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
-               ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
-  unsigned ok;
-  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-               "selp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
-  return ok != 0;
-}
-// Waits for phase `parity` of the barrier to complete, for at most
-// kWaitLimitNs; false when it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  return true;
-}
-
 template <int DT, bool LARGEST>
 __global__ void __launch_bounds__(kRowBlock, 1) rows_kernel(RowsParams a) {
   using T = typename Dt<DT>::storage;
@@ -284,7 +252,7 @@ __global__ void __launch_bounds__(kRowBlock, 1) rows_kernel(RowsParams a) {
       if (tid == 0 && row + gridDim.x < a.nsel) {
         // the buffer was read through the generic proxy; order that before
         // the bulk copy overwrites it
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fence_proxy_async_smem();
         fetch(row + gridDim.x);
       }
     }

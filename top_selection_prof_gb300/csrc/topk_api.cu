@@ -549,7 +549,8 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // The filter may launch while the fused grid finishes (its blocks leave
     // early, one block ranks at the end), not while a 16-CTA threshold
     // cluster runs: that gained nothing.
-    TK_TRY(launch_filter(p, tau, M, buf, counts, fused ? 0 : -1, st, survivor_hist ? refine_ctl : nullptr));
+    TK_TRY(launch_filter(p, tau, M, buf, counts, fused ? 0 : -1, st, survivor_hist ? refine_ctl : nullptr,
+                         &hdr->status));
     ++nl;
     TK_TRY(mark(3));
     // Where to handle a miss: inside the refinement kernel (no launch when
