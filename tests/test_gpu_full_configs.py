@@ -83,3 +83,25 @@ def test_single_row_2p26_ties1000_sorted_k10000(largest):
 def test_batchtopk_4096x65536_relu_bf16_k131072(largest):
     st = _run("batchtopk_4096x65536_relu_bf16_k131072", largest)
     assert st["path_name"] == "profk" and (st["S"], st["t"], st["M"]) == (131072, 93, 262190)
+
+
+def test_batchtopk_4096x65536_relu_bf16_k131072_unsorted():
+    """The unsorted option on the BatchTopK workload at full size: the oracle's
+    winners as a set, each returned with the input's own bits at its index
+    (the order is left open; the Prof-K paper's BatchTopK application takes
+    the set)."""
+    import torch
+    import top_selection_prof_gb300 as tk
+    name = "batchtopk_4096x65536_relu_bf16_k131072"
+    cfg = workloads.WORKLOADS[name]
+    x = _input(name, 0)
+    xd = to_device(x)
+    v, i, st = tk.select_ex(xd, cfg["k"], eps=cfg["eps"], global_=True, unsorted=1)
+    torch.cuda.synchronize()
+    del xd
+    assert st["path_name"] == "profk" and st["launches"] == 3, st
+    ov, oi = plain.topk(x, cfg["k"], global_=True)
+    gi = i.cpu().numpy().reshape(-1)
+    assert np.array_equal(np.sort(gi), np.sort(np.asarray(oi).reshape(-1))), "winner set"
+    bits = v.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
+    assert np.array_equal(bits, x.reshape(-1)[gi].view(np.uint16)), "values are the input's bits at the indices"

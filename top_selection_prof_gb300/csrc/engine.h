@@ -168,9 +168,11 @@ constexpr int kRefineGridBins = 2048;          // first-digit bins (the bin sort
 constexpr int kRefineGridLevels = 6;           // 11-bit digits of a key of up to 64 bits
 constexpr int64_t kRefineGridMaxSel = 4;       // selections one grid refines
 // Control words per selection: NOT of the smallest and the largest key (2 x
-// 64 bits), the boundary bin's placed winners, the largest sampled key (64
-// bits at kRefineGridKmaxWord), then one counter per bin and digit level,
-// then the filter's survivor histogram (kRefineGridFilterHist).
+// 64 bits), the boundary bin's placed winners, the blocks done placing
+// (kRefineGridTicketWord), the largest sampled key (64 bits at
+// kRefineGridKmaxWord), then one counter per bin and digit level, then the
+// filter's survivor histogram (kRefineGridFilterHist).
+constexpr int64_t kRefineGridTicketWord = 5;
 constexpr int64_t kRefineGridKmaxWord = 6;
 constexpr int64_t kRefineGridFilterHist = 8 + int64_t(kRefineGridLevels) * kRefineGridBins;
 constexpr int64_t kRefineGridCtlWords = kRefineGridFilterHist + kRefineGridBins;

@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "engine.h"
+#include "rank.cuh"
 
 namespace tk {
 
@@ -15,7 +16,6 @@ namespace {
 constexpr int kFilterBlock = 256;
 constexpr int kFilterUnroll = 4;
 constexpr int kWarpStage = 256;  // survivors staged per warp before a flush
-constexpr unsigned kFull = 0xffffffffu;
 
 // Division by the invariant tiles-per-row count without a divide instruction
 // (Granlund and Montgomery, "Division by Invariant Integers using

@@ -655,8 +655,13 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
     __syncthreads();  // cur is complete
   }
   TK_RG(7);
-  // (unsorted output: the exact k-th key is always found, and only winners placed)
-  const bool whole = fast || (!rg.unsorted && static_cast<int64_t>(bb_start) + bb_tot <= rg.xstride);
+  // Unsorted output: only winners are written.  From the filter's histogram,
+  // when the boundary bin is small, the bins above it are written straight
+  // out and the boundary bin is placed whole in the exchange buffer; the
+  // last block to finish ranks it (no grid barrier).  Otherwise further
+  // digits find the exact k-th key first, one grid barrier each.
+  const bool ufinish = rg.unsorted && fast && bb_tot <= static_cast<unsigned>(kPartCache);
+  const bool whole = ufinish || (!rg.unsorted && (fast || static_cast<int64_t>(bb_start) + bb_tot <= rg.xstride));
   uint64_t kappa = 0ull;
   if (!whole) {
     // ---- the exact k-th key: further digits inside the boundary bin
@@ -746,10 +751,42 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
     const uint64_t key = stg[i];
     const unsigned pos = mine[bin_of(key)] + i;
     if (pos >= xend) continue;
-    if (rg.unsorted) {
+    if (rg.unsorted && !(ufinish && pos >= bb_start)) {
       write_winner(fp, rg, row, static_cast<int64_t>(k), pos, key + kmin, pad_below);
     } else {
       xb[pos] = key + kmin;
+    }
+  }
+  if (ufinish) {
+    // the last block to finish placing takes the top (k - bb_start) keys of
+    // the boundary bin (distinct keys: exactly that many are >= the one of
+    // that rank) to the places after the bins above it
+    __shared__ int s_last;
+    __shared__ unsigned long long s_tmp[32];
+    __shared__ unsigned long long s_rinfo[3];
+    __shared__ unsigned s_cnt;
+    __shared__ uint64_t s_kappa;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(ctl + kRefineGridTicketWord, 1u) + 1u == gridDim.x ? 1 : 0;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      const unsigned r = static_cast<unsigned>(k) - bb_start;
+      for (unsigned i = tid; i < bb_tot; i += kFilterBlock) stg[i] = __ldcg(xb + bb_start + i);
+      __syncthreads();
+      bucket_kth<kFilterBlock>(stg, bb_tot, r, mine, s_tmp, s_rinfo, &s_cnt, &s_kappa);
+      __syncthreads();
+      const uint64_t kap = s_kappa;
+      if (tid == 0) s_cnt = 0u;
+      __syncthreads();
+      for (unsigned base = 0; base < bb_tot; base += kFilterBlock) {
+        const unsigned i = base + tid;
+        const uint64_t key = i < bb_tot ? stg[i] : 0ull;
+        const bool w = i < bb_tot && key >= kap;
+        const unsigned slot = warp_append_slot(&s_cnt, w);
+        if (w && slot < r) write_winner(fp, rg, row, static_cast<int64_t>(k), bb_start + slot, key, 0ull);
+      }
     }
   }
   if (!rg.unsorted) {
@@ -807,7 +844,7 @@ __global__ void __launch_bounds__(kFilterBlock, 2) refine_grid_kernel(RefineGrid
   // a rebuilt buffer is complete once every block has filtered its tiles
   if (missed > 0 && !grid_barrier(a.fb.fs)) return;
   uint64_t* cache = &stage[0][0];
-  const bool hist_ok = rg.tau != nullptr && !rg.unsorted && missed == 0;
+  const bool hist_ok = rg.tau != nullptr && missed == 0;
   for (int64_t row = 0; row < a.fb.fp.nsel; ++row)
     if (!partition_row(a, row, cache, part_smem, hist_ok)) return;
   TK_TL_END(3);

@@ -693,21 +693,26 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     }
     __syncthreads();
     await_cluster();
-    // push this CTA's result into every CTA (remote stores need no reply)
-    if (warp == 0 && static_cast<unsigned>(lane) < G) {
-      unsigned long long* rx = cluster.map_shared_rank(xch, static_cast<unsigned>(lane));
-      rx[24 + 2 * crank] = xch[0];
-      rx[25 + 2 * crank] = xch[1];
-    }
-    TK_STAMP(20);
-    gsync();  // every CTA's OR / AND has arrived
-    TK_STAMP(21);
-    TK_CTA(2, globaltimer_ns());
-    all_or = 0ull;
-    all_and = ~0ull;
-    for (unsigned c = 0; c < G; ++c) {
-      all_or |= xch[24 + 2 * c];
-      all_and &= xch[25 + 2 * c];
+    if (G == 1) {  // one CTA: its own result is the answer
+      all_or = xch[0];
+      all_and = xch[1];
+    } else {
+      // push this CTA's result into every CTA (remote stores need no reply)
+      if (warp == 0 && static_cast<unsigned>(lane) < G) {
+        unsigned long long* rx = cluster.map_shared_rank(xch, static_cast<unsigned>(lane));
+        rx[24 + 2 * crank] = xch[0];
+        rx[25 + 2 * crank] = xch[1];
+      }
+      TK_STAMP(20);
+      gsync();  // every CTA's OR / AND has arrived
+      TK_STAMP(21);
+      TK_CTA(2, globaltimer_ns());
+      all_or = 0ull;
+      all_and = ~0ull;
+      for (unsigned c = 0; c < G; ++c) {
+        all_or |= xch[24 + 2 * c];
+        all_and &= xch[25 + 2 * c];
+      }
     }
   }
   TK_STAMP(2);
@@ -1038,7 +1043,42 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
     // (each chunk is read into registers before any of it is overwritten).
     if (tid == 0) s_cnt = 0u;
     __syncthreads();
-    if (cached) {
+    if (cached && k <= static_cast<int64_t>(NB)) {
+      // Few winners: appended to the counters' space (free once tau is
+      // known; NB keys fit), so no chunk of the cache has to be held in
+      // registers while the front of it is overwritten; then copied to the
+      // front of the cache.
+      uint64_t* win = reinterpret_cast<uint64_t*>(h2);
+      for (unsigned base = 0; base < cache_n; base += 8 * BLOCK) {
+        uint64_t kk[8];
+        unsigned wm = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const unsigned i = base + j * BLOCK + tid;
+          kk[j] = i < cache_n ? cache[i] : 0ull;
+          wm |= (i < cache_n && kk[j] >= tau ? 1u : 0u) << j;
+        }
+        const unsigned c = __popc(wm);
+        unsigned incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += y;
+        }
+        unsigned wbase = 0;
+        if (lane == 31 && incl) wbase = atomicAdd(&s_cnt, incl);
+        wbase = __shfl_sync(kFull, wbase, 31);
+        unsigned slot = wbase + incl - c;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if ((wm >> j) & 1u) {
+            if (slot < static_cast<unsigned>(k)) win[slot] = kk[j];
+            ++slot;
+          }
+      }
+      __syncthreads();
+      for (int i = tid; i < static_cast<int>(k); i += BLOCK) bufA[i] = win[i];
+    } else if (cached) {
       for (unsigned base = 0; base < cache_n; base += 8 * BLOCK) {
         uint64_t kk[8];
         unsigned wm = 0;

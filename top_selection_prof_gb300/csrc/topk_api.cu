@@ -500,7 +500,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     refine_ctl = reinterpret_cast<unsigned*>(copies + parity * kRefineCtlCopyBytes);
     refine_ctl_next = reinterpret_cast<unsigned*>(copies + (parity ^ 1u) * kRefineCtlCopyBytes);
   }
-  const bool survivor_hist = grid_refine && fused && !unsorted_out;
+  const bool survivor_hist = grid_refine && fused;
   bool fallback_launched = false;
   int nl = 0;  // kernels launched
   if (plan.path == TOPK_PATH_PROFK) {
