@@ -337,17 +337,22 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
   if (!s_last) return;
   TK_STL(0);
   __threadfence();
-  const unsigned gn = *reinterpret_cast<volatile unsigned*>(gctl);
+  // every slot of the gather buffer and its count in one round of loads
+  // (the slots past the count are dropped below)
+  constexpr int kPerThread = kTauGather / BLOCK;
+  uint64_t raw[kPerThread];
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) raw[j] = __ldcg(gat + tid + j * BLOCK);
+  const unsigned gn = __ldcg(gctl);
   const unsigned n = gn < static_cast<unsigned>(kTauGather) ? gn : static_cast<unsigned>(kTauGather);
   if (small_t) {
     // the union (at most kTauGather keys: eight a thread), its t-th largest
-    constexpr int kPerThread = kTauGather / BLOCK;
     uint64_t v[kPerThread];
     int c = 0;
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) {
       const unsigned i = tid + j * BLOCK;
-      v[j] = i < n ? __ldcg(gat + i) : 0ull;
+      v[j] = i < n ? raw[j] : 0ull;
       c += i < n ? 1 : 0;
     }
     if (tid == 0) {
@@ -365,7 +370,9 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
     }
     __syncthreads();
   } else {
-    for (unsigned i = tid; i < n; i += BLOCK) gk[i] = __ldcg(gat + i);
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j)
+      if (tid + j * BLOCK < static_cast<int>(n)) gk[tid + j * BLOCK] = raw[j];
     if (tid == 0) {
       s_tau = 0ull;
       if (gn > static_cast<unsigned>(kTauGather)) atomicCAS(status, kDevOk, kDevBadState);

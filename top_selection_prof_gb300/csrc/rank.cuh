@@ -88,23 +88,51 @@ __device__ __forceinline__ unsigned rank_in_slots(const uint64_t* src, unsigned 
   return r;
 }
 
+// rank_in_slots counted over the slots [j0, j1) only.
+__device__ __forceinline__ unsigned rank_in_slot_range(const uint64_t* src, unsigned j0, unsigned j1, unsigned i) {
+  const uint64_t v = src[i];
+  unsigned r = 0;
+  for (unsigned j = j0; j < j1; j += 8) {
+    uint64_t t[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) t[q] = j + q < j1 ? src[j + q] : 0ull;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      r += (j + q < j1 && (t[q] > v || (t[q] == v && j + q < i))) ? 1u : 0u;
+  }
+  return r;
+}
+
 // The key of 1-based descending rank `rank` among g[0..n) (in shared or
 // global memory; equal keys count once each, ranked in slot order); the
 // thread that finds it writes it to *out (the caller synchronises before
-// reading).  Few keys are ranked by counting
-// directly (up to 128); more are first narrowed by 8-bit radix passes below
-// their highest varying bit to at most 32, since counting all n keys against
-// each other costs n^2 compares on the block's few busy warps (measured: 152
-// keys ranked directly 5 us, narrowed first 1.5 us).  lh holds 256 counters;
-// s_tmp 32 words; s_info 3.  Every thread of the block calls it.
+// reading).  Few keys (up to 128) are ranked by counting directly, each key
+// by a group of p consecutive lanes that count a slice of the slots each
+// (p as large as the block allows, at most 32).  More keys are first
+// narrowed by 8-bit radix passes below their highest varying bit to at most
+// 32, since counting all n keys against each other costs n^2 compares on
+// the block's few busy warps (measured: 152 keys ranked directly by one
+// thread each 5 us, narrowed first 1.5 us).  lh holds 256 counters; s_tmp 32
+// words; s_info 3.  Every thread of the block calls it.
 template <int BLOCK>
 __device__ void bucket_kth(const uint64_t* g, unsigned n, unsigned long long rank, unsigned* lh,
                            unsigned long long* s_tmp, unsigned long long* s_info, unsigned* s_cnt, uint64_t* out) {
   const int tid = threadIdx.x, lane = tid & 31;
   if (n <= 128u) {
     __syncthreads();
-    for (unsigned i = tid; i < n; i += BLOCK)
-      if (rank_in_slots(g, n, i) == rank - 1) *out = g[i];
+    unsigned p = 1;
+    while (p < 32u && 2u * p * n <= static_cast<unsigned>(BLOCK)) p *= 2u;
+    const unsigned i = static_cast<unsigned>(tid) / p, part = static_cast<unsigned>(tid) % p;
+    unsigned r = 0;
+    if (i < n) {
+      const unsigned per = (n + p - 1u) / p;
+      const unsigned j0 = part * per < n ? part * per : n;
+      const unsigned j1 = j0 + per < n ? j0 + per : n;
+      r = rank_in_slot_range(g, j0, j1, i);
+    }
+    // (p divides 32: a key's group of lanes lies inside one warp)
+    for (unsigned o = 1; o < p; o <<= 1) r += __shfl_xor_sync(kFull, r, o);
+    if (i < n && part == 0u && r == rank - 1) *out = g[i];
     return;
   }
   uint64_t* small = reinterpret_cast<uint64_t*>(s_tmp);  // <= 32 keys (the scans are done by then)
