@@ -92,8 +92,9 @@ __global__ void __launch_bounds__(kFilterBlock, kRingBlocksPerSm) filter_ring_ke
     for (int s = 0; s < kRingStages; ++s) mbar_init(&full[s], 1u);
     s_abort = 0;
     // the input does not come from the preceding grid: these copies may
-    // start before it has finished
-    for (int64_t i = 0; i < kRingStages && i < mine; ++i) issue(i);
+    // start before it has finished (half the ring: the rest of the stream
+    // would queue in front of that grid's last loads)
+    for (int64_t i = 0; i < kRingStages / 2 && i < mine; ++i) issue(i);
   }
   if (HIST)
     for (int i = tid; i < kRefineGridBins; i += kFilterBlock) sh_hist[i] = 0u;
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kFilterBlock, kRingBlocksPerSm) filter_ring_ke
   grid_dependency_wait();  // tau and the zeroed counters come from the previous grid
   grid_launch_dependents();
   if (tid == 0) {
+    for (int64_t i = kRingStages / 2; i < kRingStages && i < mine; ++i) issue(i);
     s_words[0] = __ldcg(fp.tau);
     if (HIST) s_words[1] = sampled_kmax(fp.refine_ctl, 0);
   }
