@@ -150,9 +150,12 @@ constexpr int64_t kFallbackTile = 4096;
 // kRefineGridFilterHist, 2048 bins of their offset above tau: bin = 2047 -
 // ((key - tau) >> shift), or 0 when that exceeds 2046, with shift =
 // survivor_shift(tau, largest sampled key) (filter_core.cuh).
+// region (nullable; one selection with refine_ctl only): each filter block
+// also places its survivors in bin regions of kBinRegionCap keys at its end
+// (kRefineGridBinnedWord of refine_ctl set when they do not fit).
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
                           unsigned long long* counts, int reserved_sms, cudaStream_t st,
-                          unsigned* refine_ctl = nullptr, int* status = nullptr);
+                          unsigned* refine_ctl = nullptr, int* status = nullptr, uint64_t* region = nullptr);
 // force: 0 = only rows that missed, 1 = every row (fault injection / exact path).
 cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,
                             unsigned long long* counts, const FallbackScratch& fs, int force,
@@ -171,11 +174,17 @@ constexpr int64_t kRefineGridMaxSel = 4;       // selections one grid refines
 // 64 bits), the boundary bin's placed winners, the blocks done placing
 // (kRefineGridTicketWord), the largest sampled key (64 bits at
 // kRefineGridKmaxWord), then one counter per bin and digit level, then the
-// filter's survivor histogram (kRefineGridFilterHist).
+// filter's survivor histogram (kRefineGridFilterHist), then a word the
+// filter sets when its bin regions are incomplete (kRefineGridBinnedWord).
 constexpr int64_t kRefineGridTicketWord = 5;
 constexpr int64_t kRefineGridKmaxWord = 6;
 constexpr int64_t kRefineGridFilterHist = 8 + int64_t(kRefineGridLevels) * kRefineGridBins;
-constexpr int64_t kRefineGridCtlWords = kRefineGridFilterHist + kRefineGridBins;
+constexpr int64_t kRefineGridBinnedWord = kRefineGridFilterHist + kRefineGridBins;
+constexpr int64_t kRefineGridCtlWords = kRefineGridBinnedWord + 4;
+// Bin regions (one selection): the filter may also place its survivors by
+// the bin of the survivor histogram, kBinRegionCap keys a bin, bin b's keys
+// at [b * kBinRegionCap, ...) in no particular order.
+constexpr int64_t kBinRegionCap = 2048;
 struct RefineGridScratch {
   unsigned* ctl;          // this call's control words: kRefineGridCtlWords per selection, zero on entry
   unsigned* ctl_next;     // the other copy (kRefineGridMaxSel selections), cleared here for the next call
@@ -197,6 +206,10 @@ struct RefineGridScratch {
   // pass, no grid barrier) when no selection missed, the top bin is empty
   // and the boundary bin fits the exchange buffer.
   const uint64_t* tau = nullptr;
+  // Non-null when the filter also placed its survivors in bin regions (one
+  // selection, kBinRegionCap keys a bin): with the histogram usable and the
+  // regions complete, the winners are copied from them in place order.
+  const uint64_t* region = nullptr;
 };
 // The padding of relaxed recall for one output element: value bits of -inf
 // (+inf when the smallest are selected), as f32 or bf16 bits.

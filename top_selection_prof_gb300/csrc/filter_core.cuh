@@ -55,7 +55,17 @@ struct FilterParams {
   // receive the counts
   unsigned* refine_ctl = nullptr;
   int* status = nullptr;  // nullable: the call's device status word (a wait that gave up)
+  // nullable (one selection, with refine_ctl): the survivors stay in the
+  // warps' stages until the block ends, which places them in bin regions
+  // of kBinRegionCap keys (the filter_ring_kernel's end)
+  uint64_t* region = nullptr;
 };
+
+// The word a filter block sets when its survivors did not all stay in its
+// stages or a bin region overflowed: the regions are then incomplete.
+__device__ __forceinline__ unsigned* binned_bad_word(const FilterParams& fp, int64_t row) {
+  return fp.refine_ctl + row * kRefineGridCtlWords + kRefineGridBinnedWord;
+}
 
 __device__ __forceinline__ unsigned long long sampled_kmax(const unsigned* refine_ctl, int64_t row) {
   return __ldcg(reinterpret_cast<const unsigned long long*>(refine_ctl + row * kRefineGridCtlWords +
@@ -271,19 +281,26 @@ __device__ __forceinline__ uint32_t exact_mask(const uint4& v, int64_t pos, cons
 }
 
 // Appends the elements of `mask` to the warp's stage with one shared atomic;
-// what does not fit is appended to the buffer directly.  HIST: each survivor
-// is also counted into the block's histogram of its offset above tau.
+// what does not fit is appended to the buffer directly (and, when the block
+// bins its survivors, marks the bin regions incomplete).  HIST: each
+// survivor is also counted into the block's histogram of its offset above tau.
 template <int DT, int VEC, bool HIST>
-__device__ __forceinline__ void lane_append(uint32_t mask, const uint4& v, int64_t pos, int ib, uint32_t flip,
-                                            const Stage& st, int64_t row, int64_t cap, uint64_t* buf,
-                                            unsigned long long* counts, const RowTau& t, unsigned* sh_hist) {
+__device__ __forceinline__ void lane_append(uint32_t mask, const uint4& v, int64_t pos, const FilterParams& fp,
+                                            const Stage& st, int64_t row, const RowTau& t, unsigned* sh_hist) {
+  const int ib = fp.ib;
+  const uint32_t flip = fp.flip;
+  const int64_t cap = fp.cap;
+  uint64_t* buf = fp.buf;
   const unsigned n = __popc(mask);
   const unsigned slot = atomicAdd(st.n, n);
   const unsigned fit = slot >= static_cast<unsigned>(kWarpStage)
                            ? 0u
                            : (slot + n <= static_cast<unsigned>(kWarpStage) ? n : kWarpStage - slot);
   unsigned long long gbase = 0;
-  if (fit < n) gbase = atomicAdd(counts + row, static_cast<unsigned long long>(n - fit));
+  if (fit < n) {
+    gbase = atomicAdd(fp.counts + row, static_cast<unsigned long long>(n - fit));
+    if (fp.region) *binned_bad_word(fp, row) = 1u;
+  }
   unsigned j = 0;
   while (mask) {
     const int e = __ffs(mask) - 1;
@@ -322,7 +339,7 @@ __device__ __forceinline__ bool test_group(const uint4& v, int64_t pos, const Ro
   if (group_candidate<DT, LARGEST, VEC>(v, t.value) || t.nan) {
     const uint32_t mask = exact_mask<DT, LARGEST, VEC>(v, pos, t, fp.ib, fp.flip);
     if (mask) {
-      lane_append<DT, VEC, HIST>(mask, v, pos, fp.ib, fp.flip, st, row, fp.cap, fp.buf, fp.counts, t, sh_hist);
+      lane_append<DT, VEC, HIST>(mask, v, pos, fp, st, row, t, sh_hist);
       return true;
     }
   }
@@ -350,7 +367,7 @@ __device__ __forceinline__ void drain_groups(const GroupQueue& q, unsigned first
     const uint4 v = q.v[first + lane];
     const int64_t pos = q.pos[first + lane];
     const uint32_t mask = exact_mask<DT, LARGEST, VEC>(v, pos, t, fp.ib, fp.flip);
-    if (mask) lane_append<DT, VEC, HIST>(mask, v, pos, fp.ib, fp.flip, st, row, fp.cap, fp.buf, fp.counts, t, sh_hist);
+    if (mask) lane_append<DT, VEC, HIST>(mask, v, pos, fp, st, row, t, sh_hist);
   }
   __syncwarp();
 }
@@ -397,8 +414,9 @@ __device__ __forceinline__ void single_tile_groups(const uint4 (&v)[kFilterUnrol
     for (int u = 0; u < kFilterUnroll; ++u)
       queue_group<DT, LARGEST, VEC, HIST>(cand[u], v[u], base + u * kFilterBlock * VEC, q, qn, t, fp, st, 0,
                                           sh_hist);
-    // a warp-uniform point: move the stage out once it is half full
-    if (__shfl_sync(kFull, *st.n, 0) >= static_cast<unsigned>(kWarpStage / 2))
+    // a warp-uniform point: move the stage out once it is half full (unless
+    // the block bins its survivors at its end: they stay)
+    if (!fp.region && __shfl_sync(kFull, *st.n, 0) >= static_cast<unsigned>(kWarpStage / 2))
       stage_flush(st, 0, fp.cap, fp.buf, fp.counts);
   }
 }

@@ -517,15 +517,21 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   // ---- this block's slice of the buffer: bounds fixed by the capacity (the
   // host checks cap <= gridDim.x * kPartCache), so its loads are in flight
   // before R is known; keys at or beyond the valid count are dropped below
+  // (when the filter also placed the survivors in bin regions they are
+  // usually copied from there, and the slice is loaded only if not)
   const int64_t sb = fp.cap * blockIdx.x / gridDim.x, se = fp.cap * (blockIdx.x + 1) / gridDim.x;
   const uint64_t* src = fp.buf + row * fp.cap + sb;
   constexpr int kSliceLoads = kPartCache / kFilterBlock;
   uint64_t kv[kSliceLoads];
+  auto load_slice = [&]() {
 #pragma unroll
-  for (int q = 0; q < kSliceLoads; ++q) {
-    const int64_t i = tid + q * kFilterBlock;
-    kv[q] = i < se - sb ? __ldcg(src + i) : 0ull;
-  }
+    for (int q = 0; q < kSliceLoads; ++q) {
+      const int64_t i = tid + q * kFilterBlock;
+      kv[q] = i < se - sb ? __ldcg(src + i) : 0ull;
+    }
+  };
+  const bool regions = hist_ok && rg.region != nullptr;
+  if (!regions) load_slice();
 
   // ---- the filter's histogram of the survivors' offsets above tau, when it
   // was kept and the buffer holds exactly the survivors it counted (no miss):
@@ -534,12 +540,13 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   // tau) and the boundary bin fits the exchange buffer after the bins above.
   // The words every block reads are loaded by one thread each and shared: R,
   // the relaxed-recall tau, tau and the largest sampled key.
-  __shared__ unsigned long long s_words[4];
+  __shared__ unsigned long long s_words[5];
   if (tid == 0) {
     s_words[0] = __ldcg(fp.counts + row);
     s_words[1] = fs.relax_tau ? __ldcg(fs.relax_tau + row) : 0ull;
     s_words[2] = hist_ok ? __ldcg(rg.tau + row) : 0ull;
     s_words[3] = hist_ok ? sampled_kmax(rg.ctl, row) : 0ull;
+    s_words[4] = hist_ok && rg.region ? __ldcg(ctl + kRefineGridBinnedWord) : 1ull;  // 0: bin regions complete
   }
   bool fast = false;
   unsigned bb = 0, bb_start = 0, bb_tot = 0;
@@ -552,9 +559,116 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
       fast = bst[1] == 0u && static_cast<int64_t>(bb_start) + bb_tot <= rg.xstride;  // top bin empty
     }
   }
+  TK_RG(4);
   __syncthreads();  // s_info is rewritten below; s_words are visible
 
+  // ---- bin regions: the filter left every survivor in its bin's region,
+  // so the winners' bins are copied out in place order -- no slice, no
+  // histogram, no atomics here.  Sorted output: places [0, end of the
+  // boundary bin) to the exchange buffer, as the partition below would have
+  // placed them, for the bin sort.  Unsorted: the bins above the boundary
+  // straight to the outputs, and block 0 ranks the boundary bin.
+  if (regions && fast && s_words[4] == 0ull && (!rg.unsorted || bb_tot <= static_cast<unsigned>(kPartCache))) {
+    TK_RG(3);
+    const uint64_t tau = s_words[2];
+    const int hs = survivor_shift(tau, s_words[3]);
+    const unsigned xend = bb_start + bb_tot;
+    // places copied here (unsorted: those of the bins above the boundary,
+    // by every block but the last, which ranks the boundary bin)
+    const unsigned pend = rg.unsorted ? bb_start : xend;
+    const unsigned ncopy = rg.unsorted && gridDim.x > 1 ? gridDim.x - 1 : gridDim.x;
+    const unsigned per = (pend + ncopy - 1) / ncopy;
+    const unsigned p0 = blockIdx.x < ncopy && blockIdx.x * per < pend ? blockIdx.x * per : pend;
+    const unsigned p1 = p0 + per < pend ? p0 + per : pend;
+    uint64_t* xb = rg.xbuf + row * rg.xstride;
+    // each place's bin by a binary search over the bin starts (the last of
+    // bins 0..bb starting at or before it), four places of a thread at once
+    // so that their searches and loads overlap (walking the bins in order
+    // instead costs a step per bin, and the top bins are mostly empty)
+    constexpr int kCopyPer = 4;
+    for (unsigned base = p0; base < p1; base += kCopyPer * kFilterBlock) {
+      unsigned pl[kCopyPer], bl[kCopyPer];
+      uint64_t key[kCopyPer];
+#pragma unroll
+      for (int j = 0; j < kCopyPer; ++j) {
+        pl[j] = base + j * kFilterBlock + tid;
+        bl[j] = 0u;
+      }
+      // (bst is non-decreasing and bst[0] = 0: the largest bin <= bb whose
+      // start is <= the place, in a fixed number of steps)
+#pragma unroll
+      for (unsigned stp = kRefineGridBins / 2; stp > 0; stp >>= 1)
+#pragma unroll
+        for (int j = 0; j < kCopyPer; ++j)
+          if (bl[j] + stp <= bb && bst[bl[j] + stp] <= pl[j]) bl[j] += stp;
+#pragma unroll
+      for (int j = 0; j < kCopyPer; ++j)
+        key[j] = pl[j] < p1 ? __ldcg(rg.region + static_cast<int64_t>(bl[j]) * kBinRegionCap + (pl[j] - bst[bl[j]]))
+                            : 0ull;
+#pragma unroll
+      for (int j = 0; j < kCopyPer; ++j) {
+        if (pl[j] >= p1) continue;
+        if (rg.unsorted) write_winner(fp, rg, row, static_cast<int64_t>(k), pl[j], key[j], 0ull);
+        else xb[pl[j]] = key[j];
+      }
+    }
+    TK_RG(5);
+    if (rg.unsorted) {
+      if (blockIdx.x == gridDim.x - 1) {
+        // the top (k - bb_start) keys of the boundary bin (distinct keys:
+        // exactly that many are >= the one of that rank)
+        __shared__ unsigned long long s_tmp[32];
+        __shared__ unsigned long long s_rinfo[3];
+        __shared__ unsigned s_cnt;
+        __shared__ uint64_t s_kappa;
+        const unsigned r = static_cast<unsigned>(k) - bb_start;
+        const uint64_t* rb = rg.region + static_cast<int64_t>(bb) * kBinRegionCap;
+        for (unsigned i = tid; i < bb_tot; i += kFilterBlock) stg[i] = __ldcg(rb + i);
+        __syncthreads();
+        TK_RG(6);
+        bucket_kth<kFilterBlock>(stg, bb_tot, r, mine, s_tmp, s_rinfo, &s_cnt, &s_kappa);
+        __syncthreads();
+        TK_RG(7);
+        const uint64_t kap = s_kappa;
+        if (tid == 0) s_cnt = 0u;
+        __syncthreads();
+        for (unsigned base = 0; base < bb_tot; base += kFilterBlock) {
+          const unsigned i = base + tid;
+          const uint64_t key = i < bb_tot ? stg[i] : 0ull;
+          const bool w = i < bb_tot && key >= kap;
+          const unsigned slot = warp_append_slot(&s_cnt, w);
+          if (w && slot < r) write_winner(fp, rg, row, static_cast<int64_t>(k), bb_start + slot, key, 0ull);
+        }
+      }
+    } else {
+      // the bin sort's view, as below: digits of key - tau with the filter's shift
+      unsigned* bo = rg.binfo + row * binfo_words(static_cast<int64_t>(k));
+      const int bper = (kRefineGridBins + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+      if (tid < bper && static_cast<int>(blockIdx.x) * bper + tid < kRefineGridBins)
+        bo[blockIdx.x * bper + tid] = bst[blockIdx.x * bper + tid];
+      publish_chunks(bst, xend, static_cast<int64_t>(k), bo + kRefineGridBins + 8,
+                     static_cast<int>(blockIdx.x) + tid * static_cast<int>(gridDim.x),
+                     static_cast<int>(gridDim.x) * kFilterBlock);
+      if (blockIdx.x == 0 && tid == 0) {
+        const uint64_t pm = hs + kPartDigit >= 64 ? 0ull : (~0ull << (hs + kPartDigit));
+        bo[kRefineGridBins] = 0u;  // prefix of the first digit (no bits above it vary)
+        bo[kRefineGridBins + 1] = 0u;
+        bo[kRefineGridBins + 2] = static_cast<unsigned>(pm);
+        bo[kRefineGridBins + 3] = static_cast<unsigned>(pm >> 32);
+        bo[kRefineGridBins + 4] = static_cast<unsigned>(hs);
+        bo[kRefineGridBins + 5] = xend;
+        bo[kRefineGridBins + 6] = static_cast<unsigned>(tau);  // digits are of key - tau
+        bo[kRefineGridBins + 7] = static_cast<unsigned>(tau >> 32);
+      }
+    }
+    TK_RG(8);
+    __syncthreads();  // the shared arrays are reused by the next selection
+    TK_RG(9);
+    return true;
+  }
+
   // ---- the block's slice, cached; the base and the digit of the partition
+  if (regions) load_slice();
   const unsigned long long R = s_words[0];
   int64_t n = R < static_cast<unsigned long long>(fp.cap) ? static_cast<int64_t>(R) : fp.cap;
   // relaxed recall: a row returned short holds sentinel keys up to slot k

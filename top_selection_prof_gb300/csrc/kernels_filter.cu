@@ -143,13 +143,54 @@ __global__ void __launch_bounds__(kFilterBlock, kRingBlocksPerSm) filter_ring_ke
   if (qn) drain_groups<DT, LARGEST, VEC, HIST>(q, 0u, qn, t, fp, st, 0, sh_hist);
   const int64_t ntiles = (fp.len + kTile - 1) / kTile;
   if (ntiles > nfull && nfull % step == first) {
-    // the partial tile by the generic loop, which also moves the stage and
-    // the histogram out
-    filter_tiles<DT, LARGEST, VEC, HIST>(fp, nfull, nfull + 1, 1, st, sh_hist, nullptr);
-  } else {
-    stage_flush(st, 0, fp.cap, fp.buf, fp.counts);
-    if (HIST) hist_flush(sh_hist, fp, 0);
+    // the partial last tile: whole 16-byte groups (the length is a multiple
+    // of the group), each tested in place
+    const T* x = static_cast<const T*>(fp.x);
+#pragma unroll
+    for (int u = 0; u < kFilterUnroll; ++u) {
+      const int64_t pos = nfull * kTile + (static_cast<int64_t>(u) * kFilterBlock + tid) * VEC;
+      if (pos < fp.len) test_group<DT, LARGEST, VEC, HIST>(load_group<DT, VEC>(x + pos, pol), pos, t, fp, st, 0, sh_hist);
+    }
   }
+  if (HIST && fp.region) {
+    // Bin regions: one returning atomic per non-empty bin adds this block's
+    // counts to the histogram and returns where its keys start in each
+    // bin's region; then every survivor (all still in the warps' stages)
+    // goes to its bin's region.  A bin that would overflow its region marks
+    // the regions incomplete.
+    __syncthreads();  // every warp's stage and the block's counts are final
+    unsigned* g = fp.refine_ctl + kRefineGridFilterHist;
+    unsigned* cur = reinterpret_cast<unsigned*>(queue_v);  // (free now: 2048 counters)
+    static_assert(sizeof(queue_v) >= sizeof(unsigned) * kRefineGridBins, "bin cursors");
+    constexpr int kPer = kRefineGridBins / kFilterBlock;
+    unsigned c[kPer], r[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) c[j] = sh_hist[tid + j * kFilterBlock];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) r[j] = c[j] ? atomicAdd(g + tid + j * kFilterBlock, c[j]) : 0u;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      sh_hist[tid + j * kFilterBlock] = r[j];
+      cur[tid + j * kFilterBlock] = 0u;
+    }
+    __syncthreads();
+    bool over = false;
+    for (int idx = tid; idx < (kFilterBlock / 32) * kWarpStage; idx += kFilterBlock) {
+      const int w = idx / kWarpStage, j = idx % kWarpStage;
+      const unsigned nw = stage_n[w] < static_cast<unsigned>(kWarpStage) ? stage_n[w] : kWarpStage;
+      if (static_cast<unsigned>(j) < nw) {
+        const uint64_t key = stage[w][j];
+        const unsigned b = survivor_bin(key, t.key, t.hshift);
+        const unsigned slot = sh_hist[b] + atomicAdd(&cur[b], 1u);
+        if (slot < static_cast<unsigned>(kBinRegionCap)) fp.region[static_cast<int64_t>(b) * kBinRegionCap + slot] = key;
+        else over = true;
+      }
+    }
+    if (over) *binned_bad_word(fp, 0) = 1u;
+    __syncthreads();  // (stage_flush below clears the stage counts)
+  }
+  stage_flush(st, 0, fp.cap, fp.buf, fp.counts);
+  if (HIST && !fp.region) hist_flush(sh_hist, fp, 0);
   TK_TL_END(2);
 }
 
@@ -239,10 +280,12 @@ cudaError_t launch_filter_h(const FilterParams& fp, int reserved_sms, cudaStream
 
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
                           unsigned long long* counts, int reserved_sms, cudaStream_t st, unsigned* refine_ctl,
-                          int* status) {
+                          int* status, uint64_t* region) {
   FilterParams fp{p.x, p.nsel, p.len, p.ib, p.flip, tau, cap, buf, counts, Divider{}};
   fp.refine_ctl = refine_ctl;
   fp.status = status;
+  // (bin regions: the TMA-ring filter of one selection with the survivor histogram)
+  fp.region = (p.nsel == 1 && p.vec_ok && refine_ctl) ? region : nullptr;
   const bool largest = p.flip == 0;
   if (p.nsel == 1 && p.vec_ok) {
     // (every block of the ring grid may start late: its tiles wait in the

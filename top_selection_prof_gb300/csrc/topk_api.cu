@@ -442,6 +442,16 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   const size_t o_buf = off; off = align_up(off + sizeof(uint64_t) * nsel * M);
   const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * nsel * select_xbuf_stride(k));
   const size_t o_binfo = off; off = align_up(off + sizeof(unsigned) * nsel * select_binfo_words(k));
+  // bin regions (the grid refinement of one selection after a fused sampler
+  // and the TMA-ring filter): left out when a fixed scratch has no room
+  bool binned = plan.path == TOPK_PATH_PROFK && fused && nsel == 1 && p.vec_ok && select_binfo_words(k) > 0 &&
+                nsel <= kRefineGridMaxSel;
+  const size_t o_region = off;
+  if (binned) {
+    const size_t with = align_up(off + sizeof(uint64_t) * kRefineGridBins * kBinRegionCap);
+    if (src.fixed && with > src.fixed->bytes) binned = false;
+    else off = with;
+  }
   void* ws = nullptr;
   ScratchCounters* wcnt = nullptr;
   {
@@ -501,6 +511,8 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     refine_ctl_next = reinterpret_cast<unsigned*>(copies + (parity ^ 1u) * kRefineCtlCopyBytes);
   }
   const bool survivor_hist = grid_refine && fused;
+  binned = binned && survivor_hist;
+  auto* region = binned ? reinterpret_cast<uint64_t*>(base + o_region) : nullptr;
   bool fallback_launched = false;
   int nl = 0;  // kernels launched
   if (plan.path == TOPK_PATH_PROFK) {
@@ -550,7 +562,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // early, one block ranks at the end), not while a 16-CTA threshold
     // cluster runs: that gained nothing.
     TK_TRY(launch_filter(p, tau, M, buf, counts, fused ? 0 : -1, st, survivor_hist ? refine_ctl : nullptr,
-                         &hdr->status));
+                         &hdr->status, region));
     ++nl;
     TK_TRY(mark(3));
     // Where to handle a miss: inside the refinement kernel (no launch when
@@ -611,6 +623,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     rg.ctl = refine_ctl;
     rg.ctl_next = refine_ctl_next;
     rg.tau = survivor_hist ? tau : nullptr;
+    rg.region = region;
     rg.xbuf = xbuf;
     rg.xstride = rj.xbuf_stride;
     rg.binfo = rj.binfo;
