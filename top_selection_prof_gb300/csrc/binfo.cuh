@@ -1,9 +1,11 @@
 // The bin information a partition publishes for the bin sort (kernels_select.cu),
 // shared by its two producers: the refinement cluster (kernels_select.cu) and
 // the grid refinement (kernels_fallback.cu).  Per selection, binfo_words(k)
-// words: the kRefineGridBins bin starts (bins in descending key order), eight
-// words describing the first digit (prefix, mask, shift, the end of the
-// placed keys, the base the digits are relative to), then one descriptor of
+// words: the kRefineGridBins bin starts (bins in descending key order),
+// kBinfoHeaderWords words describing the first digit (prefix, mask, shift,
+// the end of the placed keys, the base the digits are relative to; word 8:
+// 1 when the keys stayed in the filter's bin regions, whose bins are these
+// digits, and nothing else was published), then one descriptor of
 // kChunkWords words per chunk of kBinSortChunk output places: the first and
 // the last bin the chunk's places fall in, with the start and end of each,
 // so that a bin-sort block reads its bins with one round of loads instead of

@@ -260,13 +260,20 @@ struct SelectJob {
   // the fallback's padding sentinels (the fallback's tau_exact words), written
   // as index -1 and -inf (+inf)
   const uint64_t* relax_tau = nullptr;
+  // bin sort, one selection (nullable): the filter's survivor histogram and
+  // its bin regions, read when the refinement found them complete (the bin
+  // information's header says so) instead of the exchange buffer
+  const unsigned* fhist = nullptr;
+  const uint64_t* region = nullptr;
 };
 int64_t select_binfo_words(int64_t k);  // 0 when k is too small for the bin sort
 // Output places one bin-sort block owns, and the words of bin information
-// per selection (bin starts, the digit, one descriptor per chunk: binfo.cuh).
+// per selection (bin starts, a header describing the digit, one descriptor
+// per chunk: binfo.cuh).
 constexpr int64_t kBinSortChunk = 512;
+constexpr int kBinfoHeaderWords = 12;
 TK_HOST_DEVICE inline int64_t binfo_words(int64_t k) {
-  return kRefineGridBins + 8 + 6 * ((k + kBinSortChunk - 1) / kBinSortChunk);
+  return kRefineGridBins + kBinfoHeaderWords + 6 * ((k + kBinSortChunk - 1) / kBinSortChunk);
 }
 // The bin sort alone (job: r = k, xbuf, xbuf_stride, binfo, status, outputs),
 // after the grid refinement has partitioned the winners.

@@ -540,13 +540,42 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   // tau) and the boundary bin fits the exchange buffer after the bins above.
   // The words every block reads are loaded by one thread each and shared: R,
   // the relaxed-recall tau, tau and the largest sampled key.
-  __shared__ unsigned long long s_words[5];
+  __shared__ unsigned long long s_words[6];
   if (tid == 0) {
     s_words[0] = __ldcg(fp.counts + row);
     s_words[1] = fs.relax_tau ? __ldcg(fs.relax_tau + row) : 0ull;
     s_words[2] = hist_ok ? __ldcg(rg.tau + row) : 0ull;
     s_words[3] = hist_ok ? sampled_kmax(rg.ctl, row) : 0ull;
-    s_words[4] = hist_ok && rg.region ? __ldcg(ctl + kRefineGridBinnedWord) : 1ull;  // 0: bin regions complete
+    s_words[4] = regions ? __ldcg(ctl + kRefineGridBinnedWord) : 1ull;  // 0: bin regions complete
+    s_words[5] = regions ? __ldcg(ctl + kRefineGridFilterHist) : 1ull;  // the top (overflow) bin's count
+  }
+  if (regions && !rg.unsorted) {
+    // Sorted output from complete bin regions whose top bin is empty (so
+    // the bins are a plain digit of key - tau): nothing to place here.  The
+    // bin sort reads the filter's histogram and the regions itself; this
+    // kernel only checked the miss (no miss: R is within [k, M] and the
+    // histogram counts exactly the survivors) and publishes the digit.
+    __syncthreads();
+    if (s_words[4] == 0ull && s_words[5] == 0ull) {
+      if (blockIdx.x == 0 && tid == 0) {
+        const uint64_t tau = s_words[2];
+        const int hs = survivor_shift(tau, s_words[3]);
+        const uint64_t pm = hs + kPartDigit >= 64 ? 0ull : (~0ull << (hs + kPartDigit));
+        unsigned* bo = rg.binfo + row * binfo_words(static_cast<int64_t>(k));
+        bo[kRefineGridBins] = 0u;
+        bo[kRefineGridBins + 1] = 0u;
+        bo[kRefineGridBins + 2] = static_cast<unsigned>(pm);
+        bo[kRefineGridBins + 3] = static_cast<unsigned>(pm >> 32);
+        bo[kRefineGridBins + 4] = static_cast<unsigned>(hs);
+        bo[kRefineGridBins + 5] = 0u;  // (the bin sort finds the end of the boundary bin)
+        bo[kRefineGridBins + 6] = static_cast<unsigned>(tau);
+        bo[kRefineGridBins + 7] = static_cast<unsigned>(tau >> 32);
+        bo[kRefineGridBins + 8] = 1u;  // the keys are in the bin regions
+      }
+      __syncthreads();  // (s_words is rewritten by the next selection)
+      TK_RG(9);
+      return true;
+    }
   }
   bool fast = false;
   unsigned bb = 0, bb_start = 0, bb_tot = 0;
@@ -568,23 +597,20 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   // boundary bin) to the exchange buffer, as the partition below would have
   // placed them, for the bin sort.  Unsorted: the bins above the boundary
   // straight to the outputs, and block 0 ranks the boundary bin.
-  if (regions && fast && s_words[4] == 0ull && (!rg.unsorted || bb_tot <= static_cast<unsigned>(kPartCache))) {
+  if (regions && rg.unsorted && fast && s_words[4] == 0ull && bb_tot <= static_cast<unsigned>(kPartCache)) {
+    // Unsorted output from complete bin regions: the bins above the
+    // boundary go straight to the outputs, split over every block but the
+    // last, which ranks the boundary bin.
     TK_RG(3);
-    const uint64_t tau = s_words[2];
-    const int hs = survivor_shift(tau, s_words[3]);
-    const unsigned xend = bb_start + bb_tot;
-    // places copied here (unsorted: those of the bins above the boundary,
-    // by every block but the last, which ranks the boundary bin)
-    const unsigned pend = rg.unsorted ? bb_start : xend;
-    const unsigned ncopy = rg.unsorted && gridDim.x > 1 ? gridDim.x - 1 : gridDim.x;
+    const unsigned pend = bb_start;
+    const unsigned ncopy = gridDim.x > 1 ? gridDim.x - 1 : 1u;
     const unsigned per = (pend + ncopy - 1) / ncopy;
     const unsigned p0 = blockIdx.x < ncopy && blockIdx.x * per < pend ? blockIdx.x * per : pend;
     const unsigned p1 = p0 + per < pend ? p0 + per : pend;
-    uint64_t* xb = rg.xbuf + row * rg.xstride;
-    // each place's bin by a binary search over the bin starts (the last of
-    // bins 0..bb starting at or before it), four places of a thread at once
-    // so that their searches and loads overlap (walking the bins in order
-    // instead costs a step per bin, and the top bins are mostly empty)
+    // each place's bin by a binary search over the bin starts, four places
+    // of a thread at once so that their searches and loads overlap (walking
+    // the bins in order instead costs a step per bin, and the top bins are
+    // mostly empty)
     constexpr int kCopyPer = 4;
     for (unsigned base = p0; base < p1; base += kCopyPer * kFilterBlock) {
       unsigned pl[kCopyPer], bl[kCopyPer];
@@ -606,59 +632,34 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
         key[j] = pl[j] < p1 ? __ldcg(rg.region + static_cast<int64_t>(bl[j]) * kBinRegionCap + (pl[j] - bst[bl[j]]))
                             : 0ull;
 #pragma unroll
-      for (int j = 0; j < kCopyPer; ++j) {
-        if (pl[j] >= p1) continue;
-        if (rg.unsorted) write_winner(fp, rg, row, static_cast<int64_t>(k), pl[j], key[j], 0ull);
-        else xb[pl[j]] = key[j];
-      }
+      for (int j = 0; j < kCopyPer; ++j)
+        if (pl[j] < p1) write_winner(fp, rg, row, static_cast<int64_t>(k), pl[j], key[j], 0ull);
     }
     TK_RG(5);
-    if (rg.unsorted) {
-      if (blockIdx.x == gridDim.x - 1) {
-        // the top (k - bb_start) keys of the boundary bin (distinct keys:
-        // exactly that many are >= the one of that rank)
-        __shared__ unsigned long long s_tmp[32];
-        __shared__ unsigned long long s_rinfo[3];
-        __shared__ unsigned s_cnt;
-        __shared__ uint64_t s_kappa;
-        const unsigned r = static_cast<unsigned>(k) - bb_start;
-        const uint64_t* rb = rg.region + static_cast<int64_t>(bb) * kBinRegionCap;
-        for (unsigned i = tid; i < bb_tot; i += kFilterBlock) stg[i] = __ldcg(rb + i);
-        __syncthreads();
-        TK_RG(6);
-        bucket_kth<kFilterBlock>(stg, bb_tot, r, mine, s_tmp, s_rinfo, &s_cnt, &s_kappa);
-        __syncthreads();
-        TK_RG(7);
-        const uint64_t kap = s_kappa;
-        if (tid == 0) s_cnt = 0u;
-        __syncthreads();
-        for (unsigned base = 0; base < bb_tot; base += kFilterBlock) {
-          const unsigned i = base + tid;
-          const uint64_t key = i < bb_tot ? stg[i] : 0ull;
-          const bool w = i < bb_tot && key >= kap;
-          const unsigned slot = warp_append_slot(&s_cnt, w);
-          if (w && slot < r) write_winner(fp, rg, row, static_cast<int64_t>(k), bb_start + slot, key, 0ull);
-        }
-      }
-    } else {
-      // the bin sort's view, as below: digits of key - tau with the filter's shift
-      unsigned* bo = rg.binfo + row * binfo_words(static_cast<int64_t>(k));
-      const int bper = (kRefineGridBins + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-      if (tid < bper && static_cast<int>(blockIdx.x) * bper + tid < kRefineGridBins)
-        bo[blockIdx.x * bper + tid] = bst[blockIdx.x * bper + tid];
-      publish_chunks(bst, xend, static_cast<int64_t>(k), bo + kRefineGridBins + 8,
-                     static_cast<int>(blockIdx.x) + tid * static_cast<int>(gridDim.x),
-                     static_cast<int>(gridDim.x) * kFilterBlock);
-      if (blockIdx.x == 0 && tid == 0) {
-        const uint64_t pm = hs + kPartDigit >= 64 ? 0ull : (~0ull << (hs + kPartDigit));
-        bo[kRefineGridBins] = 0u;  // prefix of the first digit (no bits above it vary)
-        bo[kRefineGridBins + 1] = 0u;
-        bo[kRefineGridBins + 2] = static_cast<unsigned>(pm);
-        bo[kRefineGridBins + 3] = static_cast<unsigned>(pm >> 32);
-        bo[kRefineGridBins + 4] = static_cast<unsigned>(hs);
-        bo[kRefineGridBins + 5] = xend;
-        bo[kRefineGridBins + 6] = static_cast<unsigned>(tau);  // digits are of key - tau
-        bo[kRefineGridBins + 7] = static_cast<unsigned>(tau >> 32);
+    if (blockIdx.x == gridDim.x - 1) {
+      // the top (k - bb_start) keys of the boundary bin (distinct keys:
+      // exactly that many are >= the one of that rank)
+      __shared__ unsigned long long s_tmp[32];
+      __shared__ unsigned long long s_rinfo[3];
+      __shared__ unsigned s_cnt;
+      __shared__ uint64_t s_kappa;
+      const unsigned r = static_cast<unsigned>(k) - bb_start;
+      const uint64_t* rb = rg.region + static_cast<int64_t>(bb) * kBinRegionCap;
+      for (unsigned i = tid; i < bb_tot; i += kFilterBlock) stg[i] = __ldcg(rb + i);
+      __syncthreads();
+      TK_RG(6);
+      bucket_kth<kFilterBlock>(stg, bb_tot, r, mine, s_tmp, s_rinfo, &s_cnt, &s_kappa);
+      __syncthreads();
+      TK_RG(7);
+      const uint64_t kap = s_kappa;
+      if (tid == 0) s_cnt = 0u;
+      __syncthreads();
+      for (unsigned base = 0; base < bb_tot; base += kFilterBlock) {
+        const unsigned i = base + tid;
+        const uint64_t key = i < bb_tot ? stg[i] : 0ull;
+        const bool w = i < bb_tot && key >= kap;
+        const unsigned slot = warp_append_slot(&s_cnt, w);
+        if (w && slot < r) write_winner(fp, rg, row, static_cast<int64_t>(k), bb_start + slot, key, 0ull);
       }
     }
     TK_RG(8);
@@ -911,7 +912,7 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
     const int per = (kRefineGridBins + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
     if (tid < per && static_cast<int>(blockIdx.x) * per + tid < kRefineGridBins)
       bo[blockIdx.x * per + tid] = bst[blockIdx.x * per + tid];
-    publish_chunks(bst, xend, static_cast<int64_t>(k), bo + kRefineGridBins + 8,
+    publish_chunks(bst, xend, static_cast<int64_t>(k), bo + kRefineGridBins + kBinfoHeaderWords,
                    static_cast<int>(blockIdx.x) + tid * static_cast<int>(gridDim.x),
                    static_cast<int>(gridDim.x) * kFilterBlock);
   }
@@ -926,6 +927,7 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
       bo[kRefineGridBins + 5] = xend;
       bo[kRefineGridBins + 6] = static_cast<unsigned>(kmin);  // digits are of key - kmin
       bo[kRefineGridBins + 7] = static_cast<unsigned>(kmin >> 32);
+      bo[kRefineGridBins + 8] = 0u;  // the keys are in the exchange buffer
     }
   }
   __syncthreads();  // the shared arrays are reused by the next selection

@@ -109,6 +109,11 @@ struct SelParams {
   // padding sentinels (index -1, value -inf / +inf); a selection returned
   // short holds them in its buffer up to slot r
   const uint64_t* relax_tau;
+  // bin sort of one selection (nullable): the filter's survivor histogram
+  // and its bin regions, read instead of the exchange buffer when the bin
+  // information's header says the refinement left the keys there
+  const unsigned* fhist;
+  const uint64_t* region;
 };
 
 // Published per selection for the bin sort: NB bin starts, then the
@@ -117,7 +122,7 @@ struct SelParams {
 // boundary bin), and a base the digits are taken relative to (digits,
 // prefixes and masks describe key - base; 0 from the refinement cluster).
 constexpr int kBinInfoBins = 2048;
-constexpr int kBinInfoWords = kBinInfoBins + 8;
+constexpr int kBinInfoWords = kBinInfoBins + kBinfoHeaderWords;
 
 // Source of the refinement kernel (template source 3), chosen at run time:
 // 0 = the candidate buffer, or after a miss 1 / 2 = x as f32 / bf16; and the
@@ -1205,7 +1210,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
         if (crank == 0) {
           unsigned* bo = a.binfo + row * binfo_words(k);
           for (int i = tid; i < NB; i += BLOCK) bo[i] = bst[i];
-          publish_chunks(bst, static_cast<unsigned>(xend), k, bo + NB + 8, tid, BLOCK);
+          publish_chunks(bst, static_cast<unsigned>(xend), k, bo + NB + kBinfoHeaderWords, tid, BLOCK);
           if (tid == 0) {
             bo[NB] = static_cast<unsigned>(prefix1);
             bo[NB + 1] = static_cast<unsigned>(prefix1 >> 32);
@@ -1215,6 +1220,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
             bo[NB + 5] = static_cast<unsigned>(xend);
             bo[NB + 6] = 0u;  // digits of the keys themselves (no base)
             bo[NB + 7] = 0u;
+            bo[NB + 8] = 0u;  // the keys are in the exchange buffer
           }
         }
         return;
@@ -1473,18 +1479,85 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   const unsigned* bi = a.binfo + row * binfo_words(k);
   // one round of loads, one word per thread, shared through shared memory:
   // the status word, the digit description and this block's chunk
-  // descriptor (its first and last bins with their bounds)
-  __shared__ unsigned s_words[1 + 8 + kChunkWords];
+  // descriptor (its first and last bins with their bounds); with bin regions
+  // also the filter's histogram, two 16-byte loads a thread
+  constexpr int kHw = 9;  // header words read
+  __shared__ unsigned s_words[1 + kHw + kChunkWords];
+  __shared__ __align__(16) unsigned s_bst[NB];  // bin regions: the histogram, then every bin's first place
+  __shared__ unsigned s_total;
+  static_assert(NB == 8 * BLOCK, "eight bins a thread");
   if (tid == 0) s_words[0] = static_cast<unsigned>(__ldcg(a.status));
-  else if (tid <= 8) s_words[tid] = __ldcg(bi + NB + (tid - 1));
-  else if (tid <= 8 + kChunkWords) s_words[tid] = __ldcg(bi + NB + 8 + (blockIdx.x % bp.q) * kChunkWords + (tid - 9));
+  else if (tid <= kHw) s_words[tid] = __ldcg(bi + NB + (tid - 1));
+  else if (tid <= kHw + kChunkWords)
+    s_words[tid] = __ldcg(bi + NB + kBinfoHeaderWords + (blockIdx.x % bp.q) * kChunkWords + (tid - 1 - kHw));
+  // the histogram (bin regions) comes in one bulk copy: every block reads
+  // these 8 KB, and 16-byte loads by every thread would queue ~2000 requests
+  // on each of its L2 lines (loaded before knowing whether it is needed)
+  __shared__ __align__(8) uint64_t s_bar;
+  if (a.fhist && tid == 0) {
+    mbar_init(&s_bar, 1u);
+    mbar_expect_tx(&s_bar, static_cast<unsigned>(sizeof(unsigned) * NB));
+    bulk_copy_g2s(s_bst, a.fhist, static_cast<unsigned>(sizeof(unsigned) * NB), &s_bar);
+  }
   __syncthreads();
+  const bool landed = !a.fhist || mbar_wait(&s_bar, 0u);
+  if (__syncthreads_or(!landed)) {
+    // the copy did not land in time: report it, give it a last bounded wait
+    // (it writes this block's shared memory) and stop
+    if (tid == 0) {
+      atomicCAS(a.status, kDevOk, kDevTimeout);
+      mbar_wait(&s_bar, 0u);
+    }
+    __syncthreads();
+    return;
+  }
   if (s_words[0] != static_cast<unsigned>(kDevOk)) return;  // the refinement failed
-  unsigned hw[8], cd[kChunkWords];
+  unsigned hw[kHw], cd[kChunkWords];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) hw[q] = s_words[1 + q];
+  for (int q = 0; q < kHw; ++q) hw[q] = s_words[1 + q];
 #pragma unroll
-  for (int q = 0; q < kChunkWords; ++q) cd[q] = s_words[9 + q];
+  for (int q = 0; q < kChunkWords; ++q) cd[q] = s_words[1 + kHw + q];
+  const bool binned = a.fhist && a.region && hw[8] == 1u;
+  if (binned) {
+    // The refinement left the keys in the filter's bin regions: every bin's
+    // first place from its histogram (an exclusive scan), the end of the
+    // boundary bin and this block's chunk descriptor, as the refinement
+    // would have published them.
+    unsigned c[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) c[q] = s_bst[tid * 8 + q];
+    unsigned long long sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sum += c[q];
+    const unsigned long long incl = block_scan_incl(sum, s_tmp);
+    unsigned run = static_cast<unsigned>(incl - sum);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      s_bst[tid * 8 + q] = run;
+      run += c[q];
+    }
+    if (tid == BLOCK - 1) s_total = run;
+    __syncthreads();
+    auto find = [&](unsigned p) {  // the last bin starting at or before place p
+      unsigned b = 0;
+#pragma unroll
+      for (unsigned stp = NB / 2; stp > 0; stp >>= 1)
+        if (s_bst[b + stp] <= p) b += stp;
+      return b;
+    };
+    const unsigned bk = find(static_cast<unsigned>(k - 1));  // the boundary bin
+    hw[5] = bk + 1 < static_cast<unsigned>(NB) ? s_bst[bk + 1] : s_total;  // the end of the placed keys
+    auto bin_end = [&](unsigned b) -> unsigned {
+      const unsigned e = b + 1 < static_cast<unsigned>(NB) ? s_bst[b + 1] : s_total;
+      return e < hw[5] ? e : hw[5];
+    };
+    cd[0] = find(static_cast<unsigned>(my0));
+    cd[1] = find(static_cast<unsigned>(my1 - 1));
+    cd[2] = s_bst[cd[0]];
+    cd[3] = bin_end(cd[0]);
+    cd[4] = s_bst[cd[1]];
+    cd[5] = bin_end(cd[1]);
+  }
   const uint64_t prefix1 = static_cast<uint64_t>(hw[0]) | (static_cast<uint64_t>(hw[1]) << 32);
   const uint64_t pmask1 = static_cast<uint64_t>(hw[2]) | (static_cast<uint64_t>(hw[3]) << 32);
   const int shift1 = static_cast<int>(hw[4]);
@@ -1494,6 +1567,20 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   // the first-digit bins holding places my0 and my1 - 1, and their bounds
   const unsigned bfirst = cd[0], blast = cd[1];
   const int64_t first_s = cd[2], first_e = cd[3], last_s = cd[4], last_e = cd[5];
+  // key at place p of bin b (the exchange buffer, or bin b's region)
+  auto bin_key = [&](unsigned b, int64_t p) -> uint64_t {
+    return binned ? __ldcg(a.region + static_cast<int64_t>(b) * kBinRegionCap + (p - s_bst[b])) : __ldcg(xb + p);
+  };
+  // key at place p (bin regions: the bin holding it, among bfirst..blast,
+  // by a search in a fixed number of steps, so a thread's searches overlap)
+  auto place_key = [&](int64_t p) -> uint64_t {
+    if (!binned) return __ldcg(xb + p);
+    unsigned b = bfirst;
+#pragma unroll
+    for (unsigned stp = NB / 2; stp > 0; stp >>= 1)
+      if (b + stp <= blast && s_bst[b + stp] <= p) b += stp;
+    return __ldcg(a.region + static_cast<int64_t>(b) * kBinRegionCap + (p - s_bst[b]));
+  };
   TK_BSP(1);
   const int64_t r0 = first_s < k ? first_s : k, r1 = last_e;
   uint64_t hi_key = ~0ull, lo_key = 0ull;
@@ -1516,7 +1603,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
         if (tid == 0) s_info[2] = ~0ull;
         __syncthreads();
         for (int64_t i = bs + tid; i < be; i += BLOCK) {
-          const uint64_t key = __ldcg(xb + i) - kbase;
+          const uint64_t key = bin_key(b, i) - kbase;
           if ((key & msk) == pre) atomicAdd(&lh[DM - static_cast<unsigned>((key >> sh2) & DM)], 1u);
         }
         __syncthreads();
@@ -1562,7 +1649,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
 #pragma unroll
     for (int q = 0; q < kLoads; ++q) {
       const int i = tid + q * BLOCK;
-      kv[q] = i < n_c ? __ldcg(xb + r0 + i) : 0ull;
+      kv[q] = i < n_c ? place_key(r0 + i) : 0ull;
     }
 #pragma unroll
     for (int q = 0; q < kLoads; ++q) {
@@ -1574,7 +1661,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
     __syncthreads();
     for (int64_t iw = r0 + (tid & ~31); iw < r1; iw += BLOCK) {
       const int64_t i = iw + (tid & 31);
-      const uint64_t key = i < r1 ? __ldcg(xb + i) : 0ull;
+      const uint64_t key = i < r1 ? place_key(i) : 0ull;
       const bool want = i < r1 && key - kbase <= hi_key && key - kbase >= lo_key;
       const unsigned slot = warp_append_slot(&s_cnt, want);
       if (want && slot < static_cast<unsigned>(kBinSortCap)) bufA[slot] = key;
@@ -1806,6 +1893,8 @@ cudaError_t launch_bin_sort(const Problem& p, const SelectJob& job, cudaStream_t
   a.binfo = job.binfo;
   a.handoff = 1;
   a.relax_tau = job.relax_tau;
+  a.fhist = job.fhist;
+  a.region = job.region;
   return launch_bin_sort_a(a, p.nsel, job.launch_count, st);
 }
 

@@ -602,6 +602,10 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.launch_count = &nl;
   rj.binfo = select_binfo_words(k) ? reinterpret_cast<unsigned*>(base + o_binfo) : nullptr;
   rj.relax_tau = relaxed ? tau_x : nullptr;  // the fallback's per-row padding bound
+  if (binned) {  // (the bin sort reads them when the refinement says so)
+    rj.fhist = refine_ctl + kRefineGridFilterHist;
+    rj.region = region;
+  }
   if (plan.path == TOPK_PATH_PROFK && !fallback_launched) {
     rj.check_miss = true;
     rj.force_miss = force != 0;
