@@ -243,6 +243,10 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsign
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// The same for every state space: what this thread has observed of global
+// memory (e.g. counters other blocks added before a grid barrier) before
+// its later bulk copies read it.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   unsigned ok;
   asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"

@@ -1495,6 +1495,7 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   // on each of its L2 lines (loaded before knowing whether it is needed)
   __shared__ __align__(8) uint64_t s_bar;
   if (a.fhist && tid == 0) {
+    fence_proxy_async_all();  // (the histogram is the earlier grids' writes)
     mbar_init(&s_bar, 1u);
     mbar_expect_tx(&s_bar, static_cast<unsigned>(sizeof(unsigned) * NB));
     bulk_copy_g2s(s_bst, a.fhist, static_cast<unsigned>(sizeof(unsigned) * NB), &s_bar);
