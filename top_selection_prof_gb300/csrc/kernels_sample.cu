@@ -237,11 +237,13 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
     uint64_t v[2] = {k0, k1};
     const int nt = block_top_small<BLOCK, 2>(v, (one ? 1 : 0) + (two ? 1 : 0), static_cast<int>(p.t), s_lists,
                                              s_lcount, s_top, &s_topn);
-    unsigned* gctl0 = p.sc.ctl + 2 + 2 * row;
+    // this block's fixed slots [i t, i t + t) of the gather buffer (q t <=
+    // kTauGather): no atomic to reserve them; a block with fewer than t keys
+    // fills the rest with key 0, which ranks below every key or ties a key
+    // of the same value, so the t-th largest of the union keeps its value
     uint64_t* gat0 = p.sc.gather + static_cast<int64_t>(row) * kTauGather;
-    if (tid == 0) s_cnt = nt ? atomicAdd(gctl0, static_cast<unsigned>(nt)) : 0u;
-    __syncthreads();
-    if (tid < nt && s_cnt + tid < static_cast<unsigned>(kTauGather)) gat0[s_cnt + tid] = s_top[tid];
+    const int qi = static_cast<int>(blockIdx.x) % p.q;
+    if (tid < static_cast<int>(p.t)) gat0[qi * p.t + tid] = tid < nt ? s_top[tid] : 0ull;
   } else if (p.local) {
     const int64_t first = 2 * (static_cast<int64_t>(static_cast<int>(blockIdx.x) % p.q) * BLOCK);
     const int64_t left = p.S - first;
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(kSampleBlock) sample_tau_kernel(SampleTauParam
   uint64_t raw[kPerThread];
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) raw[j] = __ldcg(gat + tid + j * BLOCK);
-  const unsigned gn = __ldcg(gctl);
+  const unsigned gn = small_t ? static_cast<unsigned>(p.q * p.t) : __ldcg(gctl);
   const unsigned n = gn < static_cast<unsigned>(kTauGather) ? gn : static_cast<unsigned>(kTauGather);
   if (small_t) {
     // the union (at most kTauGather keys: eight a thread), its t-th largest
