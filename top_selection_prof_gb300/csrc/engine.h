@@ -185,6 +185,14 @@ constexpr int64_t kRefineGridCtlWords = kRefineGridBinnedWord + 4;
 // the bin of the survivor histogram, kBinRegionCap keys a bin, bin b's keys
 // at [b * kBinRegionCap, ...) in no particular order.
 constexpr int64_t kBinRegionCap = 2048;
+// Smallest k that takes the bin regions (one selection): below it the
+// refinement cluster stays, faster there (measured on single f32 rows of
+// 2^22 to 2^28: k = 512 and 1024 lose 1-6 us on the bin regions, k = 4096
+// gains 4-8 us).
+constexpr int64_t kBinnedMinK = 4096;
+// Most keys the top (overflow) bin may hold for the bin sort to take the
+// bin regions (it never cuts that bin by digits).
+constexpr unsigned long long kBinnedTopMax = 512;
 struct RefineGridScratch {
   unsigned* ctl;          // this call's control words: kRefineGridCtlWords per selection, zero on entry
   unsigned* ctl_next;     // the other copy (kRefineGridMaxSel selections), cleared here for the next call

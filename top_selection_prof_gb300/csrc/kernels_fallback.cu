@@ -550,13 +550,16 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
     s_words[5] = regions ? __ldcg(ctl + kRefineGridFilterHist) : 1ull;  // the top (overflow) bin's count
   }
   if (regions && !rg.unsorted) {
-    // Sorted output from complete bin regions whose top bin is empty (so
-    // the bins are a plain digit of key - tau): nothing to place here.  The
+    // Sorted output from complete bin regions: nothing to place here.  The
     // bin sort reads the filter's histogram and the regions itself; this
     // kernel only checked the miss (no miss: R is within [k, M] and the
-    // histogram counts exactly the survivors) and publishes the digit.
+    // histogram counts exactly the survivors) and publishes the digit.  The
+    // bins below the top one are a plain digit of key - tau; the top bin
+    // (keys beyond 2047 << shift) is not, so it may hold only a few keys,
+    // none of them the k-th: a bin-sort block then never cuts it by digits
+    // (it cuts only a bin larger than (kBinSortCap - its places) / 2 = 768).
     __syncthreads();
-    if (s_words[4] == 0ull && s_words[5] == 0ull) {
+    if (s_words[4] == 0ull && s_words[5] <= kBinnedTopMax && s_words[5] < k) {
       if (blockIdx.x == 0 && tid == 0) {
         const uint64_t tau = s_words[2];
         const int hs = survivor_shift(tau, s_words[3]);
@@ -577,11 +580,12 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
       return true;
     }
   }
-  bool fast = false;
+  bool fast = false, found = false;
   unsigned bb = 0, bb_start = 0, bb_tot = 0;
   if (hist_ok) {
     const unsigned* fh = ctl + kRefineGridFilterHist;
     if (find_rank_bin(fh, k, bst, s_ws, s_info)) {  // (synchronises the block)
+      found = true;
       bb = s_info[0];
       bb_start = s_info[1];
       bb_tot = s_info[2];
@@ -597,10 +601,11 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
   // boundary bin) to the exchange buffer, as the partition below would have
   // placed them, for the bin sort.  Unsorted: the bins above the boundary
   // straight to the outputs, and block 0 ranks the boundary bin.
-  if (regions && rg.unsorted && fast && s_words[4] == 0ull && bb_tot <= static_cast<unsigned>(kPartCache)) {
+  if (regions && rg.unsorted && found && bb > 0u && s_words[4] == 0ull && bb_tot <= static_cast<unsigned>(kPartCache)) {
     // Unsorted output from complete bin regions: the bins above the
-    // boundary go straight to the outputs, split over every block but the
-    // last, which ranks the boundary bin.
+    // boundary (the top bin's keys too, whatever they are) go straight to
+    // the outputs, split over every block but the last, which ranks the
+    // boundary bin.
     TK_RG(3);
     const unsigned pend = bb_start;
     const unsigned ncopy = gridDim.x > 1 ? gridDim.x - 1 : 1u;

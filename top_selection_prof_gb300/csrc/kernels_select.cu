@@ -1630,11 +1630,14 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
     };
     uint64_t pre, msk;
     int64_t s0, s1;
+    // (a bin taken whole bounds nothing: its keys are exactly those of its
+    // places, which is what keeps the top bin of bin regions -- not a plain
+    // digit, and never cut -- whole)
     bool ok = cut(bfirst, first_s, first_e, my0, pre, msk, s0, s1);
-    hi_key = pre | ~msk;
+    hi_key = (s0 == first_s && s1 == first_e) ? ~0ull : (pre | ~msk);
     place0 = s0;
     ok = ok && cut(blast, last_s, last_e, my1 - 1, pre, msk, s0, s1);
-    lo_key = pre;
+    lo_key = (s0 == last_s && s1 == last_e) ? 0ull : pre;
     place1 = s1;
     TK_BS(1, cut_iters | (static_cast<unsigned>(first_s < k ? first_e - first_s : 0) << 8));
     if (!ok || place1 - place0 > kBinSortCap || place1 < place0) {
@@ -1877,7 +1880,7 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
 }
 
 cudaError_t launch_bin_sort(const Problem& p, const SelectJob& job, cudaStream_t st) {
-  if (!job.binfo || !job.xbuf || job.xbuf_stride < job.r || job.r < kBinSortMinK) return cudaErrorInvalidValue;
+  if (!job.binfo || !job.xbuf || job.xbuf_stride < job.r || job.r < 1) return cudaErrorInvalidValue;
   SelParams a{};
   a.x = p.x;
   a.len = p.len;

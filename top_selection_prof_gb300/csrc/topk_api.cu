@@ -439,13 +439,20 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   const size_t o_ghist = off; off = align_up(off + sizeof(unsigned) * 8 * 256);
   const size_t o_tiles = off; off = align_up(off + sizeof(unsigned) * ntile);
   const size_t o_samples = off; off = align_up(off + (fused ? 0 : sizeof(uint64_t) * nsel * S));
+  // One selection over 16-byte aligned data after the fused sampler: the
+  // TMA-ring filter places its survivors in bin regions, from which the grid
+  // refinement and the bin sort take them -- also for k below the bin
+  // sort's usual bound, from kBinnedMinK (the refinement cluster's radix
+  // passes and its 2-CTA collection then go).  Left out when a fixed
+  // scratch has no room for the regions.
+  const bool region_route = plan.path == TOPK_PATH_PROFK && fused && nsel == 1 && p.vec_ok &&
+                            (select_binfo_words(k) > 0 || k >= kBinnedMinK);
+  const int64_t binfo_w = region_route ? binfo_words(k) : select_binfo_words(k);
+  const int64_t xstride = region_route ? 2 * k : select_xbuf_stride(k);
   const size_t o_buf = off; off = align_up(off + sizeof(uint64_t) * nsel * M);
-  const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * nsel * select_xbuf_stride(k));
-  const size_t o_binfo = off; off = align_up(off + sizeof(unsigned) * nsel * select_binfo_words(k));
-  // bin regions (the grid refinement of one selection after a fused sampler
-  // and the TMA-ring filter): left out when a fixed scratch has no room
-  bool binned = plan.path == TOPK_PATH_PROFK && fused && nsel == 1 && p.vec_ok && select_binfo_words(k) > 0 &&
-                nsel <= kRefineGridMaxSel;
+  const size_t o_xbuf = off; off = align_up(off + sizeof(uint64_t) * nsel * xstride);
+  const size_t o_binfo = off; off = align_up(off + sizeof(unsigned) * nsel * binfo_w);
+  bool binned = region_route;
   const size_t o_region = off;
   if (binned) {
     const size_t with = align_up(off + sizeof(uint64_t) * kRefineGridBins * kBinRegionCap);
@@ -483,7 +490,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   // Large k and a few selections: the miss check, the fallback and the
   // partition of the winners run on one cooperative grid over every SM, and
   // the bin sort follows (no refinement cluster).
-  const bool grid_refine = select_binfo_words(k) > 0 && nsel <= kRefineGridMaxSel &&
+  const bool grid_refine = (select_binfo_words(k) > 0 || binned) && nsel <= kRefineGridMaxSel &&
                            M <= refine_grid_capacity(p);
   // Winners in no particular order (allowed by the caller): the grid
   // refinement writes them itself and no sort follows.
@@ -596,11 +603,11 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   rj.out_idx = out_idx;
   rj.status = &hdr->status;
   rj.xbuf = xbuf;
-  rj.xbuf_stride = select_xbuf_stride(k);
+  rj.xbuf_stride = grid_refine ? xstride : select_xbuf_stride(k);
   rj.clear_words = reinterpret_cast<unsigned*>(base + ws_tau_ctl_offset());  // the fused threshold grid's
   rj.n_clear = kTauCtlWords;
   rj.launch_count = &nl;
-  rj.binfo = select_binfo_words(k) ? reinterpret_cast<unsigned*>(base + o_binfo) : nullptr;
+  rj.binfo = (grid_refine || select_binfo_words(k) > 0) && binfo_w ? reinterpret_cast<unsigned*>(base + o_binfo) : nullptr;
   rj.relax_tau = relaxed ? tau_x : nullptr;  // the fallback's per-row padding bound
   if (binned) {  // (the bin sort reads them when the refinement says so)
     rj.fhist = refine_ctl + kRefineGridFilterHist;
