@@ -61,6 +61,10 @@ struct FilterParams {
   uint64_t* region = nullptr;
 };
 
+// (with bin regions) set when some survivors of this block left its stages;
+// initialised by the filter kernel that bins
+__shared__ int s_filter_block_bad;
+
 // The word a filter block sets when its survivors did not all stay in its
 // stages or a bin region overflowed: the regions are then incomplete.
 __device__ __forceinline__ unsigned* binned_bad_word(const FilterParams& fp, int64_t row) {
@@ -299,7 +303,10 @@ __device__ __forceinline__ void lane_append(uint32_t mask, const uint4& v, int64
   unsigned long long gbase = 0;
   if (fit < n) {
     gbase = atomicAdd(fp.counts + row, static_cast<unsigned long long>(n - fit));
-    if (fp.region) *binned_bad_word(fp, row) = 1u;
+    if (fp.region) {
+      *binned_bad_word(fp, row) = 1u;
+      s_filter_block_bad = 1;
+    }
   }
   unsigned j = 0;
   while (mask) {
@@ -414,10 +421,18 @@ __device__ __forceinline__ void single_tile_groups(const uint4 (&v)[kFilterUnrol
     for (int u = 0; u < kFilterUnroll; ++u)
       queue_group<DT, LARGEST, VEC, HIST>(cand[u], v[u], base + u * kFilterBlock * VEC, q, qn, t, fp, st, 0,
                                           sh_hist);
-    // a warp-uniform point: move the stage out once it is half full (unless
-    // the block bins its survivors at its end: they stay)
-    if (!fp.region && __shfl_sync(kFull, *st.n, 0) >= static_cast<unsigned>(kWarpStage / 2))
+    // a warp-uniform point: move the stage out once it is half full; when
+    // the block bins its survivors at its end they stay, unless the stage
+    // is three quarters full (a crowded stretch of the input, as a sorted
+    // one): then it is moved out and the bin regions marked incomplete
+    const unsigned fill = __shfl_sync(kFull, *st.n, 0);
+    if (fill >= static_cast<unsigned>(fp.region ? kWarpStage * 3 / 4 : kWarpStage / 2)) {
+      if (fp.region && (threadIdx.x & 31) == 0) {
+        *binned_bad_word(fp, 0) = 1u;
+        s_filter_block_bad = 1;  // (this block then skips its own placement)
+      }
       stage_flush(st, 0, fp.cap, fp.buf, fp.counts);
+    }
   }
 }
 

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kFilterBlock, kRingBlocksPerSm) filter_ring_ke
   if (tid == 0) {
     for (int s = 0; s < kRingStages; ++s) mbar_init(&full[s], 1u);
     s_abort = 0;
+    s_filter_block_bad = 0;
     // the input does not come from the preceding grid: these copies may
     // start before it has finished (half the ring: the rest of the stream
     // would queue in front of that grid's last loads)
@@ -152,13 +153,17 @@ __global__ void __launch_bounds__(kFilterBlock, kRingBlocksPerSm) filter_ring_ke
       if (pos < fp.len) test_group<DT, LARGEST, VEC, HIST>(load_group<DT, VEC>(x + pos, pol), pos, t, fp, st, 0, sh_hist);
     }
   }
-  if (HIST && fp.region) {
+  __syncthreads();  // every warp's stage, the block's counts and its flag are final
+  if (HIST && fp.region && s_filter_block_bad) {
+    // some survivors of this block left its stages: the regions are marked
+    // incomplete, so only the histogram is added
+    hist_flush(sh_hist, fp, 0);
+  } else if (HIST && fp.region) {
     // Bin regions: one returning atomic per non-empty bin adds this block's
     // counts to the histogram and returns where its keys start in each
     // bin's region; then every survivor (all still in the warps' stages)
     // goes to its bin's region.  A bin that would overflow its region marks
     // the regions incomplete.
-    __syncthreads();  // every warp's stage and the block's counts are final
     unsigned* g = fp.refine_ctl + kRefineGridFilterHist;
     unsigned* cur = reinterpret_cast<unsigned*>(queue_v);  // (free now: 2048 counters)
     static_assert(sizeof(queue_v) >= sizeof(unsigned) * kRefineGridBins, "bin cursors");

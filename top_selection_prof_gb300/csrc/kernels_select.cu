@@ -1430,7 +1430,7 @@ struct BinSortParams {
   int q;        // blocks per selection
 };
 
-__device__ __forceinline__ void bin_sort_body(const BinSortParams& bp);
+__device__ __forceinline__ void bin_sort_body(const BinSortParams& bp, uint64_t* hbar, int* hcopy);
 cudaError_t launch_bin_sort_a(const SelParams& a, int64_t nsel, int* launch_count, cudaStream_t st);
 static_assert(kBinInfoBins == kRefineGridBins, "the grid refinement publishes the bin sort's bins");
 
@@ -1445,19 +1445,35 @@ __device__ unsigned g_bs_info[1024][4];          // debug: set size, cut iterati
 #endif
 
 __global__ void __launch_bounds__(kBinSortBlock) bin_sort_kernel(BinSortParams bp) {
+  // a bulk copy of the filter's histogram, issued before the block knows
+  // whether it needs it: in flight (hcopy) until waited for, here at the end
+  // at the latest, since it writes this block's shared memory
+  __shared__ __align__(8) uint64_t s_hbar;
+  __shared__ int s_hcopy;
   TK_TL_BEGIN(4);
 #ifdef TK_PHASE_TIMING
   grid_dependency_wait();
   TK_BSP(0);
 #endif
-  bin_sort_body(bp);
+  if (threadIdx.x == 0) s_hcopy = 0;
+  __syncthreads();
+  bin_sort_body(bp, &s_hbar, &s_hcopy);
+  __syncthreads();
+  if (s_hcopy) {
+    const bool landed = mbar_wait(&s_hbar, 0u);
+    if (threadIdx.x == 0 && !landed) {
+      atomicCAS(bp.a.status, kDevOk, kDevTimeout);
+      mbar_wait(&s_hbar, 0u);
+    }
+    __syncthreads();
+  }
   TK_TL_END(4);
 #ifdef TK_PHASE_TIMING
   TK_BSP(7);
 #endif
 }
 
-__device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
+__device__ __forceinline__ void bin_sort_body(const BinSortParams& bp, uint64_t* hbar, int* hcopy) {
   constexpr int BLOCK = kBinSortBlock;
   constexpr int NB = kBinInfoBins;
   constexpr unsigned DM = 255u;  // 8-bit sub-digits
@@ -1490,28 +1506,18 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   else if (tid <= kHw) s_words[tid] = __ldcg(bi + NB + (tid - 1));
   else if (tid <= kHw + kChunkWords)
     s_words[tid] = __ldcg(bi + NB + kBinfoHeaderWords + (blockIdx.x % bp.q) * kChunkWords + (tid - 1 - kHw));
-  // the histogram (bin regions) comes in one bulk copy: every block reads
-  // these 8 KB, and 16-byte loads by every thread would queue ~2000 requests
-  // on each of its L2 lines (loaded before knowing whether it is needed)
-  __shared__ __align__(8) uint64_t s_bar;
+  // the histogram (bin regions) comes in one bulk copy, issued with the
+  // words above before it is known to be needed (every block reads these
+  // 8 KB, and 16-byte loads by every thread would queue ~2000 requests on
+  // each of its L2 lines); it is waited for only when used, else at the end
   if (a.fhist && tid == 0) {
     fence_proxy_async_all();  // (the histogram is the earlier grids' writes)
-    mbar_init(&s_bar, 1u);
-    mbar_expect_tx(&s_bar, static_cast<unsigned>(sizeof(unsigned) * NB));
-    bulk_copy_g2s(s_bst, a.fhist, static_cast<unsigned>(sizeof(unsigned) * NB), &s_bar);
+    mbar_init(hbar, 1u);
+    mbar_expect_tx(hbar, static_cast<unsigned>(sizeof(unsigned) * NB));
+    bulk_copy_g2s(s_bst, a.fhist, static_cast<unsigned>(sizeof(unsigned) * NB), hbar);
+    *hcopy = 1;
   }
   __syncthreads();
-  const bool landed = !a.fhist || mbar_wait(&s_bar, 0u);
-  if (__syncthreads_or(!landed)) {
-    // the copy did not land in time: report it, give it a last bounded wait
-    // (it writes this block's shared memory) and stop
-    if (tid == 0) {
-      atomicCAS(a.status, kDevOk, kDevTimeout);
-      mbar_wait(&s_bar, 0u);
-    }
-    __syncthreads();
-    return;
-  }
   if (s_words[0] != static_cast<unsigned>(kDevOk)) return;  // the refinement failed
   unsigned hw[kHw], cd[kChunkWords];
 #pragma unroll
@@ -1520,6 +1526,12 @@ __device__ __forceinline__ void bin_sort_body(const BinSortParams& bp) {
   for (int q = 0; q < kChunkWords; ++q) cd[q] = s_words[1 + kHw + q];
   const bool binned = a.fhist && a.region && hw[8] == 1u;
   if (binned) {
+    const bool landed = mbar_wait(hbar, 0u);
+    if (__syncthreads_or(!landed)) {
+      if (tid == 0) atomicCAS(a.status, kDevOk, kDevTimeout);
+      return;  // (the kernel waits for the copy once more before leaving)
+    }
+    if (tid == 0) *hcopy = 0;
     // The refinement left the keys in the filter's bin regions: every bin's
     // first place from its histogram (an exclusive scan), the end of the
     // boundary bin and this block's chunk descriptor, as the refinement
