@@ -24,7 +24,9 @@
  *     default stream) and does no host synchronisation, except that
  *     topk_select_ex synchronises the stream when `stats` is non-NULL.
  *   - The library keeps a per-(device, stream) workspace for the sample, the
- *     threshold, the candidate buffer and counters; it grows on demand with
+ *     threshold, the candidate buffer and counters (and, for one selection
+ *     with k >= 4096 over 16-byte aligned data, 32 MiB of bin regions into
+ *     which the filter places its survivors); it grows on demand with
  *     stream-ordered allocation and is never shrunk.  Calls that share a
  *     stream are ordered; calls on different streams use different workspaces.
  *   - Errors are returned as topk_status_t codes; nothing is thrown across the

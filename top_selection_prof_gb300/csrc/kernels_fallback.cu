@@ -592,7 +592,6 @@ __device__ bool partition_row(const RefineGridParams& a, int64_t row, uint64_t* 
       fast = bst[1] == 0u && static_cast<int64_t>(bb_start) + bb_tot <= rg.xstride;  // top bin empty
     }
   }
-  TK_RG(4);
   __syncthreads();  // s_info is rewritten below; s_words are visible
 
   // ---- bin regions: the filter left every survivor in its bin's region,
