@@ -84,9 +84,9 @@ def test_keys_beyond_the_top_bin(unsorted):
 
 
 @pytest.mark.parametrize("unsorted", [False, True])
-@pytest.mark.parametrize("kind,k", [("normal", 4096), ("pareto15", 6000), ("ties1000", 5000)])
+@pytest.mark.parametrize("kind,k", [("uniform", 3072), ("normal", 4096), ("pareto15", 6000), ("ties1000", 5000)])
 def test_mid_k_single_rows(kind, k, unsorted):
-    # k from 4096 up to the bin sort's own bound: one aligned row takes the
+    # k from 3072 up to the bin sort's own bound: one aligned row takes the
     # bin regions too (grid refinement + bin sort instead of the cluster)
     x = workloads.make(kind, 1, 1 << 22, seed=37)
     st = _check(x, k, unsorted=unsorted)

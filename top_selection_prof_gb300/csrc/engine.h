@@ -187,9 +187,10 @@ constexpr int64_t kRefineGridCtlWords = kRefineGridBinnedWord + 4;
 constexpr int64_t kBinRegionCap = 2048;
 // Smallest k that takes the bin regions (one selection): below it the
 // refinement cluster stays, faster there (measured on single f32 rows of
-// 2^22 to 2^28: k = 512 and 1024 lose 1-6 us on the bin regions, k = 4096
-// gains 4-8 us).
-constexpr int64_t kBinnedMinK = 4096;
+// 2^22 to 2^28: k = 512 and 1024 lose 1-6 us on the bin regions, k = 2048
+// wins or loses up to 3 us by size, k = 3072 gains 3-6 us from 2^24 on,
+// k = 4096 gains 4-8 us).
+constexpr int64_t kBinnedMinK = 3072;
 // Most keys the top (overflow) bin may hold for the bin sort to take the
 // bin regions (it never cuts that bin by digits).
 constexpr unsigned long long kBinnedTopMax = 512;
