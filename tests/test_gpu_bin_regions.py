@@ -92,3 +92,15 @@ def test_mid_k_single_rows(kind, k, unsorted):
     st = _check(x, k, unsorted=unsorted)
     assert st["launches"] == (3 if unsorted else 4), st
     _check(x, k, largest=False, unsorted=unsorted)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("largest", [True, False])
+@pytest.mark.parametrize("kind,k", [("pareto15", 2048), ("normal", 512)])
+def test_refinement_cluster_reads_the_regions(kind, k, largest):
+    # k below 3072 and survivors expected beyond one refinement CTA's cache
+    # (2^27 elements, eps = 1e-6): CTA 0 of the cluster takes the winners
+    # straight from the bin regions
+    x = workloads.make(kind, 1, 1 << 27, seed=38)
+    st = _check(x, k, largest=largest, eps=1e-6)
+    assert st["launches"] == 3, st

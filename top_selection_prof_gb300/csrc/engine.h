@@ -153,9 +153,13 @@ constexpr int64_t kFallbackTile = 4096;
 // region (nullable; one selection with refine_ctl only): each filter block
 // also places its survivors in bin regions of kBinRegionCap keys at its end
 // (kRefineGridBinnedWord of refine_ctl set when they do not fit).
+// refine_ctl_next (with region, nullable): the other copy of the control
+// words, cleared by the filter's blocks for the next call (when no grid
+// refinement, which clears it otherwise, follows).
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
                           unsigned long long* counts, int reserved_sms, cudaStream_t st,
-                          unsigned* refine_ctl = nullptr, int* status = nullptr, uint64_t* region = nullptr);
+                          unsigned* refine_ctl = nullptr, int* status = nullptr, uint64_t* region = nullptr,
+                          unsigned* refine_ctl_next = nullptr);
 // force: 0 = only rows that missed, 1 = every row (fault injection / exact path).
 cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,
                             unsigned long long* counts, const FallbackScratch& fs, int force,
@@ -191,6 +195,13 @@ constexpr int64_t kBinRegionCap = 2048;
 // wins or loses up to 3 us by size, k = 3072 gains 3-6 us from 2^24 on,
 // k = 4096 gains 4-8 us).
 constexpr int64_t kBinnedMinK = 3072;
+// Smallest k whose refinement cluster reads the bin regions (one selection;
+// below kBinnedMinK: CTA 0 takes the winners from the regions), when the
+// expected survivors would need more than one CTA of it (measured on f32
+// rows at k = 512..2048: 3.5-4.5 us faster at 2^28 elements, where the
+// cluster takes two CTAs, 3-5 us slower at 2^24-2^26, where one CTA holds
+// every survivor).
+constexpr int64_t kBinnedSelMinK = 512;
 // Most keys the top (overflow) bin may hold for the bin sort to take the
 // bin regions (it never cuts that bin by digits).
 constexpr unsigned long long kBinnedTopMax = 512;
@@ -274,8 +285,12 @@ struct SelectJob {
   // information's header says so) instead of the exchange buffer
   const unsigned* fhist = nullptr;
   const uint64_t* region = nullptr;
+  // refinement cluster of one selection whose filter placed its survivors
+  // in bin regions (nullable): this call's control words
+  const unsigned* rctl = nullptr;
 };
 int64_t select_binfo_words(int64_t k);  // 0 when k is too small for the bin sort
+int64_t select_cta_cache();              // candidates one refinement CTA holds in shared memory
 // Output places one bin-sort block owns, and the words of bin information
 // per selection (bin starts, a header describing the digit, one descriptor
 // per chunk: binfo.cuh).

@@ -59,6 +59,7 @@ struct FilterParams {
   // warps' stages until the block ends, which places them in bin regions
   // of kBinRegionCap keys (the filter_ring_kernel's end)
   uint64_t* region = nullptr;
+  unsigned* refine_ctl_next = nullptr;  // (with region, nullable) cleared by the blocks for the next call
 };
 
 // (with bin regions) set when some survivors of this block left its stages;

@@ -100,6 +100,10 @@ __global__ void __launch_bounds__(kFilterBlock, kRingBlocksPerSm) filter_ring_ke
   if (HIST)
     for (int i = tid; i < kRefineGridBins; i += kFilterBlock) sh_hist[i] = 0u;
   if ((tid & 31) == 0) stage_n[tid >> 5] = 0u;
+  if (fp.refine_ctl_next)  // the next call's control words (no kernel of this call uses them)
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kFilterBlock + tid; i < kRefineGridMaxSel * kRefineGridCtlWords;
+         i += static_cast<int64_t>(gridDim.x) * kFilterBlock)
+      fp.refine_ctl_next[i] = 0u;
   grid_dependency_wait();  // tau and the zeroed counters come from the previous grid
   grid_launch_dependents();
   if (tid == 0) {
@@ -285,12 +289,13 @@ cudaError_t launch_filter_h(const FilterParams& fp, int reserved_sms, cudaStream
 
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
                           unsigned long long* counts, int reserved_sms, cudaStream_t st, unsigned* refine_ctl,
-                          int* status, uint64_t* region) {
+                          int* status, uint64_t* region, unsigned* refine_ctl_next) {
   FilterParams fp{p.x, p.nsel, p.len, p.ib, p.flip, tau, cap, buf, counts, Divider{}};
   fp.refine_ctl = refine_ctl;
   fp.status = status;
   // (bin regions: the TMA-ring filter of one selection with the survivor histogram)
   fp.region = (p.nsel == 1 && p.vec_ok && refine_ctl) ? region : nullptr;
+  fp.refine_ctl_next = fp.region ? refine_ctl_next : nullptr;
   const bool largest = p.flip == 0;
   if (p.nsel == 1 && p.vec_ok) {
     // (every block of the ring grid may start late: its tiles wait in the

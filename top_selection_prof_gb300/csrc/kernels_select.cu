@@ -114,6 +114,10 @@ struct SelParams {
   // information's header says the refinement left the keys there
   const unsigned* fhist;
   const uint64_t* region;
+  // refinement of one selection whose filter placed its survivors in bin
+  // regions (nullable): this call's control words (the survivor histogram,
+  // the "incomplete" flag)
+  const unsigned* rctl;
 };
 
 // Published per selection for the bin sort: NB bin starts, then the
@@ -1368,6 +1372,147 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
   }
 }
 
+// Refinement of one selection whose filter left its survivors in bin regions
+// (2048 bins of the survivors' offset above tau, kBinRegionCap keys a bin):
+// the k winners are the keys of the bins above the boundary bin and the top
+// of that bin, read straight from the regions by CTA 0 -- no pass over the
+// candidate buffer, no exchange between the cluster's CTAs.  Every CTA reads
+// the same words and the same histogram, so all take the same decision;
+// false (everywhere) when the regions cannot serve: incomplete, more than
+// kBinnedTopMax keys beyond the top bin or the k-th among them, or more keys
+// down to the boundary bin than the first buffer holds.  The caller then
+// selects from the buffer as usual.  No miss (checked by the caller).
+template <int BLOCK, int P, int CB, int NB>
+__device__ bool select_from_regions(const SelParams& a) {
+  if constexpr (NB != kBinInfoBins) {
+    return false;
+  } else {
+    using L = Layout<BLOCK, P, CB, NB>;
+    constexpr int kPer = NB / BLOCK;
+    static_assert(kPer == 4, "one 16-byte load of counters a thread");
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint64_t* bufA = reinterpret_cast<uint64_t*>(smem + L::kBufA);
+    uint64_t* bufB = reinterpret_cast<uint64_t*>(smem + L::kBufB);
+    unsigned* h2 = reinterpret_cast<unsigned*>(smem + L::kH2);
+    unsigned* work = reinterpret_cast<unsigned*>(smem + L::kWork);
+    unsigned* bst = work;  // every bin's first place (NB words)
+    __shared__ unsigned long long r_tmp[32];
+    __shared__ unsigned long long r_info[6];
+    __shared__ unsigned r_cnt;
+    __shared__ uint64_t r_kappa;
+    __shared__ unsigned long long r_words[2];
+    const int tid = threadIdx.x;
+    const int64_t k = a.r;
+    const int64_t row = 0;
+    if (tid == 0) {
+      r_words[0] = __ldcg(a.rctl + kRefineGridBinnedWord);  // 0: the regions are complete
+      r_info[0] = ~0ull;
+    }
+    const uint4 hc = ldcg_u4(a.rctl + kRefineGridFilterHist + tid * kPer);
+    const unsigned c[kPer] = {hc.x, hc.y, hc.z, hc.w};
+    unsigned long long sum = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) sum += c[q];
+    const unsigned long long incl = block_scan_incl(sum, r_tmp);  // (synchronises the block)
+    unsigned run = static_cast<unsigned>(incl - sum);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const unsigned b = tid * kPer + q;
+      bst[b] = run;
+      if (run < static_cast<unsigned long long>(k) && static_cast<unsigned long long>(k) <= run + static_cast<unsigned long long>(c[q])) {
+        r_info[0] = b;
+        r_info[1] = run;
+        r_info[2] = c[q];
+      }
+      run += c[q];
+    }
+    __syncthreads();
+    const unsigned bb = static_cast<unsigned>(r_info[0]);
+    const unsigned bb_start = static_cast<unsigned>(r_info[1]), bb_tot = static_cast<unsigned>(r_info[2]);
+    const unsigned top = bst[1];  // the top bin's keys (those beyond 2047 << shift)
+    const bool ok = r_words[0] == 0ull && r_info[0] != ~0ull && bb > 0u && top <= kBinnedTopMax &&
+                    static_cast<int64_t>(bb_start) + bb_tot <= static_cast<int64_t>(P);
+    if (!ok) {
+      __syncthreads();  // (bst and the words are rewritten by the usual selection)
+      return false;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    if (cluster.block_rank() != 0) return true;
+    TK_STAMP(37);
+    // the keys of bins 0..bb, in place order: each place's bin by a search
+    // of the bin starts in a fixed number of steps, four places of a thread
+    // at once so that their searches and loads overlap
+    const unsigned n = bb_start + bb_tot;
+    constexpr int kJ = 4;
+    for (unsigned base = 0; base < n; base += kJ * BLOCK) {
+      unsigned pl[kJ], bl[kJ];
+      uint64_t key[kJ];
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        pl[j] = base + j * BLOCK + tid;
+        bl[j] = 0u;
+      }
+#pragma unroll
+      for (unsigned stp = NB / 2; stp > 0; stp >>= 1)
+#pragma unroll
+        for (int j = 0; j < kJ; ++j)
+          if (bl[j] + stp <= bb && bst[bl[j] + stp] <= pl[j]) bl[j] += stp;
+#pragma unroll
+      for (int j = 0; j < kJ; ++j)
+        key[j] = pl[j] < n ? __ldcg(a.region + static_cast<int64_t>(bl[j]) * kBinRegionCap + (pl[j] - bst[bl[j]]))
+                           : 0ull;
+#pragma unroll
+      for (int j = 0; j < kJ; ++j)
+        if (pl[j] < n) bufA[pl[j]] = key[j];
+    }
+    __syncthreads();
+    TK_STAMP(38);
+    // the boundary bin's top (k - bb_start) keys: its key of that rank, then
+    // those at or above it (distinct keys: exactly that many) after the bins
+    // above, through the second buffer
+    const unsigned r = static_cast<unsigned>(k) - bb_start;
+    bucket_kth<BLOCK>(bufA + bb_start, bb_tot, r, h2, r_tmp, r_info, &r_cnt, &r_kappa);
+    __syncthreads();
+    TK_STAMP(39);
+    const uint64_t kap = r_kappa;
+    if (tid == 0) r_cnt = 0u;
+    __syncthreads();
+    for (unsigned b0 = 0; b0 < bb_tot; b0 += BLOCK) {
+      const unsigned i = b0 + tid;
+      const uint64_t key = i < bb_tot ? bufA[bb_start + i] : 0ull;
+      const bool w = i < bb_tot && key >= kap;
+      const unsigned slot = warp_append_slot(&r_cnt, w);
+      if (w && slot < r) bufB[slot] = key;
+    }
+    __syncthreads();
+    if (r_cnt != r) {
+      if (tid == 0) atomicCAS(a.status, kDevOk, kDevBadState);
+      return true;
+    }
+    for (unsigned i = tid; i < r; i += BLOCK) bufA[bb_start + i] = bufB[i];
+    __syncthreads();
+    TK_STAMP(40);
+    // the k winners sorted and written (as the selection below does)
+    const int n_c = static_cast<int>(k);
+    const KeySpan sp = block_span<BLOCK>(bufA, n_c);
+    constexpr int kFewGroups = NB > 512 && BLOCK <= 512 ? 512 : NB;
+    const bool placed =
+        n_c <= 1024 ? place_by_groups<BLOCK, kFewGroups>(bufA, n_c, sp.kmin, sp.kmax, 0u, ~0u, bufB, work,
+                                                         work + kFewGroups, work + 2 * kFewGroups, r_tmp, 512u, a,
+                                                         row, k, 0, 0, k)
+                    : place_by_groups<BLOCK, NB>(bufA, n_c, sp.kmin, sp.kmax, 0u, ~0u, bufB, work, work + NB,
+                                                 work + 2 * NB, r_tmp, 512u, a, row, k, 0, 0, k);
+    if (placed) {
+      TK_STAMP(41);
+      return true;
+    }
+    const uint64_t* sorted = lsd_sort<BLOCK, P>(bufA, bufB, n_c, sp.all_or ^ sp.all_and, h2);
+    for (int i = tid; i < n_c; i += BLOCK) write_out(a, row, k, i, sorted[i]);
+    TK_STAMP(42);
+    return true;
+  }
+}
+
 template <int BLOCK, int P, int CB, int NB, int SRC>
 __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelParams a) {
 #ifdef TK_PHASE_TIMING
@@ -1402,6 +1547,10 @@ __global__ void __launch_bounds__(BLOCK, min_blocks<BLOCK>()) select_kernel(SelP
       }
     }
     __syncthreads();
+    if (a.rctl && a.want_topk && s_source == 0 && select_from_regions<BLOCK, P, CB, NB>(a)) {
+      TK_TL_END(a.want_topk ? 3 : 1);
+      return;
+    }
   }
   select_body<BLOCK, P, CB, NB, SRC>(a);
   TK_TL_END(a.want_topk ? 3 : 1);
@@ -1801,6 +1950,7 @@ int sm_count() {
 
 int64_t select_max_k() { return static_cast<int64_t>(kMaxCluster) * kBigP; }
 int64_t select_binfo_words(int64_t k) { return k >= kBinSortMinK ? binfo_words(k) : 0; }
+int64_t select_cta_cache() { return kBigP + kBigCB; }
 int64_t select_xbuf_stride(int64_t k) { return k >= kBinSortMinK ? 2 * k : k; }
 
 #ifdef TK_PHASE_TIMING
@@ -1841,6 +1991,10 @@ cudaError_t launch_select(const Problem& p, const SelectJob& job, int64_t source
   a.relax_tau = job.relax_tau;
   a.xstride = job.xbuf_stride > job.r ? job.xbuf_stride : job.r;
   a.shist = job.want_topk ? nullptr : job.sample_hist;
+  if (job.want_topk && job.rctl && job.region && p.nsel == 1) {
+    a.rctl = job.rctl;
+    a.region = job.region;
+  }
   if (job.want_topk && job.keys && job.check_miss) {
     a.miss_src = p.dtype == kF32 ? 1 : 2;
     a.force = job.force_miss ? 1 : 0;

@@ -445,8 +445,17 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   // sort's usual bound, from kBinnedMinK (the refinement cluster's radix
   // passes and its 2-CTA collection then go).  Left out when a fixed
   // scratch has no room for the regions.
-  const bool region_route = plan.path == TOPK_PATH_PROFK && fused && nsel == 1 && p.vec_ok &&
-                            (select_binfo_words(k) > 0 || k >= kBinnedMinK);
+  // (below kBinnedMinK the refinement cluster reads the regions only when it
+  // would otherwise need more than one CTA for the expected survivors, with
+  // headroom: one CTA holding them all selects faster from its cache)
+  const double expect_r = plan.path == TOPK_PATH_PROFK
+                              ? static_cast<double>(plan.t) * (static_cast<double>(p.len) + 1.0) /
+                                    (static_cast<double>(S) + 1.0)
+                              : 0.0;
+  const bool region_route =
+      plan.path == TOPK_PATH_PROFK && fused && nsel == 1 && p.vec_ok &&
+      (select_binfo_words(k) > 0 || k >= kBinnedMinK ||
+       (k >= kBinnedSelMinK && 1.5 * expect_r > static_cast<double>(select_cta_cache())));
   const int64_t binfo_w = region_route ? binfo_words(k) : select_binfo_words(k);
   const int64_t xstride = region_route ? 2 * k : select_xbuf_stride(k);
   const size_t o_buf = off; off = align_up(off + sizeof(uint64_t) * nsel * M);
@@ -490,7 +499,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   // Large k and a few selections: the miss check, the fallback and the
   // partition of the winners run on one cooperative grid over every SM, and
   // the bin sort follows (no refinement cluster).
-  const bool grid_refine = (select_binfo_words(k) > 0 || binned) && nsel <= kRefineGridMaxSel &&
+  const bool grid_refine = (select_binfo_words(k) > 0 || (binned && k >= kBinnedMinK)) && nsel <= kRefineGridMaxSel &&
                            M <= refine_grid_capacity(p);
   // Winners in no particular order (allowed by the caller): the grid
   // refinement writes them itself and no sort follows.
@@ -507,7 +516,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   // for the refinement to start from.
   unsigned* refine_ctl = nullptr;
   unsigned* refine_ctl_next = nullptr;
-  if (grid_refine) {
+  if (grid_refine || binned) {
     uint64_t parity;
     {
       std::lock_guard<std::mutex> lock(g_ws_mu);
@@ -517,7 +526,9 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     refine_ctl = reinterpret_cast<unsigned*>(copies + parity * kRefineCtlCopyBytes);
     refine_ctl_next = reinterpret_cast<unsigned*>(copies + (parity ^ 1u) * kRefineCtlCopyBytes);
   }
-  const bool survivor_hist = grid_refine && fused;
+  // (the refinement cluster of one selection reads the histogram only with
+  // the bin regions; the grid refinement also without)
+  const bool survivor_hist = fused && (grid_refine || binned);
   binned = binned && survivor_hist;
   auto* region = binned ? reinterpret_cast<uint64_t*>(base + o_region) : nullptr;
   bool fallback_launched = false;
@@ -569,7 +580,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // early, one block ranks at the end), not while a 16-CTA threshold
     // cluster runs: that gained nothing.
     TK_TRY(launch_filter(p, tau, M, buf, counts, fused ? 0 : -1, st, survivor_hist ? refine_ctl : nullptr,
-                         &hdr->status, region));
+                         &hdr->status, region, grid_refine ? nullptr : refine_ctl_next));
     ++nl;
     TK_TRY(mark(3));
     // Where to handle a miss: inside the refinement kernel (no launch when
@@ -612,6 +623,7 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
   if (binned) {  // (the bin sort reads them when the refinement says so)
     rj.fhist = refine_ctl + kRefineGridFilterHist;
     rj.region = region;
+    if (!grid_refine) rj.rctl = refine_ctl;  // (the refinement cluster: it checks them itself)
   }
   if (plan.path == TOPK_PATH_PROFK && !fallback_launched) {
     rj.check_miss = true;
