@@ -1378,8 +1378,7 @@ __device__ __forceinline__ void select_body(const SelParams& a) {
 // of that bin, read straight from the regions by CTA 0 -- no pass over the
 // candidate buffer, no exchange between the cluster's CTAs.  Every CTA reads
 // the same words and the same histogram, so all take the same decision;
-// false (everywhere) when the regions cannot serve: incomplete, more than
-// kBinnedTopMax keys beyond the top bin or the k-th among them, or more keys
+// false (everywhere) when the regions cannot serve: incomplete, or more keys
 // down to the boundary bin than the first buffer holds.  The caller then
 // selects from the buffer as usual.  No miss (checked by the caller).
 template <int BLOCK, int P, int CB, int NB>
@@ -1429,8 +1428,9 @@ __device__ bool select_from_regions(const SelParams& a) {
     __syncthreads();
     const unsigned bb = static_cast<unsigned>(r_info[0]);
     const unsigned bb_start = static_cast<unsigned>(r_info[1]), bb_tot = static_cast<unsigned>(r_info[2]);
-    const unsigned top = bst[1];  // the top bin's keys (those beyond 2047 << shift)
-    const bool ok = r_words[0] == 0ull && r_info[0] != ~0ull && bb > 0u && top <= kBinnedTopMax &&
+    // (the top bin -- keys beyond 2047 << shift, no plain digit -- needs no
+    // care here: its keys are ranked and sorted as keys, like any other)
+    const bool ok = r_words[0] == 0ull && r_info[0] != ~0ull &&
                     static_cast<int64_t>(bb_start) + bb_tot <= static_cast<int64_t>(P);
     if (!ok) {
       __syncthreads();  // (bst and the words are rewritten by the usual selection)
