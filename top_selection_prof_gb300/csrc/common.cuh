@@ -238,6 +238,11 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsign
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
       ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy) : "memory");
 }
+// Asks L2 to fetch [src, src + bytes) from global memory (no destination, no
+// completion): src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // Orders this thread's earlier generic-proxy accesses of shared memory before
 // later bulk copies (async proxy) into it.
 __device__ __forceinline__ void fence_proxy_async_smem() {

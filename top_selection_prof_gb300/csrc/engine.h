@@ -110,6 +110,9 @@ struct SampleTauScratch {
 // Whether the fused grid fits on the device at once (else launch_sample and
 // a threshold select are used).
 bool sample_tau_supported(const Problem& p, int64_t S);
+// Whether the fused grid ranks without a grid barrier: every block keeps its
+// own t largest draws and the last block ranks their union.
+bool sample_tau_local(int64_t S, int64_t t);
 cudaError_t launch_sample_tau(const Problem& p, int64_t S, int64_t t, uint64_t seed, uint64_t counter,
                               unsigned long long* counts_to_zero, DevHeader* hdr, const SampleTauScratch& sc,
                               uint64_t* tau_out, cudaStream_t st);
@@ -156,10 +159,22 @@ constexpr int64_t kFallbackTile = 4096;
 // refine_ctl_next (with region, nullable): the other copy of the control
 // words, cleared by the filter's blocks for the next call (when no grid
 // refinement, which clears it otherwise, follows).
+// l2_ahead (one selection over 16-byte aligned data): tiles past the first
+// ring stages that each block of the TMA-ring filter asks L2 to fetch before
+// tau is known -- for a preceding grid that leaves HBM idle (0: none).
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
                           unsigned long long* counts, int reserved_sms, cudaStream_t st,
                           unsigned* refine_ctl = nullptr, int* status = nullptr, uint64_t* region = nullptr,
-                          unsigned* refine_ctl_next = nullptr);
+                          unsigned* refine_ctl_next = nullptr, int l2_ahead = 0);
+// Tiles (16 KB) each of the ring filter's blocks asks L2 to fetch while the
+// fused sampler ranks in its local mode (no grid barrier: it waits on L2
+// atomics of no other block, and its draws have landed), at most half of a
+// block's tiles, and the smallest input (bytes) that gains from it.  On a
+// GB300, single f32 rows with k = 1024 back to back: 2^28 175.3 -> 169.4 us,
+// 2^26 69.8 -> 66.5, 2^25 51.6 -> 48.3 (13 tiles); 2^24 unchanged; 32 tiles
+// lost 2.5 us at 2^25 and 2^26.
+constexpr int kRingL2Ahead = 24;
+constexpr int64_t kRingL2AheadMinBytes = int64_t{1} << 27;
 // force: 0 = only rows that missed, 1 = every row (fault injection / exact path).
 cudaError_t launch_fallback(const Problem& p, int64_t k, int64_t cap, uint64_t* buf,
                             unsigned long long* counts, const FallbackScratch& fs, int force,

@@ -60,6 +60,9 @@ struct FilterParams {
   // of kBinRegionCap keys (the filter_ring_kernel's end)
   uint64_t* region = nullptr;
   unsigned* refine_ctl_next = nullptr;  // (with region, nullable) cleared by the blocks for the next call
+  // (TMA-ring filter) tiles past its first ring stages that each block asks
+  // L2 to fetch before tau is known
+  int l2_ahead = 0;
 };
 
 // (with bin regions) set when some survivors of this block left its stages;

@@ -96,6 +96,12 @@ __global__ void __launch_bounds__(kFilterBlock, kRingBlocksPerSm) filter_ring_ke
     // start before it has finished (half the ring: the rest of the stream
     // would queue in front of that grid's last loads)
     for (int64_t i = 0; i < kRingStages / 2 && i < mine; ++i) issue(i);
+    // where the preceding grid leaves HBM idle, the block's next tiles go to
+    // L2 meanwhile, and their ring copies later hit there (at most half its
+    // tiles: more crowds L2 and costs more than it saves)
+    const int64_t ahead = fp.l2_ahead < mine / 2 ? fp.l2_ahead : mine / 2;
+    for (int64_t i = kRingStages / 2; i < kRingStages / 2 + ahead && i < mine; ++i)
+      bulk_prefetch_l2(xb + (first + i * step) * kTile * static_cast<int64_t>(sizeof(T)), kRingStageBytes);
   }
   if (HIST)
     for (int i = tid; i < kRefineGridBins; i += kFilterBlock) sh_hist[i] = 0u;
@@ -289,8 +295,9 @@ cudaError_t launch_filter_h(const FilterParams& fp, int reserved_sms, cudaStream
 
 cudaError_t launch_filter(const Problem& p, const uint64_t* tau, int64_t cap, uint64_t* buf,
                           unsigned long long* counts, int reserved_sms, cudaStream_t st, unsigned* refine_ctl,
-                          int* status, uint64_t* region, unsigned* refine_ctl_next) {
+                          int* status, uint64_t* region, unsigned* refine_ctl_next, int l2_ahead) {
   FilterParams fp{p.x, p.nsel, p.len, p.ib, p.flip, tau, cap, buf, counts, Divider{}};
+  fp.l2_ahead = l2_ahead > 0 ? l2_ahead : 0;
   fp.refine_ctl = refine_ctl;
   fp.status = status;
   // (bin regions: the TMA-ring filter of one selection with the survivor histogram)

@@ -417,6 +417,12 @@ bool sample_tau_supported(const Problem& p, int64_t S) {
   return q * p.nsel <= cap;
 }
 
+bool sample_tau_local(int64_t S, int64_t t) {
+  const int64_t q = ((S + 1) / 2 + kSampleBlock - 1) / kSampleBlock;
+  // (one key of slack per block: equal keys at a block's bound are all kept)
+  return q * (t + 1) <= kTauGather;
+}
+
 cudaError_t launch_sample_tau(const Problem& p, int64_t S, int64_t t, uint64_t seed, uint64_t counter,
                               unsigned long long* counts_to_zero, DevHeader* hdr, const SampleTauScratch& sc,
                               uint64_t* tau_out, cudaStream_t st) {
@@ -436,8 +442,7 @@ cudaError_t launch_sample_tau(const Problem& p, int64_t S, int64_t t, uint64_t s
   sp.refine_ctl = sc.refine_ctl;
   sp.t = t;
   sp.q = static_cast<int>(((S + 1) / 2 + kSampleBlock - 1) / kSampleBlock);
-  // (one key of slack per block: equal keys at a block's bound are all kept)
-  sp.local = static_cast<int64_t>(sp.q) * (t + 1) <= kTauGather ? 1 : 0;
+  sp.local = sample_tau_local(S, t) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sp.q * p.nsel), 1, 1);
   cfg.blockDim = dim3(kSampleBlock, 1, 1);

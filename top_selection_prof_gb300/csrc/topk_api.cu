@@ -579,8 +579,14 @@ int run(const void* x, int dtype, int64_t rows, int64_t n, int64_t k, int larges
     // The filter may launch while the fused grid finishes (its blocks leave
     // early, one block ranks at the end), not while a 16-CTA threshold
     // cluster runs: that gained nothing.
+    // (a fused sampler without grid barriers leaves HBM idle once its draws
+    // have landed: the filter's blocks start fetching their tiles into L2)
+    const int l2_ahead = fused && sample_tau_local(S, plan.t) &&
+                                 p.nsel * p.len * static_cast<int64_t>(p.dtype == kF32 ? 4 : 2) >= kRingL2AheadMinBytes
+                             ? kRingL2Ahead
+                             : 0;
     TK_TRY(launch_filter(p, tau, M, buf, counts, fused ? 0 : -1, st, survivor_hist ? refine_ctl : nullptr,
-                         &hdr->status, region, grid_refine ? nullptr : refine_ctl_next));
+                         &hdr->status, region, grid_refine ? nullptr : refine_ctl_next, l2_ahead));
     ++nl;
     TK_TRY(mark(3));
     // Where to handle a miss: inside the refinement kernel (no launch when
