@@ -25,10 +25,12 @@
  *     topk_select_ex synchronises the stream when `stats` is non-NULL.
  *   - The library keeps a per-(device, stream) workspace for the sample, the
  *     threshold, the candidate buffer and counters (and, for one selection
- *     with k >= 4096 over 16-byte aligned data, 32 MiB of bin regions into
- *     which the filter places its survivors); it grows on demand with
- *     stream-ordered allocation and is never shrunk.  Calls that share a
- *     stream are ordered; calls on different streams use different workspaces.
+ *     over 16-byte aligned data with k >= 3072, or with 512 <= k < 3072 and
+ *     more expected survivors than one refinement block caches, 32 MiB of
+ *     bin regions into which the filter places its survivors); it grows on
+ *     demand with stream-ordered allocation and is never shrunk.  Calls that
+ *     share a stream are ordered; calls on different streams use different
+ *     workspaces.
  *   - Errors are returned as topk_status_t codes; nothing is thrown across the
  *     ABI and no message is printed.
  */
