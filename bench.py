@@ -153,26 +153,33 @@ class ClockSampler:
             self.proc.kill()
         self.file.flush()
         with open(self.file.name) as fh:
-            rows = [ln.strip().split(", ") for ln in fh if ln.strip()]
+            lines = fh.readlines()
         os.unlink(self.file.name)
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-                power.append(float(r[3]))
-            except ValueError:
-                continue
-            for nm, val in zip(names, r[5:9]):
-                if val.strip().lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+        return summarize_clocks(lines)
+
+
+def summarize_clocks(lines):
+    """Median SM clock, the largest max clock and power, and every throttle reason seen Active, from the
+    nvidia-smi CSV rows of ClockSampler.FIELDS (noheader, nounits); rows that do not parse are skipped."""
+    sm, smax, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        r = ln.strip().split(", ")
+        if len(r) < 9:
+            continue
+        try:
+            sm.append(float(r[1]))
+            smax.append(float(r[2]))
+            power.append(float(r[3]))
+        except ValueError:
+            continue
+        for nm, val in zip(names, r[5:9]):
+            if val.strip().lower() == "active":
+                reasons.add(nm)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+            "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
 # ---------------------------------------------------------------------------
